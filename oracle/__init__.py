@@ -1,0 +1,11 @@
+"""CPU oracle for paged-KV attention (TEST INFRASTRUCTURE).
+
+Only ``tests/``, the smoke check in ``__graft_entry__`` and the CPU-baseline
+leg of ``bench.py`` may import this package.  The product path never does,
+and this package imports nothing from the product.
+"""
+from .paged_attention import (  # noqa: F401
+    gather_request_kv, visible_keys, softmax_attention, paged_attention,
+    paged_decode, visible_block_range, splitk_partials, lse_combine, run_batch,
+)
+from .brute_force import brute_force_attention  # noqa: F401

@@ -1,0 +1,46 @@
+"""Plant one mistake at a time in a copy of the oracle; the pins must catch each.
+
+Runs on the CPU only.  Every mutation is a plausible slip (window off by one,
+wrong GQA grouping, cap applied to the unscaled logit, dropped scale, wrong
+slot in the table walk, causal offset, wrong LSE, wrong combine weights, split
+ranges not anchored at the visible start) and must make the pin suite fail.
+"""
+import os
+import shutil
+import subprocess
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+MUTATIONS = [
+    ("window off by one", "keep &= t > pos - window", "keep &= t >= pos - window"),
+    ("GQA as h % Hkv", "heads = slice(kvh * G, (kvh + 1) * G)", "heads = slice(kvh, Hq, Hkv)"),
+    ("cap on unscaled ratio", "s = softcap * np.tanh(s / softcap)", "s = softcap * np.tanh(s)"),
+    ("dropped scale", "s = scale * (keys @ q_rows.T)", "s = (keys @ q_rows.T)"),
+    ("wrong slot", "t % block_size, :]", "(t + 1) % block_size, :]"),
+    ("causal offset", "pos = L - n + i", "pos = L - n + i - 1"),
+    ("half LSE", "lse = m + np.log(l)", "lse = m + 0.5 * np.log(l)"),
+    ("combine weights squared", "np.exp(partial_lse - Ms[..., None])",
+     "np.exp(2.0 * (partial_lse - Ms[..., None]))"),
+    ("splits not anchored", "j0 = jlo + s * split_blocks", "j0 = s * split_blocks"),
+]
+
+
+@pytest.mark.parametrize("name,old,new", MUTATIONS, ids=[m[0] for m in MUTATIONS])
+def test_pins_catch_planted_mistake(tmp_path, name, old, new):
+    shutil.copytree(os.path.join(ROOT, "oracle"), tmp_path / "oracle",
+                    ignore=shutil.ignore_patterns("__pycache__", "*.so", "*.o"))
+    (tmp_path / "tests").mkdir()
+    for f in ("conftest.py", "problems.py", "test_oracle_pins.py"):
+        shutil.copy(os.path.join(ROOT, "tests", f), tmp_path / "tests" / f)
+    src = (tmp_path / "oracle" / "paged_attention.py").read_text()
+    assert src.count(old) >= 1, f"mutation site for {name!r} not found"
+    (tmp_path / "oracle" / "paged_attention.py").write_text(src.replace(old, new))
+    env = dict(os.environ, PYTHONPATH=str(tmp_path), PYTHONDONTWRITEBYTECODE="1")
+    r = subprocess.run([sys.executable, "-m", "pytest", "-q", "-x", "-p", "no:cacheprovider",
+                        "tests/test_oracle_pins.py"], cwd=tmp_path, env=env,
+                       capture_output=True, text=True, timeout=600)
+    assert r.returncode == 1, f"pins did not catch {name!r}:\n{r.stdout[-2000:]}"
+    assert "failed" in r.stdout
