@@ -1,0 +1,398 @@
+#!/usr/bin/env python3
+"""Benchmark of the paged-KV attention hot path on GB300.
+
+Workload (one step): the serving-shaped decode batch -- B=32 requests,
+seq_lens ~ U[512, 4096], Hq=8, Hkv=2, head_dim=256, block_size=16, a pool of
+16384 blocks in shuffled order, bf16 N(0,1) K/V, tanh softcap 50 -- run
+through two layers with separate pools: a global layer (window 0) and a
+sliding layer (window 512).  Each layer is one split-K decode launch plus
+one combine launch.
+
+Metric: paged-decode KV GB/s, counting algorithmic bytes (K/V rows of every
+visible key plus the query rows) per step over the device time of the step.
+The L2 is flushed (a 512 MiB write) before every timed step; the flush is
+outside the per-step CUDA-event window.
+
+``--impl reference`` times the fp64 CPU oracle on a bounded sample of the
+same workload on the host cores instead.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+# The CPU baseline (fp64 oracle) runs on one host thread; keep BLAS at one too.
+for _v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+    os.environ.setdefault(_v, "1")
+
+WORKLOAD_NAME = ("decode serving: B=32, seq_lens~U[512,4096], Hq=8, Hkv=2, head_dim=256, "
+                 "block_size=16, pool 16384 shuffled blocks, bf16 N(0,1), softcap 50, "
+                 "two layers per step (window 0 and window 512)")
+METRIC = "paged-decode KV GB/s"
+FALLBACK_HBM_GBS = 6800.0
+PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "decode_splitk_serving.md")
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=50)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--seed", type=int, default=0)
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--cpu-seconds", type=float, default=15.0,
+                   help="budget of the oracle sample (CPU baseline)")
+    return p.parse_args()
+
+
+def step_bytes(calls) -> float:
+    """Algorithmic bytes of one step: K and V rows of every visible key, plus q."""
+    total = 0
+    for b in calls:
+        kv_row = 2 * b.num_kv_heads * b.head_dim * 2  # K and V, bf16
+        for L in b.seq_lens_host:
+            vis = L if b.window <= 0 else min(L, b.window)
+            total += vis * kv_row
+        total += b.q.numel() * 2
+    return float(total)
+
+
+def launch_bytes(batch) -> float:
+    kv_row = 2 * batch.num_kv_heads * batch.head_dim * 2
+    vis = sum(L if batch.window <= 0 else min(L, batch.window) for L in batch.seq_lens_host)
+    return float(vis * kv_row + batch.q.numel() * 2)
+
+
+def hbm_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        try:
+            d = json.load(open(path))
+            for key in ("hbm_gbs", "hbm_GBps", "hbm"):
+                if key in d and isinstance(d[key], (int, float)):
+                    return float(d[key]), "measured"
+        except Exception:
+            pass
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+def traffic_from_profile():
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current decode kernel source (else None)."""
+    import hashlib
+    if not os.path.exists(PROFILE_SUMMARY):
+        return None
+    src = os.path.join(ROOT, "paged_kv_attention_12_gb300", "csrc", "decode.cu")
+    h = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    vals = {}
+    for line in open(PROFILE_SUMMARY):
+        if ":" in line and line.strip().startswith("- "):
+            k, v = line.strip()[2:].split(":", 1)
+            vals[k.strip()] = v.strip()
+    if vals.get("decode.cu sha256[:16]") != h:
+        return None
+    try:
+        return float(vals["dram bytes per launch (avg)"])
+    except (KeyError, ValueError):
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi SM clock / throttle-reason samples during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        import tempfile
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.2)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        os.unlink(self.path)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def cpu_baseline(calls, budget_s: float):
+    """The fp64 oracle on a bounded sample (first requests of each layer)."""
+    import numpy as np  # noqa: F401
+    import oracle
+    from paged_kv_attention_12_gb300 import workload
+    done_bytes = 0.0
+    t_used = 0.0
+    reqs_done = 0
+    per_layer = max(1, budget_s / len(calls))
+    for batch in calls:
+        t_layer = 0.0
+        for b in range(batch.num_requests):
+            if t_layer >= per_layer:
+                break
+            arr = workload.to_numpy_f64(batch, [b])
+            t0 = time.perf_counter()
+            oracle.run_batch(arr)
+            dt = time.perf_counter() - t0
+            t_layer += dt
+            L = batch.seq_lens_host[b]
+            vis = L if batch.window <= 0 else min(L, batch.window)
+            done_bytes += vis * 2 * batch.num_kv_heads * batch.head_dim * 2 + \
+                batch.num_q_heads * batch.head_dim * 2
+            reqs_done += 1
+        t_used += t_layer
+    return {"value": done_bytes / t_used / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"{reqs_done} of {sum(c.num_requests for c in calls)} decode requests "
+                      f"(first requests of each layer, same workload), fp64 numpy oracle, "
+                      f"one thread, {t_used:.1f} s"}
+
+
+def dist_setup(args):
+    import torch
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device(f"cuda:{local}"))
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world <= 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def run_reference(args):
+    """Oracle arm: each step is a bounded sample of the workload on host cores."""
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    from paged_kv_attention_12_gb300 import workload
+    calls = workload.decode_serving(args.seed, "cpu")
+    import oracle
+    per_step = []
+    step_budget = max(1.0, 60.0 / max(1, args.steps + args.warmup))
+    vals = []
+    for it in range(args.warmup + args.steps):
+        done, t = 0.0, 0.0
+        for batch in calls:
+            b = it % batch.num_requests
+            arr = workload.to_numpy_f64(batch, [b])
+            t0 = time.perf_counter()
+            oracle.run_batch(arr)
+            t += time.perf_counter() - t0
+            L = batch.seq_lens_host[b]
+            vis = L if batch.window <= 0 else min(L, batch.window)
+            done += vis * 2 * batch.num_kv_heads * batch.head_dim * 2 + \
+                batch.num_q_heads * batch.head_dim * 2
+            if t > step_budget:
+                break
+        if it >= args.warmup:
+            vals.append(done / t / 1e9)
+            per_step.append(t)
+    value = statistics.median(vals)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * statistics.median(per_step), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": WORKLOAD_NAME, "sample": "one request per layer per step"},
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": "one decode request of each layer per step, fp64 numpy "
+                                   "oracle, one thread"},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+    return 0
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        return run_reference(args)
+    import torch
+    world, rank, local = dist_setup(args)
+    dev = torch.device(f"cuda:{local}")
+    torch.cuda.set_device(dev)
+    from paged_kv_attention_12_gb300 import _build, binding, workload
+    if rank == 0 or world > 1:
+        _build.build()
+    binding.lib()
+
+    calls = workload.decode_serving(args.seed + 1000 * rank, dev)
+    runners = [binding.DecodeSplitK(b) for b in calls]
+    bytes_step = step_bytes(calls)
+    flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step(kernel_events=None):
+        for i, (b, r) in enumerate(zip(calls, runners)):
+            if kernel_events is not None:
+                kernel_events[i][0].record(stream)
+            binding.paged_decode_splitk(b.q, r.partial_o, r.partial_lse, b.k_pool, b.v_pool,
+                                        b.block_tables, b.seq_lens, b.max_seq_len,
+                                        r.num_splits, r.split_blocks, scale=b.scale,
+                                        softcap=b.softcap, window=b.window)
+            if kernel_events is not None:
+                kernel_events[i][1].record(stream)
+            binding.paged_decode_splitk_combine(r.partial_o, r.partial_lse, r.out)
+
+    for _ in range(args.warmup):
+        flush.fill_(1.0)
+        step()
+    torch.cuda.synchronize()
+
+    sampler = ClockSampler(local) if rank == 0 else None
+    if sampler:
+        sampler.start()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    kev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+            for _ in calls] for _ in range(args.steps)]
+    barrier(world)
+    torch.cuda.synchronize()
+    t_wall = time.perf_counter()
+    for s in range(args.steps):
+        flush.fill_(float(s))
+        ev[s][0].record(stream)
+        step(kev[s])
+        ev[s][1].record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    wall = time.perf_counter() - t_wall
+    clocks = sampler.stop() if sampler else None
+    step_ms = [a.elapsed_time(b) for a, b in ev]
+    kern_ms = [sum(a.elapsed_time(b) for a, b in ks) for ks in kev]
+    total_ms = max_over_ranks(sum(step_ms), world)
+    ms_per_step = total_ms / args.steps
+    value = world * bytes_step / (ms_per_step * 1e-3) / 1e9
+
+    # end to end through the public API with pinned host buffers
+    e2e = None
+    if not args.no_e2e:
+        host_in = []
+        for b in calls:
+            host_in.append((b.q.cpu().pin_memory(), b.block_tables.cpu().pin_memory(),
+                            b.seq_lens.cpu().pin_memory()))
+        host_out = [torch.empty(r.out.shape, dtype=r.out.dtype).pin_memory() for r in runners]
+        h2d = sum(x.numel() * x.element_size() for t in host_in for x in t)
+        d2h = sum(x.numel() * x.element_size() for x in host_out)
+        e_ms = []
+        for s in range(args.warmup + args.steps):
+            flush.fill_(float(s))
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for (hq, ht, hs), b in zip(host_in, calls):
+                b.q.copy_(hq, non_blocking=True)
+                b.block_tables.copy_(ht, non_blocking=True)
+                b.seq_lens.copy_(hs, non_blocking=True)
+            step()
+            for ho, r in zip(host_out, runners):
+                ho.copy_(r.out, non_blocking=True)
+            e1.record(stream)
+            e1.synchronize()
+            if s >= args.warmup:
+                e_ms.append(e0.elapsed_time(e1))
+        e2e_ms = max_over_ranks(sum(e_ms) / len(e_ms), world)
+        e2e = {"value": world * bytes_step / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+    if rank != 0:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+        return 0
+
+    peak, peak_kind = hbm_peak()
+    kern_avg_s = sum(kern_ms) / (len(kern_ms) * len(calls)) * 1e-3
+    achieved = (bytes_step / len(calls)) / kern_avg_s / 1e9
+    line = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": WORKLOAD_NAME, "l2": "flushed before every step (512 MiB write)",
+                   "splits": [[r.num_splits, r.split_blocks] for r in runners],
+                   "bytes_per_step": bytes_step, "parallelism": f"replicas{world}"},
+        "roofline": {"bound": "hbm", "kernel": "paged_decode_kernel (split-K)",
+                     "achieved": achieved, "peak": peak, "peak_kind": peak_kind,
+                     "unit": "GB/s", "frac": achieved / peak,
+                     "traffic": traffic_from_profile()},
+        "gpu_launches": args.steps * 2 * len(calls),
+        "wall_s": wall,
+    }
+    if e2e:
+        line["e2e"] = e2e
+    if clocks:
+        line["clocks"] = clocks
+    if not args.no_cpu_baseline and world == 1:
+        line["cpu_baseline"] = cpu_baseline(calls, args.cpu_seconds)
+    print(json.dumps(line))
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

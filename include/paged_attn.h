@@ -1,0 +1,179 @@
+/*
+ * paged_attn.h -- C ABI of the GB300 (sm_103a) paged-KV attention library.
+ *
+ * The operation is attention read through a block-paged KV cache, as the
+ * inference-server pages describe it:
+ *   - "Block-paged KV cache with refcounted blocks, window-aware sliding
+ *     layers" and "Triton paged decode and prefill kernels reading K/V
+ *     through block tables; split-K decode variant" (inference-server README,
+ *     engine feature list);
+ *   - "Block-paged per-layer KV with refcounted blocks, lazy allocation, and
+ *     SDPA gather -- vLLM/PagedAttention layout" (github README, "What's
+ *     inside", Paged KV cache row);
+ *   - "GQA with QK/V-norm + KV sharing ... softcapping" (github README,
+ *     "What's inside", Custom Gemma 4 forward row);
+ *   - mixed-batch chunked prefill, "Needs custom attention path" (architecture
+ *     page, "Phase status" table).
+ *
+ * Definitions shared by every entry point
+ * ---------------------------------------
+ *  B       requests; Hq / Hkv query / KV heads, G = Hq / Hkv in {1,2,4,8};
+ *  D       head_dim in {64, 128, 256}; bs = block_size = 16.
+ *  KV pool bf16 [num_blocks][Hkv][bs][D] for K and for V (one pool per layer;
+ *          "KV sharing" between layers is the same pool passed twice).  Each
+ *          (block, head) tile is one contiguous bs*D*2-byte run.
+ *  block_tables  int32 [B][max_blocks], device.  Token t of request b is in
+ *          block block_tables[b][t / bs], slot t % bs.  Entries at
+ *          j >= ceil(seq_len/bs), and entries of blocks that lie wholly
+ *          before every query's sliding window, are never dereferenced (they
+ *          may be -1 or point at freed blocks).  Shared prefix blocks are the
+ *          same id in several rows; the library only reads them.
+ *  seq_lens int32 [B], device: context length including the new tokens.
+ *  Query i of request b (n_b new tokens) sits at position p = L_b - n_b + i
+ *          and sees key t iff t <= p and (window <= 0 or t > p - window).
+ *  Logit   s = scale * q.k; if softcap > 0, s = softcap * tanh(s / softcap).
+ *  GQA     query head h reads KV head h / G.
+ *  Output  softmax(s) . V over the visible keys, fp32 accumulation, stored
+ *          bf16 (round to nearest even).  No visible key -> output 0.
+ *
+ * Ownership and threading: the caller owns every buffer (device memory unless
+ * stated); the library allocates nothing, never synchronises, keeps no state
+ * between calls except cached device attributes, and launches on the given
+ * stream (a cudaStream_t passed as void*; NULL = legacy default stream).
+ * Calls are asynchronous and may be captured in CUDA graphs.
+ *
+ * Errors: every entry point returns a pka_status.  Argument errors are found
+ * on the host before any launch (nothing is written).  PKA_ERR_CUDA means a
+ * launch failed; read cudaGetLastError() for the cause.  Kernels never fault
+ * on a bad table entry: an id outside [0, num_blocks) is replaced by block 0
+ * and bit PKA_DEVERR_BAD_TABLE is OR-ed into *params->err (when non-NULL);
+ * a bounded wait that runs out sets PKA_DEVERR_TIMEOUT and the CTA returns.
+ */
+#ifndef PAGED_ATTN_H_
+#define PAGED_ATTN_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  PKA_OK = 0,
+  PKA_ERR_NULL = -1,        /* a required pointer is NULL */
+  PKA_ERR_SHAPE = -2,       /* inconsistent sizes (Hq % Hkv, negative sizes, ...) */
+  PKA_ERR_ALIGN = -3,       /* q/out/pool pointer not 16-byte aligned */
+  PKA_ERR_UNSUPPORTED = -4, /* head_dim, block_size or G outside the supported set */
+  PKA_ERR_WORKSPACE = -5,   /* split-K partition does not cover max_seq_len */
+  PKA_ERR_BAD_TABLE = -6,   /* (host view of PKA_DEVERR_BAD_TABLE) */
+  PKA_ERR_TIMEOUT = -7,     /* (host view of PKA_DEVERR_TIMEOUT) */
+  PKA_ERR_CUDA = -8         /* a CUDA runtime call or launch failed */
+} pka_status;
+
+/* Bits OR-ed into the optional device error word (pka_attn_params.err). */
+#define PKA_DEVERR_BAD_TABLE 1  /* a table id was outside [0, num_blocks) */
+#define PKA_DEVERR_TIMEOUT 2    /* a bounded mbarrier wait ran out */
+#define PKA_DEVERR_SEQ_LEN 4    /* seq_len beyond max_blocks*bs or the split cover */
+
+/* One layer's K/V block pool.  k and v are device pointers, 16-byte aligned,
+ * bf16 [num_blocks][num_kv_heads][block_size][head_dim]. */
+typedef struct {
+  const void* k;
+  const void* v;
+  int32_t num_blocks;
+  int32_t num_kv_heads;
+  int32_t block_size;
+  int32_t head_dim;
+} pka_kv_pool;
+
+/* Attention parameters.  scale multiplies q.k; softcap <= 0 disables the tanh
+ * cap; window <= 0 is full (causal) attention, else the W-key sliding window
+ * described above.  err: optional device int32 the kernels OR error bits into
+ * (never cleared by the library). */
+typedef struct {
+  float scale;
+  float softcap;
+  int32_t window;
+  int32_t* err;
+} pka_attn_params;
+
+/* Library version (major*10000 + minor*100 + patch). */
+int pka_version(void);
+
+/* Human-readable name of a pka_status (static string). */
+const char* pka_status_string(int status);
+
+/* Decode: one query token per request (engine feature list, "Triton paged
+ * decode ... kernels reading K/V through block tables").
+ * q   bf16 [B][Hq][D], out bf16 [B][Hq][D] (device, 16-byte aligned).
+ * One CTA per (request, KV head) streams that request's visible blocks; use
+ * the split-K entry points below when B*Hkv is small next to the SM count. */
+int paged_decode_attn(const void* q, void* out, const pka_kv_pool* kv,
+                      const int32_t* block_tables, int32_t max_blocks,
+                      const int32_t* seq_lens, int32_t B, int32_t Hq,
+                      int32_t max_seq_len, const pka_attn_params* params,
+                      void* stream);
+
+/* Split-K plan (host only, no CUDA call when sm_count > 0): picks the number
+ * of splits S and the split size C (in blocks) for a decode launch so that
+ * B*Hkv*S CTAs cover the GPU.  max_seq_len is a host upper bound of seq_lens.
+ * sm_count <= 0 queries the current device. */
+int paged_decode_splitk_plan(int32_t B, int32_t Hkv, int32_t max_seq_len,
+                             int32_t block_size, int32_t window, int32_t sm_count,
+                             int32_t* num_splits, int32_t* split_blocks);
+
+/* Bytes of fp32 partials a split-K launch writes: B*Hq*S*(D+1)*4. */
+size_t paged_decode_splitk_workspace_bytes(int32_t B, int32_t Hq, int32_t D,
+                                           int32_t num_splits);
+
+/* Split-K decode ("split-K decode variant", engine feature list).
+ * Split s of request b covers logical blocks [jlo + s*C, jlo + (s+1)*C) of
+ * the request's visible block range [jlo, jhi) (jlo = block of the first
+ * visible key), C = split_blocks.  Each (b, h, s) writes its softmax-
+ * normalised partial output partial_o fp32 [B][Hq][S][D] and its natural-log
+ * LSE partial_lse fp32 [B][Hq][S]; an empty split writes 0 and -inf.
+ * num_splits*split_blocks must cover the visible blocks of max_seq_len
+ * (else PKA_ERR_WORKSPACE). */
+int paged_decode_splitk(const void* q, float* partial_o, float* partial_lse,
+                        const pka_kv_pool* kv, const int32_t* block_tables,
+                        int32_t max_blocks, const int32_t* seq_lens, int32_t B,
+                        int32_t Hq, int32_t max_seq_len, int32_t num_splits,
+                        int32_t split_blocks, const pka_attn_params* params,
+                        void* stream);
+
+/* Log-sum-exp merge of split partials (the merge a split-K softmax needs):
+ * M = max_s LSE_s, w_s = exp(LSE_s - M),
+ * out = sum_s w_s*O_s / sum_s w_s (bf16 [B][Hq][D]),
+ * lse_out = M + ln sum_s w_s (fp32 [B][Hq], may be NULL). */
+int paged_decode_splitk_combine(const float* partial_o, const float* partial_lse,
+                                int32_t B, int32_t Hq, int32_t D, int32_t num_splits,
+                                void* out, float* lse_out, void* stream);
+
+/* Prefill / mixed batch ("Prefill in three modes: monolithic, chunked ...,
+ * batched", engine feature list; mixed-batch chunked prefill, architecture
+ * page "Phase status").  Varlen: request b owns query rows
+ * [query_start_loc[b], query_start_loc[b+1]) of q bf16 [total_q][Hq][D]; rows
+ * with one token (decode) and chunks of many tokens may be mixed in one
+ * launch.  Causal over cached prefix + chunk.  out bf16 [total_q][Hq][D].
+ * max_query_len / max_seq_len are host upper bounds. */
+int paged_prefill_attn(const void* q, void* out, const pka_kv_pool* kv,
+                       const int32_t* block_tables, int32_t max_blocks,
+                       const int32_t* query_start_loc, const int32_t* seq_lens,
+                       int32_t B, int32_t Hq, int32_t total_q, int32_t max_query_len,
+                       int32_t max_seq_len, const pka_attn_params* params,
+                       void* stream);
+
+/* Checked mode: validates, on the device, every table entry a call would
+ * dereference (j < ceil(seq_len/bs)) against [0, num_blocks), and seq_len
+ * against [0, max_blocks*bs]; OR-s PKA_DEVERR_* bits into *err (device int32,
+ * required).  Reads only the tables and seq_lens. */
+int paged_attn_check_tables(const int32_t* block_tables, int32_t max_blocks,
+                            const int32_t* seq_lens, int32_t B, int32_t num_blocks,
+                            int32_t block_size, int32_t* err, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PAGED_ATTN_H_ */

@@ -1,0 +1,220 @@
+"""ctypes binding of the C ABI in ``include/paged_attn.h``.
+
+Argument marshalling only: every function here forwards device pointers,
+sizes and the current CUDA stream to the library, where all of the work runs
+in CUDA kernels.  There is no CPU fallback: if the library is missing or was
+built for another machine, loading it raises.
+
+The raw C functions are available under their C names on :func:`lib`; the
+helpers below take torch tensors for convenience (the tensors are only used
+for their device pointers, shapes and the current stream).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "lib", "libpaged_attn.so")
+
+PKA_OK = 0
+STATUS = {
+    0: "PKA_OK", -1: "PKA_ERR_NULL", -2: "PKA_ERR_SHAPE", -3: "PKA_ERR_ALIGN",
+    -4: "PKA_ERR_UNSUPPORTED", -5: "PKA_ERR_WORKSPACE", -6: "PKA_ERR_BAD_TABLE",
+    -7: "PKA_ERR_TIMEOUT", -8: "PKA_ERR_CUDA",
+}
+DEVERR_BAD_TABLE = 1
+DEVERR_TIMEOUT = 2
+DEVERR_SEQ_LEN = 4
+
+EXPORTS = [
+    "pka_version", "pka_status_string", "paged_decode_attn", "paged_decode_splitk_plan",
+    "paged_decode_splitk_workspace_bytes", "paged_decode_splitk",
+    "paged_decode_splitk_combine", "paged_prefill_attn", "paged_attn_check_tables",
+]
+
+
+class PkaKvPool(ctypes.Structure):
+    _fields_ = [("k", ctypes.c_void_p), ("v", ctypes.c_void_p),
+                ("num_blocks", ctypes.c_int32), ("num_kv_heads", ctypes.c_int32),
+                ("block_size", ctypes.c_int32), ("head_dim", ctypes.c_int32)]
+
+
+class PkaAttnParams(ctypes.Structure):
+    _fields_ = [("scale", ctypes.c_float), ("softcap", ctypes.c_float),
+                ("window", ctypes.c_int32), ("err", ctypes.c_void_p)]
+
+
+class PagedAttnError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        super().__init__(f"{fn} returned {STATUS.get(status, status)}")
+        self.status = status
+
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """Load the CUDA library (raises if it is missing)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError(
+            f"{LIB_PATH} is missing: build it first (python -c 'import __graft_entry__ as g; g.build()')")
+    L = ctypes.CDLL(LIB_PATH)
+    P, I32, VP = ctypes.POINTER, ctypes.c_int32, ctypes.c_void_p
+    L.pka_version.restype = ctypes.c_int
+    L.pka_version.argtypes = []
+    L.pka_status_string.restype = ctypes.c_char_p
+    L.pka_status_string.argtypes = [ctypes.c_int]
+    L.paged_decode_attn.restype = ctypes.c_int
+    L.paged_decode_attn.argtypes = [VP, VP, P(PkaKvPool), VP, I32, VP, I32, I32, I32,
+                                    P(PkaAttnParams), VP]
+    L.paged_decode_splitk_plan.restype = ctypes.c_int
+    L.paged_decode_splitk_plan.argtypes = [I32, I32, I32, I32, I32, I32, P(I32), P(I32)]
+    L.paged_decode_splitk_workspace_bytes.restype = ctypes.c_size_t
+    L.paged_decode_splitk_workspace_bytes.argtypes = [I32, I32, I32, I32]
+    L.paged_decode_splitk.restype = ctypes.c_int
+    L.paged_decode_splitk.argtypes = [VP, VP, VP, P(PkaKvPool), VP, I32, VP, I32, I32, I32,
+                                      I32, I32, P(PkaAttnParams), VP]
+    L.paged_decode_splitk_combine.restype = ctypes.c_int
+    L.paged_decode_splitk_combine.argtypes = [VP, VP, I32, I32, I32, I32, VP, VP, VP]
+    L.paged_prefill_attn.restype = ctypes.c_int
+    L.paged_prefill_attn.argtypes = [VP, VP, P(PkaKvPool), VP, I32, VP, VP, I32, I32, I32,
+                                     I32, I32, P(PkaAttnParams), VP]
+    L.paged_attn_check_tables.restype = ctypes.c_int
+    L.paged_attn_check_tables.argtypes = [VP, I32, VP, I32, I32, I32, VP, VP]
+    _lib = L
+    return L
+
+
+def _check(fn: str, status: int) -> None:
+    if status != PKA_OK:
+        raise PagedAttnError(fn, status)
+
+
+def _ptr(t) -> Optional[int]:
+    return None if t is None else t.data_ptr()
+
+
+def _stream(stream) -> Optional[int]:
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream
+
+
+def kv_pool(k_pool, v_pool) -> PkaKvPool:
+    nb, hkv, bs, d = k_pool.shape
+    return PkaKvPool(k_pool.data_ptr(), v_pool.data_ptr(), nb, hkv, bs, d)
+
+
+def attn_params(scale: float, softcap: float = 0.0, window: int = 0, err=None) -> PkaAttnParams:
+    return PkaAttnParams(float(scale), float(softcap), int(window), _ptr(err))
+
+
+# ------------------------------------------------------------------ helpers
+def paged_decode_attn(q, out, k_pool, v_pool, block_tables, seq_lens, max_seq_len, *,
+                      scale, softcap=0.0, window=0, err=None, stream=None):
+    pool = kv_pool(k_pool, v_pool)
+    par = attn_params(scale, softcap, window, err)
+    st = lib().paged_decode_attn(q.data_ptr(), out.data_ptr(), ctypes.byref(pool),
+                                 block_tables.data_ptr(), block_tables.shape[1],
+                                 seq_lens.data_ptr(), q.shape[0], q.shape[1], int(max_seq_len),
+                                 ctypes.byref(par), _stream(stream))
+    _check("paged_decode_attn", st)
+
+
+def paged_decode_splitk_plan(B, Hkv, max_seq_len, block_size=16, window=0, sm_count=0):
+    s, c = ctypes.c_int32(), ctypes.c_int32()
+    st = lib().paged_decode_splitk_plan(B, Hkv, int(max_seq_len), block_size, int(window),
+                                        int(sm_count), ctypes.byref(s), ctypes.byref(c))
+    _check("paged_decode_splitk_plan", st)
+    return s.value, c.value
+
+
+def paged_decode_splitk_workspace_bytes(B, Hq, D, num_splits) -> int:
+    return int(lib().paged_decode_splitk_workspace_bytes(B, Hq, D, num_splits))
+
+
+def paged_decode_splitk(q, partial_o, partial_lse, k_pool, v_pool, block_tables, seq_lens,
+                        max_seq_len, num_splits, split_blocks, *, scale, softcap=0.0, window=0,
+                        err=None, stream=None):
+    pool = kv_pool(k_pool, v_pool)
+    par = attn_params(scale, softcap, window, err)
+    st = lib().paged_decode_splitk(q.data_ptr(), partial_o.data_ptr(), partial_lse.data_ptr(),
+                                   ctypes.byref(pool), block_tables.data_ptr(),
+                                   block_tables.shape[1], seq_lens.data_ptr(), q.shape[0],
+                                   q.shape[1], int(max_seq_len), int(num_splits),
+                                   int(split_blocks), ctypes.byref(par), _stream(stream))
+    _check("paged_decode_splitk", st)
+
+
+def paged_decode_splitk_combine(partial_o, partial_lse, out, lse_out=None, stream=None):
+    B, Hq, S, D = partial_o.shape
+    st = lib().paged_decode_splitk_combine(partial_o.data_ptr(), partial_lse.data_ptr(), B, Hq,
+                                           D, S, out.data_ptr(), _ptr(lse_out), _stream(stream))
+    _check("paged_decode_splitk_combine", st)
+
+
+def paged_prefill_attn(q, out, k_pool, v_pool, block_tables, query_start_loc, seq_lens,
+                       max_query_len, max_seq_len, *, scale, softcap=0.0, window=0, err=None,
+                       stream=None):
+    pool = kv_pool(k_pool, v_pool)
+    par = attn_params(scale, softcap, window, err)
+    st = lib().paged_prefill_attn(q.data_ptr(), out.data_ptr(), ctypes.byref(pool),
+                                  block_tables.data_ptr(), block_tables.shape[1],
+                                  query_start_loc.data_ptr(), seq_lens.data_ptr(),
+                                  seq_lens.shape[0], q.shape[1], q.shape[0], int(max_query_len),
+                                  int(max_seq_len), ctypes.byref(par), _stream(stream))
+    _check("paged_prefill_attn", st)
+
+
+def paged_attn_check_tables(block_tables, seq_lens, num_blocks, err, block_size=16, stream=None):
+    st = lib().paged_attn_check_tables(block_tables.data_ptr(), block_tables.shape[1],
+                                       seq_lens.data_ptr(), seq_lens.shape[0], int(num_blocks),
+                                       block_size, err.data_ptr(), _stream(stream))
+    _check("paged_attn_check_tables", st)
+
+
+# ------------------------------------------------------------ batch runners
+class DecodeSplitK:
+    """Split-K decode of one batch: plan once, own the fp32 partials, run.
+
+    ``run`` issues two launches (split-K partials, then the combine) on the
+    current stream.
+    """
+
+    def __init__(self, batch, sm_count: int = 0):
+        import torch
+        self.batch = batch
+        B, Hkv, D, Hq = batch.num_requests, batch.num_kv_heads, batch.head_dim, batch.num_q_heads
+        self.num_splits, self.split_blocks = paged_decode_splitk_plan(
+            B, Hkv, batch.max_seq_len, batch.block_size, batch.window, sm_count)
+        dev = batch.q.device
+        self.partial_o = torch.empty((B, Hq, self.num_splits, D), dtype=torch.float32, device=dev)
+        self.partial_lse = torch.empty((B, Hq, self.num_splits), dtype=torch.float32, device=dev)
+        self.out = torch.empty_like(batch.q)
+
+    def run(self, err=None, lse_out=None):
+        b = self.batch
+        paged_decode_splitk(b.q, self.partial_o, self.partial_lse, b.k_pool, b.v_pool,
+                            b.block_tables, b.seq_lens, b.max_seq_len, self.num_splits,
+                            self.split_blocks, scale=b.scale, softcap=b.softcap,
+                            window=b.window, err=err)
+        paged_decode_splitk_combine(self.partial_o, self.partial_lse, self.out, lse_out)
+        return self.out
+
+
+def run_batch(batch, out=None, err=None):
+    """Attention of one batch through the library (decode or varlen prefill)."""
+    import torch
+    if out is None:
+        out = torch.empty_like(batch.q)
+    paged_prefill_attn(batch.q, out, batch.k_pool, batch.v_pool, batch.block_tables,
+                       batch.query_start_loc, batch.seq_lens, batch.max_query_len,
+                       batch.max_seq_len, scale=batch.scale, softcap=batch.softcap,
+                       window=batch.window, err=err)
+    return out

@@ -1,0 +1,70 @@
+// Internal launch interface between the C-ABI layer and the kernels.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace pka {
+
+// Arguments of the decode kernel (direct output or split-K partials).
+struct DecodeArgs {
+  const uint16_t* q;               // bf16 [rows][Hq][D]
+  void* out;                       // bf16 [rows][Hq][D] (direct mode)
+  float* partial_o;                // fp32 [B][Hq][S][D] (split mode)
+  float* partial_lse;              // fp32 [B][Hq][S]    (split mode)
+  const uint16_t* k;               // bf16 [num_blocks][Hkv][bs][D]
+  const uint16_t* v;
+  const int32_t* tables;           // int32 [B][max_blocks]
+  const int32_t* seq_lens;         // int32 [B]
+  const int32_t* query_start_loc;  // optional: the request's query row is qsl[b+1]-1
+  int32_t* err;
+  int32_t batch, Hq, Hkv, num_blocks, max_blocks;
+  int32_t num_splits;              // items per (request, head); 1 in direct mode
+  int32_t split_blocks;            // blocks per split; <= 0: direct mode (whole range)
+  float scale, softcap;
+  int32_t window;
+};
+
+cudaError_t launch_decode(const DecodeArgs& a, int head_dim, int group, int grid,
+                          cudaStream_t stream);
+
+struct CombineArgs {
+  const float* partial_o;    // [B*Hq][S][D]
+  const float* partial_lse;  // [B*Hq][S]
+  uint16_t* out;             // bf16 [B*Hq][D]
+  float* lse_out;            // [B*Hq] or null
+  int32_t rows, num_splits, head_dim;
+};
+
+cudaError_t launch_combine(const CombineArgs& a, cudaStream_t stream);
+
+struct CheckArgs {
+  const int32_t* tables;
+  const int32_t* seq_lens;
+  int32_t* err;
+  int32_t batch, max_blocks, num_blocks, block_size;
+};
+
+cudaError_t launch_check_tables(const CheckArgs& a, cudaStream_t stream);
+
+// Prefill / mixed varlen batch.
+struct PrefillArgs {
+  const uint16_t* q;               // bf16 [total_q][Hq][D]
+  uint16_t* out;                   // bf16 [total_q][Hq][D]
+  const uint16_t* k;
+  const uint16_t* v;
+  const int32_t* tables;
+  const int32_t* seq_lens;
+  const int32_t* query_start_loc;  // [B+1]
+  int32_t* err;
+  int32_t batch, Hq, Hkv, num_blocks, max_blocks, total_q, max_query_len;
+  float scale, softcap;
+  int32_t window;
+};
+
+cudaError_t launch_prefill(const PrefillArgs& a, int head_dim, int group, int sm_count,
+                           cudaStream_t stream);
+
+int device_sm_count();
+
+}  // namespace pka

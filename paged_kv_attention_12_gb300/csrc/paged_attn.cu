@@ -1,0 +1,276 @@
+// C-ABI layer: argument validation, split-K planning and kernel dispatch.
+//
+// Every argument error is found here, on the host, before anything is
+// launched; the kernels themselves only guard against data-dependent faults
+// (table ids, sequence lengths) and report those through the device error
+// word.  Nothing here allocates or synchronises.
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "kernels.h"
+#include "paged_attn.h"
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+int g_sm_count[kMaxDevices] = {0};
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool supported_dim(int d) { return d == 128 || d == 256; }
+bool supported_group(int g) { return g == 1 || g == 2 || g == 4 || g == 8; }
+
+// Largest number of blocks a decode query's visible keys can span.
+int max_visible_blocks(int max_seq_len, int window, int bs) {
+  if (max_seq_len <= 0) return 0;
+  const int full = (max_seq_len + bs - 1) / bs;
+  if (window <= 0) return full;
+  const int win = (window - 1) / bs + 2;
+  return full < win ? full : win;
+}
+
+int check_pool(const pka_kv_pool* kv, int Hq) {
+  if (kv == nullptr || kv->k == nullptr || kv->v == nullptr) return PKA_ERR_NULL;
+  if (kv->num_blocks <= 0 || kv->num_kv_heads <= 0 || Hq <= 0) return PKA_ERR_SHAPE;
+  if (Hq % kv->num_kv_heads != 0) return PKA_ERR_SHAPE;
+  if (kv->block_size != 16) return PKA_ERR_UNSUPPORTED;
+  if (!supported_dim(kv->head_dim)) return PKA_ERR_UNSUPPORTED;
+  if (!supported_group(Hq / kv->num_kv_heads)) return PKA_ERR_UNSUPPORTED;
+  if (!aligned16(kv->k) || !aligned16(kv->v)) return PKA_ERR_ALIGN;
+  return PKA_OK;
+}
+
+int check_common(const void* q, const pka_kv_pool* kv, const int32_t* block_tables,
+                 int32_t max_blocks, const int32_t* seq_lens, int32_t B, int32_t Hq,
+                 int32_t max_seq_len, const pka_attn_params* params) {
+  if (q == nullptr || block_tables == nullptr || seq_lens == nullptr || params == nullptr)
+    return PKA_ERR_NULL;
+  const int st = check_pool(kv, Hq);
+  if (st != PKA_OK) return st;
+  if (B < 0 || max_blocks <= 0 || max_seq_len < 0) return PKA_ERR_SHAPE;
+  if (static_cast<int64_t>(max_seq_len) > static_cast<int64_t>(max_blocks) * kv->block_size)
+    return PKA_ERR_SHAPE;
+  if (!(params->scale == params->scale) || !(params->softcap == params->softcap))
+    return PKA_ERR_SHAPE;  // NaN scale or cap
+  if (!aligned16(q)) return PKA_ERR_ALIGN;
+  return PKA_OK;
+}
+
+pka::DecodeArgs decode_args(const void* q, const pka_kv_pool* kv, const int32_t* block_tables,
+                            int32_t max_blocks, const int32_t* seq_lens, int32_t B, int32_t Hq,
+                            const pka_attn_params* p) {
+  pka::DecodeArgs a{};
+  a.q = static_cast<const uint16_t*>(q);
+  a.k = static_cast<const uint16_t*>(kv->k);
+  a.v = static_cast<const uint16_t*>(kv->v);
+  a.tables = block_tables;
+  a.seq_lens = seq_lens;
+  a.query_start_loc = nullptr;
+  a.err = p->err;
+  a.batch = B;
+  a.Hq = Hq;
+  a.Hkv = kv->num_kv_heads;
+  a.num_blocks = kv->num_blocks;
+  a.max_blocks = max_blocks;
+  a.scale = p->scale;
+  a.softcap = p->softcap;
+  a.window = p->window;
+  return a;
+}
+
+}  // namespace
+
+namespace pka {
+
+int device_sm_count() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (dev >= 0 && dev < kMaxDevices && g_sm_count[dev] > 0) return g_sm_count[dev];
+  int n = 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  if (dev >= 0 && dev < kMaxDevices) g_sm_count[dev] = n;
+  return n;
+}
+
+}  // namespace pka
+
+extern "C" {
+
+int pka_version(void) { return 100; }
+
+const char* pka_status_string(int status) {
+  switch (status) {
+    case PKA_OK: return "ok";
+    case PKA_ERR_NULL: return "null pointer argument";
+    case PKA_ERR_SHAPE: return "inconsistent sizes";
+    case PKA_ERR_ALIGN: return "pointer not 16-byte aligned";
+    case PKA_ERR_UNSUPPORTED: return "unsupported head_dim, block_size or GQA group";
+    case PKA_ERR_WORKSPACE: return "split-K partition does not cover max_seq_len";
+    case PKA_ERR_BAD_TABLE: return "block table id out of range";
+    case PKA_ERR_TIMEOUT: return "bounded device wait timed out";
+    case PKA_ERR_CUDA: return "CUDA launch or runtime error";
+    default: return "unknown status";
+  }
+}
+
+int paged_decode_attn(const void* q, void* out, const pka_kv_pool* kv,
+                      const int32_t* block_tables, int32_t max_blocks,
+                      const int32_t* seq_lens, int32_t B, int32_t Hq, int32_t max_seq_len,
+                      const pka_attn_params* params, void* stream) {
+  if (out == nullptr) return PKA_ERR_NULL;
+  int st = check_common(q, kv, block_tables, max_blocks, seq_lens, B, Hq, max_seq_len, params);
+  if (st != PKA_OK) return st;
+  if (!aligned16(out)) return PKA_ERR_ALIGN;
+  if (B == 0) return PKA_OK;
+  pka::DecodeArgs a = decode_args(q, kv, block_tables, max_blocks, seq_lens, B, Hq, params);
+  a.out = out;
+  a.num_splits = 1;
+  a.split_blocks = 0;
+  const int items = B * kv->num_kv_heads;
+  const int sms = pka::device_sm_count();
+  if (sms <= 0) return PKA_ERR_CUDA;
+  const int grid = items < sms ? items : sms;
+  cudaError_t e = pka::launch_decode(a, kv->head_dim, Hq / kv->num_kv_heads, grid,
+                                     static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? PKA_OK : PKA_ERR_CUDA;
+}
+
+int paged_decode_splitk_plan(int32_t B, int32_t Hkv, int32_t max_seq_len, int32_t block_size,
+                             int32_t window, int32_t sm_count, int32_t* num_splits,
+                             int32_t* split_blocks) {
+  if (num_splits == nullptr || split_blocks == nullptr) return PKA_ERR_NULL;
+  if (B <= 0 || Hkv <= 0 || max_seq_len < 0 || block_size <= 0) return PKA_ERR_SHAPE;
+  if (sm_count <= 0) sm_count = pka::device_sm_count();
+  if (sm_count <= 0) return PKA_ERR_CUDA;
+  const int T = max_visible_blocks(max_seq_len, window, block_size);
+  if (T <= 0) {
+    *num_splits = 1;
+    *split_blocks = 1;
+    return PKA_OK;
+  }
+  const int64_t pairs = static_cast<int64_t>(B) * Hkv;
+  // Aim at about eight work items per persistent CTA (one CTA per SM) so the
+  // static round-robin assignment balances ragged lengths; keep splits at
+  // least four blocks long so the per-item merge stays small next to the
+  // streaming.
+  int64_t S = (8LL * sm_count + pairs - 1) / pairs;
+  if (S < 1) S = 1;
+  int64_t C = (T + S - 1) / S;
+  if (C < 4) C = 4;
+  if (C > T) C = T;
+  S = (T + C - 1) / C;
+  *num_splits = static_cast<int32_t>(S);
+  *split_blocks = static_cast<int32_t>(C);
+  return PKA_OK;
+}
+
+size_t paged_decode_splitk_workspace_bytes(int32_t B, int32_t Hq, int32_t D, int32_t num_splits) {
+  if (B <= 0 || Hq <= 0 || D <= 0 || num_splits <= 0) return 0;
+  return static_cast<size_t>(B) * Hq * num_splits * (static_cast<size_t>(D) + 1) * sizeof(float);
+}
+
+int paged_decode_splitk(const void* q, float* partial_o, float* partial_lse,
+                        const pka_kv_pool* kv, const int32_t* block_tables, int32_t max_blocks,
+                        const int32_t* seq_lens, int32_t B, int32_t Hq, int32_t max_seq_len,
+                        int32_t num_splits, int32_t split_blocks,
+                        const pka_attn_params* params, void* stream) {
+  if (partial_o == nullptr || partial_lse == nullptr) return PKA_ERR_NULL;
+  int st = check_common(q, kv, block_tables, max_blocks, seq_lens, B, Hq, max_seq_len, params);
+  if (st != PKA_OK) return st;
+  if (num_splits <= 0 || split_blocks <= 0) return PKA_ERR_SHAPE;
+  if (!aligned16(partial_o)) return PKA_ERR_ALIGN;
+  const int T = max_visible_blocks(max_seq_len, params->window, kv->block_size);
+  if (static_cast<int64_t>(num_splits) * split_blocks < T) return PKA_ERR_WORKSPACE;
+  if (B == 0) return PKA_OK;
+  pka::DecodeArgs a = decode_args(q, kv, block_tables, max_blocks, seq_lens, B, Hq, params);
+  a.partial_o = partial_o;
+  a.partial_lse = partial_lse;
+  a.num_splits = num_splits;
+  a.split_blocks = split_blocks;
+  const int64_t items = static_cast<int64_t>(B) * kv->num_kv_heads * num_splits;
+  if (items > 0x7fffffffLL) return PKA_ERR_SHAPE;
+  const int sms = pka::device_sm_count();
+  if (sms <= 0) return PKA_ERR_CUDA;
+  const int grid = items < sms ? static_cast<int>(items) : sms;
+  cudaError_t e = pka::launch_decode(a, kv->head_dim, Hq / kv->num_kv_heads, grid,
+                                     static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? PKA_OK : PKA_ERR_CUDA;
+}
+
+int paged_decode_splitk_combine(const float* partial_o, const float* partial_lse, int32_t B,
+                                int32_t Hq, int32_t D, int32_t num_splits, void* out,
+                                float* lse_out, void* stream) {
+  if (partial_o == nullptr || partial_lse == nullptr || out == nullptr) return PKA_ERR_NULL;
+  if (B < 0 || Hq <= 0 || num_splits <= 0) return PKA_ERR_SHAPE;
+  if (!supported_dim(D)) return PKA_ERR_UNSUPPORTED;
+  if (!aligned16(partial_o) || !aligned16(out)) return PKA_ERR_ALIGN;
+  if (B == 0) return PKA_OK;
+  pka::CombineArgs a{};
+  a.partial_o = partial_o;
+  a.partial_lse = partial_lse;
+  a.out = static_cast<uint16_t*>(out);
+  a.lse_out = lse_out;
+  a.rows = B * Hq;
+  a.num_splits = num_splits;
+  a.head_dim = D;
+  cudaError_t e = pka::launch_combine(a, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? PKA_OK : PKA_ERR_CUDA;
+}
+
+int paged_prefill_attn(const void* q, void* out, const pka_kv_pool* kv,
+                       const int32_t* block_tables, int32_t max_blocks,
+                       const int32_t* query_start_loc, const int32_t* seq_lens, int32_t B,
+                       int32_t Hq, int32_t total_q, int32_t max_query_len, int32_t max_seq_len,
+                       const pka_attn_params* params, void* stream) {
+  if (out == nullptr || query_start_loc == nullptr) return PKA_ERR_NULL;
+  int st = check_common(q, kv, block_tables, max_blocks, seq_lens, B, Hq, max_seq_len, params);
+  if (st != PKA_OK) return st;
+  if (total_q < 0 || max_query_len < 0 || max_query_len > max_seq_len) return PKA_ERR_SHAPE;
+  if (!aligned16(out)) return PKA_ERR_ALIGN;
+  if (B == 0 || total_q == 0) return PKA_OK;
+  pka::PrefillArgs a{};
+  a.q = static_cast<const uint16_t*>(q);
+  a.out = static_cast<uint16_t*>(out);
+  a.k = static_cast<const uint16_t*>(kv->k);
+  a.v = static_cast<const uint16_t*>(kv->v);
+  a.tables = block_tables;
+  a.seq_lens = seq_lens;
+  a.query_start_loc = query_start_loc;
+  a.err = params->err;
+  a.batch = B;
+  a.Hq = Hq;
+  a.Hkv = kv->num_kv_heads;
+  a.num_blocks = kv->num_blocks;
+  a.max_blocks = max_blocks;
+  a.total_q = total_q;
+  a.max_query_len = max_query_len;
+  a.scale = params->scale;
+  a.softcap = params->softcap;
+  a.window = params->window;
+  const int sms = pka::device_sm_count();
+  if (sms <= 0) return PKA_ERR_CUDA;
+  cudaError_t e = pka::launch_prefill(a, kv->head_dim, Hq / kv->num_kv_heads, sms,
+                                      static_cast<cudaStream_t>(stream));
+  if (e == cudaErrorNotSupported) return PKA_ERR_UNSUPPORTED;
+  return e == cudaSuccess ? PKA_OK : PKA_ERR_CUDA;
+}
+
+int paged_attn_check_tables(const int32_t* block_tables, int32_t max_blocks,
+                            const int32_t* seq_lens, int32_t B, int32_t num_blocks,
+                            int32_t block_size, int32_t* err, void* stream) {
+  if (block_tables == nullptr || seq_lens == nullptr || err == nullptr) return PKA_ERR_NULL;
+  if (B < 0 || max_blocks <= 0 || num_blocks <= 0 || block_size <= 0) return PKA_ERR_SHAPE;
+  if (B == 0) return PKA_OK;
+  pka::CheckArgs a{};
+  a.tables = block_tables;
+  a.seq_lens = seq_lens;
+  a.err = err;
+  a.batch = B;
+  a.max_blocks = max_blocks;
+  a.num_blocks = num_blocks;
+  a.block_size = block_size;
+  cudaError_t e = pka::launch_check_tables(a, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? PKA_OK : PKA_ERR_CUDA;
+}
+
+}  // extern "C"

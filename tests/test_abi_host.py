@@ -1,0 +1,122 @@
+"""Host-side checks of the C ABI that need no GPU.
+
+The library must load and export every function ``include/paged_attn.h``
+declares, and argument errors must be rejected on the host before any CUDA
+call (so these run on a machine without a GPU).
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+from paged_kv_attention_12_gb300 import _build, binding
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    _build.build()
+    return binding.lib()
+
+
+def declared_functions():
+    names = []
+    for f in os.listdir(os.path.join(ROOT, "include")):
+        if f.endswith(".h"):
+            text = open(os.path.join(ROOT, "include", f)).read()
+            text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+            names += re.findall(r"^\s*(?:const\s+)?[A-Za-z_][\w\s\*]*?\b([a-z_][a-z0-9_]*)\s*\(",
+                                text, flags=re.M)
+    return sorted(set(names))
+
+
+def test_library_exports_every_declared_function(L):
+    names = declared_functions()
+    assert "paged_decode_attn" in names and "paged_prefill_attn" in names
+    for n in names:
+        assert hasattr(L, n), f"{n} declared in include/ but not exported"
+    assert set(binding.EXPORTS) <= set(names)
+
+
+def test_version_and_status_strings(L):
+    assert L.pka_version() >= 100
+    for code in binding.STATUS:
+        assert L.pka_status_string(code)
+    assert L.pka_status_string(12345) == b"unknown status"
+
+
+def _pool(**kw):
+    d = dict(k=16, v=16, num_blocks=8, num_kv_heads=2, block_size=16, head_dim=128)
+    d.update(kw)
+    return binding.PkaKvPool(d["k"], d["v"], d["num_blocks"], d["num_kv_heads"],
+                             d["block_size"], d["head_dim"])
+
+
+def _decode(L, q=32, out=32, pool=None, tables=64, max_blocks=4, seq=64, B=2, Hq=8,
+            max_seq_len=64, params=True):
+    pool = pool or _pool()
+    par = binding.PkaAttnParams(0.1, 0.0, 0, None)
+    return L.paged_decode_attn(q, out, ctypes.byref(pool), tables, max_blocks, seq, B, Hq,
+                               max_seq_len, ctypes.byref(par) if params else None, None)
+
+
+def test_decode_argument_errors_are_host_side(L):
+    assert _decode(L, q=None) == -1
+    assert _decode(L, out=None) == -1
+    assert _decode(L, tables=None) == -1
+    assert _decode(L, params=False) == -1
+    assert _decode(L, pool=_pool(k=None)) == -1
+    assert _decode(L, Hq=7) == -2                       # Hq % Hkv
+    assert _decode(L, Hq=6) == -4                       # G = 3
+    assert _decode(L, pool=_pool(head_dim=96)) == -4
+    assert _decode(L, pool=_pool(block_size=32)) == -4
+    assert _decode(L, Hq=32) == -4                      # G = 16
+    assert _decode(L, q=40) == -3                       # misaligned q
+    assert _decode(L, pool=_pool(v=24)) == -3
+    assert _decode(L, max_seq_len=65) == -2             # beyond max_blocks * bs
+    assert _decode(L, B=-1) == -2
+
+
+def test_splitk_plan_and_workspace(L):
+    S, C = binding.paged_decode_splitk_plan(32, 2, 4096, 16, 0, sm_count=152)
+    assert S * C >= 256 and C >= 4
+    assert 32 * 2 * S >= 152
+    S, C = binding.paged_decode_splitk_plan(4, 4, 131072, 16, 0, sm_count=152)
+    assert S * C >= 8192 and 4 * 4 * S >= 148
+    # a window bounds the visible blocks: 512 keys span at most 33 blocks
+    S, C = binding.paged_decode_splitk_plan(32, 2, 4096, 16, 512, sm_count=152)
+    assert S * C >= 33 and S * C < 33 + C
+    assert binding.paged_decode_splitk_workspace_bytes(4, 16, 128, 10) == 4 * 16 * 10 * 129 * 4
+    assert binding.paged_decode_splitk_workspace_bytes(0, 16, 128, 10) == 0
+
+
+def test_splitk_rejects_uncovering_partition(L):
+    pool = _pool()
+    par = binding.PkaAttnParams(0.1, 0.0, 0, None)
+    # 64 tokens = 4 blocks; 1 split of 3 blocks does not cover them
+    st = L.paged_decode_splitk(32, 64, 96, ctypes.byref(pool), 64, 4, 64, 2, 8, 64, 1, 3,
+                               ctypes.byref(par), None)
+    assert st == -5
+    st = L.paged_decode_splitk(32, None, 96, ctypes.byref(pool), 64, 4, 64, 2, 8, 64, 1, 4,
+                               ctypes.byref(par), None)
+    assert st == -1
+
+
+def test_combine_and_prefill_and_check_argument_errors(L):
+    assert L.paged_decode_splitk_combine(None, 16, 1, 8, 128, 2, 32, None, None) == -1
+    assert L.paged_decode_splitk_combine(16, 16, 1, 8, 96, 2, 32, None, None) == -4
+    assert L.paged_decode_splitk_combine(16, 16, 1, 8, 128, 0, 32, None, None) == -2
+    pool = _pool()
+    par = binding.PkaAttnParams(0.1, 0.0, 0, None)
+    assert L.paged_prefill_attn(32, 32, ctypes.byref(pool), 64, 4, None, 64, 2, 8, 10, 5, 64,
+                                ctypes.byref(par), None) == -1
+    assert L.paged_prefill_attn(32, 32, ctypes.byref(pool), 64, 4, 80, 64, 2, 8, 10, 65, 64,
+                                ctypes.byref(par), None) == -2
+    assert L.paged_attn_check_tables(64, 4, 64, 2, 8, 16, None, None) == -1
+    assert L.paged_attn_check_tables(64, 0, 64, 2, 8, 16, 32, None) == -2
+
+
+def test_zero_batch_is_a_no_op(L):
+    assert _decode(L, B=0) == 0

@@ -1,0 +1,233 @@
+"""GPU parity of paged decode (direct and split-K + combine) against the oracle.
+
+Inputs come from the seeded workload generator; unreferenced blocks and tail
+slots are NaN-poisoned so that a stray read shows up as a non-finite output.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from paged_kv_attention_12_gb300 import _build, binding, workload
+from tests.parity import assert_close, to_f64
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda:0"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    _build.build()
+    binding.lib()
+
+
+def oracle_decode(batch, reqs=None):
+    arr = workload.to_numpy_f64(batch, reqs)
+    out, lse = oracle.run_batch(arr)
+    return out, lse, arr
+
+
+def run_direct(batch, err=None):
+    out = torch.full_like(batch.q, float("nan"))
+    binding.paged_decode_attn(batch.q, out, batch.k_pool, batch.v_pool, batch.block_tables,
+                              batch.seq_lens, batch.max_seq_len, scale=batch.scale,
+                              softcap=batch.softcap, window=batch.window, err=err)
+    return out
+
+
+def run_splitk(batch, err=None, lse=None):
+    runner = binding.DecodeSplitK(batch)
+    return runner.run(err=err, lse_out=lse), runner
+
+
+def new_err():
+    return torch.zeros(1, dtype=torch.int32, device=DEV)
+
+
+# ----------------------------------------------------------------- configs
+@pytest.mark.parametrize("seed", range(5))
+def test_decode_tiny_direct_and_splitk(seed):
+    batch = workload.decode_tiny(seed, DEV, poison=True)
+    ref, ref_lse, _ = oracle_decode(batch)
+    err = new_err()
+    assert_close(to_f64(run_direct(batch, err)), ref, f"direct seed {seed}")
+    lse = torch.empty(batch.q.shape[:2], dtype=torch.float32, device=DEV)
+    out, _ = run_splitk(batch, err, lse)
+    assert_close(to_f64(out), ref, f"splitk seed {seed}")
+    np.testing.assert_allclose(lse.cpu().numpy(), ref_lse, rtol=1e-4, atol=1e-4)
+    torch.cuda.synchronize()
+    assert err.item() == 0
+
+
+@pytest.mark.parametrize("seed", range(3))
+def test_decode_serving_small_both_layers(seed):
+    """Scaled-down serving workload: W=0 and a sliding layer, softcap 50,
+    with blocks wholly outside the window pointed at a NaN block."""
+    for batch in workload.decode_serving(seed, DEV, poison=True, scale_down=True,
+                                         drop_out_of_window=True):
+        ref, _, _ = oracle_decode(batch)
+        err = new_err()
+        assert_close(to_f64(run_direct(batch, err)), ref, f"{batch.name} direct")
+        out, _ = run_splitk(batch, err)
+        assert_close(to_f64(out), ref, f"{batch.name} splitk")
+        torch.cuda.synchronize()
+        assert err.item() == 0
+
+
+@pytest.mark.parametrize("seed", range(3))
+def test_decode_long_small(seed):
+    batch = workload.decode_long(seed, DEV, poison=True, scale_down=True)
+    ref, ref_lse, _ = oracle_decode(batch)
+    err = new_err()
+    assert_close(to_f64(run_direct(batch, err)), ref, "direct")
+    lse = torch.empty(batch.q.shape[:2], dtype=torch.float32, device=DEV)
+    out, _ = run_splitk(batch, err, lse)
+    assert_close(to_f64(out), ref, "splitk")
+    np.testing.assert_allclose(lse.cpu().numpy(), ref_lse, rtol=1e-4, atol=1e-4)
+    torch.cuda.synchronize()
+    assert err.item() == 0
+
+
+@pytest.mark.parametrize("D,G,Hkv", [(128, 1, 3), (128, 2, 2), (128, 8, 1), (256, 1, 2),
+                                     (256, 2, 1), (256, 8, 1)])
+def test_decode_head_shapes(D, G, Hkv):
+    g = torch.Generator().manual_seed(D * 10 + G)
+    L = torch.randint(1, 300, (5,), generator=g).tolist() + [16, 17, 1]
+    batch = workload.make_batch(seq_lens=L, q_lens=[1] * len(L), num_q_heads=G * Hkv,
+                                num_kv_heads=Hkv, head_dim=D, num_blocks=200, softcap=7.0,
+                                window=45, cfg_id=9, seed=D + G, device=DEV, poison=True)
+    ref, _, _ = oracle_decode(batch)
+    assert_close(to_f64(run_direct(batch)), ref, "direct")
+    out, _ = run_splitk(batch)
+    assert_close(to_f64(out), ref, "splitk")
+
+
+def test_splitk_partials_match_oracle_partials():
+    batch = workload.decode_long(1, DEV, poison=True, scale_down=True)
+    runner = binding.DecodeSplitK(batch)
+    runner.run()
+    arr = workload.to_numpy_f64(batch)
+    po, pl = oracle.splitk_partials(arr["q"], arr["k_pool"], arr["v_pool"], arr["block_tables"],
+                                    arr["seq_lens"], batch.scale, batch.softcap, batch.window,
+                                    runner.num_splits, runner.split_blocks)
+    got_lse = runner.partial_lse.cpu().numpy()
+    assert np.array_equal(np.isneginf(got_lse), np.isneginf(pl))
+    fin = np.isfinite(pl)
+    np.testing.assert_allclose(got_lse[fin], pl[fin], rtol=1e-4, atol=1e-4)
+    assert_close(runner.partial_o.cpu().numpy()[fin], po[fin], "partials")
+
+
+@pytest.mark.parametrize("S,C", [(1, 200), (3, 60), (200, 1)])
+def test_split_count_does_not_change_result(S, C):
+    batch = workload.decode_long(2, DEV, poison=True, scale_down=True)
+    ref, _, _ = oracle_decode(batch)
+    B, Hq, D = batch.q.shape
+    po = torch.empty((B, Hq, S, D), dtype=torch.float32, device=DEV)
+    pl = torch.empty((B, Hq, S), dtype=torch.float32, device=DEV)
+    out = torch.empty_like(batch.q)
+    binding.paged_decode_splitk(batch.q, po, pl, batch.k_pool, batch.v_pool, batch.block_tables,
+                                batch.seq_lens, batch.max_seq_len, S, C, scale=batch.scale)
+    binding.paged_decode_splitk_combine(po, pl, out)
+    assert_close(to_f64(out), ref, f"S={S} C={C}")
+
+
+# -------------------------------------------------------- full-size samples
+@pytest.mark.parametrize("cfg", [2, 3])
+def test_full_size_sampled_requests(cfg):
+    """Full-size workloads in the benchmark's launch configuration (split-K +
+    combine); the oracle checks a sample of requests one by one."""
+    calls = workload.workload(cfg, seed=0, device=DEV, poison=True)
+    for batch in calls:
+        out, _ = run_splitk(batch)
+        B = batch.num_requests
+        reqs = sorted({0, B - 1, B // 2, int(np.argmax(batch.seq_lens_host)),
+                       int(np.argmin(batch.seq_lens_host))})
+        if cfg == 3:  # 100k-token requests: check the shortest and the longest
+            reqs = sorted({int(np.argmax(batch.seq_lens_host)),
+                           int(np.argmin(batch.seq_lens_host))})
+        ref, _, _ = oracle_decode(batch, reqs)
+        assert_close(to_f64(out[reqs]), ref, f"cfg{cfg} {batch.name}")
+        del out
+    torch.cuda.empty_cache()
+
+
+# ------------------------------------------------------------ bit-exactness
+def test_one_hot_keys_return_exact_value_rows():
+    """A key equal to c*q (logit gap >= 200) takes all the weight: the output
+    is that key's V row exactly (every other weight underflows to 0)."""
+    B, Hkv, G, D = 3, 2, 4, 128
+    L = [37, 100, 16]
+    batch = workload.make_batch(seq_lens=L, q_lens=[1] * B, num_q_heads=Hkv * G,
+                                num_kv_heads=Hkv, head_dim=D, num_blocks=40, cfg_id=11,
+                                seed=0, device=DEV, poison=True)
+    # one query per group: every head of a group shares q, so one key wins for all
+    q = batch.q.view(B, Hkv, G, D)
+    q[:] = q[:, :, :1, :]
+    rng = np.random.default_rng(0)
+    for trial in range(4):
+        tstar = [int(rng.integers(0, l)) for l in L]
+        k = batch.k_pool.clone()
+        k.mul_(0.01)
+        for b in range(B):
+            blk = batch.tables_host[b][tstar[b] // 16]
+            for h in range(Hkv):
+                qv = q[b, h, 0].float()
+                k[blk, h, tstar[b] % 16] = (qv * (300.0 / qv.pow(2).sum())).to(torch.bfloat16) * 16.0
+        out = torch.empty_like(batch.q)
+        binding.paged_decode_attn(batch.q, out, k, batch.v_pool, batch.block_tables,
+                                  batch.seq_lens, batch.max_seq_len, scale=1.0 / 16.0)
+        outs, _ = run_splitk(workload.PagedBatch(**{**batch.__dict__, "k_pool": k}))
+        for b in range(B):
+            blk = batch.tables_host[b][tstar[b] // 16]
+            for h in range(Hkv):
+                want = batch.v_pool[blk, h, tstar[b] % 16]
+                for gi in range(G):
+                    assert torch.equal(out[b, h * G + gi], want), (trial, b, h)
+                    assert torch.equal(outs[b, h * G + gi], want), (trial, b, h)
+
+
+# ---------------------------------------------------------- error reporting
+def test_bad_table_id_is_reported_not_faulted():
+    batch = workload.decode_tiny(0, DEV, poison=False)
+    bt = batch.block_tables.clone()
+    bt[1, 0] = batch.num_blocks + 5  # out of range id
+    bt[2, 0] = -7
+    err = new_err()
+    out = torch.empty_like(batch.q)
+    binding.paged_decode_attn(batch.q, out, batch.k_pool, batch.v_pool, bt, batch.seq_lens,
+                              batch.max_seq_len, scale=batch.scale, err=err)
+    torch.cuda.synchronize()
+    assert err.item() & binding.DEVERR_BAD_TABLE
+    err2 = new_err()
+    binding.paged_attn_check_tables(bt, batch.seq_lens, batch.num_blocks, err2)
+    torch.cuda.synchronize()
+    assert err2.item() & binding.DEVERR_BAD_TABLE
+    err3 = new_err()
+    binding.paged_attn_check_tables(batch.block_tables, batch.seq_lens, batch.num_blocks, err3)
+    torch.cuda.synchronize()
+    assert err3.item() == 0
+
+
+def test_seq_len_beyond_table_is_reported():
+    batch = workload.decode_tiny(1, DEV)
+    sl = batch.seq_lens.clone()
+    sl[0] = batch.max_blocks * 16 + 40
+    err = new_err()
+    out = torch.empty_like(batch.q)
+    binding.paged_decode_attn(batch.q, out, batch.k_pool, batch.v_pool, batch.block_tables, sl,
+                              batch.max_seq_len, scale=batch.scale, err=err)
+    torch.cuda.synchronize()
+    assert err.item() & binding.DEVERR_SEQ_LEN
+
+
+def test_empty_sequences_give_zero_output():
+    batch = workload.make_batch(seq_lens=[0, 20, 0], q_lens=[0, 1, 0], num_q_heads=8,
+                                num_kv_heads=2, head_dim=128, num_blocks=8, cfg_id=12,
+                                device=DEV)
+    # decode expects one query row per request: give the empty ones a row too
+    q = torch.randn((3, 8, 128), device=DEV).to(torch.bfloat16)
+    out = torch.full_like(q, float("nan"))
+    binding.paged_decode_attn(q, out, batch.k_pool, batch.v_pool, batch.block_tables,
+                              batch.seq_lens, batch.max_seq_len, scale=0.1)
+    assert torch.all(out[0] == 0) and torch.all(out[2] == 0)
+    assert torch.all(torch.isfinite(out[1].float()))
