@@ -3,8 +3,7 @@
 // The combine is the log-sum-exp merge a split-K softmax needs ("split-K
 // decode variant", inference-server README, engine feature list): with
 // M = max_s LSE_s and w_s = exp(LSE_s - M), out = sum_s w_s O_s / sum_s w_s
-// and LSE = M + ln sum_s w_s.  One warp per (request, query head); lanes
-// split the head dimension, so every partial row is read with coalesced
+// and LSE = M + ln sum_s w_s.  Every partial row is read with coalesced
 // 16-byte loads.
 #include "common.cuh"
 #include "kernels.h"
@@ -13,15 +12,22 @@ namespace pka {
 
 namespace {
 
+// One warp per (row, 128-column segment): each lane owns one float4 of the
+// output.  Split weights are computed 32 at a time (one split per lane) and
+// broadcast with shuffles; the partial loads of eight splits are issued
+// before any of them is used, so the loop is bound by bandwidth, not by the
+// latency of one load after another.
 template <int D>
 __global__ void __launch_bounds__(128) combine_kernel(const CombineArgs a) {
-  constexpr int EPL = D / 32;  // fp32 columns per lane (4 or 8)
-  const int row = blockIdx.x * 4 + threadIdx.x / 32;
+  constexpr int SEGS = D / 128;
+  const int wid = blockIdx.x * 4 + threadIdx.x / 32;
+  const int row = wid / SEGS;
+  const int seg = wid % SEGS;
   const int lane = threadIdx.x % 32;
   if (row >= a.rows) return;
   const int S = a.num_splits;
   const float* lse = a.partial_lse + static_cast<size_t>(row) * S;
-  const float* po = a.partial_o + static_cast<size_t>(row) * S * D;
+  const float* po = a.partial_o + static_cast<size_t>(row) * S * D + seg * 128 + lane * 4;
 
   float M = -INFINITY;
   for (int s = lane; s < S; s += 32) M = fmaxf(M, lse[s]);
@@ -29,35 +35,48 @@ __global__ void __launch_bounds__(128) combine_kernel(const CombineArgs a) {
   for (int o = 16; o >= 1; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
   const float Ms = (M == -INFINITY) ? 0.f : M;
 
-  float acc[EPL];
-#pragma unroll
-  for (int e = 0; e < EPL; ++e) acc[e] = 0.f;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
   float den = 0.f;
-  for (int s = 0; s < S; ++s) {
-    const float w = fast_exp2((lse[s] - Ms) * kLog2e);  // exp(-inf) = 0 for empty splits
-    if (w == 0.f) continue;                             // uniform across the warp
-    den += w;
-    const float4* src = reinterpret_cast<const float4*>(po + static_cast<size_t>(s) * D + lane * EPL);
+  for (int base = 0; base < S; base += 32) {
+    const int n = min(32, S - base);
+    // exp(-inf) = 0 for empty splits
+    const float wl = (lane < n) ? fast_exp2((lse[base + lane] - Ms) * kLog2e) : 0.f;
+    den += wl;
+    int s = 0;
+    for (; s + 8 <= n; s += 8) {
+      float4 x[8];
 #pragma unroll
-    for (int e = 0; e < EPL / 4; ++e) {
-      const float4 x = src[e];
-      acc[4 * e + 0] = fmaf(w, x.x, acc[4 * e + 0]);
-      acc[4 * e + 1] = fmaf(w, x.y, acc[4 * e + 1]);
-      acc[4 * e + 2] = fmaf(w, x.z, acc[4 * e + 2]);
-      acc[4 * e + 3] = fmaf(w, x.w, acc[4 * e + 3]);
+      for (int u = 0; u < 8; ++u)
+        x[u] = *reinterpret_cast<const float4*>(po + static_cast<size_t>(base + s + u) * D);
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const float w = __shfl_sync(0xffffffffu, wl, s + u);
+        if (w != 0.f) {  // an empty split's partial is 0 but never trusted
+          acc.x = fmaf(w, x[u].x, acc.x);
+          acc.y = fmaf(w, x[u].y, acc.y);
+          acc.z = fmaf(w, x[u].z, acc.z);
+          acc.w = fmaf(w, x[u].w, acc.w);
+        }
+      }
+    }
+    for (; s < n; ++s) {
+      const float w = __shfl_sync(0xffffffffu, wl, s);
+      if (w != 0.f) {
+        const float4 x = *reinterpret_cast<const float4*>(po + static_cast<size_t>(base + s) * D);
+        acc.x = fmaf(w, x.x, acc.x);
+        acc.y = fmaf(w, x.y, acc.y);
+        acc.z = fmaf(w, x.z, acc.z);
+        acc.w = fmaf(w, x.w, acc.w);
+      }
     }
   }
-  const float inv = den > 0.f ? 1.f / den : 0.f;
-  uint16_t* dst = a.out + static_cast<size_t>(row) * D + lane * EPL;
-  uint32_t packed[EPL / 2];
 #pragma unroll
-  for (int e = 0; e < EPL / 2; ++e) packed[e] = pack_bf16x2(acc[2 * e] * inv, acc[2 * e + 1] * inv);
-  if constexpr (EPL == 8) {
-    *reinterpret_cast<uint4*>(dst) = make_uint4(packed[0], packed[1], packed[2], packed[3]);
-  } else {
-    *reinterpret_cast<uint2*>(dst) = make_uint2(packed[0], packed[1]);
-  }
-  if (a.lse_out != nullptr && lane == 0)
+  for (int o = 16; o >= 1; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
+  const float inv = den > 0.f ? 1.f / den : 0.f;
+  uint16_t* dst = a.out + static_cast<size_t>(row) * D + seg * 128 + lane * 4;
+  *reinterpret_cast<uint2*>(dst) =
+      make_uint2(pack_bf16x2(acc.x * inv, acc.y * inv), pack_bf16x2(acc.z * inv, acc.w * inv));
+  if (a.lse_out != nullptr && lane == 0 && seg == 0)
     a.lse_out[row] = den > 0.f ? M + logf(den) : -INFINITY;
 }
 
@@ -78,7 +97,8 @@ __global__ void check_tables_kernel(const CheckArgs a) {
 }  // namespace
 
 cudaError_t launch_combine(const CombineArgs& a, cudaStream_t stream) {
-  const int grid = (a.rows + 3) / 4;
+  const int warps = a.rows * (a.head_dim / 128);
+  const int grid = (warps + 3) / 4;
   if (a.head_dim == 128)
     combine_kernel<128><<<grid, 128, 0, stream>>>(a);
   else if (a.head_dim == 256)

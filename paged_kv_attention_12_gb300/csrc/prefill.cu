@@ -1,12 +1,506 @@
-// Paged prefill / mixed-batch attention (sm_103a).  Placeholder until the
-// tcgen05 kernel lands: reports "not supported".
+// Paged prefill and mixed-batch attention on the 5th-generation tensor cores
+// (tcgen05 + TMEM + TMA), sm_103a.
+//
+// The chunked-prefill contractions are dense: a chunk of new tokens attends,
+// causally, over its request's cached prefix and the chunk itself, K/V read
+// through the block table ("Triton paged decode and prefill kernels reading
+// K/V through block tables", inference-server README, engine feature list;
+// mixed-batch chunked prefill, architecture page, "Phase status").  Decode
+// rows (one token) may sit in the same varlen launch.
+//
+// Work item = (request, KV head, query tile).  A query tile packs TQ = 128/G
+// tokens x the G query heads of one KV group into the 128 rows of the MMA
+// (row = token * G + g), so all G heads share every K/V tile.  Per item:
+//
+//  * warp 4 (TMA): the Q tile (one 3-D box per 64-column chunk) and, per key
+//    tile, one 2-D box per (pool block, 64-column chunk) of K into a 2-stage
+//    ring; blocks past the request's last block get an out-of-range row
+//    coordinate so TMA fills zeros; a stage is refilled once S = Q K^T of
+//    the tile it held has completed;
+//  * warp 5 (TMA): the same for V, refilled once P V of its tile completed;
+//  * warp 6 (MMA): allocates TMEM (2 S buffers + the O accumulator), issues
+//    S_j = Q K_j^T (K-major A and B, 128B-swizzled) two tiles ahead, then
+//    O += P_j V_j (V as an MN-major operand), committing each to mbarriers;
+//    it also zeroes V rows past seq_len (stale slots of the last block, which
+//    may hold NaN) before they reach P V;
+//  * warps 0-3 (softmax): thread r owns row r.  It reads its S row from
+//    TMEM, applies scale, softcap and the causal / window mask, keeps a
+//    running max and sum in the exp2 domain, writes P (bf16, swizzled) to
+//    shared memory and signals the MMA warp.  O is rescaled in TMEM only
+//    when the row max grows by more than 2^8 (the stale reference max keeps
+//    every P <= 256, and O and the sum share it, so the result is exact);
+//  * epilogue: O / sum from TMEM to bf16 rows of the output.
+//
+// All waits are bounded; a timeout sets PKA_DEVERR_TIMEOUT, the roles stop,
+// the CTA still frees its TMEM.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
 #include "common.cuh"
 #include "kernels.h"
+#include "tcgen05.cuh"
 
 namespace pka {
 
-cudaError_t launch_prefill(const PrefillArgs&, int, int, int, cudaStream_t) {
-  return cudaErrorNotSupported;
+template <int D, int G>
+struct PrefillShape {
+  static constexpr int BM = 128;                    // MMA rows: tokens x heads
+  static constexpr int TQ = BM / G;                 // tokens per query tile
+  static constexpr int BN = (D == 256) ? 64 : 128;  // keys per key tile
+  static constexpr int DC = D / 64;                 // 128-byte chunks of a K/V/Q row
+  static constexpr int NC = BN / 64;                // 128-byte chunks of a P row
+  static constexpr int kBlocksPerTile = BN / kBlockSize;
+  static constexpr int kQChunk = BM * 128;
+  static constexpr int kKVChunk = BN * 128;
+  static constexpr int kPChunk = BM * 128;
+  static constexpr int kQBytes = BM * D * 2;
+  static constexpr int kKVBytes = BN * D * 2;
+  static constexpr int kPBytes = BM * BN * 2;
+  static constexpr int oQ = 0;
+  static constexpr int oK = oQ + kQBytes;
+  static constexpr int oV = oK + 2 * kKVBytes;
+  static constexpr int oP = oV + 2 * kKVBytes;
+  static constexpr int oBar = oP + 2 * kPBytes;
+  static constexpr int kNumBars = 11;
+  static constexpr int oMisc = oBar + kNumBars * 8;
+  static constexpr int kSmemBytes = oMisc + 16 + 1024;  // + slack to align the base to 1 KiB
+  static constexpr uint32_t kTmemO = 256;               // O columns [256, 256 + D)
+  static constexpr uint32_t kTmemCols = 512;
+  static constexpr int kThreads = 7 * 32;
+  static_assert(kSmemBytes <= 232448, "shared memory");
+  static_assert(2 * BN <= 256 && D <= 256, "TMEM columns");
+};
+
+namespace {
+
+constexpr int kWarpTmaK = 4;
+constexpr int kWarpTmaV = 5;
+constexpr int kWarpMma = 6;
+
+struct Item {
+  int b, kvh, q0, n, L, it0, it1, kbase, ntiles, nblk;
+};
+
+// bar indices
+enum { B_Q = 0, B_KFULL = 1, B_VFULL = 3, B_QK = 5, B_PV = 7, B_PRDY = 9 };
+
+__device__ __forceinline__ bool stop_requested(const volatile int* flag) { return *flag != 0; }
+
+__device__ __forceinline__ bool cta_wait(uint64_t* bar, uint32_t parity, int32_t* err,
+                                         volatile int* failed) {
+  if (mbar_wait(bar, parity, err)) return true;
+  *failed = 1;
+  return false;
+}
+
+// Every lane waits; the warp agrees on one outcome so that it never diverges.
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, int32_t* err,
+                                          volatile int* failed) {
+  const bool ok = __all_sync(0xffffffffu, mbar_wait(bar, parity, err));
+  if (!ok) *failed = 1;
+  return ok;
+}
+
+// exp2-based tanh: tanh(y) = 1 - 2 / (exp(2y) + 1); absolute error ~1e-7.
+__device__ __forceinline__ float tanh_via_exp2(float y) {
+  const float e = fast_exp2(fminf(2.f * kLog2e * y, 126.f));
+  return 1.f - __fdividef(2.f, e + 1.f);
+}
+
+}  // namespace
+
+template <int D, int G>
+__global__ void __launch_bounds__(PrefillShape<D, G>::kThreads, 1)
+    paged_prefill_kernel(const PrefillArgs a, const __grid_constant__ CUtensorMap tm_q,
+                         const __grid_constant__ CUtensorMap tm_k,
+                         const __grid_constant__ CUtensorMap tm_v) {
+  using S = PrefillShape<D, G>;
+  constexpr int BN = S::BN, TQ = S::TQ, DC = S::DC;
+
+  // ---------------------------------------------------------- work item
+  Item it;
+  it.b = blockIdx.z;
+  it.kvh = blockIdx.y;
+  const int qt = gridDim.x - 1 - blockIdx.x;  // heaviest (latest) query tiles first
+  it.q0 = a.query_start_loc[it.b];
+  it.n = a.query_start_loc[it.b + 1] - it.q0;
+  it.L = a.seq_lens[it.b];
+  if (it.L > a.max_blocks * kBlockSize) {
+    if (threadIdx.x == 0 && qt == 0 && it.kvh == 0) report(a.err, PKA_DEVERR_SEQ_LEN);
+    it.L = a.max_blocks * kBlockSize;
+  }
+  if (it.n > it.L) {
+    if (threadIdx.x == 0 && qt == 0 && it.kvh == 0) report(a.err, PKA_DEVERR_SEQ_LEN);
+    return;
+  }
+  it.it0 = qt * TQ;
+  if (it.n <= 0 || it.it0 >= it.n) return;  // uniform: nothing to do for this tile
+  it.it1 = min(it.n, it.it0 + TQ) - 1;
+  const int p_first = it.L - it.n + it.it0;
+  const int p_last = it.L - it.n + it.it1;
+  const int t_lo = (a.window > 0) ? max(0, p_first - a.window + 1) : 0;
+  it.kbase = t_lo & ~(kBlockSize - 1);
+  it.ntiles = (p_last + 1 - it.kbase + BN - 1) / BN;
+  it.nblk = (it.L + kBlockSize - 1) / kBlockSize;
+
+  // ------------------------------------------------------- shared memory
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  uint8_t* sQ = smem + S::oQ;
+  uint8_t* sK = smem + S::oK;
+  uint8_t* sV = smem + S::oV;
+  uint8_t* sP = smem + S::oP;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S::oBar);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + S::oMisc);
+  volatile int* failed = reinterpret_cast<volatile int*>(smem + S::oMisc + 4);
+
+  const int warp = threadIdx.x / 32;
+  const int lane = threadIdx.x % 32;
+
+  if (threadIdx.x == 0) {
+    mbar_init(&bars[B_Q], 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&bars[B_KFULL + i], 1);
+      mbar_init(&bars[B_VFULL + i], 1);
+      mbar_init(&bars[B_QK + i], 1);
+      mbar_init(&bars[B_PV + i], 1);
+      mbar_init(&bars[B_PRDY + i], 128);
+    }
+    *failed = 0;
+    mbar_fence_init();
+  }
+  if (warp == kWarpMma) tmem_alloc(tmem_slot, S::kTmemCols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  const uint32_t oob_row = static_cast<uint32_t>(a.num_blocks) * a.Hkv * kBlockSize;
+  const int32_t* trow = a.tables + static_cast<size_t>(it.b) * a.max_blocks;
+
+  if (warp == kWarpTmaK || warp == kWarpTmaV) {
+    // ============================ TMA producers ============================
+    const bool is_k = (warp == kWarpTmaK);
+    const CUtensorMap* tm = is_k ? &tm_k : &tm_v;
+    uint8_t* ring = is_k ? sK : sV;
+    uint64_t* full = &bars[is_k ? B_KFULL : B_VFULL];
+    uint64_t* freed = &bars[is_k ? B_QK : B_PV];
+    int issued = 0;
+    if (lane == 0) {
+      prefetch_tensormap(tm);
+      if (is_k) {
+        prefetch_tensormap(&tm_q);
+        mbar_arrive_expect_tx(&bars[B_Q], S::kQBytes);
+#pragma unroll
+        for (int c = 0; c < DC; ++c)
+          tma_load_3d(sQ + c * S::kQChunk, &tm_q, c * 64, it.kvh * G, it.q0 + it.it0, &bars[B_Q]);
+      }
+      for (int j = 0; j < it.ntiles; ++j) {
+        if (stop_requested(failed)) break;
+        const int st = j & 1;
+        if (j >= 2 && !cta_wait(&freed[st], ((j - 2) >> 1) & 1, a.err, failed)) break;
+        mbar_arrive_expect_tx(&full[st], S::kKVBytes);
+        uint8_t* dst = ring + st * S::kKVBytes;
+#pragma unroll
+        for (int kb = 0; kb < S::kBlocksPerTile; ++kb) {
+          const int jb = it.kbase / kBlockSize + j * S::kBlocksPerTile + kb;
+          uint32_t row = oob_row;  // past the request's last block: TMA fills zeros
+          if (jb < it.nblk) {
+            const int id = trow[jb];
+            if (static_cast<unsigned>(id) < static_cast<unsigned>(a.num_blocks))
+              row = (static_cast<uint32_t>(id) * a.Hkv + it.kvh) * kBlockSize;
+            else
+              report(a.err, PKA_DEVERR_BAD_TABLE);
+          }
+#pragma unroll
+          for (int c = 0; c < DC; ++c)
+            tma_load_2d(dst + c * S::kKVChunk + kb * kBlockSize * 128, tm, c * 64,
+                        static_cast<int>(row), &full[st]);
+        }
+        issued = j + 1;
+      }
+      // every issued copy must land before the CTA may finish
+      for (int j = issued - 2 < 0 ? 0 : issued - 2; j < issued; ++j)
+        mbar_wait(&full[j & 1], (j >> 1) & 1, a.err);
+      if (is_k && stop_requested(failed)) mbar_wait(&bars[B_Q], 0, a.err);
+    }
+    __syncwarp();
+  } else if (warp == kWarpMma) {
+    // ================================ MMA ================================
+    constexpr uint32_t idesc_qk = idesc_bf16_f32(128, BN, 0, 0);
+    constexpr uint32_t idesc_pv = idesc_bf16_f32(128, D, 0, 1);
+    const uint32_t aQ = smem_u32(sQ), aK = smem_u32(sK), aV = smem_u32(sV), aP = smem_u32(sP);
+    int committed_pv = 0;  // number of P V tiles issued
+    bool ok = warp_wait(&bars[B_Q], 0, a.err, failed);
+    auto issue_qk = [&](int j) -> bool {
+      const int st = j & 1;
+      if (!warp_wait(&bars[B_KFULL + st], (j >> 1) & 1, a.err, failed)) return false;
+      tc_fence_after();
+      if (lane == 0) {
+        const uint32_t kst = aK + st * S::kKVBytes;
+#pragma unroll
+        for (int c = 0; c < DC; ++c)
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+            const uint64_t da = smem_desc_sw128(aQ + c * S::kQChunk + kk * 32, 16, 1024);
+            const uint64_t db = smem_desc_sw128(kst + c * S::kKVChunk + kk * 32, 16, 1024);
+            umma_bf16(tmem + st * BN, da, db, idesc_qk, (c | kk) != 0);
+          }
+        umma_commit(&bars[B_QK + st]);
+      }
+      __syncwarp();
+      return true;
+    };
+    if (ok) ok = issue_qk(0);
+    if (ok && it.ntiles > 1) ok = issue_qk(1);
+    for (int j = 0; ok && j < it.ntiles; ++j) {
+      if (__any_sync(0xffffffffu, stop_requested(failed))) break;
+      const int st = j & 1;
+      const uint32_t ph = (j >> 1) & 1;
+      if (!warp_wait(&bars[B_VFULL + st], ph, a.err, failed)) break;
+      // V rows at positions >= seq_len (stale slots of the last block) -> 0
+      const int t0 = it.kbase + j * BN;
+      const int z0 = it.L - t0;
+      const int z1 = min(BN, it.nblk * kBlockSize - t0);
+      if (z0 > 0 && z0 < z1) {
+        uint8_t* vst = sV + st * S::kKVBytes;
+        const int nrows = z1 - z0;
+        for (int idx = lane; idx < nrows * DC * 8; idx += 32) {
+          const int r = z0 + idx / (DC * 8);
+          const int c = (idx / 8) % DC;
+          const int q = idx % 8;
+          *reinterpret_cast<uint4*>(vst + c * S::kKVChunk + r * 128 + q * 16) =
+              make_uint4(0u, 0u, 0u, 0u);
+        }
+        fence_proxy_async_smem();
+      }
+      __syncwarp();
+      if (!warp_wait(&bars[B_PRDY + st], ph, a.err, failed)) break;
+      tc_fence_after();
+      if (lane == 0) {
+        const uint32_t pst = aP + st * S::kPBytes;
+        const uint32_t vst = aV + st * S::kKVBytes;
+#pragma unroll
+        for (int k = 0; k < BN / 16; ++k) {
+          const uint64_t da = smem_desc_sw128(pst + (k / 4) * S::kPChunk + (k % 4) * 32, 16, 1024);
+          const uint64_t db = smem_desc_sw128(vst + k * 16 * 128, S::kKVChunk, 1024);
+          umma_bf16(tmem + S::kTmemO, da, db, idesc_pv, (j > 0 || k > 0) ? 1u : 0u);
+        }
+        umma_commit(&bars[B_PV + st]);
+      }
+      __syncwarp();
+      committed_pv = j + 1;
+      if (j + 2 < it.ntiles) ok = issue_qk(j + 2);
+    }
+    // the last P V must finish before TMEM is freed
+    if (committed_pv > 0)
+      mbar_wait(&bars[B_PV + ((committed_pv - 1) & 1)], ((committed_pv - 1) >> 1) & 1, a.err);
+  } else {
+    // ============================== softmax ==============================
+    const int r = threadIdx.x;  // row of the tile, TMEM lane
+    const int tok = r / G;
+    const int g = r % G;
+    const int qi = it.it0 + tok;
+    const bool row_valid = qi <= it.it1;
+    const int p = it.L - it.n + qi;
+    const int kmin = (a.window > 0) ? p - a.window + 1 : -0x40000000;
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+    const bool capped = a.softcap > 0.f;
+    const float sl2 = a.scale * kLog2e;
+    const float cap_in = capped ? a.scale / a.softcap : 0.f;
+    const float cap_out = a.softcap * kLog2e;
+    float m_ref = -INFINITY;
+    float l = 0.f;
+    bool ok = true;
+    for (int j = 0; j < it.ntiles; ++j) {
+      if (__any_sync(0xffffffffu, stop_requested(failed))) {
+        ok = false;
+        break;
+      }
+      const int st = j & 1;
+      const uint32_t ph = (j >> 1) & 1;
+      if (!warp_wait(&bars[B_QK + st], ph, a.err, failed)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      float s[BN];
+#pragma unroll
+      for (int c = 0; c < BN / 32; ++c) {
+        float t[32];
+        tmem_ld32(lane_base + st * BN + c * 32, t);
+#pragma unroll
+        for (int e = 0; e < 32; ++e) s[c * 32 + e] = t[e];
+      }
+      const int t0 = it.kbase + j * BN;
+      const int c_hi = row_valid ? min(BN - 1, p - t0) : -1;
+      const int c_lo = max(0, kmin - t0);
+      float mx = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < BN; ++c) {
+        float x = capped ? cap_out * tanh_via_exp2(s[c] * cap_in) : s[c] * sl2;
+        x = (c >= c_lo && c <= c_hi) ? x : -INFINITY;
+        s[c] = x;
+        mx = fmaxf(mx, x);
+      }
+      const float m_new = fmaxf(m_ref, mx);
+      const bool resc = (j > 0) && (m_new > m_ref + 8.f);
+      if (__any_sync(0xffffffffu, resc)) {
+        // O must hold P_{j-1} V_{j-1} before it is rescaled
+        if (!warp_wait(&bars[B_PV + ((j - 1) & 1)], ((j - 1) >> 1) & 1, a.err, failed)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const float f = resc ? fast_exp2(m_ref - m_new) : 1.f;
+#pragma unroll 1
+        for (int c = 0; c < D / 32; ++c) {
+          float o[32];
+          tmem_ld32(lane_base + S::kTmemO + c * 32, o);
+#pragma unroll
+          for (int e = 0; e < 32; ++e) o[e] *= f;
+          tmem_st32(lane_base + S::kTmemO + c * 32, o);
+        }
+      }
+      if (resc) l *= fast_exp2(m_ref - m_new);
+      if (j == 0 || resc) m_ref = m_new;
+      const float ms = (m_ref == -INFINITY) ? 0.f : m_ref;
+      // P buffer st was last read by P_{j-2} V_{j-2}
+      if (j >= 2 && !warp_wait(&bars[B_PV + st], ((j - 2) >> 1) & 1, a.err, failed)) {
+        ok = false;
+        break;
+      }
+      uint8_t* prow = sP + st * S::kPBytes + r * 128;
+      float lsum = 0.f;
+#pragma unroll
+      for (int q = 0; q < BN / 8; ++q) {
+        float pv8[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          pv8[e] = fast_exp2(s[q * 8 + e] - ms);
+          lsum += pv8[e];
+        }
+        const uint4 w = make_uint4(pack_bf16x2(pv8[0], pv8[1]), pack_bf16x2(pv8[2], pv8[3]),
+                                   pack_bf16x2(pv8[4], pv8[5]), pack_bf16x2(pv8[6], pv8[7]));
+        const int region = q / 8;
+        const int chunk = (q % 8) ^ (r & 7);
+        *reinterpret_cast<uint4*>(prow + region * S::kPChunk + chunk * 16) = w;
+      }
+      l += lsum;
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(&bars[B_PRDY + st]);
+    }
+    // ------------------------------------------------------------ epilogue
+    if (ok) {
+      const int jl = it.ntiles - 1;
+      ok = warp_wait(&bars[B_PV + (jl & 1)], (jl >> 1) & 1, a.err, failed);
+    }
+    if (ok) {
+      tc_fence_after();
+      const float inv = (l > 0.f) ? 1.f / l : 0.f;
+      uint16_t* orow = a.out + (static_cast<size_t>(it.q0 + qi) * a.Hq + it.kvh * G + g) * D;
+#pragma unroll 1
+      for (int c = 0; c < D / 32; ++c) {
+        float o[32];
+        tmem_ld32(lane_base + S::kTmemO + c * 32, o);
+        if (row_valid) {
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const uint4 w = make_uint4(pack_bf16x2(o[q * 8 + 0] * inv, o[q * 8 + 1] * inv),
+                                       pack_bf16x2(o[q * 8 + 2] * inv, o[q * 8 + 3] * inv),
+                                       pack_bf16x2(o[q * 8 + 4] * inv, o[q * 8 + 5] * inv),
+                                       pack_bf16x2(o[q * 8 + 6] * inv, o[q * 8 + 7] * inv));
+            *reinterpret_cast<uint4*>(orow + c * 32 + q * 8) = w;
+          }
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == kWarpMma) tmem_dealloc(tmem, S::kTmemCols);
+}
+
+// ------------------------------------------------------------- launchers
+namespace {
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (fn == nullptr) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return nullptr;
+    fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  return fn;
+}
+
+bool make_map(CUtensorMap* m, const void* base, int rank, const cuuint64_t* dims,
+              const cuuint64_t* strides_bytes, const cuuint32_t* box) {
+  auto fn = encode_fn();
+  if (fn == nullptr) return false;
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(base), dims,
+                  strides_bytes, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+template <int D, int G>
+cudaError_t launch_prefill_t(const PrefillArgs& a, cudaStream_t stream) {
+  using S = PrefillShape<D, G>;
+  CUtensorMap tq, tk, tv;
+  {
+    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(a.Hq),
+                                static_cast<cuuint64_t>(a.total_q)};
+    const cuuint64_t str[2] = {static_cast<cuuint64_t>(D) * 2,
+                               static_cast<cuuint64_t>(a.Hq) * D * 2};
+    const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(G), static_cast<cuuint32_t>(S::TQ)};
+    if (!make_map(&tq, a.q, 3, dims, str, box)) return cudaErrorInvalidValue;
+  }
+  {
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(D),
+                                static_cast<cuuint64_t>(a.num_blocks) * a.Hkv * kBlockSize};
+    const cuuint64_t str[1] = {static_cast<cuuint64_t>(D) * 2};
+    const cuuint32_t box[2] = {64, static_cast<cuuint32_t>(kBlockSize)};
+    if (!make_map(&tk, a.k, 2, dims, str, box)) return cudaErrorInvalidValue;
+    if (!make_map(&tv, a.v, 2, dims, str, box)) return cudaErrorInvalidValue;
+  }
+  auto kern = paged_prefill_kernel<D, G>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       S::kSmemBytes);
+  if (e != cudaSuccess) return e;
+  const int qtiles = (a.max_query_len + S::TQ - 1) / S::TQ;
+  dim3 grid(qtiles, a.Hkv, a.batch);
+  kern<<<grid, S::kThreads, S::kSmemBytes, stream>>>(a, tq, tk, tv);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_prefill(const PrefillArgs& a, int head_dim, int group, int /*sm_count*/,
+                           cudaStream_t stream) {
+  if (a.batch > 65535) return cudaErrorInvalidValue;
+#define PKA_PRE(D_, G_) \
+  if (head_dim == D_ && group == G_) return launch_prefill_t<D_, G_>(a, stream);
+  PKA_PRE(128, 1)
+  PKA_PRE(128, 2)
+  PKA_PRE(128, 4)
+  PKA_PRE(128, 8)
+  PKA_PRE(256, 1)
+  PKA_PRE(256, 2)
+  PKA_PRE(256, 4)
+  PKA_PRE(256, 8)
+#undef PKA_PRE
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace pka

@@ -1,0 +1,133 @@
+"""GPU parity of the tcgen05 prefill / mixed-batch kernel against the oracle.
+
+Ordered from the smallest case up, so that a layout or descriptor slip shows
+on a one-tile problem first.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from paged_kv_attention_12_gb300 import _build, binding, workload
+from tests.parity import assert_close, to_f64
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda:0"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    _build.build()
+    binding.lib()
+
+
+def run(batch, err=None):
+    out = torch.full_like(batch.q, float("nan"))
+    binding.run_batch(batch, out, err)
+    return out
+
+
+def check(batch, what, reqs=None):
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    out = run(batch, err)
+    arr = workload.to_numpy_f64(batch, reqs)
+    ref, _ = oracle.run_batch(arr)
+    got = out[arr["q_rows"]] if reqs is not None else out
+    ma, rl = assert_close(to_f64(got), ref, what)
+    torch.cuda.synchronize()
+    assert err.item() == 0, f"{what}: device error word {err.item()}"
+    return ma, rl
+
+
+def small(seq_lens, q_lens, D=128, G=4, Hkv=1, **kw):
+    return workload.make_batch(seq_lens=seq_lens, q_lens=q_lens, num_q_heads=G * Hkv,
+                               num_kv_heads=Hkv, head_dim=D,
+                               num_blocks=kw.pop("num_blocks", sum(-(-L // 16) for L in seq_lens) + 8),
+                               device=DEV, poison=True, cfg_id=kw.pop("cfg_id", 21), **kw)
+
+
+def test_one_tile_no_prefix():
+    check(small([32], [32]), "L=32 n=32")
+
+
+def test_one_tile_ragged():
+    check(small([23], [23]), "L=23 n=23")
+
+
+@pytest.mark.parametrize("D", [128, 256])
+def test_prefix_plus_chunk(D):
+    check(small([100, 300, 77], [40, 64, 77], D=D, Hkv=2, seed=1), f"D={D}")
+
+
+@pytest.mark.parametrize("D,G", [(128, 1), (128, 2), (128, 8), (256, 1), (256, 2), (256, 8)])
+def test_group_sizes(D, G):
+    check(small([150, 61], [90, 61], D=D, G=G, Hkv=2 if G < 8 else 1, seed=G), f"D={D} G={G}")
+
+
+@pytest.mark.parametrize("window,softcap", [(0, 30.0), (37, 0.0), (100, 50.0)])
+def test_window_and_softcap(window, softcap):
+    check(small([400, 130, 57], [130, 1, 57], D=256, Hkv=2, window=window, softcap=softcap,
+                seed=window), f"W={window} cap={softcap}")
+
+
+def test_decode_rows_in_varlen_batch():
+    check(small([33, 700, 1, 16, 17], [1, 1, 1, 16, 1], D=128, Hkv=2, seed=5), "decode rows")
+
+
+@pytest.mark.parametrize("seed", range(3))
+def test_chunked_prefill_small(seed):
+    check(workload.chunked_prefill(seed, DEV, poison=True, scale_down=True), f"cfg4 small {seed}")
+
+
+@pytest.mark.parametrize("seed", range(3))
+def test_mixed_batch_small(seed):
+    b = workload.mixed_batch(seed, DEV, poison=True, scale_down=True, drop_out_of_window=True)
+    check(b, f"cfg5 small {seed}")
+
+
+def test_one_hot_prefill_exact():
+    """Each query row's own key is c*q (every other weight underflows): the
+    output row is exactly that key's V row."""
+    G, Hkv, D = 4, 1, 128
+    L, n = 50, 20
+    batch = small([L], [n], D=D, G=G, Hkv=Hkv, seed=9)
+    q = batch.q.view(n, Hkv, G, D)
+    q[:] = q[:, :, :1, :]
+    k = batch.k_pool.mul(0.01)
+    blocks = batch.tables_host[0]
+    for i in range(n):
+        t = L - n + i
+        qv = q[i, 0, 0].float()
+        k[blocks[t // 16], 0, t % 16] = (qv * (300.0 / qv.pow(2).sum()) * 16.0).to(torch.bfloat16)
+    # with window 1 each query sees only its own key
+    b2 = workload.PagedBatch(**{**batch.__dict__, "k_pool": k, "window": 1, "scale": 1.0 / 16})
+    out = run(b2)
+    for i in range(n):
+        t = L - n + i
+        want = batch.v_pool[blocks[t // 16], 0, t % 16]
+        for g in range(G):
+            assert torch.equal(out[i, g], want), (i, g)
+    # full causal attention: the own key still dominates every earlier key
+    b3 = workload.PagedBatch(**{**batch.__dict__, "k_pool": k, "scale": 1.0 / 16})
+    out = run(b3)
+    for i in range(n):
+        t = L - n + i
+        want = batch.v_pool[blocks[t // 16], 0, t % 16]
+        assert torch.equal(out[i, 0], want), i
+
+
+@pytest.mark.parametrize("cfg", [4, 5])
+def test_full_size_sampled_requests(cfg):
+    batch = workload.workload(cfg, seed=0, device=DEV, poison=True)[0]
+    B = batch.num_requests
+    if cfg == 4:
+        reqs = sorted({0, 3, 4, B - 1, int(np.argmax(batch.seq_lens_host))})
+    else:
+        reqs = [0, 31, 32, 63, 64, B - 1]
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    out = run(batch, err)
+    arr = workload.to_numpy_f64(batch, reqs)
+    ref, _ = oracle.run_batch(arr)
+    assert_close(to_f64(out[arr["q_rows"]]), ref, f"cfg{cfg} full size")
+    torch.cuda.synchronize()
+    assert err.item() == 0
