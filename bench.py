@@ -37,6 +37,7 @@ WORKLOAD_NAME = ("decode serving: B=32, seq_lens~U[512,4096], Hq=8, Hkv=2, head_
                  "two layers per step (window 0 and window 512)")
 METRIC = "paged-decode KV GB/s"
 FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
 PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "decode_splitk_serving.md")
 
 
@@ -49,6 +50,8 @@ def parse():
     p.add_argument("--seed", type=int, default=0)
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-other", action="store_true",
+                   help="skip the per-workload measurements of the other configurations")
     p.add_argument("--cpu-seconds", type=float, default=15.0,
                    help="budget of the oracle sample (CPU baseline)")
     return p.parse_args()
@@ -190,6 +193,97 @@ def cpu_baseline(calls, budget_s: float):
             "sample": f"{reqs_done} of {sum(c.num_requests for c in calls)} decode requests "
                       f"(first requests of each layer, same workload), fp64 numpy oracle, "
                       f"one thread, {t_used:.1f} s"}
+
+
+def bf16_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        try:
+            d = json.load(open(path))
+            for key in ("bf16_tflops", "bf16_TFLOPs", "bf16"):
+                if key in d and isinstance(d[key], (int, float)):
+                    return float(d[key]), "measured"
+        except Exception:
+            pass
+    return FALLBACK_BF16_TFLOPS, "fallback"
+
+
+def attention_pairs(batch) -> int:
+    """Visible (query, key) pairs of a varlen batch."""
+    pairs = 0
+    for L, n in zip(batch.seq_lens_host, batch.q_lens_host):
+        for i in range(n):
+            pos = L - n + i
+            lo = 0 if batch.window <= 0 else max(0, pos - batch.window + 1)
+            pairs += pos - lo + 1
+    return pairs
+
+
+def batch_kv_bytes(batch) -> float:
+    """K/V rows of every key some query of the request sees (each once)."""
+    kv_row = 2 * batch.num_kv_heads * batch.head_dim * 2
+    total = 0
+    for L, n in zip(batch.seq_lens_host, batch.q_lens_host):
+        if n == 0:
+            continue
+        lo = 0 if batch.window <= 0 else max(0, L - n - batch.window + 1)
+        total += (L - lo) * kv_row
+    return float(total + batch.q.numel() * 2)
+
+
+def time_launches(fn, flush, iters, warmup):
+    """Median CUDA-event time (ms) of fn(), L2 flushed before every call."""
+    import torch
+    stream = torch.cuda.current_stream()
+    for _ in range(warmup):
+        flush.fill_(1.0)
+        fn()
+    torch.cuda.synchronize()
+    ts = []
+    for i in range(iters):
+        flush.fill_(float(i))
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        fn()
+        e1.record(stream)
+        ts.append((e0, e1))
+    torch.cuda.synchronize()
+    return statistics.median(a.elapsed_time(b) for a, b in ts)
+
+
+def other_workloads(dev, flush, iters=10, warmup=3):
+    """The tiny decode, long-context split-K, chunked-prefill and mixed-batch
+    workloads, each timed alone (L2 flushed first)."""
+    import torch
+    from paged_kv_attention_12_gb300 import binding, workload
+    hbm, hbm_kind = hbm_peak()
+    tc, tc_kind = bf16_peak()
+    res = {}
+    for cfg in (1, 3, 4, 5):
+        batch = workload.workload(cfg, seed=0, device=dev)[0]
+        nbytes = batch_kv_bytes(batch)
+        flops = 4.0 * batch.head_dim * batch.num_q_heads * attention_pairs(batch)
+        if cfg in (1, 3):
+            r = binding.DecodeSplitK(batch)
+            fn, path = r.run, "paged_decode_splitk + combine"
+        else:
+            out = torch.empty_like(batch.q)
+            fn, path = (lambda b=batch, o=out: binding.run_batch(b, o)), "paged_prefill_attn"
+        ms = time_launches(fn, flush, iters, warmup)
+        gbs = nbytes / (ms * 1e-3) / 1e9
+        tfs = flops / (ms * 1e-3) / 1e12
+        entry = {"workload": workload.WORKLOADS[cfg], "path": path, "ms": ms,
+                 "kv_gbs": gbs, "tflops": tfs, "bytes": nbytes, "flops": flops}
+        if cfg == 4:
+            entry["roofline"] = {"bound": "tensor", "achieved": tfs, "peak": tc,
+                                 "peak_kind": tc_kind, "unit": "TFLOP/s", "frac": tfs / tc}
+        else:
+            entry["roofline"] = {"bound": "hbm", "achieved": gbs, "peak": hbm,
+                                 "peak_kind": hbm_kind, "unit": "GB/s", "frac": gbs / hbm}
+        res[str(cfg)] = entry
+        del batch, fn
+        torch.cuda.empty_cache()
+    return res
 
 
 def dist_setup(args):
@@ -385,6 +479,8 @@ def main():
         line["e2e"] = e2e
     if clocks:
         line["clocks"] = clocks
+    if not args.no_other and world == 1:
+        line["other_workloads"] = other_workloads(dev, flush)
     if not args.no_cpu_baseline and world == 1:
         line["cpu_baseline"] = cpu_baseline(calls, args.cpu_seconds)
     print(json.dumps(line))

@@ -18,7 +18,7 @@
  * Definitions shared by every entry point
  * ---------------------------------------
  *  B       requests; Hq / Hkv query / KV heads, G = Hq / Hkv in {1,2,4,8};
- *  D       head_dim in {64, 128, 256}; bs = block_size = 16.
+ *  D       head_dim in {128, 256}; bs = block_size = 16.
  *  KV pool bf16 [num_blocks][Hkv][bs][D] for K and for V (one pool per layer;
  *          "KV sharing" between layers is the same pool passed twice).  Each
  *          (block, head) tile is one contiguous bs*D*2-byte run.
@@ -115,10 +115,13 @@ int paged_decode_attn(const void* q, void* out, const pka_kv_pool* kv,
                       int32_t max_seq_len, const pka_attn_params* params,
                       void* stream);
 
-/* Split-K plan (host only, no CUDA call when sm_count > 0): picks the number
- * of splits S and the split size C (in blocks) for a decode launch so that
- * B*Hkv*S CTAs cover the GPU.  max_seq_len is a host upper bound of seq_lens.
- * sm_count <= 0 queries the current device. */
+/* Split-K plan (host only, makes no CUDA call): the workspace shape of a
+ * split-K launch for requests of at most max_seq_len tokens.
+ *   split_blocks (C): the smallest chunk of 16-key tiles one CTA streams;
+ *   num_splits (S):   partial slots per (request, query head),
+ *                     ceil(T / C) + 1 for T = most visible blocks of a query.
+ * sm_count is accepted for compatibility and not needed: the partition
+ * adapts to the GPU it runs on. */
 int paged_decode_splitk_plan(int32_t B, int32_t Hkv, int32_t max_seq_len,
                              int32_t block_size, int32_t window, int32_t sm_count,
                              int32_t* num_splits, int32_t* split_blocks);
@@ -128,13 +131,17 @@ size_t paged_decode_splitk_workspace_bytes(int32_t B, int32_t Hq, int32_t D,
                                            int32_t num_splits);
 
 /* Split-K decode ("split-K decode variant", engine feature list).
- * Split s of request b covers logical blocks [jlo + s*C, jlo + (s+1)*C) of
- * the request's visible block range [jlo, jhi) (jlo = block of the first
- * visible key), C = split_blocks.  Each (b, h, s) writes its softmax-
- * normalised partial output partial_o fp32 [B][Hq][S][D] and its natural-log
- * LSE partial_lse fp32 [B][Hq][S]; an empty split writes 0 and -inf.
- * num_splits*split_blocks must cover the visible blocks of max_seq_len
- * (else PKA_ERR_WORKSPACE). */
+ * Work partition: a segment is one (request, KV head) with n_b visible
+ * blocks ("tiles", blocks [jlo_b, jlo_b + n_b), jlo_b = block of the first
+ * visible key).  Segments are laid end to end in (request, head) order,
+ * T = Hkv * sum_b n_b tiles in all, and cut into chunks of
+ * q = max(C, ceil(T / grid)) tiles, grid = the GPU's SM count; chunk c is
+ * streamed by CTA c.  The part of a segment starting at tile A that falls
+ * in chunk c is written to slot c - floor(A / q): its softmax-normalised
+ * partial output partial_o fp32 [B][Hq][S][D] and its natural-log LSE
+ * partial_lse fp32 [B][Hq][S].  Slots a segment does not use get LSE -inf
+ * (their partial_o is left untouched).  Needs S >= ceil(T_max / C) + 1 for
+ * T_max the visible blocks of max_seq_len (else PKA_ERR_WORKSPACE). */
 int paged_decode_splitk(const void* q, float* partial_o, float* partial_lse,
                         const pka_kv_pool* kv, const int32_t* block_tables,
                         int32_t max_blocks, const int32_t* seq_lens, int32_t B,
@@ -145,7 +152,8 @@ int paged_decode_splitk(const void* q, float* partial_o, float* partial_lse,
 /* Log-sum-exp merge of split partials (the merge a split-K softmax needs):
  * M = max_s LSE_s, w_s = exp(LSE_s - M),
  * out = sum_s w_s*O_s / sum_s w_s (bf16 [B][Hq][D]),
- * lse_out = M + ln sum_s w_s (fp32 [B][Hq], may be NULL). */
+ * lse_out = M + ln sum_s w_s (fp32 [B][Hq], may be NULL).
+ * Slots with LSE -inf are skipped without reading their partial_o. */
 int paged_decode_splitk_combine(const float* partial_o, const float* partial_lse,
                                 int32_t B, int32_t Hq, int32_t D, int32_t num_splits,
                                 void* out, float* lse_out, void* stream);

@@ -28,11 +28,12 @@ Conventions where the pages are silent (each is one reading, stated once):
 * LSE is the natural-log log-sum-exp of the (capped) logits; an empty
   visible set gives output 0 and LSE ``-inf``.
 * Split-K ("split-K decode variant", inference-server README feature list):
-  split ``s`` of a request covers logical blocks
-  ``[jlo + s*C, jlo + (s+1)*C)`` of the request's visible block range, where
-  ``jlo`` is the block of the first visible key and ``C`` the split size in
-  blocks; the partials are (softmax-normalised output, LSE) of each split and
-  the combine is the log-sum-exp merge of those partials.
+  the pages give no partition, and the combined result does not depend on
+  it, so the partition is an input: each split covers a contiguous range of
+  the request's visible blocks; its partial is the (softmax-normalised
+  output, LSE) over that range and the combine is the log-sum-exp merge of
+  the partials.  ``balanced_split_ranges`` states the partition the library
+  uses, as integer arithmetic.
 """
 from __future__ import annotations
 
@@ -140,9 +141,15 @@ def visible_block_range(seq_len: int, window: int, block_size: int):
 
 
 def splitk_partials(q, k_pool, v_pool, block_tables, seq_lens, scale, softcap,
-                    window, num_splits, split_blocks):
+                    window, num_splits, split_blocks=None, ranges=None):
     """Per-split (output, LSE) of decode attention.
 
+    The split of each request's visible keys is an input.  Either
+    ``ranges[b][s] = (j0, j1)`` (logical blocks of split ``s``, or ``None``
+    for an unused split) or, when only ``split_blocks`` C is given, the fixed
+    partition: split ``s`` covers blocks ``[jlo + s*C, jlo + (s+1)*C)``.
+    The same ranges apply to every KV head of a request unless ``ranges``
+    is indexed ``ranges[b][kvh][s]`` (a list per head).
     Returns partial_o [B][Hq][S][D] and partial_lse [B][Hq][S]; an empty
     split has output 0 and LSE ``-inf``.
     """
@@ -164,18 +171,59 @@ def splitk_partials(q, k_pool, v_pool, block_tables, seq_lens, scale, softcap,
         Vb = np.zeros((L, Hkv, v_pool.shape[3]))
         Kb[T_all] = gather_request_kv(k_pool, block_tables[b], L, bs)[T_all]
         Vb[T_all] = gather_request_kv(v_pool, block_tables[b], L, bs)[T_all]
-        for s in range(num_splits):
-            j0 = jlo + s * split_blocks
-            j1 = min(jhi, j0 + split_blocks)
-            T = T_all[(T_all >= j0 * bs) & (T_all < j1 * bs)]
-            for kvh in range(Hkv):
-                heads = slice(kvh * G, (kvh + 1) * G)
+        for kvh in range(Hkv):
+            heads = slice(kvh * G, (kvh + 1) * G)
+            for s in range(num_splits):
+                if ranges is None:
+                    j0 = jlo + s * split_blocks
+                    rng = (j0, min(jhi, j0 + split_blocks))
+                else:
+                    per = ranges[b][kvh] if isinstance(ranges[b][0], list) else ranges[b]
+                    rng = per[s] if s < len(per) else None
+                if rng is None:
+                    continue
+                j0, j1 = rng
+                T = T_all[(T_all >= j0 * bs) & (T_all < j1 * bs)]
                 o, l = softmax_attention(q[b, heads, :], Kb[T, kvh, :], Vb[T, kvh, :],
                                          scale, softcap)
                 po[b, heads, s, :] = o
                 pl[b, heads, s] = l
     return po, pl
 
+
+def balanced_split_ranges(seq_lens, window, block_size, num_kv_heads, grid, min_chunk):
+    """The library's split-K work partition, as plain integer arithmetic.
+
+    Segments (request, KV head) of n_b visible blocks each are laid end to
+    end, ``T = Hkv * sum(n_b)`` tiles, cut into chunks of
+    ``q = max(min_chunk, ceil(T / grid))``; the part of a segment starting at
+    tile ``A`` inside chunk ``c`` is split ``c - A // q``.  Returns
+    ``ranges[b][kvh]`` = list of (j0, j1) per split (None where unused).
+    """
+    nb = []
+    jl = []
+    for L in seq_lens:
+        j0, j1 = visible_block_range(int(L), window, block_size)
+        nb.append(j1 - j0)
+        jl.append(j0)
+    T = num_kv_heads * sum(nb)
+    q = max(min_chunk, -(-T // grid)) if T > 0 else max(min_chunk, 1)
+    out = []
+    A = 0
+    for b, n in enumerate(nb):
+        per_head = []
+        for kvh in range(num_kv_heads):
+            splits = []
+            if n > 0:
+                c0 = A // q
+                for c in range(c0, (A + n - 1) // q + 1):
+                    t0 = max(A, c * q)
+                    t1 = min(A + n, (c + 1) * q)
+                    splits.append((jl[b] + t0 - A, jl[b] + t1 - A))
+            per_head.append(splits)
+            A += n
+        out.append(per_head)
+    return out
 
 def lse_combine(partial_o, partial_lse):
     """Log-sum-exp merge of split partials over the split axis.
@@ -207,6 +255,7 @@ def run_batch(arrays):
 
 __all__ = [
     "gather_request_kv", "visible_keys", "softmax_attention", "paged_attention",
-    "paged_decode", "visible_block_range", "splitk_partials", "lse_combine",
+    "paged_decode", "visible_block_range", "splitk_partials", "balanced_split_ranges",
+    "lse_combine",
     "run_batch",
 ]

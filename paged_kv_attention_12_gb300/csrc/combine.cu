@@ -13,10 +13,10 @@ namespace pka {
 namespace {
 
 // One warp per (row, 128-column segment): each lane owns one float4 of the
-// output.  Split weights are computed 32 at a time (one split per lane) and
-// broadcast with shuffles; the partial loads of eight splits are issued
-// before any of them is used, so the loop is bound by bandwidth, not by the
-// latency of one load after another.
+// output.  Split weights are computed 32 at a time (one split per lane);
+// only splits with a non-zero weight are read, and the loads of eight of them
+// are issued before any is used, so the loop is bound by bandwidth, not by
+// the latency of one load after another.
 template <int D>
 __global__ void __launch_bounds__(128) combine_kernel(const CombineArgs a) {
   constexpr int SEGS = D / 128;
@@ -39,34 +39,32 @@ __global__ void __launch_bounds__(128) combine_kernel(const CombineArgs a) {
   float den = 0.f;
   for (int base = 0; base < S; base += 32) {
     const int n = min(32, S - base);
-    // exp(-inf) = 0 for empty splits
+    // exp(-inf) = 0: a split with no keys (or a slot no CTA wrote) is skipped
+    // without touching its partial output
     const float wl = (lane < n) ? fast_exp2((lse[base + lane] - Ms) * kLog2e) : 0.f;
     den += wl;
-    int s = 0;
-    for (; s + 8 <= n; s += 8) {
+    const unsigned live = __ballot_sync(0xffffffffu, wl != 0.f);
+    const int cnt = __popc(live);
+    for (int k = 0; k < cnt; k += 8) {
       float4 x[8];
-#pragma unroll
-      for (int u = 0; u < 8; ++u)
-        x[u] = *reinterpret_cast<const float4*>(po + static_cast<size_t>(base + s + u) * D);
+      float w[8];
 #pragma unroll
       for (int u = 0; u < 8; ++u) {
-        const float w = __shfl_sync(0xffffffffu, wl, s + u);
-        if (w != 0.f) {  // an empty split's partial is 0 but never trusted
-          acc.x = fmaf(w, x[u].x, acc.x);
-          acc.y = fmaf(w, x[u].y, acc.y);
-          acc.z = fmaf(w, x[u].z, acc.z);
-          acc.w = fmaf(w, x[u].w, acc.w);
+        if (k + u < cnt) {  // uniform across the warp
+          const int sb = static_cast<int>(__fns(live, 0, k + u + 1));
+          w[u] = __shfl_sync(0xffffffffu, wl, sb);
+          x[u] = *reinterpret_cast<const float4*>(po + static_cast<size_t>(base + sb) * D);
+        } else {
+          w[u] = 0.f;
+          x[u] = make_float4(0.f, 0.f, 0.f, 0.f);
         }
       }
-    }
-    for (; s < n; ++s) {
-      const float w = __shfl_sync(0xffffffffu, wl, s);
-      if (w != 0.f) {
-        const float4 x = *reinterpret_cast<const float4*>(po + static_cast<size_t>(base + s) * D);
-        acc.x = fmaf(w, x.x, acc.x);
-        acc.y = fmaf(w, x.y, acc.y);
-        acc.z = fmaf(w, x.z, acc.z);
-        acc.w = fmaf(w, x.w, acc.w);
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        acc.x = fmaf(w[u], x[u].x, acc.x);
+        acc.y = fmaf(w[u], x[u].y, acc.y);
+        acc.z = fmaf(w[u], x[u].z, acc.z);
+        acc.w = fmaf(w[u], x[u].w, acc.w);
       }
     }
   }

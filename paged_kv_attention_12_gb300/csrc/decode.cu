@@ -4,27 +4,37 @@
 // block through the request's block table ("Triton paged decode ... kernels
 // reading K/V through block tables; split-K decode variant", inference-server
 // README, engine feature list).  Decode is bound by HBM: every K/V byte is
-// read once, so the design is about keeping enough bytes in flight and doing
-// the arithmetic on CUDA cores underneath the copies.
+// read once, so the design is about keeping enough bytes in flight, spreading
+// them evenly over the SMs, and doing the arithmetic on CUDA cores underneath
+// the copies.
 //
-// Work items are (request, KV head, split).  The kernel is persistent: each
-// CTA takes items blockIdx.x, blockIdx.x + gridDim.x, ...  Inside a CTA:
+// Work.  A segment is one (request, KV head): its visible blocks, each a
+// 16-key "tile".  The kernel is persistent (one CTA per SM).
+//  * split-K: the segments' tiles, laid end to end, are cut into equal
+//    contiguous chunks of q = max(min_chunk, ceil(total / grid)) tiles, one
+//    chunk per CTA.  Each piece of a segment inside a chunk gives one partial
+//    (normalised output, LSE) in slot (CTA index - CTA index of the
+//    segment's first tile); the CTA holding a segment's first tile also
+//    writes LSE = -inf into the slots the segment does not use, so the LSE
+//    combine needs nothing but the partials.  Every CTA streams the same
+//    number of tiles whatever the mix of lengths.
+//  * direct: CTA c takes whole segments c, c + grid, ... and writes bf16.
 //
-//  * one producer warp walks the items' block tables (32 ids per coalesced
-//    load) and issues, per block, two 1-D bulk copies (the (block, head) K
-//    and V tiles, each one contiguous bs*D*2-byte run of the pool) into a
-//    ring of shared-memory slots, completion counted on a "full" mbarrier;
-//  * NW consumer warps take the ring's tiles round robin.  A warp handles a
-//    tile with its lanes spread over D (8 bf16 = 16 bytes per lane, so a key
-//    row is read conflict-free in one instruction), all G query heads of the
-//    KV group at once (each K/V byte feeds G heads), partial dot products
-//    transposed-and-reduced across lanes (reduce-scatter with shuffles),
-//    online softmax in the exp2 domain, P broadcast through shared memory
-//    and P.V accumulated in fp32 registers;
-//  * at the end of an item the consumer warps merge their (max, sum, acc)
-//    states through shared memory and write the bf16 output (direct) or the
-//    fp32 partial output + natural-log LSE (split-K), while the producer is
-//    already streaming the next item's tiles.
+// Inside a CTA:
+//  * one producer warp walks the pieces' block tables (32 ids per coalesced
+//    load) and issues, per tile, two 1-D bulk copies (the (block, head) K and
+//    V tiles, each one contiguous bs*D*2-byte run of the pool) into a ring of
+//    shared-memory slots, completion counted on a "full" mbarrier;
+//  * NW consumer warps take the ring's tiles round robin.  Lanes are spread
+//    over D (8 bf16 = 16 bytes per lane, so a key row is read conflict-free
+//    in one instruction); all G query heads of the KV group are handled at
+//    once (each K/V byte feeds G heads); partial dot products are reduced
+//    across lanes with a shuffle reduce-scatter; online softmax runs in the
+//    exp2 domain; P is broadcast through shared memory; P.V accumulates in
+//    fp32 registers with packed two-wide FMAs;
+//  * at the end of a piece the consumer warps merge their (max, sum, acc)
+//    states through shared memory and write the piece's result, while the
+//    producer already streams the next piece's tiles.
 //
 // Tiles with keys outside [first visible, query position] (window start,
 // ragged tail) take a masked path that never lets a masked key's K or V --
@@ -35,6 +45,39 @@
 namespace pka {
 
 namespace {
+
+// ---------------------------------------------------------- packed fp32 x2
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
+  float2 d;
+  asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\t"
+      "mov.b64 ra, {%2, %3};\n\t"
+      "mov.b64 rb, {%4, %5};\n\t"
+      "mov.b64 rc, {%6, %7};\n\t"
+      "fma.rn.f32x2 rd, ra, rb, rc;\n\t"
+      "mov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+  return d;
+}
+
+__device__ __forceinline__ float2 fmul2(float2 a, float2 b) {
+  float2 d;
+  asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
+      "mov.b64 ra, {%2, %3};\n\t"
+      "mov.b64 rb, {%4, %5};\n\t"
+      "mul.rn.f32x2 rd, ra, rb;\n\t"
+      "mov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return d;
+}
+
+__device__ __forceinline__ void unpack8x2(const uint4& u, float2 (&f)[4]) {
+  bf16x2_to_f32(u.x, f[0].x, f[0].y);
+  bf16x2_to_f32(u.y, f[1].x, f[1].y);
+  bf16x2_to_f32(u.z, f[2].x, f[2].y);
+  bf16x2_to_f32(u.w, f[3].x, f[3].y);
+}
 
 // Reduce-scatter of N per-lane partial sums across the LPK lanes that share
 // a key: stage with xor offset O keeps the upper half of the values on lanes
@@ -74,57 +117,185 @@ __device__ __forceinline__ float warp_sum(float x) {
   return x;
 }
 
+__device__ __forceinline__ int warp_incl_scan(int x, int lane) {
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  return x;
+}
+
 // Named barrier over the consumer warps only (the producer keeps streaming).
 __device__ __forceinline__ void consumer_sync(int nthreads) {
   asm volatile("bar.sync 1, %0;" ::"r"(nthreads) : "memory");
 }
 
-struct ItemRange {
-  int b, kvh, split;
-  int j0, nblk;   // first logical block, number of blocks
-  int t_lo, pos;  // visible key positions [t_lo, pos]
-  int qrow;       // query row of the request
+// Visible keys of request b's decode query: positions [t_lo, pos], blocks
+// [jlo, jlo + nb).
+struct ReqGeo {
+  int jlo, nb, t_lo, pos;
 };
 
-__device__ __forceinline__ ItemRange item_range(const DecodeArgs& a, int item, bool report_err) {
-  ItemRange r;
-  const int S = a.num_splits;
-  r.split = item % S;
-  r.kvh = (item / S) % a.Hkv;
-  r.b = item / (S * a.Hkv);
-  int L = a.seq_lens[r.b];
-  const int cap = a.max_blocks * kBlockSize;
-  if (L > cap) {
-    if (report_err) report(a.err, PKA_DEVERR_SEQ_LEN);
-    L = cap;
-  }
-  if (L < 0) L = 0;
-  r.qrow = r.b;
-  if (a.query_start_loc != nullptr) {
-    // varlen decode rows: the request's last query row attends at L - 1
-    r.qrow = a.query_start_loc[r.b + 1] - 1;
-  }
-  r.pos = L - 1;
-  r.t_lo = (a.window > 0) ? max(0, r.pos - a.window + 1) : 0;
-  const int jlo = r.t_lo / kBlockSize;
-  const int jhi = (L + kBlockSize - 1) / kBlockSize;
-  if (L <= 0) {
-    r.j0 = 0;
-    r.nblk = 0;
-    return r;
-  }
-  if (a.split_blocks > 0) {
-    const int j0 = jlo + r.split * a.split_blocks;
-    const int j1 = min(jhi, j0 + a.split_blocks);
-    if (report_err && r.split == S - 1 && j1 < jhi) report(a.err, PKA_DEVERR_SEQ_LEN);
-    r.j0 = j0;
-    r.nblk = max(0, j1 - j0);
-  } else {
-    r.j0 = jlo;
-    r.nblk = jhi - jlo;
-  }
-  return r;
+__device__ __forceinline__ ReqGeo req_geo(const DecodeArgs& a, int b) {
+  ReqGeo g;
+  int L = a.seq_lens[b];
+  L = max(0, min(L, a.max_blocks * kBlockSize));
+  g.pos = L - 1;
+  g.t_lo = (a.window > 0) ? max(0, g.pos - a.window + 1) : 0;
+  g.jlo = g.t_lo / kBlockSize;
+  g.nb = (L > 0) ? (L + kBlockSize - 1) / kBlockSize - g.jlo : 0;
+  return g;
 }
+
+// One piece of work: tiles [first, first + ntiles) of segment (b, kvh).
+struct Piece {
+  int b, kvh;
+  int j0;        // logical block of the first tile
+  int ntiles;
+  int t_lo, pos;
+  int qrow;      // query row of the request
+  int slot;      // split-K partial slot (direct mode: unused)
+  int fill_from; // >= 0: also write LSE=-inf into slots [fill_from, num_splits)
+};
+
+// Enumerates the pieces of one CTA.  Every lane of a warp runs it in
+// lockstep (it uses warp scans), and every warp of the CTA sees the same
+// sequence.
+struct PieceIter {
+  const DecodeArgs* a;
+  bool direct;
+  // direct mode
+  int item;
+  // split mode
+  long long lo, hi, q;
+  bool last;
+  int b, kvh;
+  long long prefix;  // sum of nb over requests before b
+  ReqGeo geo;
+  bool done;
+
+  __device__ void init(const DecodeArgs& args, int lane) {
+    a = &args;
+    direct = args.split_blocks <= 0;
+    done = false;
+    if (direct) {
+      item = blockIdx.x;
+      return;
+    }
+    // total tiles T = Hkv * sum_b nb_b
+    long long T = 0;
+    for (int base = 0; base < args.batch; base += 32) {
+      const int bb = base + lane;
+      const int nb = (bb < args.batch) ? req_geo(args, bb).nb : 0;
+      T += __shfl_sync(0xffffffffu, warp_incl_scan(nb, lane), 31);
+    }
+    T *= args.Hkv;
+    const long long grid = gridDim.x;
+    q = max(static_cast<long long>(args.split_blocks), (T + grid - 1) / grid);
+    const long long weff = T > 0 ? (T + q - 1) / q : 1;
+    const long long c = blockIdx.x;
+    if (c >= weff) {
+      done = true;
+      return;
+    }
+    lo = c * q;
+    hi = min(T, lo + q);
+    last = (c == weff - 1);
+    // first request holding a segment this CTA touches: the first b with
+    // Hkv*(prefix_b + nb_b) + (nb_b == 0) > lo
+    long long run = 0;
+    b = args.batch;
+    prefix = run;
+    for (int base = 0; base < args.batch; base += 32) {
+      const int bb = base + lane;
+      const int nb = (bb < args.batch) ? req_geo(args, bb).nb : 0;
+      const int incl = warp_incl_scan(nb, lane);
+      const long long pre = run + incl - nb;
+      const bool hit = (bb < args.batch) &&
+                       (static_cast<long long>(args.Hkv) * (pre + nb) + (nb == 0 ? 1 : 0) > lo);
+      const unsigned m = __ballot_sync(0xffffffffu, hit);
+      if (m) {
+        const int first = __ffs(m) - 1;
+        b = base + first;
+        prefix = __shfl_sync(0xffffffffu, pre, first);
+        break;
+      }
+      run += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    kvh = 0;
+    if (b < args.batch) geo = req_geo(args, b);
+  }
+
+  __device__ bool next(Piece& p) {
+    if (done) return false;
+    const DecodeArgs& A = *a;
+    if (direct) {
+      const int nseg = A.batch * A.Hkv;
+      if (item >= nseg) {
+        done = true;
+        return false;
+      }
+      p.b = item / A.Hkv;
+      p.kvh = item % A.Hkv;
+      const ReqGeo g = req_geo(A, p.b);
+      p.j0 = g.jlo;
+      p.ntiles = g.nb;
+      p.t_lo = g.t_lo;
+      p.pos = g.pos;
+      p.slot = 0;
+      p.fill_from = -1;
+      item += gridDim.x;
+    } else {
+      while (true) {
+        if (b >= A.batch) {
+          done = true;
+          return false;
+        }
+        const long long seg = static_cast<long long>(A.Hkv) * prefix +
+                              static_cast<long long>(kvh) * geo.nb;  // segment start
+        const int n = geo.nb;
+        const bool before = seg + (n > 0 ? n : 1) <= lo;  // wholly before this chunk
+        const bool after = !last && seg >= hi;
+        if (after) {
+          done = true;
+          return false;
+        }
+        const int cur_b = b, cur_kvh = kvh;
+        const ReqGeo g = geo;
+        // advance to the next segment
+        if (++kvh == A.Hkv) {
+          kvh = 0;
+          prefix += geo.nb;
+          ++b;
+          if (b < A.batch) geo = req_geo(A, b);
+        }
+        if (before) continue;
+        const long long t0 = max(seg, lo);
+        const long long t1 = min(seg + n, hi);
+        p.b = cur_b;
+        p.kvh = cur_kvh;
+        p.j0 = g.jlo + static_cast<int>(t0 - seg);
+        p.ntiles = static_cast<int>(max(0LL, t1 - t0));
+        p.t_lo = g.t_lo;
+        p.pos = g.pos;
+        const long long cfirst = seg / q;
+        p.slot = static_cast<int>(static_cast<long long>(blockIdx.x) - cfirst);
+        p.fill_from = -1;
+        if (n == 0) {
+          p.fill_from = 0;
+        } else if (p.slot == 0) {
+          p.fill_from = static_cast<int>((seg + n - 1) / q - cfirst + 1);
+        }
+        if (p.ntiles == 0 && p.fill_from < 0) continue;
+        break;
+      }
+    }
+    p.qrow = p.b;
+    if (A.query_start_loc != nullptr) p.qrow = A.query_start_loc[p.b + 1] - 1;
+    return true;
+  }
+};
 
 }  // namespace
 
@@ -146,13 +317,14 @@ struct DecodeShape {
   static constexpr int kSmemBytes = kRingBytes + kBarBytes + kPBytes + kMergeBytes;
   static_assert(D % 8 == 0 && LPK <= 32 && 32 % LPK == 0, "head_dim");
   static_assert(KC % KPW == 0, "chunk");
+  static_assert(kSmemBytes <= 232448, "shared memory");
 };
 
 // Processes one KV tile (kBlockSize keys) for one consumer warp.
 template <int D, int G, int NW, int NSLOT, bool EDGE>
 __device__ __forceinline__ void decode_tile(const uint16_t* __restrict__ Kt,
                                             const uint16_t* __restrict__ Vt,
-                                            const float (&qf)[G][8], float (&acc)[G][8],
+                                            const float2 (&qf)[G][4], float2 (&acc)[G][4],
                                             float (&m)[G],
                                             float (&ls)[DecodeShape<D, G, NW, NSLOT>::NVL],
                                             float* psm, int lane, int tok0, int t_lo, int pos,
@@ -172,18 +344,15 @@ __device__ __forceinline__ void decode_tile(const uint16_t* __restrict__ Kt,
     for (int s = 0; s < KS; ++s) {
       const int key = c * KC + s * KPW + kl;
       const uint4 u = *reinterpret_cast<const uint4*>(Kt + key * D + dl * 8);
-      float kf[8];
-      unpack8(u, kf);
+      float2 kf[4];
+      unpack8x2(u, kf);
 #pragma unroll
       for (int g = 0; g < G; ++g) {
-        float d0 = qf[g][0] * kf[0];
-        float d1 = qf[g][1] * kf[1];
-#pragma unroll
-        for (int e = 2; e < 8; e += 2) {
-          d0 = fmaf(qf[g][e], kf[e], d0);
-          d1 = fmaf(qf[g][e + 1], kf[e + 1], d1);
-        }
-        part[s * G + g] = d0 + d1;
+        float2 d = fmul2(qf[g][0], kf[0]);
+        d = ffma2(qf[g][1], kf[1], d);
+        d = ffma2(qf[g][2], kf[2], d);
+        d = ffma2(qf[g][3], kf[3], d);
+        part[s * G + g] = d.x + d.y;
       }
     }
     ReduceScatter<NV, LPK / 2>::run(part, lane);
@@ -229,9 +398,11 @@ __device__ __forceinline__ void decode_tile(const uint16_t* __restrict__ Kt,
       pw[(dl / DUP) * NVL + j] = p;
     }
 #pragma unroll
-    for (int g = 0; g < G; ++g)
+    for (int g = 0; g < G; ++g) {
+      const float2 a2 = make_float2(alpha[g], alpha[g]);
 #pragma unroll
-      for (int e = 0; e < 8; ++e) acc[g][e] *= alpha[g];
+      for (int e = 0; e < 4; ++e) acc[g][e] = fmul2(acc[g][e], a2);
+    }
     __syncwarp();
 
     // ---- P.V over this lane's 8 columns
@@ -243,15 +414,28 @@ __device__ __forceinline__ void decode_tile(const uint16_t* __restrict__ Kt,
         if (t < t_lo || t > pos) continue;  // masked V row may hold NaN
       }
       const uint4 u = *reinterpret_cast<const uint4*>(Vt + key * D + dl * 8);
-      float vf[8];
-      unpack8(u, vf);
+      float2 vf[4];
+      unpack8x2(u, vf);
       float pg[G];
+      if constexpr (G % 4 == 0) {
 #pragma unroll
-      for (int g = 0; g < G; ++g) pg[g] = pw[s * G + g];
+        for (int g = 0; g < G; g += 4) {
+          const float4 t4 = *reinterpret_cast<const float4*>(pw + s * G + g);
+          pg[g] = t4.x;
+          pg[g + 1] = t4.y;
+          pg[g + 2] = t4.z;
+          pg[g + 3] = t4.w;
+        }
+      } else {
 #pragma unroll
-      for (int g = 0; g < G; ++g)
+        for (int g = 0; g < G; ++g) pg[g] = pw[s * G + g];
+      }
 #pragma unroll
-        for (int e = 0; e < 8; ++e) acc[g][e] = fmaf(pg[g], vf[e], acc[g][e]);
+      for (int g = 0; g < G; ++g) {
+        const float2 p2 = make_float2(pg[g], pg[g]);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) acc[g][e] = ffma2(p2, vf[e], acc[g][e]);
+      }
     }
     __syncwarp();
   }
@@ -275,7 +459,6 @@ __global__ void __launch_bounds__((NW + 1) * 32, 1) paged_decode_kernel(const De
 
   const int warp = threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
-  const int num_items = a.batch * a.Hkv * a.num_splits;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < NSLOT; ++i) {
@@ -286,34 +469,38 @@ __global__ void __launch_bounds__((NW + 1) * 32, 1) paged_decode_kernel(const De
   }
   __syncthreads();
 
+  PieceIter iter;
+  iter.init(a, lane);
+  Piece pc;
+
   if (warp == NW) {
     // ============================ producer warp ============================
     const uint64_t pol = policy_evict_first();
     long long issued = 0;
     bool ok = true;
-    for (int item = blockIdx.x; item < num_items && ok; item += gridDim.x) {
-      const ItemRange r = item_range(a, item, lane == 0);
-      const int32_t* trow = a.tables + static_cast<size_t>(r.b) * a.max_blocks + r.j0;
-      for (int base = 0; base < r.nblk && ok; base += 32) {
+    while (ok && iter.next(pc)) {
+      const int32_t* trow = a.tables + static_cast<size_t>(pc.b) * a.max_blocks + pc.j0;
+      for (int base = 0; base < pc.ntiles && ok; base += 32) {
         int id = 0;
-        if (base + lane < r.nblk) {
+        if (base + lane < pc.ntiles) {
           id = trow[base + lane];
           if (static_cast<unsigned>(id) >= static_cast<unsigned>(a.num_blocks)) {
             report(a.err, PKA_DEVERR_BAD_TABLE);
             id = 0;
           }
         }
-        const int cnt = min(32, r.nblk - base);
+        const int cnt = min(32, pc.ntiles - base);
         for (int k = 0; k < cnt; ++k) {
           const int phys = __shfl_sync(0xffffffffu, id, k);
           const int slot = static_cast<int>(issued % NSLOT);
           const long long round = issued / NSLOT;
           int good = 1;
           if (lane == 0) {
-            if (round > 0) good = mbar_wait(&empty[slot], static_cast<uint32_t>((round - 1) & 1), a.err);
+            if (round > 0)
+              good = mbar_wait(&empty[slot], static_cast<uint32_t>((round - 1) & 1), a.err);
             if (good) {
               mbar_arrive_expect_tx(&full[slot], 2 * S::kTileBytes);
-              const size_t off = (static_cast<size_t>(phys) * a.Hkv + r.kvh) * TE;
+              const size_t off = (static_cast<size_t>(phys) * a.Hkv + pc.kvh) * TE;
               uint16_t* dst = ring + static_cast<size_t>(slot) * 2 * TE;
               bulk_g2s_stream(dst, a.k + off, S::kTileBytes, &full[slot], pol);
               bulk_g2s_stream(dst + TE, a.v + off, S::kTileBytes, &full[slot], pol);
@@ -346,19 +533,20 @@ __global__ void __launch_bounds__((NW + 1) * 32, 1) paged_decode_kernel(const De
   long long tile_base = 0;
   bool ok = true;
 
-  for (int item = blockIdx.x; item < num_items; item += gridDim.x) {
-    const ItemRange r = item_range(a, item, false);
-    float qf[G][8], acc[G][8], m[G], ls[NVL];
+  while (iter.next(pc)) {
+    float2 qf[G][4], acc[G][4];
+    float m[G], ls[NVL];
     {
-      const uint16_t* qp = a.q + (static_cast<size_t>(r.qrow) * a.Hq + r.kvh * G) * D + dl * 8;
+      const uint16_t* qp = a.q + (static_cast<size_t>(pc.qrow) * a.Hq + pc.kvh * G) * D + dl * 8;
+      const float2 qs2 = make_float2(qscale, qscale);
 #pragma unroll
       for (int g = 0; g < G; ++g) {
         const uint4 u = *reinterpret_cast<const uint4*>(qp + g * D);
-        unpack8(u, qf[g]);
+        unpack8x2(u, qf[g]);
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          qf[g][e] *= qscale;
-          acc[g][e] = 0.f;
+        for (int e = 0; e < 4; ++e) {
+          qf[g][e] = fmul2(qf[g][e], qs2);
+          acc[g][e] = make_float2(0.f, 0.f);
         }
         m[g] = -INFINITY;
       }
@@ -366,7 +554,7 @@ __global__ void __launch_bounds__((NW + 1) * 32, 1) paged_decode_kernel(const De
       for (int j = 0; j < NVL; ++j) ls[j] = 0.f;
     }
 
-    for (int i = warp; i < r.nblk && ok; i += NW) {
+    for (int i = warp; i < pc.ntiles && ok; i += NW) {
       const long long T = tile_base + i;
       const int slot = static_cast<int>(T % NSLOT);
       const bool got = mbar_wait(&full[slot], static_cast<uint32_t>((T / NSLOT) & 1), a.err);
@@ -376,81 +564,106 @@ __global__ void __launch_bounds__((NW + 1) * 32, 1) paged_decode_kernel(const De
       }
       const uint16_t* Kt = ring + static_cast<size_t>(slot) * 2 * TE;
       const uint16_t* Vt = Kt + TE;
-      const int tok0 = (r.j0 + i) * kBlockSize;
-      if (tok0 < r.t_lo || tok0 + kBlockSize - 1 > r.pos)
-        decode_tile<D, G, NW, NSLOT, true>(Kt, Vt, qf, acc, m, ls, psm, lane, tok0, r.t_lo,
-                                           r.pos, a.softcap, inv_cap);
+      const int tok0 = (pc.j0 + i) * kBlockSize;
+      if (tok0 < pc.t_lo || tok0 + kBlockSize - 1 > pc.pos)
+        decode_tile<D, G, NW, NSLOT, true>(Kt, Vt, qf, acc, m, ls, psm, lane, tok0, pc.t_lo,
+                                           pc.pos, a.softcap, inv_cap);
       else
-        decode_tile<D, G, NW, NSLOT, false>(Kt, Vt, qf, acc, m, ls, psm, lane, tok0, r.t_lo,
-                                            r.pos, a.softcap, inv_cap);
+        decode_tile<D, G, NW, NSLOT, false>(Kt, Vt, qf, acc, m, ls, psm, lane, tok0, pc.t_lo,
+                                            pc.pos, a.softcap, inv_cap);
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[slot]);
     }
-    tile_base += r.nblk;
+    tile_base += pc.ntiles;
 
-    // ---- per-warp totals: sums per head, accumulators across key lanes
-    float lt[G];
+    const bool split = a.split_blocks > 0;
+    if (pc.ntiles > 0) {
+      // ---- per-warp totals: sums per head, accumulators across key lanes
+      float lt[G];
 #pragma unroll
-    for (int g = 0; g < G; ++g) lt[g] = 0.f;
+      for (int g = 0; g < G; ++g) lt[g] = 0.f;
 #pragma unroll
-    for (int j = 0; j < NVL; ++j) {
-      const int gj = ((dl / S::DUP) * NVL + j) % G;
+      for (int j = 0; j < NVL; ++j) {
+        const int gj = ((dl / S::DUP) * NVL + j) % G;
 #pragma unroll
-      for (int g = 0; g < G; ++g) lt[g] += (gj == g) ? ls[j] : 0.f;
-    }
+        for (int g = 0; g < G; ++g) lt[g] += (gj == g) ? ls[j] : 0.f;
+      }
 #pragma unroll
-    for (int g = 0; g < G; ++g) lt[g] = warp_sum(lt[g]) * (1.f / S::DUP);
+      for (int g = 0; g < G; ++g) lt[g] = warp_sum(lt[g]) * (1.f / S::DUP);
 #pragma unroll
-    for (int o = LPK; o < 32; o <<= 1)
+      for (int o = LPK; o < 32; o <<= 1)
 #pragma unroll
-      for (int g = 0; g < G; ++g)
+        for (int g = 0; g < G; ++g)
 #pragma unroll
-        for (int e = 0; e < 8; ++e) acc[g][e] += __shfl_xor_sync(0xffffffffu, acc[g][e], o);
+          for (int e = 0; e < 4; ++e) {
+            acc[g][e].x += __shfl_xor_sync(0xffffffffu, acc[g][e].x, o);
+            acc[g][e].y += __shfl_xor_sync(0xffffffffu, acc[g][e].y, o);
+          }
 
-    if (lane == 0) {
+      if (lane == 0) {
 #pragma unroll
-      for (int g = 0; g < G; ++g) {
-        mrg_m[warp * G + g] = m[g];
-        mrg_l[warp * G + g] = lt[g];
+        for (int g = 0; g < G; ++g) {
+          mrg_m[warp * G + g] = m[g];
+          mrg_l[warp * G + g] = lt[g];
+        }
       }
-    }
-    if (kl == 0) {
+      if (kl == 0) {
 #pragma unroll
-      for (int g = 0; g < G; ++g) {
-        float4* dst = reinterpret_cast<float4*>(mrg_acc + (warp * G + g) * D + dl * 8);
-        dst[0] = make_float4(acc[g][0], acc[g][1], acc[g][2], acc[g][3]);
-        dst[1] = make_float4(acc[g][4], acc[g][5], acc[g][6], acc[g][7]);
+        for (int g = 0; g < G; ++g) {
+          float4* dst = reinterpret_cast<float4*>(mrg_acc + (warp * G + g) * D + dl * 8);
+          dst[0] = make_float4(acc[g][0].x, acc[g][0].y, acc[g][1].x, acc[g][1].y);
+          dst[1] = make_float4(acc[g][2].x, acc[g][2].y, acc[g][3].x, acc[g][3].y);
+        }
       }
-    }
-    consumer_sync(NW * 32);
+      consumer_sync(NW * 32);
 
-    // ---- merge the warps' states and write this item's result
-    for (int idx = threadIdx.x; idx < G * D; idx += NW * 32) {
-      const int g = idx / D;
-      const int d = idx % D;
-      float M = -INFINITY;
+      // ---- merge the warps' states and write this piece's result
+      for (int idx = threadIdx.x; idx < G * D; idx += NW * 32) {
+        const int g = idx / D;
+        const int d = idx % D;
+        float M = -INFINITY;
 #pragma unroll
-      for (int w = 0; w < NW; ++w) M = fmaxf(M, mrg_m[w * G + g]);
-      const float Ms = (M == -INFINITY) ? 0.f : M;
-      float den = 0.f, num = 0.f;
+        for (int w = 0; w < NW; ++w) M = fmaxf(M, mrg_m[w * G + g]);
+        const float Ms = (M == -INFINITY) ? 0.f : M;
+        float den = 0.f, num = 0.f;
 #pragma unroll
-      for (int w = 0; w < NW; ++w) {
-        const float sc = fast_exp2(mrg_m[w * G + g] - Ms);
-        den = fmaf(sc, mrg_l[w * G + g], den);
-        num = fmaf(sc, mrg_acc[(w * G + g) * D + d], num);
+        for (int w = 0; w < NW; ++w) {
+          const float sc = fast_exp2(mrg_m[w * G + g] - Ms);
+          den = fmaf(sc, mrg_l[w * G + g], den);
+          num = fmaf(sc, mrg_acc[(w * G + g) * D + d], num);
+        }
+        const float o = (den > 0.f) ? num / den : 0.f;
+        const int h = pc.kvh * G + g;
+        if (split) {
+          if (pc.slot < a.num_splits) {
+            const size_t ph = (static_cast<size_t>(pc.b) * a.Hq + h) * a.num_splits + pc.slot;
+            a.partial_o[ph * D + d] = o;
+            if (d == 0) a.partial_lse[ph] = (den > 0.f) ? (M + log2f(den)) * kLn2 : -INFINITY;
+          }
+        } else {
+          reinterpret_cast<uint16_t*>(a.out)[(static_cast<size_t>(pc.qrow) * a.Hq + h) * D + d] =
+              f32_to_bf16_rn(o);
+        }
       }
-      const float o = (den > 0.f) ? num / den : 0.f;
-      const int h = r.kvh * G + g;
-      if (a.split_blocks > 0) {
-        const size_t ph = (static_cast<size_t>(r.b) * a.Hq + h) * a.num_splits + r.split;
-        a.partial_o[ph * D + d] = o;
-        if (d == 0) a.partial_lse[ph] = (den > 0.f) ? (M + log2f(den)) * kLn2 : -INFINITY;
-      } else {
-        reinterpret_cast<uint16_t*>(a.out)[(static_cast<size_t>(r.qrow) * a.Hq + h) * D + d] =
-            f32_to_bf16_rn(o);
+      consumer_sync(NW * 32);
+    } else if (!split) {
+      // a request with no visible key: output 0
+      for (int idx = threadIdx.x; idx < G * D; idx += NW * 32) {
+        const int h = pc.kvh * G + idx / D;
+        reinterpret_cast<uint16_t*>(a.out)[(static_cast<size_t>(pc.qrow) * a.Hq + h) * D +
+                                           idx % D] = 0;
       }
     }
-    consumer_sync(NW * 32);
+    // ---- split-K: slots of this segment no CTA fills get LSE = -inf
+    if (split && pc.fill_from >= 0) {
+      if (pc.fill_from > a.num_splits && threadIdx.x == 0) report(a.err, PKA_DEVERR_SEQ_LEN);
+      const int nfill = a.num_splits - min(pc.fill_from, a.num_splits);
+      for (int idx = threadIdx.x; idx < G * nfill; idx += NW * 32) {
+        const int h = pc.kvh * G + idx / nfill;
+        const int s = pc.fill_from + idx % nfill;
+        a.partial_lse[(static_cast<size_t>(pc.b) * a.Hq + h) * a.num_splits + s] = -INFINITY;
+      }
+    }
   }
 }
 
@@ -461,7 +674,7 @@ template <int D, int G>
 struct DecodeTuning {
   // 8 consumer warps + 1 producer warp, one CTA per SM; the ring takes what
   // the merge area leaves of the shared memory.
-  static constexpr int NW = 8;
+  static constexpr int NW = (G >= 4) ? 7 : 8;
   static constexpr int NSLOT = (D == 256) ? 10 : 20;
 };
 

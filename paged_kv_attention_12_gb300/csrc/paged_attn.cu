@@ -140,27 +140,19 @@ int paged_decode_splitk_plan(int32_t B, int32_t Hkv, int32_t max_seq_len, int32_
                              int32_t* split_blocks) {
   if (num_splits == nullptr || split_blocks == nullptr) return PKA_ERR_NULL;
   if (B <= 0 || Hkv <= 0 || max_seq_len < 0 || block_size <= 0) return PKA_ERR_SHAPE;
-  if (sm_count <= 0) sm_count = pka::device_sm_count();
-  if (sm_count <= 0) return PKA_ERR_CUDA;
+  (void)sm_count;  // the partition adapts to the SM count on the device
   const int T = max_visible_blocks(max_seq_len, window, block_size);
   if (T <= 0) {
     *num_splits = 1;
     *split_blocks = 1;
     return PKA_OK;
   }
-  const int64_t pairs = static_cast<int64_t>(B) * Hkv;
-  // Aim at about eight work items per persistent CTA (one CTA per SM) so the
-  // static round-robin assignment balances ragged lengths; keep splits at
-  // least four blocks long so the per-item merge stays small next to the
-  // streaming.
-  int64_t S = (8LL * sm_count + pairs - 1) / pairs;
-  if (S < 1) S = 1;
-  int64_t C = (T + S - 1) / S;
+  // Minimum chunk: at least four tiles, and long enough that one segment
+  // never spans more than 33 slots (bounded workspace).
+  int C = (T + 31) / 32;
   if (C < 4) C = 4;
-  if (C > T) C = T;
-  S = (T + C - 1) / C;
-  *num_splits = static_cast<int32_t>(S);
-  *split_blocks = static_cast<int32_t>(C);
+  *split_blocks = C;
+  *num_splits = (T + C - 1) / C + 1;
   return PKA_OK;
 }
 
@@ -179,19 +171,21 @@ int paged_decode_splitk(const void* q, float* partial_o, float* partial_lse,
   if (st != PKA_OK) return st;
   if (num_splits <= 0 || split_blocks <= 0) return PKA_ERR_SHAPE;
   if (!aligned16(partial_o)) return PKA_ERR_ALIGN;
+  // a segment of up to T tiles spans at most ceil(T / split_blocks) + 1 chunks
   const int T = max_visible_blocks(max_seq_len, params->window, kv->block_size);
-  if (static_cast<int64_t>(num_splits) * split_blocks < T) return PKA_ERR_WORKSPACE;
+  if (T > 0 && static_cast<int64_t>(num_splits) < (T + split_blocks - 1) / split_blocks + 1)
+    return PKA_ERR_WORKSPACE;
   if (B == 0) return PKA_OK;
   pka::DecodeArgs a = decode_args(q, kv, block_tables, max_blocks, seq_lens, B, Hq, params);
   a.partial_o = partial_o;
   a.partial_lse = partial_lse;
   a.num_splits = num_splits;
   a.split_blocks = split_blocks;
-  const int64_t items = static_cast<int64_t>(B) * kv->num_kv_heads * num_splits;
-  if (items > 0x7fffffffLL) return PKA_ERR_SHAPE;
+  if (static_cast<int64_t>(B) * Hq * num_splits > 0x7fffffffLL) return PKA_ERR_SHAPE;
   const int sms = pka::device_sm_count();
   if (sms <= 0) return PKA_ERR_CUDA;
-  const int grid = items < sms ? static_cast<int>(items) : sms;
+  // persistent: one CTA per SM, each streaming an equal share of the tiles
+  const int grid = sms;
   cudaError_t e = pka::launch_decode(a, kv->head_dim, Hq / kv->num_kv_heads, grid,
                                      static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? PKA_OK : PKA_ERR_CUDA;

@@ -80,14 +80,14 @@ def test_decode_argument_errors_are_host_side(L):
 
 
 def test_splitk_plan_and_workspace(L):
-    S, C = binding.paged_decode_splitk_plan(32, 2, 4096, 16, 0, sm_count=152)
-    assert S * C >= 256 and C >= 4
-    assert 32 * 2 * S >= 152
-    S, C = binding.paged_decode_splitk_plan(4, 4, 131072, 16, 0, sm_count=152)
-    assert S * C >= 8192 and 4 * 4 * S >= 148
-    # a window bounds the visible blocks: 512 keys span at most 33 blocks
-    S, C = binding.paged_decode_splitk_plan(32, 2, 4096, 16, 512, sm_count=152)
-    assert S * C >= 33 and S * C < 33 + C
+    # slots S = ceil(T / C) + 1 for T visible blocks and minimum chunk C >= 4
+    for (B, Hkv, L_max, W) in [(32, 2, 4096, 0), (4, 4, 131072, 0), (32, 2, 4096, 512),
+                              (4, 2, 256, 0), (1, 1, 1, 0)]:
+        S, C = binding.paged_decode_splitk_plan(B, Hkv, L_max, 16, W, sm_count=152)
+        T = -(-L_max // 16) if W <= 0 else min(-(-L_max // 16), (W - 1) // 16 + 2)
+        assert C >= 4 and S == -(-T // C) + 1 and S <= 33, (B, Hkv, L_max, W, S, C)
+    S, C = binding.paged_decode_splitk_plan(32, 2, 4096, 16, 512, sm_count=0)  # no CUDA call
+    assert (S, C) == (10, 4)
     assert binding.paged_decode_splitk_workspace_bytes(4, 16, 128, 10) == 4 * 16 * 10 * 129 * 4
     assert binding.paged_decode_splitk_workspace_bytes(0, 16, 128, 10) == 0
 
@@ -95,8 +95,8 @@ def test_splitk_plan_and_workspace(L):
 def test_splitk_rejects_uncovering_partition(L):
     pool = _pool()
     par = binding.PkaAttnParams(0.1, 0.0, 0, None)
-    # 64 tokens = 4 blocks; 1 split of 3 blocks does not cover them
-    st = L.paged_decode_splitk(32, 64, 96, ctypes.byref(pool), 64, 4, 64, 2, 8, 64, 1, 3,
+    # 64 tokens = 4 blocks; chunks of 3 blocks need ceil(4/3) + 1 = 3 slots
+    st = L.paged_decode_splitk(32, 64, 96, ctypes.byref(pool), 64, 4, 64, 2, 8, 64, 2, 3,
                                ctypes.byref(par), None)
     assert st == -5
     st = L.paged_decode_splitk(32, None, 96, ctypes.byref(pool), 64, 4, 64, 2, 8, 64, 1, 4,

@@ -102,33 +102,70 @@ def test_decode_head_shapes(D, G, Hkv):
     assert_close(to_f64(out), ref, "splitk")
 
 
-def test_splitk_partials_match_oracle_partials():
-    batch = workload.decode_long(1, DEV, poison=True, scale_down=True)
+def sm_count():
+    return torch.cuda.get_device_properties(0).multi_processor_count
+
+
+@pytest.mark.parametrize("maker", ["long", "serving_w", "tiny"])
+def test_splitk_partials_match_oracle_partials(maker):
+    """Each partial slot holds the attention over exactly the block range the
+    balanced partition assigns it; unused slots hold LSE -inf."""
+    if maker == "long":
+        batch = workload.decode_long(1, DEV, poison=True, scale_down=True)
+    elif maker == "serving_w":
+        batch = workload.decode_serving(1, DEV, poison=True, scale_down=True)[1]
+    else:
+        batch = workload.decode_tiny(3, DEV, poison=True)
     runner = binding.DecodeSplitK(batch)
+    runner.partial_lse.fill_(float("nan"))
     runner.run()
     arr = workload.to_numpy_f64(batch)
+    ranges = oracle.balanced_split_ranges(batch.seq_lens_host, batch.window, 16,
+                                          batch.num_kv_heads, sm_count(), runner.split_blocks)
     po, pl = oracle.splitk_partials(arr["q"], arr["k_pool"], arr["v_pool"], arr["block_tables"],
                                     arr["seq_lens"], batch.scale, batch.softcap, batch.window,
-                                    runner.num_splits, runner.split_blocks)
+                                    runner.num_splits, ranges=ranges)
     got_lse = runner.partial_lse.cpu().numpy()
+    assert not np.isnan(got_lse).any(), "a slot was left unwritten"
     assert np.array_equal(np.isneginf(got_lse), np.isneginf(pl))
     fin = np.isfinite(pl)
     np.testing.assert_allclose(got_lse[fin], pl[fin], rtol=1e-4, atol=1e-4)
     assert_close(runner.partial_o.cpu().numpy()[fin], po[fin], "partials")
 
 
-@pytest.mark.parametrize("S,C", [(1, 200), (3, 60), (200, 1)])
-def test_split_count_does_not_change_result(S, C):
+@pytest.mark.parametrize("C", [1, 3, 64, 500])
+def test_chunk_size_does_not_change_result(C):
     batch = workload.decode_long(2, DEV, poison=True, scale_down=True)
     ref, _, _ = oracle_decode(batch)
     B, Hq, D = batch.q.shape
+    T = -(-batch.max_seq_len // 16)
+    S = -(-T // C) + 1
     po = torch.empty((B, Hq, S, D), dtype=torch.float32, device=DEV)
     pl = torch.empty((B, Hq, S), dtype=torch.float32, device=DEV)
     out = torch.empty_like(batch.q)
+    err = new_err()
     binding.paged_decode_splitk(batch.q, po, pl, batch.k_pool, batch.v_pool, batch.block_tables,
-                                batch.seq_lens, batch.max_seq_len, S, C, scale=batch.scale)
+                                batch.seq_lens, batch.max_seq_len, S, C, scale=batch.scale, err=err)
     binding.paged_decode_splitk_combine(po, pl, out)
     assert_close(to_f64(out), ref, f"S={S} C={C}")
+    torch.cuda.synchronize()
+    assert err.item() == 0
+
+
+def test_splitk_with_empty_requests():
+    L = [0, 40, 0, 0, 700, 1, 0]
+    batch = workload.make_batch(seq_lens=L, q_lens=[1 if x else 0 for x in L], num_q_heads=8,
+                                num_kv_heads=2, head_dim=128, num_blocks=60, cfg_id=13,
+                                device=DEV, poison=True)
+    q = torch.randn((len(L), 8, 128), device=DEV).to(torch.bfloat16)
+    b2 = workload.PagedBatch(**{**batch.__dict__, "q": q,
+                                "q_lens_host": [1] * len(L)})
+    out = binding.DecodeSplitK(b2).run()
+    arr = workload.to_numpy_f64(b2)
+    ref, _ = oracle.run_batch(arr)
+    assert_close(to_f64(out), ref, "empty requests")
+    for b in (0, 2, 3, 6):
+        assert torch.all(out[b] == 0)
 
 
 # -------------------------------------------------------- full-size samples

@@ -372,3 +372,30 @@ def test_splitk_combine_equals_full(window):
     po, pl = splitk_partials(p["q"], p["k_pool"], p["v_pool"], p["block_tables"],
                              p["seq_lens"], 0.5, 1.5, window, 4, 1)
     assert np.isneginf(pl[1, :, 1:]).all()  # L=3 -> one block
+
+
+@pytest.mark.parametrize("grid,min_chunk", [(1, 1), (3, 2), (7, 4), (64, 1)])
+def test_balanced_partition_covers_and_combines(grid, min_chunk):
+    """The library's split partition: ranges of each (request, head) are
+    disjoint, contiguous and cover exactly the visible blocks; combining the
+    partials over them gives full attention."""
+    from oracle import balanced_split_ranges
+    rng = np.random.default_rng(20 + grid)
+    L = [57, 0, 3, 100, 16, 1]
+    p = problem(rng, L, [1 if x else 0 for x in L], Hq=4, Hkv=2, D=8, bs=4)
+    q = rng.standard_normal((len(L), 4, 8))
+    for window in (0, 9):
+        ranges = balanced_split_ranges(L, window, 4, 2, grid, min_chunk)
+        S = max(len(r) for per in ranges for r in per) or 1
+        for b, per in enumerate(ranges):
+            jlo, jhi = visible_block_range(L[b], window, 4)
+            for splits in per:
+                covered = [j for (j0, j1) in splits for j in range(j0, j1)]
+                assert covered == list(range(jlo, jhi))
+        full, lf = paged_decode(q, p["k_pool"], p["v_pool"], p["block_tables"],
+                                np.array(L), 0.5, 0.0, window)
+        po, pl = splitk_partials(q, p["k_pool"], p["v_pool"], p["block_tables"], np.array(L),
+                                 0.5, 0.0, window, S, ranges=ranges)
+        out, lse = lse_combine(po, pl)
+        np.testing.assert_allclose(out, full, rtol=1e-12, atol=1e-13)
+        np.testing.assert_allclose(lse, lf, rtol=1e-12, atol=1e-13)
