@@ -140,7 +140,10 @@ struct ReqGeo {
 __device__ __forceinline__ ReqGeo req_geo(const DecodeArgs& a, int b) {
   ReqGeo g;
   int L = a.seq_lens[b];
-  L = max(0, min(L, a.max_blocks * kBlockSize));
+  if (L > a.max_blocks * kBlockSize || L < 0) {
+    report(a.err, PKA_DEVERR_SEQ_LEN);  // error path only: tables cannot hold it
+    L = max(0, min(L, a.max_blocks * kBlockSize));
+  }
   g.pos = L - 1;
   g.t_lo = (a.window > 0) ? max(0, g.pos - a.window + 1) : 0;
   g.jlo = g.t_lo / kBlockSize;
