@@ -50,6 +50,7 @@ def parse():
     p.add_argument("--seed", type=int, default=0)
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-clocks", action="store_true", help="do not sample nvidia-smi clocks")
     p.add_argument("--no-other", action="store_true",
                    help="skip the per-workload measurements of the other configurations")
     p.add_argument("--cpu-seconds", type=float, default=15.0,
@@ -128,7 +129,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "100"],
+                 "--format=csv,noheader,nounits", "-lms", "200"],
                 stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
         except Exception:
             self.proc = None
@@ -396,7 +397,7 @@ def main():
         step()
     torch.cuda.synchronize()
 
-    sampler = ClockSampler(local) if rank == 0 else None
+    sampler = ClockSampler(local) if (rank == 0 and not args.no_clocks) else None
     if sampler:
         sampler.start()
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
@@ -416,6 +417,7 @@ def main():
     wall = time.perf_counter() - t_wall
     clocks = sampler.stop() if sampler else None
     step_ms = [a.elapsed_time(b) for a, b in ev]
+    print("step ms: " + " ".join(f"{x:.3f}" for x in step_ms), file=sys.stderr)
     kern_ms = [sum(a.elapsed_time(b) for a, b in ks) for ks in kev]
     total_ms = max_over_ranks(sum(step_ms), world)
     ms_per_step = total_ms / args.steps

@@ -7,6 +7,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <mutex>
+
 #include "paged_attn.h"
 
 namespace pka {
@@ -135,6 +137,27 @@ __device__ __forceinline__ uint16_t f32_to_bf16_rn(float x) {
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return static_cast<uint32_t>(f32_to_bf16_rn(lo)) |
          (static_cast<uint32_t>(f32_to_bf16_rn(hi)) << 16);
+}
+
+// Raises a kernel's dynamic shared-memory limit once per (kernel, device):
+// the call takes a driver lock, so it stays off the per-launch path.
+inline cudaError_t set_smem_once(const void* kernel, int bytes) {
+  struct Entry {
+    const void* kernel;
+    int device;
+  };
+  static std::mutex mu;
+  static Entry done[256];
+  static int count = 0;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lock(mu);
+  for (int i = 0; i < count; ++i)
+    if (done[i].kernel == kernel && done[i].device == dev) return cudaSuccess;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess && count < 256) done[count++] = Entry{kernel, dev};
+  return e;
 }
 
 }  // namespace pka

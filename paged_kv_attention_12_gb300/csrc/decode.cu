@@ -687,8 +687,7 @@ cudaError_t launch_decode_t(const DecodeArgs& a, int grid, cudaStream_t stream) 
   constexpr int NSLOT = DecodeTuning<D, G>::NSLOT;
   using S = DecodeShape<D, G, NW, NSLOT>;
   auto kern = paged_decode_kernel<D, G, NW, NSLOT>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       S::kSmemBytes);
+  cudaError_t e = set_smem_once(reinterpret_cast<const void*>(kern), S::kSmemBytes);
   if (e != cudaSuccess) return e;
   kern<<<grid, (NW + 1) * 32, S::kSmemBytes, stream>>>(a);
   return cudaGetLastError();

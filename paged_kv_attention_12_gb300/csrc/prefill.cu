@@ -475,8 +475,7 @@ cudaError_t launch_prefill_t(const PrefillArgs& a, cudaStream_t stream) {
     if (!make_map(&tv, a.v, 2, dims, str, box)) return cudaErrorInvalidValue;
   }
   auto kern = paged_prefill_kernel<D, G>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       S::kSmemBytes);
+  cudaError_t e = set_smem_once(reinterpret_cast<const void*>(kern), S::kSmemBytes);
   if (e != cudaSuccess) return e;
   const int qtiles = (a.max_query_len + S::TQ - 1) / S::TQ;
   dim3 grid(qtiles, a.Hkv, a.batch);

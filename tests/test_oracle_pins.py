@@ -399,3 +399,17 @@ def test_balanced_partition_covers_and_combines(grid, min_chunk):
         out, lse = lse_combine(po, pl)
         np.testing.assert_allclose(out, full, rtol=1e-12, atol=1e-13)
         np.testing.assert_allclose(lse, lf, rtol=1e-12, atol=1e-13)
+
+
+def test_golden_regression_anchor():
+    """The oracle still reproduces the stored small case (tests/golden)."""
+    import json
+    import os
+    path = os.path.join(os.path.dirname(__file__), "golden", "decode_small.json")
+    d = json.load(open(path))
+    out, lse = paged_attention(np.array(d["q"]), np.array(d["k_pool"]), np.array(d["v_pool"]),
+                               np.array(d["block_tables"]), np.array(d["seq_lens"]),
+                               np.array(d["query_start_loc"]), d["scale"], d["softcap"],
+                               d["window"])
+    np.testing.assert_allclose(out, np.array(d["out"]), rtol=1e-13, atol=1e-15)
+    np.testing.assert_allclose(lse, np.array(d["lse"]), rtol=1e-13, atol=1e-15)
