@@ -25,7 +25,9 @@
 //    load) and issues, per tile, two 1-D bulk copies (the (block, head) K and
 //    V tiles, each one contiguous bs*D*2-byte run of the pool) into a ring of
 //    shared-memory slots, completion counted on a "full" mbarrier;
-//  * NW consumer warps take the ring's tiles round robin.  Lanes are spread
+//  * NW consumer warps take the ring's tiles round robin; every slot has
+//    one owner warp, so each slot's mbarrier phases are consumed in order.
+//    Lanes are spread
 //    over D (8 bf16 = 16 bytes per lane, so a key row is read conflict-free
 //    in one instruction); all G query heads of the KV group are handled at
 //    once (each K/V byte feeds G heads); partial dot products are reduced
@@ -321,6 +323,7 @@ struct DecodeShape {
   static_assert(D % 8 == 0 && LPK <= 32 && 32 % LPK == 0, "head_dim");
   static_assert(KC % KPW == 0, "chunk");
   static_assert(kSmemBytes <= 232448, "shared memory");
+  static_assert(NSLOT % NW == 0, "each ring slot must have exactly one owner warp");
 };
 
 // Processes one KV tile (kBlockSize keys) for one consumer warp.
@@ -557,7 +560,12 @@ __global__ void __launch_bounds__((NW + 1) * 32, 1) paged_decode_kernel(const De
       for (int j = 0; j < NVL; ++j) ls[j] = 0.f;
     }
 
-    for (int i = warp; i < pc.ntiles && ok; i += NW) {
+    // Tile T of the CTA's stream lives in slot T % NSLOT and belongs to warp
+    // T % NW; NSLOT is a multiple of NW, so every slot has one owner warp that
+    // consumes its phases in order (a phase-parity wait can never alias an
+    // older phase of the same slot).
+    const int i0 = static_cast<int>((warp - tile_base % NW + NW) % NW);
+    for (int i = i0; i < pc.ntiles && ok; i += NW) {
       const long long T = tile_base + i;
       const int slot = static_cast<int>(T % NSLOT);
       const bool got = mbar_wait(&full[slot], static_cast<uint32_t>((T / NSLOT) & 1), a.err);
@@ -675,10 +683,12 @@ namespace {
 
 template <int D, int G>
 struct DecodeTuning {
-  // 8 consumer warps + 1 producer warp, one CTA per SM; the ring takes what
+  // NW consumer warps + 1 producer warp, one CTA per SM.  The ring has
+  // slots-per-warp x NW slots (each slot owned by one warp) and takes what
   // the merge area leaves of the shared memory.
-  static constexpr int NW = (G >= 4) ? 7 : 8;
-  static constexpr int NSLOT = (D == 256) ? 10 : 20;
+  static constexpr int NW = (D == 256) ? (G == 8 ? 5 : 6) : 7;
+  static constexpr int SPW = (D == 256) ? 2 : 3;
+  static constexpr int NSLOT = NW * SPW;
 };
 
 template <int D, int G>

@@ -131,3 +131,15 @@ def test_full_size_sampled_requests(cfg):
     assert_close(to_f64(out[arr["q_rows"]]), ref, f"cfg{cfg} full size")
     torch.cuda.synchronize()
     assert err.item() == 0
+
+
+def test_repeated_launches_are_deterministic_and_never_time_out():
+    batch = workload.mixed_batch(1, DEV, scale_down=True)
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    ref = run(batch, err).clone()
+    out = torch.empty_like(batch.q)
+    for it in range(100):
+        binding.run_batch(batch, out, err)
+    torch.cuda.synchronize()
+    assert err.item() == 0
+    assert torch.equal(out, ref)
