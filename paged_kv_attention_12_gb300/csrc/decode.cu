@@ -316,14 +316,21 @@ struct DecodeShape {
   static constexpr int NVL = NV >= LPK ? NV / LPK : 1;
   static constexpr int DUP = NV >= LPK ? 1 : LPK / NV;
   static constexpr int kRingBytes = NSLOT * 2 * kTileBytes;
-  static constexpr int kBarBytes = 2 * NSLOT * 8;
-  static constexpr int kPBytes = NW * KPW * NV * 4;
-  static constexpr int kMergeBytes = NW * G * (D + 2) * 4;
+  static constexpr int kBarBytes = (2 * NSLOT * 8 + 15) / 16 * 16;
+  static constexpr int kPBytes = (NW * KPW * NV * 4 + 15) / 16 * 16;
+  // merge area: m and l of every (warp, head), padded to 16 bytes, then the
+  // [NW][G][D] fp32 accumulators (written with 16-byte stores)
+  static constexpr int kMergeMLFloats = (2 * NW * G + 3) / 4 * 4;
+  static constexpr int kMergeBytes = (kMergeMLFloats + NW * G * D) * 4;
   static constexpr int kSmemBytes = kRingBytes + kBarBytes + kPBytes + kMergeBytes;
   static_assert(D % 8 == 0 && LPK <= 32 && 32 % LPK == 0, "head_dim");
   static_assert(KC % KPW == 0, "chunk");
   static_assert(kSmemBytes <= 232448, "shared memory");
   static_assert(NSLOT % NW == 0, "each ring slot must have exactly one owner warp");
+  static_assert(kTileBytes % 16 == 0 && kRingBytes % 16 == 0, "bulk-copy destinations 16-byte aligned");
+  static_assert((kRingBytes + kBarBytes) % 16 == 0, "P area 16-byte aligned");
+  static_assert((kRingBytes + kBarBytes + kPBytes) % 16 == 0, "merge area 16-byte aligned");
+  static_assert((KPW * NV * 4) % 16 == 0 || G % 4 != 0, "per-warp P rows 16-byte aligned");
 };
 
 // Processes one KV tile (kBlockSize keys) for one consumer warp.
@@ -459,9 +466,9 @@ __global__ void __launch_bounds__((NW + 1) * 32, 1) paged_decode_kernel(const De
   uint64_t* empty = full + NSLOT;
   float* psm_all = reinterpret_cast<float*>(smem + S::kRingBytes + S::kBarBytes);
   float* merge = reinterpret_cast<float*>(smem + S::kRingBytes + S::kBarBytes + S::kPBytes);
-  float* mrg_m = merge;                  // [NW][G]
-  float* mrg_l = merge + NW * G;         // [NW][G]
-  float* mrg_acc = merge + 2 * NW * G;   // [NW][G][D]
+  float* mrg_m = merge;                       // [NW][G]
+  float* mrg_l = merge + NW * G;              // [NW][G]
+  float* mrg_acc = merge + S::kMergeMLFloats;  // [NW][G][D], 16-byte aligned
 
   const int warp = threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
