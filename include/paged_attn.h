@@ -180,6 +180,28 @@ int paged_attn_check_tables(const int32_t* block_tables, int32_t max_blocks,
                             const int32_t* seq_lens, int32_t B, int32_t num_blocks,
                             int32_t block_size, int32_t* err, void* stream);
 
+/* Decode for callers that cannot allocate device memory.  The pages have no
+ * counterpart: this is a service of this library.  Some callers cannot call
+ * cudaMalloc -- a plugin running while another allocator owns all device
+ * memory, code in a region where allocation calls are not allowed -- yet
+ * split-K decode needs room for its fp32 partials.  This entry point gives
+ * the same result as paged_decode_splitk_plan + paged_decode_splitk +
+ * paged_decode_splitk_combine, with the partials in a 16 MiB array compiled
+ * into the library, so it allocates nothing; q, out and the pool are the
+ * caller's, as for paged_decode_attn.
+ * Limit: B*Hq*S*(D+1)*4 bytes <= 16 MiB for the S paged_decode_splitk_plan
+ * gives; larger calls return PKA_ERR_WORKSPACE before launching anything.
+ * The first call on each device looks up the array's device address (make
+ * that first call before any stream capture).  Every GPU that loads the
+ * library holds the array until the process exits.  All calls share the one
+ * array: calls that overlap on the GPU (other streams, other threads) race
+ * and must be serialised by the caller. */
+int paged_decode_attn_noalloc(const void* q, void* out, const pka_kv_pool* kv,
+                              const int32_t* block_tables, int32_t max_blocks,
+                              const int32_t* seq_lens, int32_t B, int32_t Hq,
+                              int32_t max_seq_len, const pka_attn_params* params,
+                              void* stream);
+
 #ifdef __cplusplus
 }
 #endif

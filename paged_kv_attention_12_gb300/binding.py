@@ -32,6 +32,7 @@ EXPORTS = [
     "pka_version", "pka_status_string", "paged_decode_attn", "paged_decode_splitk_plan",
     "paged_decode_splitk_workspace_bytes", "paged_decode_splitk",
     "paged_decode_splitk_combine", "paged_prefill_attn", "paged_attn_check_tables",
+    "paged_decode_attn_noalloc",
 ]
 
 
@@ -86,6 +87,9 @@ def lib() -> ctypes.CDLL:
                                      I32, I32, P(PkaAttnParams), VP]
     L.paged_attn_check_tables.restype = ctypes.c_int
     L.paged_attn_check_tables.argtypes = [VP, I32, VP, I32, I32, I32, VP, VP]
+    L.paged_decode_attn_noalloc.restype = ctypes.c_int
+    L.paged_decode_attn_noalloc.argtypes = [VP, VP, P(PkaKvPool), VP, I32, VP, I32, I32, I32,
+                                            P(PkaAttnParams), VP]
     _lib = L
     return L
 
@@ -125,6 +129,20 @@ def paged_decode_attn(q, out, k_pool, v_pool, block_tables, seq_lens, max_seq_le
                                  seq_lens.data_ptr(), q.shape[0], q.shape[1], int(max_seq_len),
                                  ctypes.byref(par), _stream(stream))
     _check("paged_decode_attn", st)
+
+
+def paged_decode_attn_noalloc(q, out, k_pool, v_pool, block_tables, seq_lens, max_seq_len, *,
+                              scale, softcap=0.0, window=0, err=None, stream=None):
+    """Split-K decode with the partials in the library's own fixed array (no
+    device allocation by anyone); raises PagedAttnError(PKA_ERR_WORKSPACE)
+    when the partials would not fit its 16 MiB."""
+    pool = kv_pool(k_pool, v_pool)
+    par = attn_params(scale, softcap, window, err)
+    st = lib().paged_decode_attn_noalloc(q.data_ptr(), out.data_ptr(), ctypes.byref(pool),
+                                         block_tables.data_ptr(), block_tables.shape[1],
+                                         seq_lens.data_ptr(), q.shape[0], q.shape[1],
+                                         int(max_seq_len), ctypes.byref(par), _stream(stream))
+    _check("paged_decode_attn_noalloc", st)
 
 
 def paged_decode_splitk_plan(B, Hkv, max_seq_len, block_size=16, window=0, sm_count=0):
