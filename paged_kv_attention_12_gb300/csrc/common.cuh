@@ -126,17 +126,15 @@ __device__ __forceinline__ void unpack8(const uint4& u, float (&f)[8]) {
   bf16x2_to_f32(u.w, f[6], f[7]);
 }
 
-// fp32 -> bf16 round to nearest even (NaN kept quiet).
-__device__ __forceinline__ uint16_t f32_to_bf16_rn(float x) {
-  uint32_t u = __float_as_uint(x);
-  if ((u & 0x7fffffffu) > 0x7f800000u) return static_cast<uint16_t>((u >> 16) | 0x40u);
-  u += 0x7fffu + ((u >> 16) & 1u);
-  return static_cast<uint16_t>(u >> 16);
+// Two fp32 -> packed bf16x2 (round to nearest even), one hardware convert.
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
 }
 
-__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
-  return static_cast<uint32_t>(f32_to_bf16_rn(lo)) |
-         (static_cast<uint32_t>(f32_to_bf16_rn(hi)) << 16);
+__device__ __forceinline__ uint16_t f32_to_bf16_rn(float x) {
+  return static_cast<uint16_t>(pack_bf16x2(x, 0.f) & 0xffffu);
 }
 
 // Raises a kernel's dynamic shared-memory limit once per (kernel, device):

@@ -74,6 +74,17 @@ __device__ __forceinline__ float2 fmul2(float2 a, float2 b) {
   return d;
 }
 
+// Select kept opaque to the compiler: a chain of these over a small array
+// must stay a chain of selects (left visible, the compiler turns it into a
+// runtime-indexed array in local memory).
+__device__ __forceinline__ float opaque_sel(bool c, float a, float b) {
+  float r;
+  asm("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %1, 0;\n\tselp.f32 %0, %2, %3, p;\n\t}"
+      : "=f"(r)
+      : "r"(static_cast<int>(c)), "f"(a), "f"(b));
+  return r;
+}
+
 __device__ __forceinline__ void unpack8x2(const uint4& u, float2 (&f)[4]) {
   bf16x2_to_f32(u.x, f[0].x, f[0].y);
   bf16x2_to_f32(u.y, f[1].x, f[1].y);
@@ -188,11 +199,13 @@ struct PieceIter {
       item = blockIdx.x;
       return;
     }
-    // total tiles T = Hkv * sum_b nb_b
+    // total tiles T = Hkv * sum_b nb_b (the first 32 requests' counts stay in
+    // a register, so batches of up to 32 requests read seq_lens once)
     long long T = 0;
+    const int nb0 = (lane < args.batch) ? req_geo(args, lane).nb : 0;
     for (int base = 0; base < args.batch; base += 32) {
       const int bb = base + lane;
-      const int nb = (bb < args.batch) ? req_geo(args, bb).nb : 0;
+      const int nb = (base == 0) ? nb0 : ((bb < args.batch) ? req_geo(args, bb).nb : 0);
       T += __shfl_sync(0xffffffffu, warp_incl_scan(nb, lane), 31);
     }
     T *= args.Hkv;
@@ -214,7 +227,7 @@ struct PieceIter {
     prefix = run;
     for (int base = 0; base < args.batch; base += 32) {
       const int bb = base + lane;
-      const int nb = (bb < args.batch) ? req_geo(args, bb).nb : 0;
+      const int nb = (base == 0) ? nb0 : ((bb < args.batch) ? req_geo(args, bb).nb : 0);
       const int incl = warp_incl_scan(nb, lane);
       const long long pre = run + incl - nb;
       const bool hit = (bb < args.batch) &&
@@ -333,9 +346,11 @@ struct DecodeShape {
   static_assert((KPW * NV * 4) % 16 == 0 || G % 4 != 0, "per-warp P rows 16-byte aligned");
 };
 
-// Processes one KV tile (kBlockSize keys) for one consumer warp.
-template <int D, int G, int NW, int NSLOT, bool EDGE>
-__device__ __forceinline__ void decode_tile(const uint16_t* __restrict__ Kt,
+// Processes one KV tile (kBlockSize keys) for one consumer warp.  EDGE (warp
+// uniform) selects the masked path for tiles with keys outside the visible
+// range.
+template <int D, int G, int NW, int NSLOT>
+__device__ __forceinline__ void decode_tile(const bool EDGE, const uint16_t* __restrict__ Kt,
                                             const uint16_t* __restrict__ Vt,
                                             const float2 (&qf)[G][4], float2 (&acc)[G][4],
                                             float (&m)[G],
@@ -387,7 +402,7 @@ __device__ __forceinline__ void decode_tile(const uint16_t* __restrict__ Kt,
       }
       part[j] = x;
 #pragma unroll
-      for (int g = 0; g < G; ++g) mloc[g] = (gj[j] == g) ? fmaxf(mloc[g], x) : mloc[g];
+      for (int g = 0; g < G; ++g) mloc[g] = opaque_sel(gj[j] == g, fmaxf(mloc[g], x), mloc[g]);
     }
     float alpha[G], mref[G];
 #pragma unroll
@@ -403,8 +418,8 @@ __device__ __forceinline__ void decode_tile(const uint16_t* __restrict__ Kt,
       float a = alpha[0], r = mref[0];
 #pragma unroll
       for (int g = 1; g < G; ++g) {
-        a = (gj[j] == g) ? alpha[g] : a;
-        r = (gj[j] == g) ? mref[g] : r;
+        a = opaque_sel(gj[j] == g, alpha[g], a);
+        r = opaque_sel(gj[j] == g, mref[g], r);
       }
       const float p = fast_exp2(part[j] - r);
       ls[j] = ls[j] * a + p;
@@ -455,7 +470,8 @@ __device__ __forceinline__ void decode_tile(const uint16_t* __restrict__ Kt,
 }
 
 template <int D, int G, int NW, int NSLOT>
-__global__ void __launch_bounds__((NW + 1) * 32, 1) paged_decode_kernel(const DecodeArgs a) {
+__global__ void __launch_bounds__((NW + 1) * 32, 1)
+    paged_decode_kernel(const __grid_constant__ DecodeArgs a) {
   using S = DecodeShape<D, G, NW, NSLOT>;
   constexpr int TE = S::kTileElems;
   constexpr int NVL = S::NVL, LPK = S::LPK;
@@ -546,16 +562,22 @@ __global__ void __launch_bounds__((NW + 1) * 32, 1) paged_decode_kernel(const De
   long long tile_base = 0;
   bool ok = true;
 
-  while (iter.next(pc)) {
+  // The next piece's query rows are loaded while the current piece is merged.
+  bool have = iter.next(pc);
+  uint4 qraw[G];
+  if (have) {
+    const uint16_t* qp = a.q + (static_cast<size_t>(pc.qrow) * a.Hq + pc.kvh * G) * D + dl * 8;
+#pragma unroll
+    for (int g = 0; g < G; ++g) qraw[g] = *reinterpret_cast<const uint4*>(qp + g * D);
+  }
+  while (have) {
     float2 qf[G][4], acc[G][4];
     float m[G], ls[NVL];
     {
-      const uint16_t* qp = a.q + (static_cast<size_t>(pc.qrow) * a.Hq + pc.kvh * G) * D + dl * 8;
       const float2 qs2 = make_float2(qscale, qscale);
 #pragma unroll
       for (int g = 0; g < G; ++g) {
-        const uint4 u = *reinterpret_cast<const uint4*>(qp + g * D);
-        unpack8x2(u, qf[g]);
+        unpack8x2(qraw[g], qf[g]);
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           qf[g][e] = fmul2(qf[g][e], qs2);
@@ -583,16 +605,21 @@ __global__ void __launch_bounds__((NW + 1) * 32, 1) paged_decode_kernel(const De
       const uint16_t* Kt = ring + static_cast<size_t>(slot) * 2 * TE;
       const uint16_t* Vt = Kt + TE;
       const int tok0 = (pc.j0 + i) * kBlockSize;
-      if (tok0 < pc.t_lo || tok0 + kBlockSize - 1 > pc.pos)
-        decode_tile<D, G, NW, NSLOT, true>(Kt, Vt, qf, acc, m, ls, psm, lane, tok0, pc.t_lo,
-                                           pc.pos, a.softcap, inv_cap);
-      else
-        decode_tile<D, G, NW, NSLOT, false>(Kt, Vt, qf, acc, m, ls, psm, lane, tok0, pc.t_lo,
-                                            pc.pos, a.softcap, inv_cap);
+      const bool edge = (tok0 < pc.t_lo || tok0 + kBlockSize - 1 > pc.pos);
+      decode_tile<D, G, NW, NSLOT>(edge, Kt, Vt, qf, acc, m, ls, psm, lane, tok0, pc.t_lo, pc.pos,
+                                   a.softcap, inv_cap);
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[slot]);
     }
     tile_base += pc.ntiles;
+
+    Piece nx;
+    const bool have_next = iter.next(nx);
+    if (have_next) {
+      const uint16_t* qp = a.q + (static_cast<size_t>(nx.qrow) * a.Hq + nx.kvh * G) * D + dl * 8;
+#pragma unroll
+      for (int g = 0; g < G; ++g) qraw[g] = *reinterpret_cast<const uint4*>(qp + g * D);
+    }
 
     const bool split = a.split_blocks > 0;
     if (pc.ntiles > 0) {
@@ -604,7 +631,7 @@ __global__ void __launch_bounds__((NW + 1) * 32, 1) paged_decode_kernel(const De
       for (int j = 0; j < NVL; ++j) {
         const int gj = ((dl / S::DUP) * NVL + j) % G;
 #pragma unroll
-        for (int g = 0; g < G; ++g) lt[g] += (gj == g) ? ls[j] : 0.f;
+        for (int g = 0; g < G; ++g) lt[g] += opaque_sel(gj == g, ls[j], 0.f);
       }
 #pragma unroll
       for (int g = 0; g < G; ++g) lt[g] = warp_sum(lt[g]) * (1.f / S::DUP);
@@ -682,6 +709,8 @@ __global__ void __launch_bounds__((NW + 1) * 32, 1) paged_decode_kernel(const De
         a.partial_lse[(static_cast<size_t>(pc.b) * a.Hq + h) * a.num_splits + s] = -INFINITY;
       }
     }
+    pc = nx;
+    have = have_next;
   }
 }
 

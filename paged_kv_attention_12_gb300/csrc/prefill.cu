@@ -111,7 +111,8 @@ __device__ __forceinline__ float tanh_via_exp2(float y) {
 
 template <int D, int G>
 __global__ void __launch_bounds__(PrefillShape<D, G>::kThreads, 1)
-    paged_prefill_kernel(const PrefillArgs a, const __grid_constant__ CUtensorMap tm_q,
+    paged_prefill_kernel(const __grid_constant__ PrefillArgs a,
+                         const __grid_constant__ CUtensorMap tm_q,
                          const __grid_constant__ CUtensorMap tm_k,
                          const __grid_constant__ CUtensorMap tm_v) {
   using S = PrefillShape<D, G>;
@@ -119,9 +120,12 @@ __global__ void __launch_bounds__(PrefillShape<D, G>::kThreads, 1)
 
   // ---------------------------------------------------------- work item
   Item it;
-  it.b = blockIdx.z;
+  // Grid (request, KV head, query tile) with the query tile slowest and
+  // reversed: CTAs launch in blockIdx order, so every request's last (most
+  // expensive) tiles go first and the cheap first tiles fill in the tail.
+  it.b = blockIdx.x;
   it.kvh = blockIdx.y;
-  const int qt = gridDim.x - 1 - blockIdx.x;  // heaviest (latest) query tiles first
+  const int qt = gridDim.z - 1 - blockIdx.z;
   it.q0 = a.query_start_loc[it.b];
   it.n = a.query_start_loc[it.b + 1] - it.q0;
   it.L = a.seq_lens[it.b];
@@ -337,12 +341,25 @@ __global__ void __launch_bounds__(PrefillShape<D, G>::kThreads, 1)
       const int c_hi = row_valid ? min(BN - 1, p - t0) : -1;
       const int c_lo = max(0, kmin - t0);
       float mx = -INFINITY;
+      if (capped) {
 #pragma unroll
-      for (int c = 0; c < BN; ++c) {
-        float x = capped ? cap_out * tanh_via_exp2(s[c] * cap_in) : s[c] * sl2;
-        x = (c >= c_lo && c <= c_hi) ? x : -INFINITY;
-        s[c] = x;
-        mx = fmaxf(mx, x);
+        for (int c = 0; c < BN; ++c) s[c] = cap_out * tanh_via_exp2(s[c] * cap_in);
+      } else {
+#pragma unroll
+        for (int c = 0; c < BN; ++c) s[c] *= sl2;
+      }
+      // Only rows on a causal diagonal or a window edge need the per-column
+      // mask; the warp takes the masked loop only if one of its rows does.
+      if (__any_sync(0xffffffffu, c_lo > 0 || c_hi < BN - 1)) {
+#pragma unroll
+        for (int c = 0; c < BN; ++c) {
+          const float x = (c >= c_lo && c <= c_hi) ? s[c] : -INFINITY;
+          s[c] = x;
+          mx = fmaxf(mx, x);
+        }
+      } else {
+#pragma unroll
+        for (int c = 0; c < BN; ++c) mx = fmaxf(mx, s[c]);
       }
       const float m_new = fmaxf(m_ref, mx);
       const bool resc = (j > 0) && (m_new > m_ref + 8.f);
@@ -478,7 +495,7 @@ cudaError_t launch_prefill_t(const PrefillArgs& a, cudaStream_t stream) {
   cudaError_t e = set_smem_once(reinterpret_cast<const void*>(kern), S::kSmemBytes);
   if (e != cudaSuccess) return e;
   const int qtiles = (a.max_query_len + S::TQ - 1) / S::TQ;
-  dim3 grid(qtiles, a.Hkv, a.batch);
+  dim3 grid(a.batch, a.Hkv, qtiles);
   kern<<<grid, S::kThreads, S::kSmemBytes, stream>>>(a, tq, tk, tv);
   return cudaGetLastError();
 }
@@ -487,7 +504,7 @@ cudaError_t launch_prefill_t(const PrefillArgs& a, cudaStream_t stream) {
 
 cudaError_t launch_prefill(const PrefillArgs& a, int head_dim, int group, int /*sm_count*/,
                            cudaStream_t stream) {
-  if (a.batch > 65535) return cudaErrorInvalidValue;
+  if (a.Hkv > 65535 || (a.max_query_len + 127) / 128 * 8 > 65535) return cudaErrorInvalidValue;
 #define PKA_PRE(D_, G_) \
   if (head_dim == D_ && group == G_) return launch_prefill_t<D_, G_>(a, stream);
   PKA_PRE(128, 1)
