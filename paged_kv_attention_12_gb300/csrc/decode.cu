@@ -319,11 +319,16 @@ struct PieceIter {
 
 template <int D, int G, int NW, int NSLOT>
 struct DecodeShape {
-  static constexpr int kTileElems = kBlockSize * D;
+  // A ring slot holds TK keys of one (block, head) tile: a whole block for
+  // D=128, half a block for D=256 (8 KB of K + V either way), so that many
+  // consumer warps fit next to a deep ring.
+  static constexpr int TK = (D == 256) ? 8 : 16;
+  static constexpr int SUB = kBlockSize / TK;  // slots per pool block
+  static constexpr int kTileElems = TK * D;
   static constexpr int kTileBytes = kTileElems * 2;
   static constexpr int LPK = D / 8;       // lanes per key row (16 bytes per lane)
   static constexpr int KPW = 32 / LPK;    // keys per warp step
-  static constexpr int KC = (kBlockSize * G / KPW > 64) ? 8 : 16;  // keys per chunk
+  static constexpr int KC = (TK * G / KPW > 64) ? 8 : TK;  // keys per chunk
   static constexpr int KS = KC / KPW;     // warp steps per chunk
   static constexpr int NV = KS * G;       // partial dots per lane per chunk
   static constexpr int NVL = NV >= LPK ? NV / LPK : 1;
@@ -346,8 +351,8 @@ struct DecodeShape {
   static_assert((KPW * NV * 4) % 16 == 0 || G % 4 != 0, "per-warp P rows 16-byte aligned");
 };
 
-// Processes one KV tile (kBlockSize keys) for one consumer warp.  EDGE (warp
-// uniform) selects the masked path for tiles with keys outside the visible
+// Processes one ring slot (TK keys) for one consumer warp.  EDGE (warp
+// uniform) selects the masked path for slots with keys outside the visible
 // range.
 template <int D, int G, int NW, int NSLOT>
 __device__ __forceinline__ void decode_tile(const bool EDGE, const uint16_t* __restrict__ Kt,
@@ -365,7 +370,7 @@ __device__ __forceinline__ void decode_tile(const bool EDGE, const uint16_t* __r
   float* pw = psm + kl * NV;
 
 #pragma unroll
-  for (int c = 0; c < kBlockSize / KC; ++c) {
+  for (int c = 0; c < S::TK / KC; ++c) {
     // ---- partial q.k over this lane's 8 elements, every key step, every head
     float part[NV];
 #pragma unroll
@@ -519,8 +524,8 @@ __global__ void __launch_bounds__((NW + 1) * 32, 1)
           }
         }
         const int cnt = min(32, pc.ntiles - base);
-        for (int k = 0; k < cnt; ++k) {
-          const int phys = __shfl_sync(0xffffffffu, id, k);
+        for (int k = 0; k < cnt * S::SUB; ++k) {
+          const int phys = __shfl_sync(0xffffffffu, id, k / S::SUB);
           const int slot = static_cast<int>(issued % NSLOT);
           const long long round = issued / NSLOT;
           int good = 1;
@@ -529,7 +534,8 @@ __global__ void __launch_bounds__((NW + 1) * 32, 1)
               good = mbar_wait(&empty[slot], static_cast<uint32_t>((round - 1) & 1), a.err);
             if (good) {
               mbar_arrive_expect_tx(&full[slot], 2 * S::kTileBytes);
-              const size_t off = (static_cast<size_t>(phys) * a.Hkv + pc.kvh) * TE;
+              const size_t off = (static_cast<size_t>(phys) * a.Hkv + pc.kvh) * kBlockSize * D +
+                                 static_cast<size_t>(k % S::SUB) * TE;
               uint16_t* dst = ring + static_cast<size_t>(slot) * 2 * TE;
               bulk_g2s_stream(dst, a.k + off, S::kTileBytes, &full[slot], pol);
               bulk_g2s_stream(dst + TE, a.v + off, S::kTileBytes, &full[slot], pol);
@@ -593,8 +599,9 @@ __global__ void __launch_bounds__((NW + 1) * 32, 1)
     // T % NW; NSLOT is a multiple of NW, so every slot has one owner warp that
     // consumes its phases in order (a phase-parity wait can never alias an
     // older phase of the same slot).
+    const int nsub = pc.ntiles * S::SUB;
     const int i0 = static_cast<int>((warp - tile_base % NW + NW) % NW);
-    for (int i = i0; i < pc.ntiles && ok; i += NW) {
+    for (int i = i0; i < nsub && ok; i += NW) {
       const long long T = tile_base + i;
       const int slot = static_cast<int>(T % NSLOT);
       const bool got = mbar_wait(&full[slot], static_cast<uint32_t>((T / NSLOT) & 1), a.err);
@@ -604,14 +611,14 @@ __global__ void __launch_bounds__((NW + 1) * 32, 1)
       }
       const uint16_t* Kt = ring + static_cast<size_t>(slot) * 2 * TE;
       const uint16_t* Vt = Kt + TE;
-      const int tok0 = (pc.j0 + i) * kBlockSize;
-      const bool edge = (tok0 < pc.t_lo || tok0 + kBlockSize - 1 > pc.pos);
+      const int tok0 = (pc.j0 + i / S::SUB) * kBlockSize + (i % S::SUB) * S::TK;
+      const bool edge = (tok0 < pc.t_lo || tok0 + S::TK - 1 > pc.pos);
       decode_tile<D, G, NW, NSLOT>(edge, Kt, Vt, qf, acc, m, ls, psm, lane, tok0, pc.t_lo, pc.pos,
                                    a.softcap, inv_cap);
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[slot]);
     }
-    tile_base += pc.ntiles;
+    tile_base += nsub;
 
     Piece nx;
     const bool have_next = iter.next(nx);
@@ -719,11 +726,12 @@ namespace {
 
 template <int D, int G>
 struct DecodeTuning {
-  // NW consumer warps + 1 producer warp, one CTA per SM.  The ring has
-  // slots-per-warp x NW slots (each slot owned by one warp) and takes what
+  // NW consumer warps + 1 producer warp, one CTA per SM, at most 168
+  // registers a thread so that three warps fit each scheduler.  The ring has
+  // SPW slots per consumer warp (each slot owned by one warp) and takes what
   // the merge area leaves of the shared memory.
-  static constexpr int NW = (D == 256) ? (G == 8 ? 5 : 6) : 7;
-  static constexpr int SPW = (D == 256) ? 2 : 3;
+  static constexpr int NW = (G == 8) ? 7 : 11;
+  static constexpr int SPW = 2;
   static constexpr int NSLOT = NW * SPW;
 };
 
