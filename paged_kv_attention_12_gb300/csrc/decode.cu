@@ -726,12 +726,11 @@ namespace {
 
 template <int D, int G>
 struct DecodeTuning {
-  // NW consumer warps + 1 producer warp, one CTA per SM, at most 168
-  // registers a thread so that three warps fit each scheduler.  The ring has
-  // SPW slots per consumer warp (each slot owned by one warp) and takes what
-  // the merge area leaves of the shared memory.
-  static constexpr int NW = (G == 8) ? 7 : 11;
-  static constexpr int SPW = 2;
+  // NW consumer warps + 1 producer warp, one CTA per SM: eight warps, two per
+  // scheduler, so a thread may hold up to 255 registers (no spills).  The
+  // ring has SPW slots per consumer warp (each slot owned by one warp).
+  static constexpr int NW = 7;
+  static constexpr int SPW = (G == 8) ? 2 : 3;
   static constexpr int NSLOT = NW * SPW;
 };
 

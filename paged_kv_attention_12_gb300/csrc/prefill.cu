@@ -67,6 +67,9 @@ struct PrefillShape {
   static constexpr uint32_t kTmemO = 256;               // O columns [256, 256 + D)
   static constexpr uint32_t kTmemCols = 512;
   static constexpr int kThreads = 7 * 32;
+  // cost buckets of the heaviest-first ranking (scratch in the K stages)
+  static constexpr int kCostBuckets = 4096;
+  static_assert((kCostBuckets + 64) * 4 <= 2 * kKVBytes, "ranking scratch");
   static_assert(kSmemBytes <= 232448, "shared memory");
   static_assert(2 * BN <= 256 && D <= 256, "TMEM columns");
 };
@@ -107,6 +110,108 @@ __device__ __forceinline__ float tanh_via_exp2(float y) {
   return 1.f - __fdividef(2.f, e + 1.f);
 }
 
+// Cost of query tile qt of request b in key tiles (0: no query row there).
+template <int TQ, int BN>
+__device__ __forceinline__ int tile_cost(const PrefillArgs& a, int b, int qt) {
+  const int q0 = a.query_start_loc[b];
+  const int n = a.query_start_loc[b + 1] - q0;
+  const int L = min(a.seq_lens[b], a.max_blocks * kBlockSize);
+  const int it0 = qt * TQ;
+  if (n <= 0 || n > L || it0 >= n) return 0;
+  const int it1 = min(n, it0 + TQ) - 1;
+  const int p_first = L - n + it0;
+  const int p_last = L - n + it1;
+  const int t_lo = (a.window > 0) ? max(0, p_first - a.window + 1) : 0;
+  return (p_last + 1 - (t_lo & ~(kBlockSize - 1)) + BN - 1) / BN + 1;
+}
+
+// Block-wide exclusive scan of one int per thread (blockDim.x <= 1024).
+__device__ __forceinline__ int block_excl_scan(int x, int* warp_sums, int* total) {
+  const int lane = threadIdx.x % 32, warp = threadIdx.x / 32, nw = (blockDim.x + 31) / 32;
+  int incl = x;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  if (lane == 31) warp_sums[warp] = incl;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int run = 0;
+    for (int w = 0; w < nw; ++w) {
+      const int t = warp_sums[w];
+      warp_sums[w] = run;
+      run += t;
+    }
+    *total = run;
+  }
+  __syncthreads();
+  const int r = warp_sums[warp] + incl - x;
+  __syncthreads();
+  return r;
+}
+
+// Longest-processing-time-first order of the (request, query tile) pairs.
+// Every CTA ranks all pairs by cost (heaviest first, ties by index) with a
+// counting sort in shared memory and returns the pair of rank `rank`; the
+// hardware launches CTAs in blockIdx order, so the heaviest tiles start first
+// and the light ones fill the tail.  All CTAs compute the same order.
+template <int TQ, int BN>
+__device__ int lpt_pair(const PrefillArgs& a, int qtiles, int rank, int* scratch, int nbuck) {
+  int* hist = scratch;                  // [nbuck]
+  int* warp_sums = scratch + nbuck;     // [32]
+  int* misc = warp_sums + 32;           // [4]
+  const int npairs = a.batch * qtiles;
+  for (int k = threadIdx.x; k < nbuck; k += blockDim.x) hist[k] = 0;
+  __syncthreads();
+  for (int i = threadIdx.x; i < npairs; i += blockDim.x)
+    atomicAdd(&hist[min(tile_cost<TQ, BN>(a, i / qtiles, i % qtiles), nbuck - 1)], 1);
+  __syncthreads();
+  // start of bucket k in the descending order: pairs in buckets > k.  Each
+  // thread owns a run of buckets counted from the top.
+  const int per = (nbuck + blockDim.x - 1) / blockDim.x;
+  const int hi_k = nbuck - 1 - static_cast<int>(threadIdx.x) * per;  // first bucket of the run
+  int mine = 0;
+  for (int u = 0; u < per; ++u)
+    if (hi_k - u >= 0) mine += hist[hi_k - u];
+  int run = block_excl_scan(mine, warp_sums, &misc[0]);
+  for (int u = 0; u < per; ++u) {
+    const int k = hi_k - u;
+    if (k < 0) break;
+    const int c = hist[k];
+    if (rank >= run && rank < run + c) {  // exactly one thread matches
+      misc[1] = k;
+      misc[2] = rank - run;
+    }
+    run += c;
+  }
+  __syncthreads();
+  const int kb = misc[1], off = misc[2];
+  // the off-th pair (in index order) of bucket kb
+  const int chunk = (npairs + blockDim.x - 1) / blockDim.x;
+  const int i0 = threadIdx.x * chunk, i1 = min(npairs, i0 + chunk);
+  int cnt = 0;
+  for (int i = i0; i < i1; ++i)
+    cnt += (min(tile_cost<TQ, BN>(a, i / qtiles, i % qtiles), nbuck - 1) == kb);
+  const int before = block_excl_scan(cnt, warp_sums, &misc[0]);
+  if (off >= before && off < before + cnt) {
+    int seen = before;
+    for (int i = i0; i < i1; ++i) {
+      if (min(tile_cost<TQ, BN>(a, i / qtiles, i % qtiles), nbuck - 1) == kb) {
+        if (seen == off) {
+          misc[3] = i;
+          break;
+        }
+        ++seen;
+      }
+    }
+  }
+  __syncthreads();
+  const int pair = misc[3];
+  __syncthreads();
+  return pair;
+}
+
 }  // namespace
 
 template <int D, int G>
@@ -119,13 +224,22 @@ __global__ void __launch_bounds__(PrefillShape<D, G>::kThreads, 1)
   constexpr int BN = S::BN, TQ = S::TQ, DC = S::DC;
 
   // ---------------------------------------------------------- work item
+  // ------------------------------------------------------- shared memory
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+
+  // ---------------------------------------------------------- work item
+  // 1-D grid over (pair rank, KV head): CTA r takes the (r / Hkv)-th heaviest
+  // (request, query tile) pair, KV head r % Hkv.  The K stage buffers are
+  // free until the first TMA load, so the ranking uses them as scratch.
   Item it;
-  // Grid (request, KV head, query tile) with the query tile slowest and
-  // reversed: CTAs launch in blockIdx order, so every request's last (most
-  // expensive) tiles go first and the cheap first tiles fill in the tail.
-  it.b = blockIdx.x;
-  it.kvh = blockIdx.y;
-  const int qt = gridDim.z - 1 - blockIdx.z;
+  const int qtiles = (a.max_query_len + TQ - 1) / TQ;
+  const int pair = lpt_pair<TQ, BN>(a, qtiles, blockIdx.x / a.Hkv,
+                                    reinterpret_cast<int*>(smem + S::oK), S::kCostBuckets);
+  it.b = pair / qtiles;
+  it.kvh = blockIdx.x % a.Hkv;
+  const int qt = pair % qtiles;
   it.q0 = a.query_start_loc[it.b];
   it.n = a.query_start_loc[it.b + 1] - it.q0;
   it.L = a.seq_lens[it.b];
@@ -147,10 +261,6 @@ __global__ void __launch_bounds__(PrefillShape<D, G>::kThreads, 1)
   it.ntiles = (p_last + 1 - it.kbase + BN - 1) / BN;
   it.nblk = (it.L + kBlockSize - 1) / kBlockSize;
 
-  // ------------------------------------------------------- shared memory
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                             ~static_cast<uintptr_t>(1023));
   uint8_t* sQ = smem + S::oQ;
   uint8_t* sK = smem + S::oK;
   uint8_t* sV = smem + S::oV;
@@ -495,7 +605,9 @@ cudaError_t launch_prefill_t(const PrefillArgs& a, cudaStream_t stream) {
   cudaError_t e = set_smem_once(reinterpret_cast<const void*>(kern), S::kSmemBytes);
   if (e != cudaSuccess) return e;
   const int qtiles = (a.max_query_len + S::TQ - 1) / S::TQ;
-  dim3 grid(a.batch, a.Hkv, qtiles);
+  const long long ctas = static_cast<long long>(a.batch) * qtiles * a.Hkv;
+  if (ctas > 0x7fffffffLL) return cudaErrorInvalidValue;
+  dim3 grid(static_cast<unsigned>(ctas));
   kern<<<grid, S::kThreads, S::kSmemBytes, stream>>>(a, tq, tk, tv);
   return cudaGetLastError();
 }
@@ -504,7 +616,7 @@ cudaError_t launch_prefill_t(const PrefillArgs& a, cudaStream_t stream) {
 
 cudaError_t launch_prefill(const PrefillArgs& a, int head_dim, int group, int /*sm_count*/,
                            cudaStream_t stream) {
-  if (a.Hkv > 65535 || (a.max_query_len + 127) / 128 * 8 > 65535) return cudaErrorInvalidValue;
+
 #define PKA_PRE(D_, G_) \
   if (head_dim == D_ && group == G_) return launch_prefill_t<D_, G_>(a, stream);
   PKA_PRE(128, 1)
