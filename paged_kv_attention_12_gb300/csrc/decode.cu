@@ -1,12 +1,13 @@
-// Paged decode attention, direct and split-K (sm_103a, CUDA cores + TMA bulk).
+// Paged decode attention, direct and split-K (sm_103a: TMA tensor tiles,
+// mbarrier ring, warp-level tensor-core MMA, shuffle online softmax).
 //
 // One query token per request attends over its visible keys, read block by
 // block through the request's block table ("Triton paged decode ... kernels
 // reading K/V through block tables; split-K decode variant", inference-server
 // README, engine feature list).  Decode is bound by HBM: every K/V byte is
 // read once, so the design is about keeping enough bytes in flight, spreading
-// them evenly over the SMs, and doing the arithmetic on CUDA cores underneath
-// the copies.
+// them evenly over the SMs, and keeping the per-byte arithmetic far below the
+// copy time.
 //
 // Work.  A segment is one (request, KV head): its visible blocks, each a
 // 16-key "tile".  The kernel is persistent (one CTA per SM).
@@ -22,27 +23,30 @@
 //
 // Inside a CTA:
 //  * one producer warp walks the pieces' block tables (32 ids per coalesced
-//    load) and issues, per tile, two 1-D bulk copies (the (block, head) K and
-//    V tiles, each one contiguous bs*D*2-byte run of the pool) into a ring of
+//    load) and loads, per tile, the (block, head) K and V tiles as 16-row x
+//    64-column TMA boxes with the 128-byte swizzle into a ring of
 //    shared-memory slots, completion counted on a "full" mbarrier;
-//  * NW consumer warps take the ring's tiles round robin; every slot has
-//    one owner warp, so each slot's mbarrier phases are consumed in order.
-//    Lanes are spread
-//    over D (8 bf16 = 16 bytes per lane, so a key row is read conflict-free
-//    in one instruction); all G query heads of the KV group are handled at
-//    once (each K/V byte feeds G heads); partial dot products are reduced
-//    across lanes with a shuffle reduce-scatter; online softmax runs in the
-//    exp2 domain; P is broadcast through shared memory; P.V accumulates in
-//    fp32 registers with packed two-wide FMAs;
+//  * NW consumer warps take the ring's tiles round robin; every slot has one
+//    owner warp, so each slot's mbarrier phases are consumed in order.  A
+//    warp computes S^T = K q^T and O^T += V^T P^T with m16n8k16 MMAs (keys
+//    or head-dim rows on M, the G <= 8 query heads of the KV group on N, so
+//    every K/V byte feeds all G heads), operands by conflict-free ldmatrix
+//    from the swizzled tiles; the online softmax runs in the exp2 domain on
+//    the accumulator fragments with shuffles; P goes to the PV operand
+//    layout through shuffles, in bf16;
 //  * at the end of a piece the consumer warps merge their (max, sum, acc)
 //    states through shared memory and write the piece's result, while the
 //    producer already streams the next piece's tiles.
 //
 // Tiles with keys outside [first visible, query position] (window start,
-// ragged tail) take a masked path that never lets a masked key's K or V --
-// which may be stale or NaN -- reach the arithmetic.
+// ragged tail) are masked on the fragments; V rows past the sequence end
+// (stale slots that may hold NaN) are zeroed in shared memory before P V.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
 #include "common.cuh"
 #include "kernels.h"
+#include "tcgen05.cuh"
 
 namespace pka {
 
@@ -317,179 +321,183 @@ struct PieceIter {
 
 }  // namespace
 
+// ------------------------------------------------------ warp-level MMA
+// mma.sync m16n8k16 (bf16 in, fp32 accumulate) and ldmatrix, as inline PTX.
+__device__ __forceinline__ void mma_bf16_16816(float (&d)[4], const uint32_t (&a)[4],
+                                               uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
+      "{%8, %9}, {%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ void ldmatrix_x4(uint32_t (&r)[4], uint32_t addr) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr)
+               : "memory");
+}
+
+__device__ __forceinline__ void ldmatrix_x4_trans(uint32_t (&r)[4], uint32_t addr) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr)
+               : "memory");
+}
+
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+  uint32_t r;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(sel));
+  return r;
+}
+
 template <int D, int G, int NW, int NSLOT>
 struct DecodeShape {
-  // A ring slot holds TK keys of one (block, head) tile: a whole block for
-  // D=128, half a block for D=256 (8 KB of K + V either way), so that many
-  // consumer warps fit next to a deep ring.
-  static constexpr int TK = (D == 256) ? 8 : 16;
-  static constexpr int SUB = kBlockSize / TK;  // slots per pool block
-  static constexpr int kTileElems = TK * D;
-  static constexpr int kTileBytes = kTileElems * 2;
-  static constexpr int LPK = D / 8;       // lanes per key row (16 bytes per lane)
-  static constexpr int KPW = 32 / LPK;    // keys per warp step
-  static constexpr int KC = (TK * G / KPW > 64) ? 8 : TK;  // keys per chunk
-  static constexpr int KS = KC / KPW;     // warp steps per chunk
-  static constexpr int NV = KS * G;       // partial dots per lane per chunk
-  static constexpr int NVL = NV >= LPK ? NV / LPK : 1;
-  static constexpr int DUP = NV >= LPK ? 1 : LPK / NV;
+  static constexpr int DC = D / 64;                        // 64-column boxes of a key row
+  static constexpr int kBoxBytes = kBlockSize * 128;       // one 16-row x 64-column box
+  static constexpr int kTileBytes = kBlockSize * D * 2;    // one block's K (or V) tile
+  static constexpr int KSTEPS = D / 16;                    // k-steps of S = K q^T
+  static constexpr int MTILES = D / 16;                    // 16-row tiles of O^T = V^T P^T
   static constexpr int kRingBytes = NSLOT * 2 * kTileBytes;
   static constexpr int kBarBytes = (2 * NSLOT * 8 + 15) / 16 * 16;
-  static constexpr int kPBytes = (NW * KPW * NV * 4 + 15) / 16 * 16;
-  // merge area: m and l of every (warp, head), padded to 16 bytes, then the
-  // [NW][G][D] fp32 accumulators (written with 16-byte stores)
   static constexpr int kMergeMLFloats = (2 * NW * G + 3) / 4 * 4;
   static constexpr int kMergeBytes = (kMergeMLFloats + NW * G * D) * 4;
-  static constexpr int kSmemBytes = kRingBytes + kBarBytes + kPBytes + kMergeBytes;
-  static_assert(D % 8 == 0 && LPK <= 32 && 32 % LPK == 0, "head_dim");
-  static_assert(KC % KPW == 0, "chunk");
+  // + 1 KiB so the ring can start on a 1024-byte boundary (128B swizzle)
+  static constexpr int kSmemBytes = 1024 + kRingBytes + kBarBytes + kMergeBytes;
+  static_assert(G >= 1 && G <= 8, "the query heads of a group are the MMA's N = 8 columns");
   static_assert(kSmemBytes <= 232448, "shared memory");
   static_assert(NSLOT % NW == 0, "each ring slot must have exactly one owner warp");
-  static_assert(kTileBytes % 16 == 0 && kRingBytes % 16 == 0, "bulk-copy destinations 16-byte aligned");
-  static_assert((kRingBytes + kBarBytes) % 16 == 0, "P area 16-byte aligned");
-  static_assert((kRingBytes + kBarBytes + kPBytes) % 16 == 0, "merge area 16-byte aligned");
-  static_assert((KPW * NV * 4) % 16 == 0 || G % 4 != 0, "per-warp P rows 16-byte aligned");
 };
 
-// Processes one ring slot (TK keys) for one consumer warp.  EDGE (warp
-// uniform) selects the masked path for slots with keys outside the visible
-// range.
+// One ring slot (a block's 16 keys) for one consumer warp, on the tensor
+// cores at warp level: S^T[16 keys x 8] = K[16 x D] q^T[D x 8] (the G query
+// heads are the N columns, the rest zero), online softmax on the fragments
+// with shuffles, then O^T[D x 8] += V^T[D x 16] P^T[16 x 8].  K and V come
+// from 128B-swizzled boxes, so every ldmatrix is bank-conflict free.
+// Fragment roles (g = lane / 4, t = lane % 4): S^T holds keys g and g+8 of
+// heads 2t and 2t+1; O^T tile mt holds rows mt*16 + g (+8) of heads 2t, 2t+1.
 template <int D, int G, int NW, int NSLOT>
-__device__ __forceinline__ void decode_tile(const bool EDGE, const uint16_t* __restrict__ Kt,
-                                            const uint16_t* __restrict__ Vt,
-                                            const float2 (&qf)[G][4], float2 (&acc)[G][4],
-                                            float (&m)[G],
-                                            float (&ls)[DecodeShape<D, G, NW, NSLOT>::NVL],
-                                            float* psm, int lane, int tok0, int t_lo, int pos,
-                                            float softcap, float inv_cap) {
+__device__ __forceinline__ void decode_slot(
+    const bool edge, uint32_t k_addr, uint8_t* v_ptr, const uint32_t (&bq)[D / 16][2],
+    float (&o)[D / 16][4], float (&m)[2], float (&l)[2], int lane, int tok0, int t_lo, int pos,
+    float qscale, float softcap, float inv_cap) {
   using S = DecodeShape<D, G, NW, NSLOT>;
-  constexpr int LPK = S::LPK, KPW = S::KPW, KC = S::KC, KS = S::KS, NV = S::NV;
-  constexpr int NVL = S::NVL, DUP = S::DUP;
-  const int kl = lane / LPK;
-  const int dl = lane % LPK;
-  float* pw = psm + kl * NV;
+  const int g = lane >> 2, t = lane & 3;
 
+  // ---- S^T = K q^T
+  float s[4] = {0.f, 0.f, 0.f, 0.f};
+  {
+    const int row = (lane & 7) + ((lane >> 3) & 1) * 8;
+    const int hi = lane >> 4;
+    const uint32_t rbase = k_addr + row * 128;
 #pragma unroll
-  for (int c = 0; c < S::TK / KC; ++c) {
-    // ---- partial q.k over this lane's 8 elements, every key step, every head
-    float part[NV];
-#pragma unroll
-    for (int s = 0; s < KS; ++s) {
-      const int key = c * KC + s * KPW + kl;
-      const uint4 u = *reinterpret_cast<const uint4*>(Kt + key * D + dl * 8);
-      float2 kf[4];
-      unpack8x2(u, kf);
-#pragma unroll
-      for (int g = 0; g < G; ++g) {
-        float2 d = fmul2(qf[g][0], kf[0]);
-        d = ffma2(qf[g][1], kf[1], d);
-        d = ffma2(qf[g][2], kf[2], d);
-        d = ffma2(qf[g][3], kf[3], d);
-        part[s * G + g] = d.x + d.y;
-      }
+    for (int kk = 0; kk < S::KSTEPS; ++kk) {
+      uint32_t a[4];
+      const int j = (kk & 3) * 2 + hi;
+      ldmatrix_x4(a, rbase + (kk >> 2) * S::kBoxBytes + ((j ^ (row & 7)) << 4));
+      mma_bf16_16816(s, a, bq[kk][0], bq[kk][1]);
     }
-    ReduceScatter<NV, LPK / 2>::run(part, lane);
-
-    // ---- logits (log2 domain), mask, chunk max per head
-    float mloc[G];
+  }
+  // ---- logits (log2 domain), mask, online softmax on the fragment
+  const bool head_ok0 = (2 * t) < G, head_ok1 = (2 * t + 1) < G;
+  bool key_ok_lo = true, key_ok_hi = true;
+  if (edge) {
+    key_ok_lo = (tok0 + g >= t_lo) && (tok0 + g <= pos);
+    key_ok_hi = (tok0 + g + 8 >= t_lo) && (tok0 + g + 8 <= pos);
+  }
+  float x[4];
 #pragma unroll
-    for (int g = 0; g < G; ++g) mloc[g] = -INFINITY;
-    int gj[NVL];
+  for (int i = 0; i < 4; ++i) {
+    float v = s[i];
+    if (softcap > 0.f) v = softcap * tanhf(v * qscale * inv_cap) * kLog2e;
+    else v *= qscale;
+    const bool ok = ((i & 1) ? head_ok1 : head_ok0) && ((i & 2) ? key_ok_hi : key_ok_lo);
+    x[i] = ok ? v : -INFINITY;
+  }
+  float alpha[2], ms[2];
 #pragma unroll
-    for (int j = 0; j < NVL; ++j) {
-      const int i = (dl / DUP) * NVL + j;
-      gj[j] = i % G;
-      float x = part[j];
-      if (softcap > 0.f) x = softcap * tanhf(x * inv_cap) * kLog2e;
-      if (EDGE) {
-        const int t = tok0 + c * KC + (i / G) * KPW + kl;
-        if (t < t_lo || t > pos) x = -INFINITY;
-      }
-      part[j] = x;
+  for (int j = 0; j < 2; ++j) {
+    float mx = fmaxf(x[j], x[j + 2]);
 #pragma unroll
-      for (int g = 0; g < G; ++g) mloc[g] = opaque_sel(gj[j] == g, fmaxf(mloc[g], x), mloc[g]);
+    for (int off = 4; off < 32; off <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+    const float mn = fmaxf(m[j], mx);
+    ms[j] = (mn == -INFINITY) ? 0.f : mn;
+    alpha[j] = fast_exp2(m[j] - ms[j]);
+    m[j] = mn;
+  }
+  float p[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) p[i] = fast_exp2(x[i] - ms[i & 1]);
+  l[0] = l[0] * alpha[0] + p[0] + p[2];
+  l[1] = l[1] * alpha[1] + p[1] + p[3];
+  if (__any_sync(0xffffffffu, alpha[0] != 1.f || alpha[1] != 1.f)) {
+#pragma unroll
+    for (int mt = 0; mt < S::MTILES; ++mt) {
+      o[mt][0] *= alpha[0];
+      o[mt][1] *= alpha[1];
+      o[mt][2] *= alpha[0];
+      o[mt][3] *= alpha[1];
     }
-    float alpha[G], mref[G];
-#pragma unroll
-    for (int g = 0; g < G; ++g) {
-      const float mn = fmaxf(m[g], warp_max(mloc[g]));
-      mref[g] = (mn == -INFINITY) ? 0.f : mn;
-      alpha[g] = fast_exp2(m[g] - mref[g]);
-      m[g] = mn;
+  }
+  // ---- P^T as the B fragment: this thread needs keys 2t, 2t+1 (+8) of head g
+  const uint32_t wlo = pack_bf16x2(p[0], p[1]);  // key g,   heads 2t, 2t+1
+  const uint32_t whi = pack_bf16x2(p[2], p[3]);  // key g+8, heads 2t, 2t+1
+  const int src0 = 8 * t + (g >> 1), src1 = src0 + 4;
+  const uint32_t a0 = __shfl_sync(0xffffffffu, wlo, src0);
+  const uint32_t a1 = __shfl_sync(0xffffffffu, wlo, src1);
+  const uint32_t c0 = __shfl_sync(0xffffffffu, whi, src0);
+  const uint32_t c1 = __shfl_sync(0xffffffffu, whi, src1);
+  const uint32_t sel = (g & 1) ? 0x7632u : 0x5410u;
+  const uint32_t pb0 = prmt(a0, a1, sel);
+  const uint32_t pb1 = prmt(c0, c1, sel);
+  // ---- stale slots past the sequence end may hold NaN: zero those V rows
+  if (edge && tok0 + kBlockSize - 1 > pos) {
+    const int z0 = max(0, pos - tok0 + 1);
+    const int nz = (kBlockSize - z0) * S::DC * 8;
+    for (int idx = lane; idx < nz; idx += 32) {
+      const int r = z0 + idx / (S::DC * 8);
+      const int c = (idx / 8) % S::DC;
+      const int q = idx % 8;
+      *reinterpret_cast<uint4*>(v_ptr + c * S::kBoxBytes + r * 128 + q * 16) =
+          make_uint4(0u, 0u, 0u, 0u);
     }
-    // ---- probabilities, lane-local sums, broadcast through shared memory
-#pragma unroll
-    for (int j = 0; j < NVL; ++j) {
-      float a = alpha[0], r = mref[0];
-#pragma unroll
-      for (int g = 1; g < G; ++g) {
-        a = opaque_sel(gj[j] == g, alpha[g], a);
-        r = opaque_sel(gj[j] == g, mref[g], r);
-      }
-      const float p = fast_exp2(part[j] - r);
-      ls[j] = ls[j] * a + p;
-      pw[(dl / DUP) * NVL + j] = p;
-    }
-#pragma unroll
-    for (int g = 0; g < G; ++g) {
-      const float2 a2 = make_float2(alpha[g], alpha[g]);
-#pragma unroll
-      for (int e = 0; e < 4; ++e) acc[g][e] = fmul2(acc[g][e], a2);
-    }
+    // the slot is refilled by TMA later: order these writes before it
+    fence_proxy_async_smem();
     __syncwarp();
-
-    // ---- P.V over this lane's 8 columns
+  }
+  // ---- O^T += V^T P^T
+  {
+    const int mi = lane >> 3, rr = lane & 7;
+    const int key = rr + 8 * (mi >> 1);
+    const uint32_t vbase = smem_u32(v_ptr) + key * 128;
 #pragma unroll
-    for (int s = 0; s < KS; ++s) {
-      const int key = c * KC + s * KPW + kl;
-      if (EDGE) {
-        const int t = tok0 + key;
-        if (t < t_lo || t > pos) continue;  // masked V row may hold NaN
-      }
-      const uint4 u = *reinterpret_cast<const uint4*>(Vt + key * D + dl * 8);
-      float2 vf[4];
-      unpack8x2(u, vf);
-      float pg[G];
-      if constexpr (G % 4 == 0) {
-#pragma unroll
-        for (int g = 0; g < G; g += 4) {
-          const float4 t4 = *reinterpret_cast<const float4*>(pw + s * G + g);
-          pg[g] = t4.x;
-          pg[g + 1] = t4.y;
-          pg[g + 2] = t4.z;
-          pg[g + 3] = t4.w;
-        }
-      } else {
-#pragma unroll
-        for (int g = 0; g < G; ++g) pg[g] = pw[s * G + g];
-      }
-#pragma unroll
-      for (int g = 0; g < G; ++g) {
-        const float2 p2 = make_float2(pg[g], pg[g]);
-#pragma unroll
-        for (int e = 0; e < 4; ++e) acc[g][e] = ffma2(p2, vf[e], acc[g][e]);
-      }
+    for (int mt = 0; mt < S::MTILES; ++mt) {
+      const int dch = mt * 2 + (mi & 1);  // 16-byte chunk along D
+      uint32_t a[4];
+      ldmatrix_x4_trans(a, vbase + (dch >> 3) * S::kBoxBytes + (((dch & 7) ^ (key & 7)) << 4));
+      mma_bf16_16816(o[mt], a, pb0, pb1);
     }
-    __syncwarp();
   }
 }
 
 template <int D, int G, int NW, int NSLOT>
 __global__ void __launch_bounds__((NW + 1) * 32, 1)
-    paged_decode_kernel(const __grid_constant__ DecodeArgs a) {
+    paged_decode_kernel(const __grid_constant__ DecodeArgs a,
+                        const __grid_constant__ CUtensorMap tm_k,
+                        const __grid_constant__ CUtensorMap tm_v) {
   using S = DecodeShape<D, G, NW, NSLOT>;
-  constexpr int TE = S::kTileElems;
-  constexpr int NVL = S::NVL, LPK = S::LPK;
 
-  extern __shared__ __align__(128) uint8_t smem[];
-  uint16_t* ring = reinterpret_cast<uint16_t*>(smem);
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  uint8_t* ring = smem;
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + S::kRingBytes);
   uint64_t* empty = full + NSLOT;
-  float* psm_all = reinterpret_cast<float*>(smem + S::kRingBytes + S::kBarBytes);
-  float* merge = reinterpret_cast<float*>(smem + S::kRingBytes + S::kBarBytes + S::kPBytes);
-  float* mrg_m = merge;                       // [NW][G]
-  float* mrg_l = merge + NW * G;              // [NW][G]
-  float* mrg_acc = merge + S::kMergeMLFloats;  // [NW][G][D], 16-byte aligned
+  float* merge = reinterpret_cast<float*>(smem + S::kRingBytes + S::kBarBytes);
+  float* mrg_m = merge;                        // [NW][G]
+  float* mrg_l = merge + NW * G;               // [NW][G]
+  float* mrg_acc = merge + S::kMergeMLFloats;  // [NW][G][D]
 
   const int warp = threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
@@ -509,23 +517,27 @@ __global__ void __launch_bounds__((NW + 1) * 32, 1)
 
   if (warp == NW) {
     // ============================ producer warp ============================
-    const uint64_t pol = policy_evict_first();
+    if (lane == 0) {
+      prefetch_tensormap(&tm_k);
+      prefetch_tensormap(&tm_v);
+    }
+    const uint32_t oob_row = static_cast<uint32_t>(a.num_blocks) * a.Hkv * kBlockSize;
     long long issued = 0;
     bool ok = true;
     while (ok && iter.next(pc)) {
       const int32_t* trow = a.tables + static_cast<size_t>(pc.b) * a.max_blocks + pc.j0;
       for (int base = 0; base < pc.ntiles && ok; base += 32) {
-        int id = 0;
+        uint32_t row = oob_row;  // a bad id reads zeros (reported) instead of faulting
         if (base + lane < pc.ntiles) {
-          id = trow[base + lane];
-          if (static_cast<unsigned>(id) >= static_cast<unsigned>(a.num_blocks)) {
+          const int id = trow[base + lane];
+          if (static_cast<unsigned>(id) < static_cast<unsigned>(a.num_blocks))
+            row = (static_cast<uint32_t>(id) * a.Hkv + pc.kvh) * kBlockSize;
+          else
             report(a.err, PKA_DEVERR_BAD_TABLE);
-            id = 0;
-          }
         }
         const int cnt = min(32, pc.ntiles - base);
-        for (int k = 0; k < cnt * S::SUB; ++k) {
-          const int phys = __shfl_sync(0xffffffffu, id, k / S::SUB);
+        for (int k = 0; k < cnt; ++k) {
+          const uint32_t r0 = __shfl_sync(0xffffffffu, row, k);
           const int slot = static_cast<int>(issued % NSLOT);
           const long long round = issued / NSLOT;
           int good = 1;
@@ -534,11 +546,14 @@ __global__ void __launch_bounds__((NW + 1) * 32, 1)
               good = mbar_wait(&empty[slot], static_cast<uint32_t>((round - 1) & 1), a.err);
             if (good) {
               mbar_arrive_expect_tx(&full[slot], 2 * S::kTileBytes);
-              const size_t off = (static_cast<size_t>(phys) * a.Hkv + pc.kvh) * kBlockSize * D +
-                                 static_cast<size_t>(k % S::SUB) * TE;
-              uint16_t* dst = ring + static_cast<size_t>(slot) * 2 * TE;
-              bulk_g2s_stream(dst, a.k + off, S::kTileBytes, &full[slot], pol);
-              bulk_g2s_stream(dst + TE, a.v + off, S::kTileBytes, &full[slot], pol);
+              uint8_t* dst = ring + static_cast<size_t>(slot) * 2 * S::kTileBytes;
+#pragma unroll
+              for (int c = 0; c < S::DC; ++c) {
+                tma_load_2d(dst + c * S::kBoxBytes, &tm_k, c * 64, static_cast<int>(r0),
+                            &full[slot]);
+                tma_load_2d(dst + S::kTileBytes + c * S::kBoxBytes, &tm_v, c * 64,
+                            static_cast<int>(r0), &full[slot]);
+              }
             }
           }
           good = __shfl_sync(0xffffffffu, good, 0);
@@ -560,48 +575,40 @@ __global__ void __launch_bounds__((NW + 1) * 32, 1)
   }
 
   // ============================ consumer warps ============================
-  const int kl = lane / LPK;
-  const int dl = lane % LPK;
-  float* psm = psm_all + warp * (S::kPBytes / 4 / NW);
+  const int g = lane >> 2, t = lane & 3;
   const float inv_cap = a.softcap > 0.f ? 1.f / a.softcap : 0.f;
   const float qscale = a.scale * (a.softcap > 0.f ? 1.f : kLog2e);
   long long tile_base = 0;
   bool ok = true;
 
-  // The next piece's query rows are loaded while the current piece is merged.
-  bool have = iter.next(pc);
-  uint4 qraw[G];
-  if (have) {
-    const uint16_t* qp = a.q + (static_cast<size_t>(pc.qrow) * a.Hq + pc.kvh * G) * D + dl * 8;
+  // q^T as B fragments: head g (zero for g >= G), elements 2t, 2t+1 (+8) of
+  // every k-step.  The next piece's fragments are loaded during the merge.
+  auto load_q = [&](const Piece& P, uint32_t (&bq)[D / 16][2]) {
+    const uint32_t* qp = reinterpret_cast<const uint32_t*>(
+        a.q + (static_cast<size_t>(P.qrow) * a.Hq + P.kvh * G + (g < G ? g : 0)) * D);
 #pragma unroll
-    for (int g = 0; g < G; ++g) qraw[g] = *reinterpret_cast<const uint4*>(qp + g * D);
-  }
-  while (have) {
-    float2 qf[G][4], acc[G][4];
-    float m[G], ls[NVL];
-    {
-      const float2 qs2 = make_float2(qscale, qscale);
-#pragma unroll
-      for (int g = 0; g < G; ++g) {
-        unpack8x2(qraw[g], qf[g]);
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          qf[g][e] = fmul2(qf[g][e], qs2);
-          acc[g][e] = make_float2(0.f, 0.f);
-        }
-        m[g] = -INFINITY;
-      }
-#pragma unroll
-      for (int j = 0; j < NVL; ++j) ls[j] = 0.f;
+    for (int kk = 0; kk < D / 16; ++kk) {
+      bq[kk][0] = (g < G) ? qp[kk * 8 + t] : 0u;
+      bq[kk][1] = (g < G) ? qp[kk * 8 + 4 + t] : 0u;
     }
+  };
+
+  uint32_t bq[D / 16][2];
+  bool have = iter.next(pc);
+  if (have) load_q(pc, bq);
+  while (have) {
+    float o[D / 16][4];
+#pragma unroll
+    for (int mt = 0; mt < D / 16; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
+    float m[2] = {-INFINITY, -INFINITY};
+    float l[2] = {0.f, 0.f};
 
     // Tile T of the CTA's stream lives in slot T % NSLOT and belongs to warp
     // T % NW; NSLOT is a multiple of NW, so every slot has one owner warp that
     // consumes its phases in order (a phase-parity wait can never alias an
     // older phase of the same slot).
-    const int nsub = pc.ntiles * S::SUB;
     const int i0 = static_cast<int>((warp - tile_base % NW + NW) % NW);
-    for (int i = i0; i < nsub && ok; i += NW) {
+    for (int i = i0; i < pc.ntiles && ok; i += NW) {
       const long long T = tile_base + i;
       const int slot = static_cast<int>(T % NSLOT);
       const bool got = mbar_wait(&full[slot], static_cast<uint32_t>((T / NSLOT) & 1), a.err);
@@ -609,100 +616,81 @@ __global__ void __launch_bounds__((NW + 1) * 32, 1)
         ok = false;
         break;
       }
-      const uint16_t* Kt = ring + static_cast<size_t>(slot) * 2 * TE;
-      const uint16_t* Vt = Kt + TE;
-      const int tok0 = (pc.j0 + i / S::SUB) * kBlockSize + (i % S::SUB) * S::TK;
-      const bool edge = (tok0 < pc.t_lo || tok0 + S::TK - 1 > pc.pos);
-      decode_tile<D, G, NW, NSLOT>(edge, Kt, Vt, qf, acc, m, ls, psm, lane, tok0, pc.t_lo, pc.pos,
-                                   a.softcap, inv_cap);
+      uint8_t* kp = ring + static_cast<size_t>(slot) * 2 * S::kTileBytes;
+      const int tok0 = (pc.j0 + i) * kBlockSize;
+      const bool edge = (tok0 < pc.t_lo || tok0 + kBlockSize - 1 > pc.pos);
+      decode_slot<D, G, NW, NSLOT>(edge, smem_u32(kp), kp + S::kTileBytes, bq, o, m, l, lane,
+                                   tok0, pc.t_lo, pc.pos, qscale, a.softcap, inv_cap);
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[slot]);
     }
-    tile_base += nsub;
+    tile_base += pc.ntiles;
 
     Piece nx;
     const bool have_next = iter.next(nx);
-    if (have_next) {
-      const uint16_t* qp = a.q + (static_cast<size_t>(nx.qrow) * a.Hq + nx.kvh * G) * D + dl * 8;
-#pragma unroll
-      for (int g = 0; g < G; ++g) qraw[g] = *reinterpret_cast<const uint4*>(qp + g * D);
-    }
+    if (have_next) load_q(nx, bq);
 
     const bool split = a.split_blocks > 0;
     if (pc.ntiles > 0) {
-      // ---- per-warp totals: sums per head, accumulators across key lanes
-      float lt[G];
+      // ---- per-warp totals: sums over the 8 key rows held by lanes g
 #pragma unroll
-      for (int g = 0; g < G; ++g) lt[g] = 0.f;
+      for (int j = 0; j < 2; ++j)
 #pragma unroll
-      for (int j = 0; j < NVL; ++j) {
-        const int gj = ((dl / S::DUP) * NVL + j) % G;
+        for (int off = 4; off < 32; off <<= 1) l[j] += __shfl_xor_sync(0xffffffffu, l[j], off);
+      if (g == 0) {
 #pragma unroll
-        for (int g = 0; g < G; ++g) lt[g] += opaque_sel(gj == g, ls[j], 0.f);
-      }
-#pragma unroll
-      for (int g = 0; g < G; ++g) lt[g] = warp_sum(lt[g]) * (1.f / S::DUP);
-#pragma unroll
-      for (int o = LPK; o < 32; o <<= 1)
-#pragma unroll
-        for (int g = 0; g < G; ++g)
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            acc[g][e].x += __shfl_xor_sync(0xffffffffu, acc[g][e].x, o);
-            acc[g][e].y += __shfl_xor_sync(0xffffffffu, acc[g][e].y, o);
+        for (int j = 0; j < 2; ++j) {
+          const int h = 2 * t + j;
+          if (h < G) {
+            mrg_m[warp * G + h] = m[j];
+            mrg_l[warp * G + h] = l[j];
           }
-
-      if (lane == 0) {
-#pragma unroll
-        for (int g = 0; g < G; ++g) {
-          mrg_m[warp * G + g] = m[g];
-          mrg_l[warp * G + g] = lt[g];
         }
       }
-      if (kl == 0) {
 #pragma unroll
-        for (int g = 0; g < G; ++g) {
-          float4* dst = reinterpret_cast<float4*>(mrg_acc + (warp * G + g) * D + dl * 8);
-          dst[0] = make_float4(acc[g][0].x, acc[g][0].y, acc[g][1].x, acc[g][1].y);
-          dst[1] = make_float4(acc[g][2].x, acc[g][2].y, acc[g][3].x, acc[g][3].y);
+      for (int mt = 0; mt < D / 16; ++mt)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int h = 2 * t + (i & 1);
+          const int d = mt * 16 + g + ((i & 2) ? 8 : 0);
+          if (h < G) mrg_acc[(warp * G + h) * D + d] = o[mt][i];
         }
-      }
       consumer_sync(NW * 32);
 
       // ---- merge the warps' states and write this piece's result
       for (int idx = threadIdx.x; idx < G * D; idx += NW * 32) {
-        const int g = idx / D;
+        const int h = idx / D;
         const int d = idx % D;
         float M = -INFINITY;
 #pragma unroll
-        for (int w = 0; w < NW; ++w) M = fmaxf(M, mrg_m[w * G + g]);
+        for (int w = 0; w < NW; ++w) M = fmaxf(M, mrg_m[w * G + h]);
         const float Ms = (M == -INFINITY) ? 0.f : M;
         float den = 0.f, num = 0.f;
 #pragma unroll
         for (int w = 0; w < NW; ++w) {
-          const float sc = fast_exp2(mrg_m[w * G + g] - Ms);
-          den = fmaf(sc, mrg_l[w * G + g], den);
-          num = fmaf(sc, mrg_acc[(w * G + g) * D + d], num);
+          const float sc = fast_exp2(mrg_m[w * G + h] - Ms);
+          den = fmaf(sc, mrg_l[w * G + h], den);
+          num = fmaf(sc, mrg_acc[(w * G + h) * D + d], num);
         }
-        const float o = (den > 0.f) ? num / den : 0.f;
-        const int h = pc.kvh * G + g;
+        const float ov = (den > 0.f) ? num / den : 0.f;
+        const int hq = pc.kvh * G + h;
         if (split) {
           if (pc.slot < a.num_splits) {
-            const size_t ph = (static_cast<size_t>(pc.b) * a.Hq + h) * a.num_splits + pc.slot;
-            a.partial_o[ph * D + d] = o;
+            const size_t ph = (static_cast<size_t>(pc.b) * a.Hq + hq) * a.num_splits + pc.slot;
+            a.partial_o[ph * D + d] = ov;
             if (d == 0) a.partial_lse[ph] = (den > 0.f) ? (M + log2f(den)) * kLn2 : -INFINITY;
           }
         } else {
-          reinterpret_cast<uint16_t*>(a.out)[(static_cast<size_t>(pc.qrow) * a.Hq + h) * D + d] =
-              f32_to_bf16_rn(o);
+          reinterpret_cast<uint16_t*>(a.out)[(static_cast<size_t>(pc.qrow) * a.Hq + hq) * D + d] =
+              f32_to_bf16_rn(ov);
         }
       }
       consumer_sync(NW * 32);
     } else if (!split) {
       // a request with no visible key: output 0
       for (int idx = threadIdx.x; idx < G * D; idx += NW * 32) {
-        const int h = pc.kvh * G + idx / D;
-        reinterpret_cast<uint16_t*>(a.out)[(static_cast<size_t>(pc.qrow) * a.Hq + h) * D +
+        const int hq = pc.kvh * G + idx / D;
+        reinterpret_cast<uint16_t*>(a.out)[(static_cast<size_t>(pc.qrow) * a.Hq + hq) * D +
                                            idx % D] = 0;
       }
     }
@@ -711,9 +699,9 @@ __global__ void __launch_bounds__((NW + 1) * 32, 1)
       if (pc.fill_from > a.num_splits && threadIdx.x == 0) report(a.err, PKA_DEVERR_SEQ_LEN);
       const int nfill = a.num_splits - min(pc.fill_from, a.num_splits);
       for (int idx = threadIdx.x; idx < G * nfill; idx += NW * 32) {
-        const int h = pc.kvh * G + idx / nfill;
-        const int s = pc.fill_from + idx % nfill;
-        a.partial_lse[(static_cast<size_t>(pc.b) * a.Hq + h) * a.num_splits + s] = -INFINITY;
+        const int hq = pc.kvh * G + idx / nfill;
+        const int sl = pc.fill_from + idx % nfill;
+        a.partial_lse[(static_cast<size_t>(pc.b) * a.Hq + hq) * a.num_splits + sl] = -INFINITY;
       }
     }
     pc = nx;
@@ -726,23 +714,55 @@ namespace {
 
 template <int D, int G>
 struct DecodeTuning {
-  // NW consumer warps + 1 producer warp, one CTA per SM: eight warps, two per
-  // scheduler, so a thread may hold up to 255 registers (no spills).  The
-  // ring has SPW slots per consumer warp (each slot owned by one warp).
-  static constexpr int NW = 7;
-  static constexpr int SPW = (G == 8) ? 2 : 3;
+  // NW consumer warps + 1 producer warp, one CTA per SM.  The arithmetic of a
+  // slot is a few dozen instructions, so a few consumer warps keep up with
+  // HBM; the shared memory goes to ring slots (bytes in flight), SPW per
+  // consumer warp (each slot owned by one warp).
+  static constexpr int NW = 4;
+  static constexpr int SPW = (D == 256) ? 3 : 6;
   static constexpr int NSLOT = NW * SPW;
 };
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (fn == nullptr) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return nullptr;
+    fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  return fn;
+}
+
+// A pool viewed as a 2-D tensor [num_blocks * Hkv * 16 rows][D], read in
+// 16-row x 64-column boxes with the 128-byte swizzle.
+bool pool_map(CUtensorMap* m, const void* base, int D, long long rows) {
+  auto fn = encode_fn();
+  if (fn == nullptr) return false;
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(rows)};
+  const cuuint64_t str[1] = {static_cast<cuuint64_t>(D) * 2};
+  const cuuint32_t box[2] = {64, static_cast<cuuint32_t>(kBlockSize)};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, str, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
 
 template <int D, int G>
 cudaError_t launch_decode_t(const DecodeArgs& a, int grid, cudaStream_t stream) {
   constexpr int NW = DecodeTuning<D, G>::NW;
   constexpr int NSLOT = DecodeTuning<D, G>::NSLOT;
   using S = DecodeShape<D, G, NW, NSLOT>;
+  CUtensorMap tk, tv;
+  const long long rows = static_cast<long long>(a.num_blocks) * a.Hkv * kBlockSize;
+  if (!pool_map(&tk, a.k, D, rows) || !pool_map(&tv, a.v, D, rows)) return cudaErrorInvalidValue;
   auto kern = paged_decode_kernel<D, G, NW, NSLOT>;
   cudaError_t e = set_smem_once(reinterpret_cast<const void*>(kern), S::kSmemBytes);
   if (e != cudaSuccess) return e;
-  kern<<<grid, (NW + 1) * 32, S::kSmemBytes, stream>>>(a);
+  kern<<<grid, (NW + 1) * 32, S::kSmemBytes, stream>>>(a, tk, tv);
   return cudaGetLastError();
 }
 
