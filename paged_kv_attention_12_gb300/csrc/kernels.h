@@ -57,7 +57,7 @@ struct PrefillArgs {
   const int32_t* seq_lens;
   const int32_t* query_start_loc;  // [B+1]
   int32_t* err;
-  int32_t batch, Hq, Hkv, num_blocks, max_blocks, total_q, max_query_len;
+  int32_t batch, Hq, Hkv, num_blocks, max_blocks, total_q, max_query_len, max_seq_len;
   float scale, softcap;
   int32_t window;
 };

@@ -238,6 +238,7 @@ int paged_prefill_attn(const void* q, void* out, const pka_kv_pool* kv,
   a.max_blocks = max_blocks;
   a.total_q = total_q;
   a.max_query_len = max_query_len;
+  a.max_seq_len = max_seq_len;
   a.scale = params->scale;
   a.softcap = params->softcap;
   a.window = params->window;

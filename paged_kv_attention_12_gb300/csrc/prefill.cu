@@ -235,8 +235,10 @@ __global__ void __launch_bounds__(PrefillShape<D, G>::kThreads, 1)
   // free until the first TMA load, so the ranking uses them as scratch.
   Item it;
   const int qtiles = (a.max_query_len + TQ - 1) / TQ;
+  // costs are at most ceil(max_seq_len / BN) + 1 key tiles
+  const int nbuck = min(S::kCostBuckets, (a.max_seq_len + BN - 1) / BN + 2);
   const int pair = lpt_pair<TQ, BN>(a, qtiles, blockIdx.x / a.Hkv,
-                                    reinterpret_cast<int*>(smem + S::oK), S::kCostBuckets);
+                                    reinterpret_cast<int*>(smem + S::oK), nbuck);
   it.b = pair / qtiles;
   it.kvh = blockIdx.x % a.Hkv;
   const int qt = pair % qtiles;
