@@ -5,8 +5,10 @@ Workload (one step): the serving-shaped decode batch -- B=32 requests,
 seq_lens ~ U[512, 4096], Hq=8, Hkv=2, head_dim=256, block_size=16, a pool of
 16384 blocks in shuffled order, bf16 N(0,1) K/V, tanh softcap 50 -- run
 through two layers with separate pools: a global layer (window 0) and a
-sliding layer (window 512).  Each layer is one split-K decode launch plus
-one combine launch.
+sliding layer (window 512).
+
+Each layer is one launch of the split-K decode kernel with the LSE combine
+fused in.
 
 Metric: paged-decode KV GB/s, counting algorithmic bytes (K/V rows of every
 visible key plus the query rows) per step over the device time of the step.
@@ -265,8 +267,8 @@ def other_workloads(dev, flush, iters=10, warmup=3):
         nbytes = batch_kv_bytes(batch)
         flops = 4.0 * batch.head_dim * batch.num_q_heads * attention_pairs(batch)
         if cfg in (1, 3):
-            r = binding.DecodeSplitK(batch)
-            fn, path = r.run, "paged_decode_splitk + combine"
+            r = binding.DecodeFused(batch)
+            fn, path = r.run, "paged_decode_attn_ws (split-K, combine fused)"
         else:
             out = torch.empty_like(batch.q)
             fn, path = (lambda b=batch, o=out: binding.run_batch(b, o)), "paged_prefill_attn"
@@ -375,22 +377,22 @@ def main():
     binding.lib()
 
     calls = workload.decode_serving(args.seed + 1000 * rank, dev)
-    runners = [binding.DecodeSplitK(b) for b in calls]
+    runners = [binding.DecodeFused(b) for b in calls]
     bytes_step = step_bytes(calls)
     flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream()
 
     def step(kernel_events=None):
+        # one fused split-K decode launch per layer (the LSE combine runs in
+        # the same kernel)
         for i, (b, r) in enumerate(zip(calls, runners)):
             if kernel_events is not None:
                 kernel_events[i][0].record(stream)
-            binding.paged_decode_splitk(b.q, r.partial_o, r.partial_lse, b.k_pool, b.v_pool,
-                                        b.block_tables, b.seq_lens, b.max_seq_len,
-                                        r.num_splits, r.split_blocks, scale=b.scale,
-                                        softcap=b.softcap, window=b.window)
+            binding.paged_decode_attn_ws(b.q, r.out, b.k_pool, b.v_pool, b.block_tables,
+                                         b.seq_lens, b.max_seq_len, r.workspace, scale=b.scale,
+                                         softcap=b.softcap, window=b.window)
             if kernel_events is not None:
                 kernel_events[i][1].record(stream)
-            binding.paged_decode_splitk_combine(r.partial_o, r.partial_lse, r.out)
 
     for _ in range(args.warmup):
         flush.fill_(1.0)
@@ -468,13 +470,13 @@ def main():
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic",
         "config": {"workload": WORKLOAD_NAME, "l2": "flushed before every step (512 MiB write)",
-                   "splits": [[r.num_splits, r.split_blocks] for r in runners],
+                   "path": "paged_decode_attn_ws (split-K, combine fused)",
                    "bytes_per_step": bytes_step, "parallelism": f"replicas{world}"},
-        "roofline": {"bound": "hbm", "kernel": "paged_decode_kernel (split-K)",
+        "roofline": {"bound": "hbm", "kernel": "paged_decode_kernel (split-K, fused combine)",
                      "achieved": achieved, "peak": peak, "peak_kind": peak_kind,
                      "unit": "GB/s", "frac": achieved / peak,
                      "traffic": traffic_from_profile()},
-        "gpu_launches": args.steps * 2 * len(calls),
+        "gpu_launches": args.steps * len(calls),
         "wall_s": wall,
     }
     if e2e:

@@ -149,6 +149,24 @@ int paged_decode_splitk(const void* q, float* partial_o, float* partial_lse,
                         int32_t split_blocks, const pka_attn_params* params,
                         void* stream);
 
+/* Split-K decode with the log-sum-exp combine fused into the same launch
+ * (one launch instead of two).  Same partition and partials as
+ * paged_decode_splitk with the plan's (S, C); the CTA that finishes a
+ * segment's last piece merges its pieces and writes out bf16 [B][Hq][D].
+ * workspace: device, 16-byte aligned, at least paged_decode_attn_ws_bytes()
+ * bytes: partial outputs, partial LSEs, then B*Hkv int32 arrival counters.
+ * The counters must be zero before the first call (e.g. memset once at
+ * allocation); every call that completes leaves them zero again.  After a
+ * call that reported PKA_DEVERR_TIMEOUT, zero them before the next call.
+ * Calls sharing one workspace must not overlap on the GPU. */
+size_t paged_decode_attn_ws_bytes(int32_t B, int32_t Hq, int32_t Hkv, int32_t D,
+                                  int32_t max_seq_len, int32_t window);
+int paged_decode_attn_ws(const void* q, void* out, const pka_kv_pool* kv,
+                         const int32_t* block_tables, int32_t max_blocks,
+                         const int32_t* seq_lens, int32_t B, int32_t Hq,
+                         int32_t max_seq_len, const pka_attn_params* params,
+                         void* workspace, size_t workspace_bytes, void* stream);
+
 /* Log-sum-exp merge of split partials (the merge a split-K softmax needs):
  * M = max_s LSE_s, w_s = exp(LSE_s - M),
  * out = sum_s w_s*O_s / sum_s w_s (bf16 [B][Hq][D]),

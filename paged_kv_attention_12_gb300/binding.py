@@ -32,7 +32,7 @@ EXPORTS = [
     "pka_version", "pka_status_string", "paged_decode_attn", "paged_decode_splitk_plan",
     "paged_decode_splitk_workspace_bytes", "paged_decode_splitk",
     "paged_decode_splitk_combine", "paged_prefill_attn", "paged_attn_check_tables",
-    "paged_decode_attn_noalloc",
+    "paged_decode_attn_noalloc", "paged_decode_attn_ws_bytes", "paged_decode_attn_ws",
 ]
 
 
@@ -87,6 +87,11 @@ def lib() -> ctypes.CDLL:
                                      I32, I32, P(PkaAttnParams), VP]
     L.paged_attn_check_tables.restype = ctypes.c_int
     L.paged_attn_check_tables.argtypes = [VP, I32, VP, I32, I32, I32, VP, VP]
+    L.paged_decode_attn_ws_bytes.restype = ctypes.c_size_t
+    L.paged_decode_attn_ws_bytes.argtypes = [I32, I32, I32, I32, I32, I32]
+    L.paged_decode_attn_ws.restype = ctypes.c_int
+    L.paged_decode_attn_ws.argtypes = [VP, VP, P(PkaKvPool), VP, I32, VP, I32, I32, I32,
+                                       P(PkaAttnParams), VP, ctypes.c_size_t, VP]
     L.paged_decode_attn_noalloc.restype = ctypes.c_int
     L.paged_decode_attn_noalloc.argtypes = [VP, VP, P(PkaKvPool), VP, I32, VP, I32, I32, I32,
                                             P(PkaAttnParams), VP]
@@ -143,6 +148,22 @@ def paged_decode_attn_noalloc(q, out, k_pool, v_pool, block_tables, seq_lens, ma
                                          seq_lens.data_ptr(), q.shape[0], q.shape[1],
                                          int(max_seq_len), ctypes.byref(par), _stream(stream))
     _check("paged_decode_attn_noalloc", st)
+
+
+def paged_decode_attn_ws_bytes(B, Hq, Hkv, D, max_seq_len, window=0) -> int:
+    return int(lib().paged_decode_attn_ws_bytes(B, Hq, Hkv, D, int(max_seq_len), int(window)))
+
+
+def paged_decode_attn_ws(q, out, k_pool, v_pool, block_tables, seq_lens, max_seq_len, workspace,
+                         *, scale, softcap=0.0, window=0, err=None, stream=None):
+    pool = kv_pool(k_pool, v_pool)
+    par = attn_params(scale, softcap, window, err)
+    st = lib().paged_decode_attn_ws(q.data_ptr(), out.data_ptr(), ctypes.byref(pool),
+                                    block_tables.data_ptr(), block_tables.shape[1],
+                                    seq_lens.data_ptr(), q.shape[0], q.shape[1], int(max_seq_len),
+                                    ctypes.byref(par), workspace.data_ptr(),
+                                    workspace.numel() * workspace.element_size(), _stream(stream))
+    _check("paged_decode_attn_ws", st)
 
 
 def paged_decode_splitk_plan(B, Hkv, max_seq_len, block_size=16, window=0, sm_count=0):
@@ -223,6 +244,27 @@ class DecodeSplitK:
                             self.split_blocks, scale=b.scale, softcap=b.softcap,
                             window=b.window, err=err)
         paged_decode_splitk_combine(self.partial_o, self.partial_lse, self.out, lse_out)
+        return self.out
+
+
+class DecodeFused:
+    """Split-K decode with the combine fused in: one launch per call.  Owns a
+    zero-initialised workspace (its counters are left zero by each call)."""
+
+    def __init__(self, batch):
+        import torch
+        self.batch = batch
+        nbytes = paged_decode_attn_ws_bytes(batch.num_requests, batch.num_q_heads,
+                                            batch.num_kv_heads, batch.head_dim, batch.max_seq_len,
+                                            batch.window)
+        self.workspace = torch.zeros(max(nbytes, 16), dtype=torch.uint8, device=batch.q.device)
+        self.out = torch.empty_like(batch.q)
+
+    def run(self, err=None):
+        b = self.batch
+        paged_decode_attn_ws(b.q, self.out, b.k_pool, b.v_pool, b.block_tables, b.seq_lens,
+                             b.max_seq_len, self.workspace, scale=b.scale, softcap=b.softcap,
+                             window=b.window, err=err)
         return self.out
 
 

@@ -177,6 +177,7 @@ struct Piece {
   int qrow;      // query row of the request
   int slot;      // split-K partial slot (direct mode: unused)
   int fill_from; // >= 0: also write LSE=-inf into slots [fill_from, num_splits)
+  int npieces;   // split-K: pieces (slots used) of this segment
 };
 
 // Enumerates the pieces of one CTA.  Every lane of a warp runs it in
@@ -267,6 +268,7 @@ struct PieceIter {
       p.pos = g.pos;
       p.slot = 0;
       p.fill_from = -1;
+      p.npieces = 1;
       item += gridDim.x;
     } else {
       while (true) {
@@ -304,10 +306,11 @@ struct PieceIter {
         const long long cfirst = seg / q;
         p.slot = static_cast<int>(static_cast<long long>(blockIdx.x) - cfirst);
         p.fill_from = -1;
+        p.npieces = (n == 0) ? 0 : static_cast<int>((seg + n - 1) / q - cfirst + 1);
         if (n == 0) {
           p.fill_from = 0;
         } else if (p.slot == 0) {
-          p.fill_from = static_cast<int>((seg + n - 1) / q - cfirst + 1);
+          p.fill_from = p.npieces;
         }
         if (p.ntiles == 0 && p.fill_from < 0) continue;
         break;
@@ -363,8 +366,9 @@ struct DecodeShape {
   static constexpr int kBarBytes = (2 * NSLOT * 8 + 15) / 16 * 16;
   static constexpr int kMergeMLFloats = (2 * NW * G + 3) / 4 * 4;
   static constexpr int kMergeBytes = (kMergeMLFloats + NW * G * D) * 4;
-  // + 1 KiB so the ring can start on a 1024-byte boundary (128B swizzle)
-  static constexpr int kSmemBytes = 1024 + kRingBytes + kBarBytes + kMergeBytes;
+  // + 1 KiB so the ring can start on a 1024-byte boundary (128B swizzle),
+  // + 16 bytes for the fused combine's "last piece" flag
+  static constexpr int kSmemBytes = 1024 + kRingBytes + kBarBytes + kMergeBytes + 16;
   static_assert(G >= 1 && G <= 8, "the query heads of a group are the MMA's N = 8 columns");
   static_assert(kSmemBytes <= 232448, "shared memory");
   static_assert(NSLOT % NW == 0, "each ring slot must have exactly one owner warp");
@@ -498,6 +502,8 @@ __global__ void __launch_bounds__((NW + 1) * 32, 1)
   float* mrg_m = merge;                        // [NW][G]
   float* mrg_l = merge + NW * G;               // [NW][G]
   float* mrg_acc = merge + S::kMergeMLFloats;  // [NW][G][D]
+  volatile int* last_flag =
+      reinterpret_cast<volatile int*>(smem + S::kRingBytes + S::kBarBytes + S::kMergeBytes);
 
   const int warp = threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
@@ -694,14 +700,80 @@ __global__ void __launch_bounds__((NW + 1) * 32, 1)
                                            idx % D] = 0;
       }
     }
+    const bool fused = split && a.seg_counters != nullptr;
     // ---- split-K: slots of this segment no CTA fills get LSE = -inf
-    if (split && pc.fill_from >= 0) {
+    if (split && !fused && pc.fill_from >= 0) {
       if (pc.fill_from > a.num_splits && threadIdx.x == 0) report(a.err, PKA_DEVERR_SEQ_LEN);
       const int nfill = a.num_splits - min(pc.fill_from, a.num_splits);
       for (int idx = threadIdx.x; idx < G * nfill; idx += NW * 32) {
         const int hq = pc.kvh * G + idx / nfill;
         const int sl = pc.fill_from + idx % nfill;
         a.partial_lse[(static_cast<size_t>(pc.b) * a.Hq + hq) * a.num_splits + sl] = -INFINITY;
+      }
+    }
+    // ---- fused LSE combine: the CTA that writes a segment's last piece
+    // merges all of its pieces (the other CTAs' partials are read from L2)
+    // and resets the segment's arrival counter for the next call.
+    if (fused) {
+      if (pc.npieces > a.num_splits && threadIdx.x == 0) report(a.err, PKA_DEVERR_SEQ_LEN);
+      const int np = min(pc.npieces, a.num_splits);
+      bool last = false;
+      if (pc.ntiles > 0 && pc.slot < a.num_splits) {
+        if (threadIdx.x == 0) {
+          __threadfence();  // this CTA's partials before its arrival
+          const int old = atomicAdd(&a.seg_counters[pc.b * a.Hkv + pc.kvh], 1);
+          *last_flag = (old == np - 1) ? 1 : 0;
+        }
+        consumer_sync(NW * 32);
+        last = *last_flag != 0;
+      }
+      if (last) {
+        __threadfence();  // every other piece's partials are visible now
+        // weights of the pieces, per head, into the (free) merge area
+        float* wts = mrg_acc;  // [G][np]
+        float* dens = mrg_m;   // [G]
+        for (int h = warp; h < G; h += NW) {
+          const size_t ph0 = (static_cast<size_t>(pc.b) * a.Hq + pc.kvh * G + h) * a.num_splits;
+          float M = -INFINITY;
+          for (int sl = lane; sl < np; sl += 32) M = fmaxf(M, __ldcg(a.partial_lse + ph0 + sl));
+#pragma unroll
+          for (int off = 16; off >= 1; off >>= 1)
+            M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+          const float Ms = (M == -INFINITY) ? 0.f : M;
+          float den = 0.f;
+          for (int sl = lane; sl < np; sl += 32) {
+            const float w = fast_exp2((__ldcg(a.partial_lse + ph0 + sl) - Ms) * kLog2e);
+            wts[h * np + sl] = w;
+            den += w;
+          }
+#pragma unroll
+          for (int off = 16; off >= 1; off >>= 1) den += __shfl_xor_sync(0xffffffffu, den, off);
+          if (lane == 0) dens[h] = den;
+        }
+        consumer_sync(NW * 32);
+        for (int idx = threadIdx.x; idx < G * D; idx += NW * 32) {
+          const int h = idx / D;
+          const int d = idx % D;
+          const size_t ph0 = (static_cast<size_t>(pc.b) * a.Hq + pc.kvh * G + h) * a.num_splits;
+          float num = 0.f;
+          for (int sl = 0; sl < np; ++sl) {
+            const float w = wts[h * np + sl];
+            if (w != 0.f) num = fmaf(w, __ldcg(a.partial_o + (ph0 + sl) * D + d), num);
+          }
+          const float den = dens[h];
+          reinterpret_cast<uint16_t*>(a.out)[(static_cast<size_t>(pc.qrow) * a.Hq + pc.kvh * G +
+                                              h) * D + d] = f32_to_bf16_rn(den > 0.f ? num / den
+                                                                                      : 0.f);
+        }
+        if (threadIdx.x == 0) a.seg_counters[pc.b * a.Hkv + pc.kvh] = 0;
+        consumer_sync(NW * 32);
+      } else if (pc.ntiles == 0 && pc.fill_from == 0) {
+        // a request with no visible key: output 0
+        for (int idx = threadIdx.x; idx < G * D; idx += NW * 32) {
+          const int hq = pc.kvh * G + idx / D;
+          reinterpret_cast<uint16_t*>(a.out)[(static_cast<size_t>(pc.qrow) * a.Hq + hq) * D +
+                                             idx % D] = 0;
+        }
       }
     }
     pc = nx;

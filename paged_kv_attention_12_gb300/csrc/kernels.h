@@ -21,6 +21,7 @@ struct DecodeArgs {
   int32_t batch, Hq, Hkv, num_blocks, max_blocks;
   int32_t num_splits;              // items per (request, head); 1 in direct mode
   int32_t split_blocks;            // blocks per split; <= 0: direct mode (whole range)
+  int32_t* seg_counters;           // split mode: non-null fuses the combine (zeroed [B*Hkv])
   float scale, softcap;
   int32_t window;
 };

@@ -191,6 +191,60 @@ int paged_decode_splitk(const void* q, float* partial_o, float* partial_lse,
   return e == cudaSuccess ? PKA_OK : PKA_ERR_CUDA;
 }
 
+// Workspace of the fused split-K decode: partial outputs, partial LSEs, then
+// one arrival counter per (request, KV head).
+struct FusedLayout {
+  int32_t S, C;
+  size_t o_bytes, lse_bytes, cnt_bytes;
+};
+
+int fused_layout(int32_t B, int32_t Hq, int32_t Hkv, int32_t D, int32_t max_seq_len,
+                 int32_t window, FusedLayout* L) {
+  int st = paged_decode_splitk_plan(B, Hkv, max_seq_len, 16, window, 0, &L->S, &L->C);
+  if (st != PKA_OK) return st;
+  L->o_bytes = static_cast<size_t>(B) * Hq * L->S * D * sizeof(float);
+  L->lse_bytes = (static_cast<size_t>(B) * Hq * L->S * sizeof(float) + 15) / 16 * 16;
+  L->cnt_bytes = (static_cast<size_t>(B) * Hkv * sizeof(int32_t) + 15) / 16 * 16;
+  return PKA_OK;
+}
+
+size_t paged_decode_attn_ws_bytes(int32_t B, int32_t Hq, int32_t Hkv, int32_t D,
+                                  int32_t max_seq_len, int32_t window) {
+  if (B <= 0 || Hq <= 0 || Hkv <= 0 || D <= 0) return 0;
+  FusedLayout L;
+  if (fused_layout(B, Hq, Hkv, D, max_seq_len, window, &L) != PKA_OK) return 0;
+  return L.o_bytes + L.lse_bytes + L.cnt_bytes;
+}
+
+int paged_decode_attn_ws(const void* q, void* out, const pka_kv_pool* kv,
+                         const int32_t* block_tables, int32_t max_blocks,
+                         const int32_t* seq_lens, int32_t B, int32_t Hq, int32_t max_seq_len,
+                         const pka_attn_params* params, void* workspace,
+                         size_t workspace_bytes, void* stream) {
+  if (out == nullptr || workspace == nullptr) return PKA_ERR_NULL;
+  int st = check_common(q, kv, block_tables, max_blocks, seq_lens, B, Hq, max_seq_len, params);
+  if (st != PKA_OK) return st;
+  if (!aligned16(out) || !aligned16(workspace)) return PKA_ERR_ALIGN;
+  if (B == 0) return PKA_OK;
+  FusedLayout L;
+  st = fused_layout(B, Hq, kv->num_kv_heads, kv->head_dim, max_seq_len, params->window, &L);
+  if (st != PKA_OK) return st;
+  if (workspace_bytes < L.o_bytes + L.lse_bytes + L.cnt_bytes) return PKA_ERR_WORKSPACE;
+  pka::DecodeArgs a = decode_args(q, kv, block_tables, max_blocks, seq_lens, B, Hq, params);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  a.out = out;
+  a.partial_o = reinterpret_cast<float*>(ws);
+  a.partial_lse = reinterpret_cast<float*>(ws + L.o_bytes);
+  a.seg_counters = reinterpret_cast<int32_t*>(ws + L.o_bytes + L.lse_bytes);
+  a.num_splits = L.S;
+  a.split_blocks = L.C;
+  const int sms = pka::device_sm_count();
+  if (sms <= 0) return PKA_ERR_CUDA;
+  cudaError_t e = pka::launch_decode(a, kv->head_dim, Hq / kv->num_kv_heads, sms,
+                                     static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? PKA_OK : PKA_ERR_CUDA;
+}
+
 int paged_decode_splitk_combine(const float* partial_o, const float* partial_lse, int32_t B,
                                 int32_t Hq, int32_t D, int32_t num_splits, void* out,
                                 float* lse_out, void* stream) {

@@ -168,6 +168,46 @@ def test_splitk_with_empty_requests():
         assert torch.all(out[b] == 0)
 
 
+# ------------------------------------------------------ fused split-K path
+@pytest.mark.parametrize("maker", ["tiny", "serving0", "serving1", "long", "empty"])
+def test_fused_splitk_matches_oracle_and_leaves_counters_zero(maker):
+    if maker == "tiny":
+        batch = workload.decode_tiny(2, DEV, poison=True)
+    elif maker.startswith("serving"):
+        batch = workload.decode_serving(1, DEV, poison=True, scale_down=True,
+                                        drop_out_of_window=True)[int(maker[-1])]
+    elif maker == "long":
+        batch = workload.decode_long(0, DEV, poison=True, scale_down=True)
+    else:
+        L = [0, 40, 0, 700, 1]
+        b0 = workload.make_batch(seq_lens=L, q_lens=[1 if x else 0 for x in L], num_q_heads=8,
+                                 num_kv_heads=2, head_dim=256, num_blocks=70, cfg_id=14,
+                                 device=DEV, poison=True)
+        q = torch.randn((len(L), 8, 256), device=DEV).to(torch.bfloat16)
+        batch = workload.PagedBatch(**{**b0.__dict__, "q": q, "q_lens_host": [1] * len(L)})
+    ref, _, _ = oracle_decode(batch)
+    runner = binding.DecodeFused(batch)
+    err = new_err()
+    for call in range(3):
+        out = runner.run(err=err)
+        assert_close(to_f64(out), ref, f"fused {maker} call {call}")
+    torch.cuda.synchronize()
+    assert err.item() == 0
+    S, C = binding.paged_decode_splitk_plan(batch.num_requests, batch.num_kv_heads,
+                                            batch.max_seq_len, 16, batch.window)
+    B, Hq, D, Hkv = batch.num_requests, batch.num_q_heads, batch.head_dim, batch.num_kv_heads
+    off = B * Hq * S * D * 4 + (B * Hq * S * 4 + 15) // 16 * 16
+    counters = runner.workspace[off:off + B * Hkv * 4].view(torch.int32)
+    assert torch.all(counters == 0), "arrival counters must be left zero"
+
+
+def test_fused_equals_two_launch_split_k():
+    batch = workload.decode_serving(2, DEV, scale_down=True)[0]
+    a = binding.DecodeFused(batch).run().clone()
+    b = binding.DecodeSplitK(batch).run()
+    assert torch.equal(a, b)
+
+
 # -------------------------------------------------------- full-size samples
 @pytest.mark.parametrize("cfg", [2, 3])
 def test_full_size_sampled_requests(cfg):
@@ -176,6 +216,8 @@ def test_full_size_sampled_requests(cfg):
     calls = workload.workload(cfg, seed=0, device=DEV, poison=True)
     for batch in calls:
         out, _ = run_splitk(batch)
+        outf = binding.DecodeFused(batch).run()
+        assert torch.equal(out, outf)
         B = batch.num_requests
         reqs = sorted({0, B - 1, B // 2, int(np.argmax(batch.seq_lens_host)),
                        int(np.argmin(batch.seq_lens_host))})
@@ -275,7 +317,7 @@ def test_repeated_launches_are_deterministic_and_never_time_out():
     finish without a bounded-wait timeout and give bit-identical results (the
     partition and every reduction order are fixed)."""
     calls = workload.decode_serving(0, DEV)
-    runners = [binding.DecodeSplitK(b) for b in calls]
+    runners = [binding.DecodeSplitK(b) for b in calls] + [binding.DecodeFused(b) for b in calls]
     err = new_err()
     first = [r.run(err=err).clone() for r in runners]
     for it in range(150):
