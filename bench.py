@@ -53,6 +53,9 @@ def parse():
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-clocks", action="store_true", help="do not sample nvidia-smi clocks")
+    p.add_argument("--path", choices=["fused", "split"], default="fused",
+                   help="fused: split-K decode with the combine in the same launch; "
+                        "split: split-K decode launch + combine launch")
     p.add_argument("--no-other", action="store_true",
                    help="skip the per-workload measurements of the other configurations")
     p.add_argument("--cpu-seconds", type=float, default=15.0,
@@ -377,26 +380,45 @@ def main():
     binding.lib()
 
     calls = workload.decode_serving(args.seed + 1000 * rank, dev)
-    runners = [binding.DecodeFused(b) for b in calls]
+    if args.path == "fused":
+        runners = [binding.DecodeFused(b) for b in calls]
+    else:
+        runners = [binding.DecodeSplitK(b) for b in calls]
     bytes_step = step_bytes(calls)
     flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream()
 
-    def step(kernel_events=None):
-        # one fused split-K decode launch per layer (the LSE combine runs in
-        # the same kernel)
-        for i, (b, r) in enumerate(zip(calls, runners)):
-            if kernel_events is not None:
-                kernel_events[i][0].record(stream)
+    def launch(i):
+        """The decode kernel of call i (the dominant kernel)."""
+        b, r = calls[i], runners[i]
+        if args.path == "fused":
             binding.paged_decode_attn_ws(b.q, r.out, b.k_pool, b.v_pool, b.block_tables,
                                          b.seq_lens, b.max_seq_len, r.workspace, scale=b.scale,
                                          softcap=b.softcap, window=b.window)
-            if kernel_events is not None:
-                kernel_events[i][1].record(stream)
+        else:
+            binding.paged_decode_splitk(b.q, r.partial_o, r.partial_lse, b.k_pool, b.v_pool,
+                                        b.block_tables, b.seq_lens, b.max_seq_len, r.num_splits,
+                                        r.split_blocks, scale=b.scale, softcap=b.softcap,
+                                        window=b.window)
+
+    def step():
+        for i, r in enumerate(runners):
+            launch(i)
+            if args.path == "split":
+                binding.paged_decode_splitk_combine(r.partial_o, r.partial_lse, r.out)
 
     for _ in range(args.warmup):
         flush.fill_(1.0)
         step()
+    torch.cuda.synchronize()
+    # One step as a CUDA graph: the launches of a step run back to back on the
+    # GPU, whatever the host-side cost of issuing them.
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        step()
+    for _ in range(2):
+        flush.fill_(1.0)
+        graph.replay()
     torch.cuda.synchronize()
 
     sampler = ClockSampler(local) if (rank == 0 and not args.no_clocks) else None
@@ -404,26 +426,37 @@ def main():
         sampler.start()
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
           for _ in range(args.steps)]
-    kev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-            for _ in calls] for _ in range(args.steps)]
     barrier(world)
     torch.cuda.synchronize()
     t_wall = time.perf_counter()
-    for s in range(args.steps):
-        flush.fill_(float(s))
-        ev[s][0].record(stream)
-        step(kev[s])
-        ev[s][1].record(stream)
+    for s_ in range(args.steps):
+        flush.fill_(float(s_))
+        ev[s_][0].record(stream)
+        graph.replay()
+        ev[s_][1].record(stream)
     torch.cuda.synchronize()
     barrier(world)
     wall = time.perf_counter() - t_wall
     clocks = sampler.stop() if sampler else None
     step_ms = [a.elapsed_time(b) for a, b in ev]
     print("step ms: " + " ".join(f"{x:.3f}" for x in step_ms), file=sys.stderr)
-    kern_ms = [sum(a.elapsed_time(b) for a, b in ks) for ks in kev]
     total_ms = max_over_ranks(sum(step_ms), world)
     ms_per_step = total_ms / args.steps
     value = world * bytes_step / (ms_per_step * 1e-3) / 1e9
+
+    # the dominant kernel alone: each decode launch timed by CUDA events on
+    # its stream, the L2 flushed before it
+    kern_ms = []
+    for s_ in range(args.steps):
+        for i in range(len(calls)):
+            flush.fill_(float(s_))
+            k0, k1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            k0.record(stream)
+            launch(i)
+            k1.record(stream)
+            kern_ms.append((k0, k1))
+    torch.cuda.synchronize()
+    kern_ms = [a.elapsed_time(b) for a, b in kern_ms]
 
     # end to end through the public API with pinned host buffers
     e2e = None
@@ -444,7 +477,7 @@ def main():
                 b.q.copy_(hq, non_blocking=True)
                 b.block_tables.copy_(ht, non_blocking=True)
                 b.seq_lens.copy_(hs, non_blocking=True)
-            step()
+            graph.replay()
             for ho, r in zip(host_out, runners):
                 ho.copy_(r.out, non_blocking=True)
             e1.record(stream)
@@ -462,7 +495,7 @@ def main():
         return 0
 
     peak, peak_kind = hbm_peak()
-    kern_avg_s = sum(kern_ms) / (len(kern_ms) * len(calls)) * 1e-3
+    kern_avg_s = sum(kern_ms) / len(kern_ms) * 1e-3
     achieved = (bytes_step / len(calls)) / kern_avg_s / 1e9
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
@@ -470,13 +503,15 @@ def main():
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic",
         "config": {"workload": WORKLOAD_NAME, "l2": "flushed before every step (512 MiB write)",
-                   "path": "paged_decode_attn_ws (split-K, combine fused)",
+                   "path": ("paged_decode_attn_ws (split-K, combine fused)" if args.path == "fused"
+                            else "paged_decode_splitk + paged_decode_splitk_combine"),
+                   "timing": "each step one CUDA-graph replay, CUDA events around it",
                    "bytes_per_step": bytes_step, "parallelism": f"replicas{world}"},
-        "roofline": {"bound": "hbm", "kernel": "paged_decode_kernel (split-K, fused combine)",
+        "roofline": {"bound": "hbm", "kernel": "paged_decode_kernel" + (" (split-K, fused combine)" if args.path == "fused" else " (split-K)"),
                      "achieved": achieved, "peak": peak, "peak_kind": peak_kind,
                      "unit": "GB/s", "frac": achieved / peak,
                      "traffic": traffic_from_profile()},
-        "gpu_launches": args.steps * len(calls),
+        "gpu_launches": args.steps * len(calls) * (1 if args.path == "fused" else 2),
         "wall_s": wall,
     }
     if e2e:

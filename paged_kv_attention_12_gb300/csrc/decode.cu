@@ -751,19 +751,51 @@ __global__ void __launch_bounds__((NW + 1) * 32, 1)
           if (lane == 0) dens[h] = den;
         }
         consumer_sync(NW * 32);
-        for (int idx = threadIdx.x; idx < G * D; idx += NW * 32) {
-          const int h = idx / D;
-          const int d = idx % D;
+        // one (head, 8-column chunk) per thread; the partials of four pieces
+        // are in flight at a time
+        for (int item = threadIdx.x; item < G * (D / 8); item += NW * 32) {
+          const int h = item / (D / 8);
+          const int d0 = (item % (D / 8)) * 8;
           const size_t ph0 = (static_cast<size_t>(pc.b) * a.Hq + pc.kvh * G + h) * a.num_splits;
-          float num = 0.f;
-          for (int sl = 0; sl < np; ++sl) {
-            const float w = wts[h * np + sl];
-            if (w != 0.f) num = fmaf(w, __ldcg(a.partial_o + (ph0 + sl) * D + d), num);
+          float acc8[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) acc8[e] = 0.f;
+          for (int s0 = 0; s0 < np; s0 += 4) {
+            float4 x[4][2];
+            float w[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              w[u] = (s0 + u < np) ? wts[h * np + s0 + u] : 0.f;
+              if (w[u] != 0.f) {
+                const float4* src =
+                    reinterpret_cast<const float4*>(a.partial_o + (ph0 + s0 + u) * D + d0);
+                x[u][0] = __ldcg(src);
+                x[u][1] = __ldcg(src + 1);
+              } else {
+                x[u][0] = x[u][1] = make_float4(0.f, 0.f, 0.f, 0.f);
+              }
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              acc8[0] = fmaf(w[u], x[u][0].x, acc8[0]);
+              acc8[1] = fmaf(w[u], x[u][0].y, acc8[1]);
+              acc8[2] = fmaf(w[u], x[u][0].z, acc8[2]);
+              acc8[3] = fmaf(w[u], x[u][0].w, acc8[3]);
+              acc8[4] = fmaf(w[u], x[u][1].x, acc8[4]);
+              acc8[5] = fmaf(w[u], x[u][1].y, acc8[5]);
+              acc8[6] = fmaf(w[u], x[u][1].z, acc8[6]);
+              acc8[7] = fmaf(w[u], x[u][1].w, acc8[7]);
+            }
           }
           const float den = dens[h];
-          reinterpret_cast<uint16_t*>(a.out)[(static_cast<size_t>(pc.qrow) * a.Hq + pc.kvh * G +
-                                              h) * D + d] = f32_to_bf16_rn(den > 0.f ? num / den
-                                                                                      : 0.f);
+          const float inv = den > 0.f ? 1.f / den : 0.f;
+          uint16_t* dst = reinterpret_cast<uint16_t*>(a.out) +
+                          (static_cast<size_t>(pc.qrow) * a.Hq + pc.kvh * G + h) * D + d0;
+          *reinterpret_cast<uint4*>(dst) =
+              make_uint4(pack_bf16x2(acc8[0] * inv, acc8[1] * inv),
+                         pack_bf16x2(acc8[2] * inv, acc8[3] * inv),
+                         pack_bf16x2(acc8[4] * inv, acc8[5] * inv),
+                         pack_bf16x2(acc8[6] * inv, acc8[7] * inv));
         }
         if (threadIdx.x == 0) a.seg_counters[pc.b * a.Hkv + pc.kvh] = 0;
         consumer_sync(NW * 32);
