@@ -53,7 +53,7 @@ def parse():
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-clocks", action="store_true", help="do not sample nvidia-smi clocks")
-    p.add_argument("--path", choices=["fused", "split"], default="fused",
+    p.add_argument("--path", choices=["fused", "split"], default="split",
                    help="fused: split-K decode with the combine in the same launch; "
                         "split: split-K decode launch + combine launch")
     p.add_argument("--no-other", action="store_true",

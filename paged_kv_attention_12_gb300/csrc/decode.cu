@@ -52,88 +52,6 @@ namespace pka {
 
 namespace {
 
-// ---------------------------------------------------------- packed fp32 x2
-__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
-  float2 d;
-  asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\t"
-      "mov.b64 ra, {%2, %3};\n\t"
-      "mov.b64 rb, {%4, %5};\n\t"
-      "mov.b64 rc, {%6, %7};\n\t"
-      "fma.rn.f32x2 rd, ra, rb, rc;\n\t"
-      "mov.b64 {%0, %1}, rd;\n\t}"
-      : "=f"(d.x), "=f"(d.y)
-      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
-  return d;
-}
-
-__device__ __forceinline__ float2 fmul2(float2 a, float2 b) {
-  float2 d;
-  asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
-      "mov.b64 ra, {%2, %3};\n\t"
-      "mov.b64 rb, {%4, %5};\n\t"
-      "mul.rn.f32x2 rd, ra, rb;\n\t"
-      "mov.b64 {%0, %1}, rd;\n\t}"
-      : "=f"(d.x), "=f"(d.y)
-      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
-  return d;
-}
-
-// Select kept opaque to the compiler: a chain of these over a small array
-// must stay a chain of selects (left visible, the compiler turns it into a
-// runtime-indexed array in local memory).
-__device__ __forceinline__ float opaque_sel(bool c, float a, float b) {
-  float r;
-  asm("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %1, 0;\n\tselp.f32 %0, %2, %3, p;\n\t}"
-      : "=f"(r)
-      : "r"(static_cast<int>(c)), "f"(a), "f"(b));
-  return r;
-}
-
-__device__ __forceinline__ void unpack8x2(const uint4& u, float2 (&f)[4]) {
-  bf16x2_to_f32(u.x, f[0].x, f[0].y);
-  bf16x2_to_f32(u.y, f[1].x, f[1].y);
-  bf16x2_to_f32(u.z, f[2].x, f[2].y);
-  bf16x2_to_f32(u.w, f[3].x, f[3].y);
-}
-
-// Reduce-scatter of N per-lane partial sums across the LPK lanes that share
-// a key: stage with xor offset O keeps the upper half of the values on lanes
-// with that bit set.  Afterwards lane dl holds the full sums of indices
-// (dl / DUP) * NVL + j, j < NVL (NVL = max(N / LPK, 1), DUP = max(LPK / N, 1)).
-template <int N, int O>
-struct ReduceScatter {
-  static __device__ __forceinline__ void run(float* v, int lane) {
-    if constexpr (O == 0) {
-      return;
-    } else if constexpr (N >= 2) {
-      constexpr int H = N / 2;
-      const bool upper = (lane & O) != 0;
-#pragma unroll
-      for (int k = 0; k < H; ++k) {
-        const float send = upper ? v[k] : v[k + H];
-        const float keep = upper ? v[k + H] : v[k];
-        v[k] = keep + __shfl_xor_sync(0xffffffffu, send, O);
-      }
-      ReduceScatter<H, O / 2>::run(v, lane);
-    } else {
-      v[0] += __shfl_xor_sync(0xffffffffu, v[0], O);
-      ReduceScatter<1, O / 2>::run(v, lane);
-    }
-  }
-};
-
-__device__ __forceinline__ float warp_max(float x) {
-#pragma unroll
-  for (int o = 16; o >= 1; o >>= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, o));
-  return x;
-}
-
-__device__ __forceinline__ float warp_sum(float x) {
-#pragma unroll
-  for (int o = 16; o >= 1; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
-  return x;
-}
-
 __device__ __forceinline__ int warp_incl_scan(int x, int lane) {
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
