@@ -288,7 +288,7 @@ struct DecodeShape {
   // + 16 bytes for the fused combine's "last piece" flag
   static constexpr int kSmemBytes = 1024 + kRingBytes + kBarBytes + kMergeBytes + 16;
   static_assert(G >= 1 && G <= 8, "the query heads of a group are the MMA's N = 8 columns");
-  static_assert(kSmemBytes <= 232448, "shared memory");
+  static_assert(kSmemBytes <= 232448 / 2 - 1024, "two CTAs per SM");
   static_assert(NSLOT % NW == 0, "each ring slot must have exactly one owner warp");
 };
 
@@ -404,7 +404,7 @@ __device__ __forceinline__ void decode_slot(
 }
 
 template <int D, int G, int NW, int NSLOT>
-__global__ void __launch_bounds__((NW + 1) * 32, 1)
+__global__ void __launch_bounds__((NW + 1) * 32, 2)
     paged_decode_kernel(const __grid_constant__ DecodeArgs a,
                         const __grid_constant__ CUtensorMap tm_k,
                         const __grid_constant__ CUtensorMap tm_v) {
@@ -736,12 +736,14 @@ namespace {
 
 template <int D, int G>
 struct DecodeTuning {
-  // NW consumer warps + 1 producer warp, one CTA per SM.  The arithmetic of a
-  // slot is a few dozen instructions, so a few consumer warps keep up with
-  // HBM; the shared memory goes to ring slots (bytes in flight), SPW per
-  // consumer warp (each slot owned by one warp).
-  static constexpr int NW = 4;
-  static constexpr int SPW = (D == 256) ? 3 : 6;
+  // Two persistent CTAs per SM, each with one producer warp: one thread's
+  // wait -> expect -> issue loop caps the copy rate of a CTA, so two CTAs per
+  // SM stream about 1.6x the bytes of one with the same ring depth in total.
+  // Each CTA has NW consumer warps and a ring of about 96 KB (SPW slots per
+  // consumer warp, each slot owned by one warp).
+  static constexpr int kCtasPerSm = 2;
+  static constexpr int NW = (D == 256) ? 2 : 4;
+  static constexpr int SPW = (G == 8) ? 2 : 3;
   static constexpr int NSLOT = NW * SPW;
 };
 
@@ -784,7 +786,9 @@ cudaError_t launch_decode_t(const DecodeArgs& a, int grid, cudaStream_t stream) 
   auto kern = paged_decode_kernel<D, G, NW, NSLOT>;
   cudaError_t e = set_smem_once(reinterpret_cast<const void*>(kern), S::kSmemBytes);
   if (e != cudaSuccess) return e;
-  kern<<<grid, (NW + 1) * 32, S::kSmemBytes, stream>>>(a, tk, tv);
+  // grid is given per SM count; the kernel is persistent with two CTAs per SM
+  const long long g2 = static_cast<long long>(grid) * DecodeTuning<D, G>::kCtasPerSm;
+  kern<<<static_cast<unsigned>(g2), (NW + 1) * 32, S::kSmemBytes, stream>>>(a, tk, tv);
   return cudaGetLastError();
 }
 

@@ -129,7 +129,8 @@ int paged_decode_attn(const void* q, void* out, const pka_kv_pool* kv,
   const int items = B * kv->num_kv_heads;
   const int sms = pka::device_sm_count();
   if (sms <= 0) return PKA_ERR_CUDA;
-  const int grid = items < sms ? items : sms;
+  // launch_decode runs two CTAs per unit of grid
+  const int grid = items < 2 * sms ? (items + 1) / 2 : sms;
   cudaError_t e = pka::launch_decode(a, kv->head_dim, Hq / kv->num_kv_heads, grid,
                                      static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? PKA_OK : PKA_ERR_CUDA;
