@@ -135,8 +135,8 @@ size_t paged_decode_splitk_workspace_bytes(int32_t B, int32_t Hq, int32_t D,
  * blocks ("tiles", blocks [jlo_b, jlo_b + n_b), jlo_b = block of the first
  * visible key).  Segments are laid end to end in (request, head) order,
  * T = Hkv * sum_b n_b tiles in all, and cut into chunks of
- * q = max(C, ceil(T / grid)) tiles, grid = the GPU's SM count; chunk c is
- * streamed by CTA c.  The part of a segment starting at tile A that falls
+ * q = max(C, ceil(T / grid)) tiles, grid = twice the GPU's SM count;
+ * chunk c is streamed by CTA c.  The part of a segment starting at tile A that falls
  * in chunk c is written to slot c - floor(A / q): its softmax-normalised
  * partial output partial_o fp32 [B][Hq][S][D] and its natural-log LSE
  * partial_lse fp32 [B][Hq][S].  Slots a segment does not use get LSE -inf

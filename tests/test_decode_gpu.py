@@ -102,8 +102,9 @@ def test_decode_head_shapes(D, G, Hkv):
     assert_close(to_f64(out), ref, "splitk")
 
 
-def sm_count():
-    return torch.cuda.get_device_properties(0).multi_processor_count
+def decode_grid():
+    """CTAs of a split-K decode launch: two per SM."""
+    return 2 * torch.cuda.get_device_properties(0).multi_processor_count
 
 
 @pytest.mark.parametrize("maker", ["long", "serving_w", "tiny"])
@@ -121,7 +122,7 @@ def test_splitk_partials_match_oracle_partials(maker):
     runner.run()
     arr = workload.to_numpy_f64(batch)
     ranges = oracle.balanced_split_ranges(batch.seq_lens_host, batch.window, 16,
-                                          batch.num_kv_heads, sm_count(), runner.split_blocks)
+                                          batch.num_kv_heads, decode_grid(), runner.split_blocks)
     po, pl = oracle.splitk_partials(arr["q"], arr["k_pool"], arr["v_pool"], arr["block_tables"],
                                     arr["seq_lens"], batch.scale, batch.softcap, batch.window,
                                     runner.num_splits, ranges=ranges)
