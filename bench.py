@@ -311,13 +311,20 @@ def barrier(world):
 
 
 def max_over_ranks(x: float, world: int) -> float:
+    """Largest value over the ranks (the slowest rank's time)."""
     if world <= 1:
         return x
     import torch
     import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def replica_seed(seed: int, rank: int) -> int:
+    """Each replica draws its own workload (weak scaling, no data exchange)."""
+    return seed + 1000 * rank
 
 
 def run_reference(args):
@@ -379,7 +386,7 @@ def main():
         _build.build()
     binding.lib()
 
-    calls = workload.decode_serving(args.seed + 1000 * rank, dev)
+    calls = workload.decode_serving(replica_seed(args.seed, rank), dev)
     if args.path == "fused":
         runners = [binding.DecodeFused(b) for b in calls]
     else:
