@@ -7,8 +7,8 @@ seq_lens ~ U[512, 4096], Hq=8, Hkv=2, head_dim=256, block_size=16, a pool of
 through two layers with separate pools: a global layer (window 0) and a
 sliding layer (window 512).
 
-Each layer is one launch of the split-K decode kernel with the LSE combine
-fused in.
+Each layer is one split-K decode launch followed by one LSE-combine launch
+(``--path fused`` puts the combine into the decode launch instead).
 
 Metric: paged-decode KV GB/s, counting algorithmic bytes (K/V rows of every
 visible key plus the query rows) per step over the device time of the step.
@@ -60,6 +60,9 @@ def parse():
                    help="skip the per-workload measurements of the other configurations")
     p.add_argument("--cpu-seconds", type=float, default=15.0,
                    help="budget of the oracle sample (CPU baseline)")
+    p.add_argument("--workload", type=int, choices=[1, 3, 4, 5], default=None,
+                   help="time only this other configuration (--steps launches after "
+                        "--warmup) and print its entry as the JSON line")
     return p.parse_args()
 
 
@@ -257,7 +260,7 @@ def time_launches(fn, flush, iters, warmup):
     return statistics.median(a.elapsed_time(b) for a, b in ts)
 
 
-def other_workloads(dev, flush, iters=10, warmup=3):
+def other_workloads(dev, flush, iters=10, warmup=3, cfgs=(1, 3, 4, 5)):
     """The tiny decode, long-context split-K, chunked-prefill and mixed-batch
     workloads, each timed alone (L2 flushed first)."""
     import torch
@@ -265,7 +268,7 @@ def other_workloads(dev, flush, iters=10, warmup=3):
     hbm, hbm_kind = hbm_peak()
     tc, tc_kind = bf16_peak()
     res = {}
-    for cfg in (1, 3, 4, 5):
+    for cfg in cfgs:
         batch = workload.workload(cfg, seed=0, device=dev)[0]
         nbytes = batch_kv_bytes(batch)
         flops = 4.0 * batch.head_dim * batch.num_q_heads * attention_pairs(batch)
@@ -385,6 +388,15 @@ def main():
     if rank == 0 or world > 1:
         _build.build()
     binding.lib()
+
+    if args.workload is not None:
+        flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+        entry = other_workloads(dev, flush, iters=args.steps, warmup=max(args.warmup, 1),
+                                cfgs=(args.workload,))[str(args.workload)]
+        if rank == 0:
+            print(json.dumps({"workload_only": args.workload, "n_gpus": world, "steps": args.steps,
+                              "warmup": args.warmup, "data": "synthetic", **entry}))
+        return 0
 
     calls = workload.decode_serving(replica_seed(args.seed, rank), dev)
     if args.path == "fused":
