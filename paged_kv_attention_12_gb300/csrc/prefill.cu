@@ -13,20 +13,23 @@
 // (row = token * G + g), so all G heads share every K/V tile.  Per item:
 //
 //  * warp 4 (TMA): the Q tile (one 3-D box per 64-column chunk) and, per key
-//    tile, one 2-D box per (pool block, 64-column chunk) of K into a 2-stage
+//    tile, one 2-D box per (pool block, 64-column chunk) of K into a 3-stage
 //    ring; blocks past the request's last block get an out-of-range row
 //    coordinate so TMA fills zeros; a stage is refilled once S = Q K^T of
 //    the tile it held has completed;
-//  * warp 5 (TMA): the same for V, refilled once P V of its tile completed;
+//  * warp 5 (TMA): the same for V (2 stages), refilled once P V of its tile
+//    completed;
 //  * warp 6 (MMA): allocates TMEM (2 S buffers + the O accumulator), issues
 //    S_j = Q K_j^T (K-major A and B, 128B-swizzled) two tiles ahead, then
-//    O += P_j V_j (V as an MN-major operand), committing each to mbarriers;
-//    it also zeroes V rows past seq_len (stale slots of the last block, which
-//    may hold NaN) before they reach P V;
+//    O += P_j V_j with P_j read from TMEM and V as an MN-major shared-memory
+//    operand, committing each to mbarriers; it also zeroes V rows past
+//    seq_len (stale slots of the last block, which may hold NaN) before they
+//    reach P V;
 //  * warps 0-3 (softmax): thread r owns row r.  It reads its S row from
 //    TMEM, applies scale, softcap and the causal / window mask, keeps a
-//    running max and sum in the exp2 domain, writes P (bf16, swizzled) to
-//    shared memory and signals the MMA warp.  O is rescaled in TMEM only
+//    running max and sum in the exp2 domain, writes P (bf16 pairs) back over
+//    the first half of the same TMEM row and signals the MMA warp (P never
+//    touches shared memory, which holds Q and the K/V rings).  O is rescaled in TMEM only
 //    when the row max grows by more than 2^8 (the stale reference max keeps
 //    every P <= 256, and O and the sum share it, so the result is exact);
 //  * epilogue: O / sum from TMEM to bf16 rows of the output.
@@ -48,28 +51,30 @@ struct PrefillShape {
   static constexpr int TQ = BM / G;                 // tokens per query tile
   static constexpr int BN = (D == 256) ? 64 : 128;  // keys per key tile
   static constexpr int DC = D / 64;                 // 128-byte chunks of a K/V/Q row
-  static constexpr int NC = BN / 64;                // 128-byte chunks of a P row
   static constexpr int kBlocksPerTile = BN / kBlockSize;
   static constexpr int kQChunk = BM * 128;
   static constexpr int kKVChunk = BN * 128;
-  static constexpr int kPChunk = BM * 128;
   static constexpr int kQBytes = BM * D * 2;
   static constexpr int kKVBytes = BN * D * 2;
-  static constexpr int kPBytes = BM * BN * 2;
+  static constexpr int KST = 3;                     // K ring stages
+  static constexpr int VST = 2;                     // V ring stages
   static constexpr int oQ = 0;
   static constexpr int oK = oQ + kQBytes;
-  static constexpr int oV = oK + 2 * kKVBytes;
-  static constexpr int oP = oV + 2 * kKVBytes;
-  static constexpr int oBar = oP + 2 * kPBytes;
-  static constexpr int kNumBars = 11;
+  static constexpr int oV = oK + KST * kKVBytes;
+  static constexpr int oBar = oV + VST * kKVBytes;
+  static constexpr int kNumBars = 12;
   static constexpr int oMisc = oBar + kNumBars * 8;
   static constexpr int kSmemBytes = oMisc + 16 + 1024;  // + slack to align the base to 1 KiB
-  static constexpr uint32_t kTmemO = 256;               // O columns [256, 256 + D)
+  // TMEM: S_j (fp32, BN columns) in buffer j % 2 at column (j % 2) * BN; the
+  // softmax overwrites its first BN / 2 columns with P_j (bf16 pairs), the A
+  // operand of P_j V_j; O (fp32) in columns [256, 256 + D).
+  static constexpr uint32_t kTmemO = 256;
   static constexpr uint32_t kTmemCols = 512;
   static constexpr int kThreads = 7 * 32;
   // cost buckets of the heaviest-first ranking (scratch in the K stages)
   static constexpr int kCostBuckets = 4096;
-  static_assert((kCostBuckets + 64) * 4 <= 2 * kKVBytes, "ranking scratch");
+  static_assert((kCostBuckets + 64) * 4 <= KST * kKVBytes, "ranking scratch");
+  static_assert(BN % 64 == 0, "P is stored to TMEM 32 columns (64 keys) at a time");
   static_assert(kSmemBytes <= 232448, "shared memory");
   static_assert(2 * BN <= 256 && D <= 256, "TMEM columns");
 };
@@ -85,7 +90,7 @@ struct Item {
 };
 
 // bar indices
-enum { B_Q = 0, B_KFULL = 1, B_VFULL = 3, B_QK = 5, B_PV = 7, B_PRDY = 9 };
+enum { B_Q = 0, B_KFULL = 1, B_VFULL = 4, B_QK = 6, B_PV = 8, B_PRDY = 10 };
 
 __device__ __forceinline__ bool stop_requested(const volatile int* flag) { return *flag != 0; }
 
@@ -266,7 +271,6 @@ __global__ void __launch_bounds__(PrefillShape<D, G>::kThreads, 1)
   uint8_t* sQ = smem + S::oQ;
   uint8_t* sK = smem + S::oK;
   uint8_t* sV = smem + S::oV;
-  uint8_t* sP = smem + S::oP;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S::oBar);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + S::oMisc);
   volatile int* failed = reinterpret_cast<volatile int*>(smem + S::oMisc + 4);
@@ -276,8 +280,8 @@ __global__ void __launch_bounds__(PrefillShape<D, G>::kThreads, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(&bars[B_Q], 1);
+    for (int i = 0; i < S::KST; ++i) mbar_init(&bars[B_KFULL + i], 1);
     for (int i = 0; i < 2; ++i) {
-      mbar_init(&bars[B_KFULL + i], 1);
       mbar_init(&bars[B_VFULL + i], 1);
       mbar_init(&bars[B_QK + i], 1);
       mbar_init(&bars[B_PV + i], 1);
@@ -297,7 +301,10 @@ __global__ void __launch_bounds__(PrefillShape<D, G>::kThreads, 1)
 
   if (warp == kWarpTmaK || warp == kWarpTmaV) {
     // ============================ TMA producers ============================
+    // K stage j % 3 is refilled once S_j = Q K_j^T has completed, V stage
+    // j % 2 once P_j V_j has; both "freed" barriers alternate by tile parity.
     const bool is_k = (warp == kWarpTmaK);
+    const int nst = is_k ? S::KST : S::VST;
     const CUtensorMap* tm = is_k ? &tm_k : &tm_v;
     uint8_t* ring = is_k ? sK : sV;
     uint64_t* full = &bars[is_k ? B_KFULL : B_VFULL];
@@ -314,8 +321,9 @@ __global__ void __launch_bounds__(PrefillShape<D, G>::kThreads, 1)
       }
       for (int j = 0; j < it.ntiles; ++j) {
         if (stop_requested(failed)) break;
-        const int st = j & 1;
-        if (j >= 2 && !cta_wait(&freed[st], ((j - 2) >> 1) & 1, a.err, failed)) break;
+        const int st = j % nst;
+        const int jf = j - nst;  // the tile that held this stage before
+        if (jf >= 0 && !cta_wait(&freed[jf & 1], (jf >> 1) & 1, a.err, failed)) break;
         mbar_arrive_expect_tx(&full[st], S::kKVBytes);
         uint8_t* dst = ring + st * S::kKVBytes;
 #pragma unroll
@@ -337,8 +345,8 @@ __global__ void __launch_bounds__(PrefillShape<D, G>::kThreads, 1)
         issued = j + 1;
       }
       // every issued copy must land before the CTA may finish
-      for (int j = issued - 2 < 0 ? 0 : issued - 2; j < issued; ++j)
-        mbar_wait(&full[j & 1], (j >> 1) & 1, a.err);
+      for (int j = issued - nst < 0 ? 0 : issued - nst; j < issued; ++j)
+        mbar_wait(&full[j % nst], (j / nst) & 1, a.err);
       if (is_k && stop_requested(failed)) mbar_wait(&bars[B_Q], 0, a.err);
     }
     __syncwarp();
@@ -346,15 +354,16 @@ __global__ void __launch_bounds__(PrefillShape<D, G>::kThreads, 1)
     // ================================ MMA ================================
     constexpr uint32_t idesc_qk = idesc_bf16_f32(128, BN, 0, 0);
     constexpr uint32_t idesc_pv = idesc_bf16_f32(128, D, 0, 1);
-    const uint32_t aQ = smem_u32(sQ), aK = smem_u32(sK), aV = smem_u32(sV), aP = smem_u32(sP);
+    const uint32_t aQ = smem_u32(sQ), aK = smem_u32(sK), aV = smem_u32(sV);
     int committed_pv = 0;  // number of P V tiles issued
     bool ok = warp_wait(&bars[B_Q], 0, a.err, failed);
     auto issue_qk = [&](int j) -> bool {
-      const int st = j & 1;
-      if (!warp_wait(&bars[B_KFULL + st], (j >> 1) & 1, a.err, failed)) return false;
+      const int st = j & 1;  // S buffer
+      const int ks = j % S::KST;
+      if (!warp_wait(&bars[B_KFULL + ks], (j / S::KST) & 1, a.err, failed)) return false;
       tc_fence_after();
       if (lane == 0) {
-        const uint32_t kst = aK + st * S::kKVBytes;
+        const uint32_t kst = aK + ks * S::kKVBytes;
 #pragma unroll
         for (int c = 0; c < DC; ++c)
 #pragma unroll
@@ -395,13 +404,15 @@ __global__ void __launch_bounds__(PrefillShape<D, G>::kThreads, 1)
       if (!warp_wait(&bars[B_PRDY + st], ph, a.err, failed)) break;
       tc_fence_after();
       if (lane == 0) {
-        const uint32_t pst = aP + st * S::kPBytes;
+        // A = P_j from TMEM (8 columns per 16 keys), B = V_j from the ring;
+        // the MMA pipe runs in issue order, so S_{j+2} (issued next into the
+        // same TMEM buffer) cannot overwrite P_j before this has read it
         const uint32_t vst = aV + st * S::kKVBytes;
 #pragma unroll
         for (int k = 0; k < BN / 16; ++k) {
-          const uint64_t da = smem_desc_sw128(pst + (k / 4) * S::kPChunk + (k % 4) * 32, 16, 1024);
           const uint64_t db = smem_desc_sw128(vst + k * 16 * 128, S::kKVChunk, 1024);
-          umma_bf16(tmem + S::kTmemO, da, db, idesc_pv, (j > 0 || k > 0) ? 1u : 0u);
+          umma_bf16_ts(tmem + S::kTmemO, tmem + st * BN + k * 8, db, idesc_pv,
+                       (j > 0 || k > 0) ? 1u : 0u);
         }
         umma_commit(&bars[B_PV + st]);
       }
@@ -495,29 +506,24 @@ __global__ void __launch_bounds__(PrefillShape<D, G>::kThreads, 1)
       if (resc) l *= fast_exp2(m_ref - m_new);
       if (j == 0 || resc) m_ref = m_new;
       const float ms = (m_ref == -INFINITY) ? 0.f : m_ref;
-      // P buffer st was last read by P_{j-2} V_{j-2}
-      if (j >= 2 && !warp_wait(&bars[B_PV + st], ((j - 2) >> 1) & 1, a.err, failed)) {
-        ok = false;
-        break;
-      }
-      uint8_t* prow = sP + st * S::kPBytes + r * 128;
+      // P_j (bf16 pairs) over the first BN / 2 columns of S_j's buffer.  Every
+      // earlier MMA reading that buffer (P_{j-2} V_{j-2}) was issued before
+      // S_j, whose completion this thread has waited for.
       float lsum = 0.f;
 #pragma unroll
-      for (int q = 0; q < BN / 8; ++q) {
-        float pv8[8];
+      for (int h = 0; h < BN / 64; ++h) {
+        uint32_t pk[32];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          pv8[e] = fast_exp2(s[q * 8 + e] - ms);
-          lsum += pv8[e];
+        for (int e = 0; e < 32; ++e) {
+          const float p0 = fast_exp2(s[h * 64 + 2 * e] - ms);
+          const float p1 = fast_exp2(s[h * 64 + 2 * e + 1] - ms);
+          lsum += p0 + p1;
+          pk[e] = pack_bf16x2(p0, p1);
         }
-        const uint4 w = make_uint4(pack_bf16x2(pv8[0], pv8[1]), pack_bf16x2(pv8[2], pv8[3]),
-                                   pack_bf16x2(pv8[4], pv8[5]), pack_bf16x2(pv8[6], pv8[7]));
-        const int region = q / 8;
-        const int chunk = (q % 8) ^ (r & 7);
-        *reinterpret_cast<uint4*>(prow + region * S::kPChunk + chunk * 16) = w;
+        tmem_st32_u(lane_base + st * BN + h * 32, pk);
       }
       l += lsum;
-      fence_proxy_async_smem();
+      tmem_wait_st();
       tc_fence_before();
       mbar_arrive(&bars[B_PRDY + st]);
     }
