@@ -23,8 +23,9 @@
 //
 // Inside a CTA:
 //  * one producer warp walks the pieces' block tables (32 ids per coalesced
-//    load) and loads, per tile, the (block, head) K and V tiles as 16-row x
-//    64-column TMA boxes with the 128-byte swizzle into a ring of
+//    load) and loads, per tile, the (block, head) K and V tiles with one
+//    3-D TMA copy each (D / 64 boxes of 16 rows x 64 columns, 128-byte
+//    swizzle) into a ring of
 //    shared-memory slots, completion counted on a "full" mbarrier;
 //  * NW consumer warps take the ring's tiles round robin; every slot has one
 //    owner warp, so each slot's mbarrier phases are consumed in order.  A
@@ -479,22 +480,20 @@ __global__ void __launch_bounds__((NW + 1) * 32, 2)
           if (lane == 0) {
             if (round > 0)
               good = mbar_wait(&empty[slot], static_cast<uint32_t>((round - 1) & 1), a.err);
-            if (good) {
-              mbar_arrive_expect_tx(&full[slot], 2 * S::kTileBytes);
-              uint8_t* dst = ring + static_cast<size_t>(slot) * 2 * S::kTileBytes;
-#pragma unroll
-              for (int c = 0; c < S::DC; ++c) {
-                tma_load_2d(dst + c * S::kBoxBytes, &tm_k, c * 64, static_cast<int>(r0),
-                            &full[slot]);
-                tma_load_2d(dst + S::kTileBytes + c * S::kBoxBytes, &tm_v, c * 64,
-                            static_cast<int>(r0), &full[slot]);
-              }
-            }
+            if (good) mbar_arrive_expect_tx(&full[slot], 2 * S::kTileBytes);
           }
           good = __shfl_sync(0xffffffffu, good, 0);
           if (!good) {
             ok = false;
             break;
+          }
+          // one copy per tensor (the whole 16 x D block as DC boxes of 16 rows
+          // x 64 columns), K from lane 0 and V from lane 1: one thread's
+          // copies are processed one after another
+          if (lane < 2) {
+            uint8_t* dst =
+                ring + static_cast<size_t>(slot) * 2 * S::kTileBytes + lane * S::kTileBytes;
+            tma_load_3d(dst, lane == 0 ? &tm_k : &tm_v, 0, static_cast<int>(r0), 0, &full[slot]);
           }
           ++issued;
         }
@@ -775,16 +774,21 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// A pool viewed as a 2-D tensor [num_blocks * Hkv * 16 rows][D], read in
-// 16-row x 64-column boxes with the 128-byte swizzle.
+// A pool viewed as a 3-D tensor (64 columns, num_blocks * Hkv * 16 rows,
+// D / 64 column chunks) with strides (2, 2 D, 128) bytes, read in boxes of
+// (64, 16, D / 64) with the 128-byte swizzle: one copy brings a block's
+// 16 x D tile as D / 64 consecutive 16-row x 64-column boxes, the layout the
+// consumers' ldmatrix addressing expects.  Fewer, larger copies keep the
+// TMA unit's per-copy cost off the critical path.
 bool pool_map(CUtensorMap* m, const void* base, int D, long long rows) {
   auto fn = encode_fn();
   if (fn == nullptr) return false;
-  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(rows)};
-  const cuuint64_t str[1] = {static_cast<cuuint64_t>(D) * 2};
-  const cuuint32_t box[2] = {64, static_cast<cuuint32_t>(kBlockSize)};
-  const cuuint32_t estr[2] = {1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, str, box, estr,
+  const cuuint64_t dims[3] = {64, static_cast<cuuint64_t>(rows), static_cast<cuuint64_t>(D / 64)};
+  const cuuint64_t str[2] = {static_cast<cuuint64_t>(D) * 2, 128};
+  const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(kBlockSize),
+                             static_cast<cuuint32_t>(D / 64)};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, str, box, estr,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }

@@ -27,8 +27,8 @@
 //    reach P V;
 //  * warps 0-3 (softmax): thread r owns row r.  It reads its S row from
 //    TMEM, applies scale, softcap and the causal / window mask, keeps a
-//    running max and sum in the exp2 domain, writes P (bf16 pairs) back over
-//    the first half of the same TMEM row and signals the MMA warp (P never
+//    running max and sum in the exp2 domain, writes P (bf16 pairs) to its
+//    own TMEM columns and signals the MMA warp (P never
 //    touches shared memory, which holds Q and the K/V rings).  O is rescaled in TMEM only
 //    when the row max grows by more than 2^8 (the stale reference max keeps
 //    every P <= 256, and O and the sum share it, so the result is exact);
@@ -53,28 +53,36 @@ struct PrefillShape {
   static constexpr int DC = D / 64;                 // 128-byte chunks of a K/V/Q row
   static constexpr int kBlocksPerTile = BN / kBlockSize;
   static constexpr int kQChunk = BM * 128;
-  static constexpr int kKVChunk = BN * 128;
+  static constexpr int kKVChunk = BN * 128;        // K stage: [D/64 chunks][BN rows][128 B]
+  static constexpr int kVBlock = kBlockSize * D * 2;  // V stage: [BN/16 blocks][D/64 chunks][16 rows][128 B]
   static constexpr int kQBytes = BM * D * 2;
   static constexpr int kKVBytes = BN * D * 2;
   static constexpr int KST = 3;                     // K ring stages
   static constexpr int VST = 2;                     // V ring stages
+  static constexpr int kPrefetch = 4;               // L2 prefetch distance (tiles)
   static constexpr int oQ = 0;
   static constexpr int oK = oQ + kQBytes;
   static constexpr int oV = oK + KST * kKVBytes;
   static constexpr int oBar = oV + VST * kKVBytes;
-  static constexpr int kNumBars = 12;
+  static constexpr int kNumBars = 15;
   static constexpr int oMisc = oBar + kNumBars * 8;
   static constexpr int kSmemBytes = oMisc + 16 + 1024;  // + slack to align the base to 1 KiB
-  // TMEM: S_j (fp32, BN columns) in buffer j % 2 at column (j % 2) * BN; the
-  // softmax overwrites its first BN / 2 columns with P_j (bf16 pairs), the A
-  // operand of P_j V_j; O (fp32) in columns [256, 256 + D).
+  // TMEM columns: S_j (fp32, BN columns) in buffer j % 2 at (j % 2) * BN;
+  // O (fp32) at [256, 256 + D); P_j (bf16 pairs, BN / 2 columns), the A
+  // operand of P_j V_j, in buffer j % 2 at kTmemP + (j % 2) * BN / 2.  P has
+  // columns of its own: S_{j+2} may be written while P_j V_j still reads P_j
+  // (consecutive MMAs overlap in the pipe), so P_j must not alias S_j.
   static constexpr uint32_t kTmemO = 256;
+  static constexpr uint32_t kTmemP = (D == 256) ? 2 * BN : 256 + D;
   static constexpr uint32_t kTmemCols = 512;
   static constexpr int kThreads = 7 * 32;
   // cost buckets of the heaviest-first ranking (scratch in the K stages)
   static constexpr int kCostBuckets = 4096;
   static_assert((kCostBuckets + 64) * 4 <= KST * kKVBytes, "ranking scratch");
   static_assert(BN % 64 == 0, "P is stored to TMEM 32 columns (64 keys) at a time");
+  static_assert(kTmemP >= 2 * BN && (kTmemP + BN <= kTmemO || kTmemP >= kTmemO + D) &&
+                    kTmemP + BN <= kTmemCols,
+                "P buffers clear of S and O");
   static_assert(kSmemBytes <= 232448, "shared memory");
   static_assert(2 * BN <= 256 && D <= 256, "TMEM columns");
 };
@@ -90,7 +98,11 @@ struct Item {
 };
 
 // bar indices
-enum { B_Q = 0, B_KFULL = 1, B_VFULL = 4, B_QK = 6, B_PV = 8, B_PRDY = 10 };
+// Every ring stage has its own "empty" barrier (K: B_KEMPTY, V: B_PV, whose
+// two barriers are the two V stages), so a producer waiting for use r - 1 of
+// a stage can never see the barrier one phase further on: use r cannot
+// complete before the producer has loaded it.
+enum { B_Q = 0, B_KFULL = 1, B_VFULL = 4, B_QK = 6, B_PV = 8, B_PRDY = 10, B_KEMPTY = 12 };
 
 __device__ __forceinline__ bool stop_requested(const volatile int* flag) { return *flag != 0; }
 
@@ -113,6 +125,18 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, int32_
 __device__ __forceinline__ float tanh_via_exp2(float y) {
   const float e = fast_exp2(fminf(2.f * kLog2e * y, 126.f));
   return 1.f - __fdividef(2.f, e + 1.f);
+}
+
+// tanh(y) for |y| < 0.5 from its odd Taylor series through y^11 (the first
+// omitted term, 21844 y^13 / 6081075, is below 4.5e-7 there): FMA-pipe work
+// only, where the exp2 form needs two MUFU operations.
+__device__ __forceinline__ float tanh_taylor(float y) {
+  const float y2 = y * y;
+  float q = fmaf(y2, -1382.f / 155925.f, 62.f / 2835.f);
+  q = fmaf(y2, q, -17.f / 315.f);
+  q = fmaf(y2, q, 2.f / 15.f);
+  q = fmaf(y2, q, -1.f / 3.f);
+  return fmaf(y * y2, q, y);
 }
 
 // Cost of query tile qt of request b in key tiles (0: no query row there).
@@ -224,7 +248,8 @@ __global__ void __launch_bounds__(PrefillShape<D, G>::kThreads, 1)
     paged_prefill_kernel(const __grid_constant__ PrefillArgs a,
                          const __grid_constant__ CUtensorMap tm_q,
                          const __grid_constant__ CUtensorMap tm_k,
-                         const __grid_constant__ CUtensorMap tm_v) {
+                         const __grid_constant__ CUtensorMap tm_v,
+                         const __grid_constant__ CUtensorMap tm_k3) {
   using S = PrefillShape<D, G>;
   constexpr int BN = S::BN, TQ = S::TQ, DC = S::DC;
 
@@ -280,7 +305,10 @@ __global__ void __launch_bounds__(PrefillShape<D, G>::kThreads, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(&bars[B_Q], 1);
-    for (int i = 0; i < S::KST; ++i) mbar_init(&bars[B_KFULL + i], 1);
+    for (int i = 0; i < S::KST; ++i) {
+      mbar_init(&bars[B_KFULL + i], 1);
+      mbar_init(&bars[B_KEMPTY + i], 1);
+    }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bars[B_VFULL + i], 1);
       mbar_init(&bars[B_QK + i], 1);
@@ -302,48 +330,112 @@ __global__ void __launch_bounds__(PrefillShape<D, G>::kThreads, 1)
   if (warp == kWarpTmaK || warp == kWarpTmaV) {
     // ============================ TMA producers ============================
     // K stage j % 3 is refilled once S_j = Q K_j^T has completed, V stage
-    // j % 2 once P_j V_j has; both "freed" barriers alternate by tile parity.
+    // j % 2 once P_j V_j has.
     const bool is_k = (warp == kWarpTmaK);
     const int nst = is_k ? S::KST : S::VST;
-    const CUtensorMap* tm = is_k ? &tm_k : &tm_v;
+    static_assert(S::VST == 2, "the two P V barriers double as the V stages' empty barriers");
+    const CUtensorMap* tm = &tm_k;  // 2-D K map (V uses its 3-D map directly)
     uint8_t* ring = is_k ? sK : sV;
     uint64_t* full = &bars[is_k ? B_KFULL : B_VFULL];
-    uint64_t* freed = &bars[is_k ? B_QK : B_PV];
+    uint64_t* freed = &bars[is_k ? B_KEMPTY : B_PV];
     int issued = 0;
     if (lane == 0) {
-      prefetch_tensormap(tm);
+      prefetch_tensormap(is_k ? &tm_k : &tm_v);
       if (is_k) {
+        prefetch_tensormap(&tm_k3);
         prefetch_tensormap(&tm_q);
         mbar_arrive_expect_tx(&bars[B_Q], S::kQBytes);
 #pragma unroll
         for (int c = 0; c < DC; ++c)
           tma_load_3d(sQ + c * S::kQChunk, &tm_q, c * 64, it.kvh * G, it.q0 + it.it0, &bars[B_Q]);
       }
-      for (int j = 0; j < it.ntiles; ++j) {
-        if (stop_requested(failed)) break;
-        const int st = j % nst;
-        const int jf = j - nst;  // the tile that held this stage before
-        if (jf >= 0 && !cta_wait(&freed[jf & 1], (jf >> 1) & 1, a.err, failed)) break;
-        mbar_arrive_expect_tx(&full[st], S::kKVBytes);
-        uint8_t* dst = ring + st * S::kKVBytes;
-#pragma unroll
-        for (int kb = 0; kb < S::kBlocksPerTile; ++kb) {
-          const int jb = it.kbase / kBlockSize + j * S::kBlocksPerTile + kb;
-          uint32_t row = oob_row;  // past the request's last block: TMA fills zeros
-          if (jb < it.nblk) {
-            const int id = trow[jb];
-            if (static_cast<unsigned>(id) < static_cast<unsigned>(a.num_blocks))
-              row = (static_cast<uint32_t>(id) * a.Hkv + it.kvh) * kBlockSize;
-            else
-              report(a.err, PKA_DEVERR_BAD_TABLE);
-          }
-#pragma unroll
-          for (int c = 0; c < DC; ++c)
-            tma_load_2d(dst + c * S::kKVChunk + kb * kBlockSize * 128, tm, c * 64,
-                        static_cast<int>(row), &full[st]);
-        }
-        issued = j + 1;
+    }
+    // Pool rows of the item's blocks, read by the whole warp 32 at a time
+    // (one coalesced load) into a sliding window of 64 blocks held one per
+    // lane in two registers; lane 0 takes them by shuffle.  Block b (counted
+    // from the first key tile) maps to TMA row (id * Hkv + kvh) * 16, or to an
+    // out-of-range row past the request's last block (TMA fills zeros).
+    constexpr int BPT = S::kBlocksPerTile;
+    const int jb0 = it.kbase / kBlockSize;
+    auto load_rows = [&](int base) -> uint32_t {
+      const int jb = jb0 + base + lane;
+      uint32_t row = oob_row;
+      if (jb < it.nblk) {
+        const int id = trow[jb];
+        if (static_cast<unsigned>(id) < static_cast<unsigned>(a.num_blocks))
+          row = (static_cast<uint32_t>(id) * a.Hkv + it.kvh) * kBlockSize;
+        else
+          report(a.err, PKA_DEVERR_BAD_TABLE);
       }
+      return row;
+    };
+    int win = 0;  // window = blocks [win, win + 64)
+    uint32_t rows_lo = load_rows(0), rows_hi = load_rows(32);
+    auto row_of = [&](int blk) -> uint32_t {  // blk in [win, win + 64); warp-uniform
+      const int r = blk - win;
+      const uint32_t lo = __shfl_sync(0xffffffffu, rows_lo, r & 31);
+      const uint32_t hi = __shfl_sync(0xffffffffu, rows_hi, r & 31);
+      return r < 32 ? lo : hi;
+    };
+    static_assert((S::kPrefetch + 1) * BPT <= 32 + BPT, "prefetch tile inside the id window");
+    for (int j = 0; j < it.ntiles; ++j) {
+      if (__any_sync(0xffffffffu, stop_requested(failed))) break;
+      // keep tiles j .. j + kPrefetch inside the window
+      while ((j + S::kPrefetch + 1) * BPT > win + 64) {
+        rows_lo = rows_hi;
+        rows_hi = load_rows(win + 64);
+        win += 32;
+      }
+      uint32_t rl[BPT], rp[BPT];
+#pragma unroll
+      for (int kb = 0; kb < BPT; ++kb) {
+        rl[kb] = row_of(j * BPT + kb);
+        rp[kb] = row_of((j + S::kPrefetch) * BPT + kb);
+      }
+      const int st = j % nst;
+      int good = 1;
+      if (lane == 0) {
+        if (j >= nst && !cta_wait(&freed[st], (j / nst - 1) & 1, a.err, failed)) good = 0;
+        if (good) mbar_arrive_expect_tx(&full[st], S::kKVBytes);
+      }
+      if (!__shfl_sync(0xffffffffu, good, 0)) break;
+      // The copies of a stage are issued by several lanes at once: one
+      // thread's copies are processed one after another, so a single issuing
+      // thread caps the fill rate well below what L2 delivers (a copy of L2
+      // data every ~600 cycles from one thread, ~2.5x the bytes from many).
+      uint8_t* dst = ring + st * S::kKVBytes;
+      if (is_k) {
+        // K: chunk-major (the S MMA reads 64 keys of one 64-column chunk as
+        // 8 uniformly strided 8-row groups), one box per (block, chunk)
+        if (lane < BPT * DC) {
+          const int kb = lane / DC, c = lane % DC;
+          uint32_t r = rl[0];
+#pragma unroll
+          for (int q = 1; q < BPT; ++q)
+            if (kb == q) r = rl[q];
+          tma_load_2d(dst + c * S::kKVChunk + kb * kBlockSize * 128, tm, c * 64,
+                      static_cast<int>(r), &full[st]);
+        }
+      } else if (lane < BPT) {
+        // V: block-major (each P V MMA reads one block's 16 keys), one 3-D
+        // copy per block
+        uint32_t r = rl[0];
+#pragma unroll
+        for (int q = 1; q < BPT; ++q)
+          if (lane == q) r = rl[q];
+        tma_load_3d(dst + lane * S::kVBlock, &tm_v, 0, static_cast<int>(r), 0, &full[st]);
+      }
+      // pull tile j + kPrefetch into L2, one block per lane
+      if (j + S::kPrefetch < it.ntiles && lane < BPT) {
+        uint32_t r = rp[0];
+#pragma unroll
+        for (int q = 1; q < BPT; ++q)
+          if (lane == q) r = rp[q];
+        if (r != oob_row) tma_prefetch_3d(is_k ? &tm_k3 : &tm_v, 0, static_cast<int>(r), 0);
+      }
+      issued = j + 1;
+    }
+    if (lane == 0) {
       // every issued copy must land before the CTA may finish
       for (int j = issued - nst < 0 ? 0 : issued - nst; j < issued; ++j)
         mbar_wait(&full[j % nst], (j / nst) & 1, a.err);
@@ -373,6 +465,7 @@ __global__ void __launch_bounds__(PrefillShape<D, G>::kThreads, 1)
             umma_bf16(tmem + st * BN, da, db, idesc_qk, (c | kk) != 0);
           }
         umma_commit(&bars[B_QK + st]);
+        umma_commit(&bars[B_KEMPTY + ks]);
       }
       __syncwarp();
       return true;
@@ -395,7 +488,8 @@ __global__ void __launch_bounds__(PrefillShape<D, G>::kThreads, 1)
           const int r = z0 + idx / (DC * 8);
           const int c = (idx / 8) % DC;
           const int q = idx % 8;
-          *reinterpret_cast<uint4*>(vst + c * S::kKVChunk + r * 128 + q * 16) =
+          *reinterpret_cast<uint4*>(vst + (r / kBlockSize) * S::kVBlock + c * (kBlockSize * 128) +
+                                    (r % kBlockSize) * 128 + q * 16) =
               make_uint4(0u, 0u, 0u, 0u);
         }
         fence_proxy_async_smem();
@@ -404,14 +498,13 @@ __global__ void __launch_bounds__(PrefillShape<D, G>::kThreads, 1)
       if (!warp_wait(&bars[B_PRDY + st], ph, a.err, failed)) break;
       tc_fence_after();
       if (lane == 0) {
-        // A = P_j from TMEM (8 columns per 16 keys), B = V_j from the ring;
-        // the MMA pipe runs in issue order, so S_{j+2} (issued next into the
-        // same TMEM buffer) cannot overwrite P_j before this has read it
+        // A = P_j from TMEM (8 columns per 16 keys), B = V_j from the ring
         const uint32_t vst = aV + st * S::kKVBytes;
 #pragma unroll
         for (int k = 0; k < BN / 16; ++k) {
-          const uint64_t db = smem_desc_sw128(vst + k * 16 * 128, S::kKVChunk, 1024);
-          umma_bf16_ts(tmem + S::kTmemO, tmem + st * BN + k * 8, db, idesc_pv,
+          // block k of the stage: 64-column chunks 16 x 128 B apart
+          const uint64_t db = smem_desc_sw128(vst + k * S::kVBlock, kBlockSize * 128, 1024);
+          umma_bf16_ts(tmem + S::kTmemO, tmem + S::kTmemP + st * (BN / 2) + k * 8, db, idesc_pv,
                        (j > 0 || k > 0) ? 1u : 0u);
         }
         umma_commit(&bars[B_PV + st]);
@@ -463,27 +556,34 @@ __global__ void __launch_bounds__(PrefillShape<D, G>::kThreads, 1)
       const int t0 = it.kbase + j * BN;
       const int c_hi = row_valid ? min(BN - 1, p - t0) : -1;
       const int c_lo = max(0, kmin - t0);
-      float mx = -INFINITY;
-      if (capped) {
-#pragma unroll
-        for (int c = 0; c < BN; ++c) s[c] = cap_out * tanh_via_exp2(s[c] * cap_in);
-      } else {
-#pragma unroll
-        for (int c = 0; c < BN; ++c) s[c] *= sl2;
-      }
       // Only rows on a causal diagonal or a window edge need the per-column
       // mask; the warp takes the masked loop only if one of its rows does.
-      if (__any_sync(0xffffffffu, c_lo > 0 || c_hi < BN - 1)) {
+      const bool need_mask = __any_sync(0xffffffffu, c_lo > 0 || c_hi < BN - 1);
+      if (capped) {
+        // log2-domain logits cap * tanh(s * scale / cap) * log2(e); the
+        // Taylor form when every |y| of the warp's rows is below 0.5
+        float amax = 0.f;
 #pragma unroll
-        for (int c = 0; c < BN; ++c) {
-          const float x = (c >= c_lo && c <= c_hi) ? s[c] : -INFINITY;
-          s[c] = x;
-          mx = fmaxf(mx, x);
+        for (int c = 0; c < BN; ++c) amax = fmaxf(amax, fabsf(s[c]));
+        if (__all_sync(0xffffffffu, amax * cap_in < 0.5f)) {
+#pragma unroll
+          for (int c = 0; c < BN; ++c) s[c] = cap_out * tanh_taylor(s[c] * cap_in);
+        } else {
+#pragma unroll
+          for (int c = 0; c < BN; ++c) s[c] = cap_out * tanh_via_exp2(s[c] * cap_in);
         }
-      } else {
-#pragma unroll
-        for (int c = 0; c < BN; ++c) mx = fmaxf(mx, s[c]);
       }
+      // (uncapped: s stays raw; scale > 0, so the raw max scales to the max)
+      if (need_mask) {
+#pragma unroll
+        for (int c = 0; c < BN; ++c)
+          if (!(c >= c_lo && c <= c_hi)) s[c] = -INFINITY;
+      }
+      float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+      for (int c = 0; c < BN; ++c) m4[c & 3] = fmaxf(m4[c & 3], s[c]);
+      float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+      if (!capped) mx *= sl2;
       const float m_new = fmaxf(m_ref, mx);
       const bool resc = (j > 0) && (m_new > m_ref + 8.f);
       if (__any_sync(0xffffffffu, resc)) {
@@ -506,23 +606,27 @@ __global__ void __launch_bounds__(PrefillShape<D, G>::kThreads, 1)
       if (resc) l *= fast_exp2(m_ref - m_new);
       if (j == 0 || resc) m_ref = m_new;
       const float ms = (m_ref == -INFINITY) ? 0.f : m_ref;
-      // P_j (bf16 pairs) over the first BN / 2 columns of S_j's buffer.  Every
-      // earlier MMA reading that buffer (P_{j-2} V_{j-2}) was issued before
-      // S_j, whose completion this thread has waited for.
-      float lsum = 0.f;
+      // P_j (bf16 pairs) into P buffer j % 2.  Its last reader, P_{j-2}
+      // V_{j-2}, was issued before S_j, whose completion this thread has
+      // waited for (a commit covers every earlier MMA of the issuer).
+      // p = 2^(x - ms), x the log2-domain logit (uncapped: x = s * scale * log2 e,
+      // fused into one FMA)
+      const float xs = capped ? 1.f : sl2;
+      float lsum0 = 0.f, lsum1 = 0.f;
 #pragma unroll
       for (int h = 0; h < BN / 64; ++h) {
         uint32_t pk[32];
 #pragma unroll
         for (int e = 0; e < 32; ++e) {
-          const float p0 = fast_exp2(s[h * 64 + 2 * e] - ms);
-          const float p1 = fast_exp2(s[h * 64 + 2 * e + 1] - ms);
-          lsum += p0 + p1;
+          const float p0 = fast_exp2(fmaf(s[h * 64 + 2 * e], xs, -ms));
+          const float p1 = fast_exp2(fmaf(s[h * 64 + 2 * e + 1], xs, -ms));
+          lsum0 += p0;
+          lsum1 += p1;
           pk[e] = pack_bf16x2(p0, p1);
         }
-        tmem_st32_u(lane_base + st * BN + h * 32, pk);
+        tmem_st32_u(lane_base + S::kTmemP + st * (BN / 2) + h * 32, pk);
       }
-      l += lsum;
+      l += lsum0 + lsum1;
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(&bars[B_PRDY + st]);
@@ -592,7 +696,7 @@ bool make_map(CUtensorMap* m, const void* base, int rank, const cuuint64_t* dims
 template <int D, int G>
 cudaError_t launch_prefill_t(const PrefillArgs& a, cudaStream_t stream) {
   using S = PrefillShape<D, G>;
-  CUtensorMap tq, tk, tv;
+  CUtensorMap tq, tk, tv, tk3;
   {
     const cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(a.Hq),
                                 static_cast<cuuint64_t>(a.total_q)};
@@ -607,7 +711,17 @@ cudaError_t launch_prefill_t(const PrefillArgs& a, cudaStream_t stream) {
     const cuuint64_t str[1] = {static_cast<cuuint64_t>(D) * 2};
     const cuuint32_t box[2] = {64, static_cast<cuuint32_t>(kBlockSize)};
     if (!make_map(&tk, a.k, 2, dims, str, box)) return cudaErrorInvalidValue;
-    if (!make_map(&tv, a.v, 2, dims, str, box)) return cudaErrorInvalidValue;
+  }
+  {
+    // (64 columns, rows, D / 64 chunks), strides (2 D, 128) bytes: one box is
+    // a block's 16 x D tile as D / 64 consecutive 16 x 64 boxes
+    const cuuint64_t dims[3] = {64, static_cast<cuuint64_t>(a.num_blocks) * a.Hkv * kBlockSize,
+                                static_cast<cuuint64_t>(D / 64)};
+    const cuuint64_t str[2] = {static_cast<cuuint64_t>(D) * 2, 128};
+    const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(kBlockSize),
+                               static_cast<cuuint32_t>(D / 64)};
+    if (!make_map(&tv, a.v, 3, dims, str, box)) return cudaErrorInvalidValue;
+    if (!make_map(&tk3, a.k, 3, dims, str, box)) return cudaErrorInvalidValue;
   }
   auto kern = paged_prefill_kernel<D, G>;
   cudaError_t e = set_smem_once(reinterpret_cast<const void*>(kern), S::kSmemBytes);
@@ -616,7 +730,7 @@ cudaError_t launch_prefill_t(const PrefillArgs& a, cudaStream_t stream) {
   const long long ctas = static_cast<long long>(a.batch) * qtiles * a.Hkv;
   if (ctas > 0x7fffffffLL) return cudaErrorInvalidValue;
   dim3 grid(static_cast<unsigned>(ctas));
-  kern<<<grid, S::kThreads, S::kSmemBytes, stream>>>(a, tq, tk, tv);
+  kern<<<grid, S::kThreads, S::kSmemBytes, stream>>>(a, tq, tk, tv, tk3);
   return cudaGetLastError();
 }
 

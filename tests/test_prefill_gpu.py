@@ -143,3 +143,21 @@ def test_repeated_launches_are_deterministic_and_never_time_out():
     torch.cuda.synchronize()
     assert err.item() == 0
     assert torch.equal(out, ref)
+
+
+@pytest.mark.parametrize("cfg", [4, 5])
+def test_full_size_repeated_launches_identical(cfg):
+    """A pipeline hazard (a stage or TMEM buffer reused while still being
+    read) shows up as run-to-run differences or non-finite values at full
+    size, where timing varies most: every launch must give the same bits."""
+    batch = workload.workload(cfg, seed=1, device=DEV, poison=True)[0]
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    ref = run(batch, err).clone()
+    assert torch.isfinite(ref.float()).all()
+    out = torch.empty_like(batch.q)
+    for _ in range(8):
+        out.fill_(float("nan"))
+        binding.run_batch(batch, out, err)
+        assert torch.equal(out, ref)
+    torch.cuda.synchronize()
+    assert err.item() == 0
