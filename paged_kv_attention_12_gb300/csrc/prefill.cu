@@ -12,13 +12,16 @@
 // tokens x the G query heads of one KV group into the 128 rows of the MMA
 // (row = token * G + g), so all G heads share every K/V tile.  Per item:
 //
-//  * warp 4 (TMA): the Q tile (one 3-D box per 64-column chunk) and, per key
-//    tile, one 2-D box per (pool block, 64-column chunk) of K into a 3-stage
-//    ring; blocks past the request's last block get an out-of-range row
-//    coordinate so TMA fills zeros; a stage is refilled once S = Q K^T of
-//    the tile it held has completed;
-//  * warp 5 (TMA): the same for V (2 stages), refilled once P V of its tile
+//  * warps 4 and 7 (TMA): the Q tile (one 3-D box per 64-column chunk) and,
+//    per key tile, one 2-D box per (pool block, 64-column chunk) of K into a
+//    3-stage ring, each warp half of the blocks (a TMA copy costs the issuing
+//    warp ~80 cycles whatever its size, and a tile has 16 such boxes); blocks
+//    past the request's last block get an out-of-range row coordinate so TMA
+//    fills zeros; a stage is refilled once S = Q K^T of the tile it held has
 //    completed;
+//  * warp 5 (TMA): V, one 3-D copy per block (block-major stages, which the
+//    P V MMA reads one 16-key block at a time), 2 stages, refilled once P V
+//    of its tile completed;
 //  * warp 6 (MMA): allocates TMEM (2 S buffers + the O accumulator), issues
 //    S_j = Q K_j^T (K-major A and B, 128B-swizzled) two tiles ahead, then
 //    O += P_j V_j with P_j read from TMEM and V as an MN-major shared-memory
@@ -59,7 +62,6 @@ struct PrefillShape {
   static constexpr int kKVBytes = BN * D * 2;
   static constexpr int KST = 3;                     // K ring stages
   static constexpr int VST = 2;                     // V ring stages
-  static constexpr int kPrefetch = 4;               // L2 prefetch distance (tiles)
   static constexpr int oQ = 0;
   static constexpr int oK = oQ + kQBytes;
   static constexpr int oV = oK + KST * kKVBytes;
@@ -75,7 +77,7 @@ struct PrefillShape {
   static constexpr uint32_t kTmemO = 256;
   static constexpr uint32_t kTmemP = (D == 256) ? 2 * BN : 256 + D;
   static constexpr uint32_t kTmemCols = 512;
-  static constexpr int kThreads = 7 * 32;
+  static constexpr int kThreads = 8 * 32;
   // cost buckets of the heaviest-first ranking (scratch in the K stages)
   static constexpr int kCostBuckets = 4096;
   static_assert((kCostBuckets + 64) * 4 <= KST * kKVBytes, "ranking scratch");
@@ -92,6 +94,7 @@ namespace {
 constexpr int kWarpTmaK = 4;
 constexpr int kWarpTmaV = 5;
 constexpr int kWarpMma = 6;
+constexpr int kWarpTmaK2 = 7;
 
 struct Item {
   int b, kvh, q0, n, L, it0, it1, kbase, ntiles, nblk;
@@ -248,8 +251,7 @@ __global__ void __launch_bounds__(PrefillShape<D, G>::kThreads, 1)
     paged_prefill_kernel(const __grid_constant__ PrefillArgs a,
                          const __grid_constant__ CUtensorMap tm_q,
                          const __grid_constant__ CUtensorMap tm_k,
-                         const __grid_constant__ CUtensorMap tm_v,
-                         const __grid_constant__ CUtensorMap tm_k3) {
+                         const __grid_constant__ CUtensorMap tm_v) {
   using S = PrefillShape<D, G>;
   constexpr int BN = S::BN, TQ = S::TQ, DC = S::DC;
 
@@ -327,22 +329,23 @@ __global__ void __launch_bounds__(PrefillShape<D, G>::kThreads, 1)
   const uint32_t oob_row = static_cast<uint32_t>(a.num_blocks) * a.Hkv * kBlockSize;
   const int32_t* trow = a.tables + static_cast<size_t>(it.b) * a.max_blocks;
 
-  if (warp == kWarpTmaK || warp == kWarpTmaV) {
+  if (warp == kWarpTmaK || warp == kWarpTmaK2 || warp == kWarpTmaV) {
     // ============================ TMA producers ============================
-    // K stage j % 3 is refilled once S_j = Q K_j^T has completed, V stage
-    // j % 2 once P_j V_j has.
-    const bool is_k = (warp == kWarpTmaK);
+    // K stage j % KST is refilled once S_j = Q K_j^T has completed, V stage
+    // j % VST once P_j V_j has.  Issuing a TMA copy costs its warp ~80 cycles
+    // whatever the size, so the 16 boxes of a K tile are split over two
+    // warps and V is read with one 3-D copy per block.
+    const bool is_k = (warp != kWarpTmaV);
+    const int kpart = (warp == kWarpTmaK2) ? 1 : 0;
     const int nst = is_k ? S::KST : S::VST;
-    static_assert(S::VST == 2, "the two P V barriers double as the V stages' empty barriers");
-    const CUtensorMap* tm = &tm_k;  // 2-D K map (V uses its 3-D map directly)
     uint8_t* ring = is_k ? sK : sV;
     uint64_t* full = &bars[is_k ? B_KFULL : B_VFULL];
+    static_assert(S::VST == 2, "the two P V barriers double as the V stages' empty barriers");
     uint64_t* freed = &bars[is_k ? B_KEMPTY : B_PV];
     int issued = 0;
     if (lane == 0) {
       prefetch_tensormap(is_k ? &tm_k : &tm_v);
-      if (is_k) {
-        prefetch_tensormap(&tm_k3);
+      if (warp == kWarpTmaK) {
         prefetch_tensormap(&tm_q);
         mbar_arrive_expect_tx(&bars[B_Q], S::kQBytes);
 #pragma unroll
@@ -351,11 +354,13 @@ __global__ void __launch_bounds__(PrefillShape<D, G>::kThreads, 1)
       }
     }
     // Pool rows of the item's blocks, read by the whole warp 32 at a time
-    // (one coalesced load) into a sliding window of 64 blocks held one per
-    // lane in two registers; lane 0 takes them by shuffle.  Block b (counted
-    // from the first key tile) maps to TMA row (id * Hkv + kvh) * 16, or to an
-    // out-of-range row past the request's last block (TMA fills zeros).
+    // (one coalesced load) into a window of 64 blocks held one per lane in
+    // two registers (the second half is read ahead); the issuing lanes take
+    // them by shuffle.  Block b (counted from the first key tile) maps to
+    // TMA row (id * Hkv + kvh) * 16, or to an out-of-range row past the
+    // request's last block (TMA fills zeros).
     constexpr int BPT = S::kBlocksPerTile;
+    static_assert(32 % BPT == 0, "a tile's blocks never straddle two 32-block windows");
     const int jb0 = it.kbase / kBlockSize;
     auto load_rows = [&](int base) -> uint32_t {
       const int jb = jb0 + base + lane;
@@ -369,51 +374,39 @@ __global__ void __launch_bounds__(PrefillShape<D, G>::kThreads, 1)
       }
       return row;
     };
-    int win = 0;  // window = blocks [win, win + 64)
+    int win = 0;  // rows_lo: blocks [win, win + 32); rows_hi: the next 32
     uint32_t rows_lo = load_rows(0), rows_hi = load_rows(32);
-    auto row_of = [&](int blk) -> uint32_t {  // blk in [win, win + 64); warp-uniform
-      const int r = blk - win;
-      const uint32_t lo = __shfl_sync(0xffffffffu, rows_lo, r & 31);
-      const uint32_t hi = __shfl_sync(0xffffffffu, rows_hi, r & 31);
-      return r < 32 ? lo : hi;
-    };
-    static_assert((S::kPrefetch + 1) * BPT <= 32 + BPT, "prefetch tile inside the id window");
     for (int j = 0; j < it.ntiles; ++j) {
       if (__any_sync(0xffffffffu, stop_requested(failed))) break;
-      // keep tiles j .. j + kPrefetch inside the window
-      while ((j + S::kPrefetch + 1) * BPT > win + 64) {
+      if (j * BPT >= win + 32) {
         rows_lo = rows_hi;
         rows_hi = load_rows(win + 64);
         win += 32;
       }
-      uint32_t rl[BPT], rp[BPT];
+      uint32_t rl[BPT];
 #pragma unroll
-      for (int kb = 0; kb < BPT; ++kb) {
-        rl[kb] = row_of(j * BPT + kb);
-        rp[kb] = row_of((j + S::kPrefetch) * BPT + kb);
-      }
+      for (int kb = 0; kb < BPT; ++kb)
+        rl[kb] = __shfl_sync(0xffffffffu, rows_lo, (j * BPT + kb - win) & 31);
       const int st = j % nst;
       int good = 1;
       if (lane == 0) {
         if (j >= nst && !cta_wait(&freed[st], (j / nst - 1) & 1, a.err, failed)) good = 0;
-        if (good) mbar_arrive_expect_tx(&full[st], S::kKVBytes);
+        // one expect for the whole stage (the other K warp's copies count too)
+        if (good && kpart == 0) mbar_arrive_expect_tx(&full[st], S::kKVBytes);
       }
       if (!__shfl_sync(0xffffffffu, good, 0)) break;
-      // The copies of a stage are issued by several lanes at once: one
-      // thread's copies are processed one after another, so a single issuing
-      // thread caps the fill rate well below what L2 delivers (a copy of L2
-      // data every ~600 cycles from one thread, ~2.5x the bytes from many).
       uint8_t* dst = ring + st * S::kKVBytes;
       if (is_k) {
         // K: chunk-major (the S MMA reads 64 keys of one 64-column chunk as
-        // 8 uniformly strided 8-row groups), one box per (block, chunk)
-        if (lane < BPT * DC) {
-          const int kb = lane / DC, c = lane % DC;
+        // 8 uniformly strided 8-row groups), one box per (block, chunk); this
+        // warp takes blocks [kpart * BPT / 2, (kpart + 1) * BPT / 2)
+        if (lane < (BPT / 2) * DC) {
+          const int kb = kpart * (BPT / 2) + lane / DC, c = lane % DC;
           uint32_t r = rl[0];
 #pragma unroll
           for (int q = 1; q < BPT; ++q)
             if (kb == q) r = rl[q];
-          tma_load_2d(dst + c * S::kKVChunk + kb * kBlockSize * 128, tm, c * 64,
+          tma_load_2d(dst + c * S::kKVChunk + kb * kBlockSize * 128, &tm_k, c * 64,
                       static_cast<int>(r), &full[st]);
         }
       } else if (lane < BPT) {
@@ -425,21 +418,13 @@ __global__ void __launch_bounds__(PrefillShape<D, G>::kThreads, 1)
           if (lane == q) r = rl[q];
         tma_load_3d(dst + lane * S::kVBlock, &tm_v, 0, static_cast<int>(r), 0, &full[st]);
       }
-      // pull tile j + kPrefetch into L2, one block per lane
-      if (j + S::kPrefetch < it.ntiles && lane < BPT) {
-        uint32_t r = rp[0];
-#pragma unroll
-        for (int q = 1; q < BPT; ++q)
-          if (lane == q) r = rp[q];
-        if (r != oob_row) tma_prefetch_3d(is_k ? &tm_k3 : &tm_v, 0, static_cast<int>(r), 0);
-      }
       issued = j + 1;
     }
     if (lane == 0) {
       // every issued copy must land before the CTA may finish
       for (int j = issued - nst < 0 ? 0 : issued - nst; j < issued; ++j)
         mbar_wait(&full[j % nst], (j / nst) & 1, a.err);
-      if (is_k && stop_requested(failed)) mbar_wait(&bars[B_Q], 0, a.err);
+      if (warp == kWarpTmaK && stop_requested(failed)) mbar_wait(&bars[B_Q], 0, a.err);
     }
     __syncwarp();
   } else if (warp == kWarpMma) {
@@ -696,7 +681,7 @@ bool make_map(CUtensorMap* m, const void* base, int rank, const cuuint64_t* dims
 template <int D, int G>
 cudaError_t launch_prefill_t(const PrefillArgs& a, cudaStream_t stream) {
   using S = PrefillShape<D, G>;
-  CUtensorMap tq, tk, tv, tk3;
+  CUtensorMap tq, tk, tv;
   {
     const cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(a.Hq),
                                 static_cast<cuuint64_t>(a.total_q)};
@@ -721,7 +706,6 @@ cudaError_t launch_prefill_t(const PrefillArgs& a, cudaStream_t stream) {
     const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(kBlockSize),
                                static_cast<cuuint32_t>(D / 64)};
     if (!make_map(&tv, a.v, 3, dims, str, box)) return cudaErrorInvalidValue;
-    if (!make_map(&tk3, a.k, 3, dims, str, box)) return cudaErrorInvalidValue;
   }
   auto kern = paged_prefill_kernel<D, G>;
   cudaError_t e = set_smem_once(reinterpret_cast<const void*>(kern), S::kSmemBytes);
@@ -730,7 +714,7 @@ cudaError_t launch_prefill_t(const PrefillArgs& a, cudaStream_t stream) {
   const long long ctas = static_cast<long long>(a.batch) * qtiles * a.Hkv;
   if (ctas > 0x7fffffffLL) return cudaErrorInvalidValue;
   dim3 grid(static_cast<unsigned>(ctas));
-  kern<<<grid, S::kThreads, S::kSmemBytes, stream>>>(a, tq, tk, tv, tk3);
+  kern<<<grid, S::kThreads, S::kSmemBytes, stream>>>(a, tq, tk, tv);
   return cudaGetLastError();
 }
 
