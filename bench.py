@@ -241,19 +241,27 @@ def batch_kv_bytes(batch) -> float:
 
 
 def time_launches(fn, flush, iters, warmup):
-    """Median CUDA-event time (ms) of fn(), L2 flushed before every call."""
+    """Median CUDA-event time (ms) of fn(), L2 flushed before every call.
+    fn() is captured once as a CUDA graph and replayed, as in the main step,
+    so the host's cost of issuing the launch is not in the measurement."""
     import torch
     stream = torch.cuda.current_stream()
     for _ in range(warmup):
         flush.fill_(1.0)
         fn()
     torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        fn()
+    flush.fill_(1.0)
+    graph.replay()
+    torch.cuda.synchronize()
     ts = []
     for i in range(iters):
         flush.fill_(float(i))
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
-        fn()
+        graph.replay()
         e1.record(stream)
         ts.append((e0, e1))
     torch.cuda.synchronize()
@@ -463,15 +471,22 @@ def main():
     ms_per_step = total_ms / args.steps
     value = world * bytes_step / (ms_per_step * 1e-3) / 1e9
 
-    # the dominant kernel alone: each decode launch timed by CUDA events on
-    # its stream, the L2 flushed before it
+    # the dominant kernel alone: each decode launch (one CUDA graph per call)
+    # timed by CUDA events on its stream, the L2 flushed before it
+    kgraphs = []
+    for i in range(len(calls)):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            launch(i)
+        kgraphs.append(g)
+    torch.cuda.synchronize()
     kern_ms = []
     for s_ in range(args.steps):
         for i in range(len(calls)):
             flush.fill_(float(s_))
             k0, k1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             k0.record(stream)
-            launch(i)
+            kgraphs[i].replay()
             k1.record(stream)
             kern_ms.append((k0, k1))
     torch.cuda.synchronize()

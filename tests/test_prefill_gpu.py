@@ -161,3 +161,32 @@ def test_full_size_repeated_launches_identical(cfg):
         assert torch.equal(out, ref)
     torch.cuda.synchronize()
     assert err.item() == 0
+
+
+# ---- long chunks: several query tiles (128 / G tokens each) per request,
+# odd tile counts, a one-token request and a request with no query mixed in.
+
+def long_chunk_batch(D, G, Hkv=1, window=0, softcap=0.0, extra_q=(), extra_L=(), seed=0):
+    tq = 128 // G
+    q = [int(tq * 3.3), int(tq * 2.5) + 1, int(tq * 1.7)] + list(extra_q)
+    L = [q[0] + 2 * tq + 37, q[1] + 300, q[2] + 5] + list(extra_L)
+    return small(L, q, D=D, G=G, Hkv=Hkv, window=window, softcap=softcap, seed=seed, cfg_id=23)
+
+
+@pytest.mark.parametrize("D,G", [(128, 1), (128, 4), (128, 8), (256, 1), (256, 2), (256, 4),
+                                 (256, 8)])
+def test_long_chunks_shapes(D, G):
+    check(long_chunk_batch(D, G, Hkv=2 if G < 8 else 1, seed=G), f"long chunks D={D} G={G}")
+
+
+@pytest.mark.parametrize("window,softcap", [(57, 0.0), (0, 30.0), (200, 50.0)])
+def test_long_chunks_window_softcap(window, softcap):
+    check(long_chunk_batch(256, 4, Hkv=2, window=window, softcap=softcap, seed=window),
+          f"long chunks W={window} cap={softcap}")
+
+
+def test_long_chunks_with_decode_rows_and_empty_requests():
+    """A one-token request, a request with no query at all and long chunks
+    in the same launch."""
+    check(long_chunk_batch(256, 4, Hkv=2, extra_q=(1, 0, 300), extra_L=(900, 40, 333), seed=3),
+          "long chunks + decode rows")
