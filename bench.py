@@ -300,7 +300,35 @@ def other_workloads(dev, flush, iters=10, warmup=3, cfgs=(1, 3, 4, 5)):
         res[str(cfg)] = entry
         del batch, fn
         torch.cuda.empty_cache()
+    if cfgs == (1, 3, 4, 5):
+        res["append"] = time_append(dev, flush, iters, warmup)
     return res
+
+
+def time_append(dev, flush, iters, warmup):
+    """paged_kv_append of the new tokens of a serving decode tick (B=32) and
+    of a chunked-prefill tick (8 x 512 tokens): Hkv=2, D=256, pool 16384
+    blocks, slots a random permutation; bytes = new rows read + written."""
+    import torch
+    from paged_kv_attention_12_gb300 import binding
+    hbm, hbm_kind = hbm_peak()
+    g = torch.Generator(device=dev).manual_seed(11)
+    nb, hkv, bs, d = 16384, 2, 16, 256
+    k_pool = torch.randn((nb, hkv, bs, d), generator=g, device=dev).to(torch.bfloat16)
+    v_pool = torch.randn((nb, hkv, bs, d), generator=g, device=dev).to(torch.bfloat16)
+    out = {}
+    for name, T in (("decode tick, 32 tokens", 32), ("prefill tick, 4096 tokens", 4096)):
+        k_new = torch.randn((T, hkv, d), generator=g, device=dev).to(torch.bfloat16)
+        v_new = torch.randn((T, hkv, d), generator=g, device=dev).to(torch.bfloat16)
+        slots = torch.randperm(nb * bs, generator=torch.Generator().manual_seed(T))[:T]
+        slots = slots.to(torch.int32).to(dev)
+        ms = time_launches(lambda: binding.paged_kv_append(k_new, v_new, k_pool, v_pool, slots),
+                           flush, iters, warmup)
+        nbytes = 2.0 * 2 * T * hkv * d * 2
+        out[name] = {"ms": ms, "bytes": nbytes, "gbs": nbytes / (ms * 1e-3) / 1e9,
+                     "roofline": {"bound": "hbm", "peak": hbm, "peak_kind": hbm_kind,
+                                  "frac": nbytes / (ms * 1e-3) / 1e9 / hbm}}
+    return out
 
 
 def dist_setup(args):

@@ -198,6 +198,26 @@ int paged_attn_check_tables(const int32_t* block_tables, int32_t max_blocks,
                             const int32_t* seq_lens, int32_t B, int32_t num_blocks,
                             int32_t block_size, int32_t* err, void* stream);
 
+/* Append the new tokens' K and V rows to a pool: the cache write that comes
+ * before attention on every tick ("Block-paged per-layer KV with refcounted
+ * blocks, lazy allocation, and SDPA gather -- vLLM/PagedAttention layout",
+ * github README, "What's inside", Paged KV cache row; one new token per
+ * active request per tick, architecture page, "How a single request flows
+ * through the system", step 7).
+ *   k_new, v_new  bf16 [T][Hkv][D], device, contiguous, 16-byte aligned.
+ *   k_pool, v_pool  bf16 [num_blocks][Hkv][block_size][D], device, written.
+ *   slot_mapping  int32 [T], device: token t goes to slot s = slot_mapping[t]
+ *                 = block * block_size + offset, for every KV head; s < 0
+ *                 skips the token (padding).  Slots must be distinct (with a
+ *                 repeated slot, which token's row lands there is undefined).
+ *   err           optional device int32: a slot beyond num_blocks *
+ *                 block_size is skipped and ORs PKA_DEVERR_BAD_TABLE into it.
+ * Bit-exact copy; T = 0 is a no-op.  D in {128, 256}, block_size 16. */
+int paged_kv_append(const void* k_new, const void* v_new, void* k_pool, void* v_pool,
+                    int32_t num_blocks, int32_t num_kv_heads, int32_t block_size,
+                    int32_t head_dim, const int32_t* slot_mapping, int32_t T, int32_t* err,
+                    void* stream);
+
 /* Decode for callers that cannot allocate device memory.  The pages have no
  * counterpart: this is a service of this library.  Some callers cannot call
  * cudaMalloc -- a plugin running while another allocator owns all device

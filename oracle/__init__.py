@@ -10,3 +10,4 @@ from .paged_attention import (  # noqa: F401
     run_batch,
 )
 from .brute_force import brute_force_attention  # noqa: F401
+from .kv_append import kv_append  # noqa: F401

@@ -33,6 +33,7 @@ EXPORTS = [
     "paged_decode_splitk_workspace_bytes", "paged_decode_splitk",
     "paged_decode_splitk_combine", "paged_prefill_attn", "paged_attn_check_tables",
     "paged_decode_attn_noalloc", "paged_decode_attn_ws_bytes", "paged_decode_attn_ws",
+    "paged_kv_append",
 ]
 
 
@@ -95,6 +96,8 @@ def lib() -> ctypes.CDLL:
     L.paged_decode_attn_noalloc.restype = ctypes.c_int
     L.paged_decode_attn_noalloc.argtypes = [VP, VP, P(PkaKvPool), VP, I32, VP, I32, I32, I32,
                                             P(PkaAttnParams), VP]
+    L.paged_kv_append.restype = ctypes.c_int
+    L.paged_kv_append.argtypes = [VP, VP, VP, VP, I32, I32, I32, I32, VP, I32, VP, VP]
     _lib = L
     return L
 
@@ -216,6 +219,18 @@ def paged_attn_check_tables(block_tables, seq_lens, num_blocks, err, block_size=
                                        seq_lens.data_ptr(), seq_lens.shape[0], int(num_blocks),
                                        block_size, err.data_ptr(), _stream(stream))
     _check("paged_attn_check_tables", st)
+
+
+def paged_kv_append(k_new, v_new, k_pool, v_pool, slot_mapping, err=None, stream=None):
+    """Write token t's K/V rows (``k_new``/``v_new`` bf16 [T][Hkv][D]) into
+    the pools at slot ``slot_mapping[t]`` (int32, block * bs + offset; < 0
+    skips the token)."""
+    nb, hkv, bs, d = k_pool.shape
+    st = lib().paged_kv_append(k_new.data_ptr(), v_new.data_ptr(), k_pool.data_ptr(),
+                               v_pool.data_ptr(), nb, hkv, bs, d, slot_mapping.data_ptr(),
+                               slot_mapping.shape[0], err.data_ptr() if err is not None else None,
+                               _stream(stream))
+    _check("paged_kv_append", st)
 
 
 # ------------------------------------------------------------ batch runners

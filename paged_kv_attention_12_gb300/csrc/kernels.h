@@ -66,6 +66,19 @@ struct PrefillArgs {
 cudaError_t launch_prefill(const PrefillArgs& a, int head_dim, int group, int sm_count,
                            cudaStream_t stream);
 
+// Append of new tokens' K/V rows into a pool.
+struct AppendArgs {
+  const uint16_t* k_new;        // bf16 [T][Hkv][D]
+  const uint16_t* v_new;
+  uint16_t* k_pool;             // bf16 [num_blocks][Hkv][bs][D]
+  uint16_t* v_pool;
+  const int32_t* slot_mapping;  // [T]: block * bs + offset, < 0: skip
+  int32_t* err;
+  int32_t T, Hkv, head_dim, block_size, num_blocks;
+};
+
+cudaError_t launch_kv_append(const AppendArgs& a, int sm_count, cudaStream_t stream);
+
 int device_sm_count();
 
 }  // namespace pka

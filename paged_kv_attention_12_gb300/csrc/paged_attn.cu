@@ -305,6 +305,37 @@ int paged_prefill_attn(const void* q, void* out, const pka_kv_pool* kv,
   return e == cudaSuccess ? PKA_OK : PKA_ERR_CUDA;
 }
 
+int paged_kv_append(const void* k_new, const void* v_new, void* k_pool, void* v_pool,
+                    int32_t num_blocks, int32_t num_kv_heads, int32_t block_size,
+                    int32_t head_dim, const int32_t* slot_mapping, int32_t T, int32_t* err,
+                    void* stream) {
+  if (T < 0 || num_blocks <= 0 || num_kv_heads <= 0) return PKA_ERR_SHAPE;
+  if (block_size != 16) return PKA_ERR_UNSUPPORTED;
+  if (!supported_dim(head_dim)) return PKA_ERR_UNSUPPORTED;
+  if (T == 0) return PKA_OK;
+  if (k_new == nullptr || v_new == nullptr || k_pool == nullptr || v_pool == nullptr ||
+      slot_mapping == nullptr)
+    return PKA_ERR_NULL;
+  if (!aligned16(k_new) || !aligned16(v_new) || !aligned16(k_pool) || !aligned16(v_pool))
+    return PKA_ERR_ALIGN;
+  if (static_cast<long long>(num_blocks) * block_size > 0x7fffffffLL) return PKA_ERR_SHAPE;
+  pka::AppendArgs a;
+  a.k_new = static_cast<const uint16_t*>(k_new);
+  a.v_new = static_cast<const uint16_t*>(v_new);
+  a.k_pool = static_cast<uint16_t*>(k_pool);
+  a.v_pool = static_cast<uint16_t*>(v_pool);
+  a.slot_mapping = slot_mapping;
+  a.err = err;
+  a.T = T;
+  a.Hkv = num_kv_heads;
+  a.head_dim = head_dim;
+  a.block_size = block_size;
+  a.num_blocks = num_blocks;
+  const cudaError_t e =
+      pka::launch_kv_append(a, pka::device_sm_count(), static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? PKA_OK : PKA_ERR_CUDA;
+}
+
 int paged_attn_check_tables(const int32_t* block_tables, int32_t max_blocks,
                             const int32_t* seq_lens, int32_t B, int32_t num_blocks,
                             int32_t block_size, int32_t* err, void* stream) {

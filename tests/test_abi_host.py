@@ -120,3 +120,21 @@ def test_combine_and_prefill_and_check_argument_errors(L):
 
 def test_zero_batch_is_a_no_op(L):
     assert _decode(L, B=0) == 0
+
+
+def _append(L, k_new=32, v_new=32, k_pool=64, v_pool=64, nb=8, hkv=2, bs=16, d=128,
+            slots=128, T=4):
+    return L.paged_kv_append(k_new, v_new, k_pool, v_pool, nb, hkv, bs, d, slots, T, None, None)
+
+
+def test_kv_append_host_errors(L):
+    assert _append(L, T=0) == 0                      # nothing to do, nothing launched
+    assert _append(L, T=-1) == -2
+    assert _append(L, nb=0) == -2
+    assert _append(L, hkv=0) == -2
+    assert _append(L, bs=32) == -4
+    assert _append(L, d=64) == -4
+    assert _append(L, k_new=0) == -1
+    assert _append(L, slots=0) == -1
+    assert _append(L, v_pool=72) == -3              # not 16-byte aligned
+    assert _append(L, k_new=40) == -3

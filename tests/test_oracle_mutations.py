@@ -44,3 +44,30 @@ def test_pins_catch_planted_mistake(tmp_path, name, old, new):
                        capture_output=True, text=True, timeout=600)
     assert r.returncode == 1, f"pins did not catch {name!r}:\n{r.stdout[-2000:]}"
     assert "failed" in r.stdout
+
+
+APPEND_MUTATIONS = [
+    ("block and offset swapped", "blk, off = divmod(int(s), block_size)",
+     "off, blk = divmod(int(s), block_size)"),
+    ("padding not skipped", "if s < 0:\n            continue", "if s < -1:\n            continue"),
+    ("K and V crossed", "v_out[blk, :, off, :] = v_new[t]", "v_out[blk, :, off, :] = k_new[t]"),
+    ("head axis dropped", "k_out[blk, :, off, :] = k_new[t]", "k_out[blk, 0, off, :] = k_new[t][0]"),
+]
+
+
+@pytest.mark.parametrize("name,old,new", APPEND_MUTATIONS, ids=[m[0] for m in APPEND_MUTATIONS])
+def test_append_pins_catch_planted_mistake(tmp_path, name, old, new):
+    shutil.copytree(os.path.join(ROOT, "oracle"), tmp_path / "oracle",
+                    ignore=shutil.ignore_patterns("__pycache__", "*.so", "*.o"))
+    (tmp_path / "tests").mkdir()
+    for f in ("conftest.py", "test_oracle_kv_append.py"):
+        shutil.copy(os.path.join(ROOT, "tests", f), tmp_path / "tests" / f)
+    src = (tmp_path / "oracle" / "kv_append.py").read_text()
+    assert src.count(old) >= 1, f"mutation site for {name!r} not found"
+    (tmp_path / "oracle" / "kv_append.py").write_text(src.replace(old, new))
+    env = dict(os.environ, PYTHONPATH=str(tmp_path), PYTHONDONTWRITEBYTECODE="1")
+    r = subprocess.run([sys.executable, "-m", "pytest", "-q", "-x", "-p", "no:cacheprovider",
+                        "tests/test_oracle_kv_append.py"], cwd=tmp_path, env=env,
+                       capture_output=True, text=True, timeout=600)
+    assert r.returncode == 1, f"pins did not catch {name!r}:\n{r.stdout[-2000:]}"
+    assert "failed" in r.stdout
