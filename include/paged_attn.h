@@ -198,6 +198,34 @@ int paged_attn_check_tables(const int32_t* block_tables, int32_t max_blocks,
                             const int32_t* seq_lens, int32_t B, int32_t num_blocks,
                             int32_t block_size, int32_t* err, void* stream);
 
+/* H2O attention mass.  The engine's cache offers an H2O eviction policy
+ * ("Eviction policies -- Pluggable per-session: LRU, AttentionSink, H2O",
+ * github README, "What's inside"; "H2O wiring deferred", architecture page,
+ * "Phase status"), which keeps the keys that have drawn the most attention.
+ * Two calls give what it needs from a decode step:
+ *
+ * paged_decode_splitk_logits: paged_decode_splitk that also stores every
+ *   visible key's logit: logits fp32 [B][Hq][max_blocks*16] (device, caller
+ *   owned), entry [b][h][t] = log2(e) * s_h(t) (s after scale and softcap)
+ *   for the keys t query head h of request b sees; other entries are not
+ *   written.  Arguments and errors otherwise as paged_decode_splitk.
+ * paged_decode_key_mass: after paged_decode_splitk_combine with lse_out
+ *   (natural-log LSE [B][Hq]), adds each visible key's attention probability,
+ *   summed over the G query heads of its KV head, to key_mass fp32
+ *   [B][Hkv][max_blocks*16] (device): key_mass[b][kvh][t] += sum_h
+ *   exp(s_h(t) - LSE_h).  Invisible keys are left as they are; a head with
+ *   LSE = -inf adds nothing.  Over the visible keys of one (b, kvh) the
+ *   added mass sums to G. */
+int paged_decode_splitk_logits(const void* q, float* partial_o, float* partial_lse,
+                               float* logits, const pka_kv_pool* kv,
+                               const int32_t* block_tables, int32_t max_blocks,
+                               const int32_t* seq_lens, int32_t B, int32_t Hq,
+                               int32_t max_seq_len, int32_t num_splits, int32_t split_blocks,
+                               const pka_attn_params* params, void* stream);
+int paged_decode_key_mass(const float* logits, const float* lse, const int32_t* seq_lens,
+                          int32_t B, int32_t Hq, int32_t num_kv_heads, int32_t max_blocks,
+                          int32_t block_size, int32_t window, float* key_mass, void* stream);
+
 /* Append the new tokens' K and V rows to a pool: the cache write that comes
  * before attention on every tick ("Block-paged per-layer KV with refcounted
  * blocks, lazy allocation, and SDPA gather -- vLLM/PagedAttention layout",

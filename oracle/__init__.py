@@ -11,3 +11,4 @@ from .paged_attention import (  # noqa: F401
 )
 from .brute_force import brute_force_attention  # noqa: F401
 from .kv_append import kv_append  # noqa: F401
+from .key_mass import key_mass  # noqa: F401

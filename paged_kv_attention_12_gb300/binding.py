@@ -33,7 +33,7 @@ EXPORTS = [
     "paged_decode_splitk_workspace_bytes", "paged_decode_splitk",
     "paged_decode_splitk_combine", "paged_prefill_attn", "paged_attn_check_tables",
     "paged_decode_attn_noalloc", "paged_decode_attn_ws_bytes", "paged_decode_attn_ws",
-    "paged_kv_append",
+    "paged_kv_append", "paged_decode_splitk_logits", "paged_decode_key_mass",
 ]
 
 
@@ -96,6 +96,11 @@ def lib() -> ctypes.CDLL:
     L.paged_decode_attn_noalloc.restype = ctypes.c_int
     L.paged_decode_attn_noalloc.argtypes = [VP, VP, P(PkaKvPool), VP, I32, VP, I32, I32, I32,
                                             P(PkaAttnParams), VP]
+    L.paged_decode_splitk_logits.restype = ctypes.c_int
+    L.paged_decode_splitk_logits.argtypes = [VP, VP, VP, VP, P(PkaKvPool), VP, I32, VP, I32, I32,
+                                             I32, I32, I32, P(PkaAttnParams), VP]
+    L.paged_decode_key_mass.restype = ctypes.c_int
+    L.paged_decode_key_mass.argtypes = [VP, VP, VP, I32, I32, I32, I32, I32, I32, VP, VP]
     L.paged_kv_append.restype = ctypes.c_int
     L.paged_kv_append.argtypes = [VP, VP, VP, VP, I32, I32, I32, I32, VP, I32, VP, VP]
     _lib = L
@@ -192,6 +197,34 @@ def paged_decode_splitk(q, partial_o, partial_lse, k_pool, v_pool, block_tables,
                                    q.shape[1], int(max_seq_len), int(num_splits),
                                    int(split_blocks), ctypes.byref(par), _stream(stream))
     _check("paged_decode_splitk", st)
+
+
+def paged_decode_splitk_logits(q, partial_o, partial_lse, logits, k_pool, v_pool, block_tables,
+                               seq_lens, max_seq_len, num_splits, split_blocks, *, scale,
+                               softcap=0.0, window=0, err=None, stream=None):
+    """paged_decode_splitk that also stores the visible keys' log2-domain
+    logits in ``logits`` fp32 [B][Hq][max_blocks * 16]."""
+    pool = kv_pool(k_pool, v_pool)
+    par = attn_params(scale, softcap, window, err)
+    st = lib().paged_decode_splitk_logits(q.data_ptr(), partial_o.data_ptr(),
+                                          partial_lse.data_ptr(), logits.data_ptr(),
+                                          ctypes.byref(pool), block_tables.data_ptr(),
+                                          block_tables.shape[1], seq_lens.data_ptr(), q.shape[0],
+                                          q.shape[1], int(max_seq_len), int(num_splits),
+                                          int(split_blocks), ctypes.byref(par), _stream(stream))
+    _check("paged_decode_splitk_logits", st)
+
+
+def paged_decode_key_mass(logits, lse, seq_lens, num_kv_heads, key_mass, *, window=0,
+                          block_size=16, stream=None):
+    """key_mass fp32 [B][Hkv][max_blocks * 16] += each visible key's attention
+    probability summed over its KV head's query heads (``lse``: [B][Hq]
+    natural-log LSE from the combine)."""
+    B, Hq, nk = logits.shape
+    st = lib().paged_decode_key_mass(logits.data_ptr(), lse.data_ptr(), seq_lens.data_ptr(), B,
+                                     Hq, int(num_kv_heads), nk // block_size, block_size,
+                                     int(window), key_mass.data_ptr(), _stream(stream))
+    _check("paged_decode_key_mass", st)
 
 
 def paged_decode_splitk_combine(partial_o, partial_lse, out, lse_out=None, stream=None):

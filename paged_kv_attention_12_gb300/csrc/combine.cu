@@ -92,7 +92,52 @@ __global__ void check_tables_kernel(const CheckArgs a) {
   if (__syncthreads_or(bad) && threadIdx.x == 0) atomicOr(a.err, PKA_DEVERR_BAD_TABLE);
 }
 
+// H2O key mass: mass[b][kvh][t] += sum over the G heads h of the group of
+// p_h(t) = exp(s_h(t) - LSE_h), for the keys t the decode query of request b
+// sees.  The logits are the split-K kernel's log2-domain values, so
+// p = 2^(x - LSE * log2 e).  One thread per (request, KV head, key):
+// consecutive threads read consecutive keys of each head and update
+// consecutive mass entries.
+__global__ void __launch_bounds__(256) key_mass_kernel(const float* logits, const float* lse,
+                                                       const int32_t* seq_lens, int32_t B,
+                                                       int32_t Hq, int32_t Hkv, int32_t max_keys,
+                                                       int32_t window, float* mass) {
+  const int G = Hq / Hkv;
+  const long long total = static_cast<long long>(B) * Hkv * max_keys;
+  for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
+       i += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const int t = static_cast<int>(i % max_keys);
+    const long long bk = i / max_keys;
+    const int kvh = static_cast<int>(bk % Hkv);
+    const int b = static_cast<int>(bk / Hkv);
+    const int L = min(max(seq_lens[b], 0), max_keys);
+    const int pos = L - 1;
+    const int t_lo = (window > 0) ? max(0, pos - window + 1) : 0;
+    if (t > pos || t < t_lo) continue;
+    float acc = 0.f;
+    for (int g = 0; g < G; ++g) {
+      const int h = kvh * G + g;
+      const float ls = lse[static_cast<size_t>(b) * Hq + h];
+      if (ls == -INFINITY) continue;
+      acc += fast_exp2(logits[(static_cast<size_t>(b) * Hq + h) * max_keys + t] - ls * kLog2e);
+    }
+    mass[i] += acc;
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_key_mass(const float* logits, const float* lse, const int32_t* seq_lens,
+                            int32_t B, int32_t Hq, int32_t Hkv, int32_t max_keys, int32_t window,
+                            float* key_mass, cudaStream_t stream) {
+  const long long total = static_cast<long long>(B) * Hkv * max_keys;
+  if (total == 0) return cudaSuccess;
+  const long long want = (total + 255) / 256;
+  const int grid = static_cast<int>(want < 8 * 152 ? want : 8 * 152);
+  key_mass_kernel<<<grid, 256, 0, stream>>>(logits, lse, seq_lens, B, Hq, Hkv, max_keys, window,
+                                            key_mass);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_combine(const CombineArgs& a, cudaStream_t stream) {
   const int warps = a.rows * (a.head_dim / 128);

@@ -304,7 +304,7 @@ template <int D, int G, int NW, int NSLOT>
 __device__ __forceinline__ void decode_slot(
     const bool edge, uint32_t k_addr, uint8_t* v_ptr, const uint32_t (&bq)[D / 16][2],
     float (&o)[D / 16][4], float (&m)[2], float (&l)[2], int lane, int tok0, int t_lo, int pos,
-    float qscale, float softcap, float inv_cap) {
+    float qscale, float softcap, float inv_cap, float* logits, int logit_stride) {
   using S = DecodeShape<D, G, NW, NSLOT>;
   const int g = lane >> 2, t = lane & 3;
 
@@ -348,6 +348,10 @@ __device__ __forceinline__ void decode_slot(
     else v *= qscale;
     const bool ok = ((i & 1) ? head_ok1 : head_ok0) && ((i & 2) ? key_ok_hi : key_ok_lo);
     x[i] = ok ? v : -INFINITY;
+    // optional: the visible keys' log2-domain logits of the G heads
+    // (logits points at head kvh * G, key 0 of the request)
+    if (logits != nullptr && ok)
+      logits[(2 * t + (i & 1)) * logit_stride + tok0 + g + ((i & 2) ? 8 : 0)] = v;
   }
   float alpha[2], ms[2];
 #pragma unroll
@@ -542,6 +546,10 @@ __global__ void __launch_bounds__((NW + 1) * 32, 2)
     // consumes its phases in order (a phase-parity wait can never alias an
     // older phase of the same slot).
     const int i0 = static_cast<int>((warp - tile_base % NW + NW) % NW);
+    float* lg = (a.logits == nullptr)
+                    ? nullptr
+                    : a.logits + (static_cast<size_t>(pc.b) * a.Hq + pc.kvh * G) *
+                                     (static_cast<size_t>(a.max_blocks) * kBlockSize);
     for (int i = i0; i < pc.ntiles && ok; i += NW) {
       const long long T = tile_base + i;
       const int slot = static_cast<int>(T % NSLOT);
@@ -554,7 +562,8 @@ __global__ void __launch_bounds__((NW + 1) * 32, 2)
       const int tok0 = (pc.j0 + i) * kBlockSize;
       const bool edge = (tok0 < pc.t_lo || tok0 + kBlockSize - 1 > pc.pos);
       decode_slot<D, G, NW, NSLOT>(edge, smem_u32(kp), kp + S::kTileBytes, bq, o, m, l, lane,
-                                   tok0, pc.t_lo, pc.pos, qscale, a.softcap, inv_cap);
+                                   tok0, pc.t_lo, pc.pos, qscale, a.softcap, inv_cap, lg,
+                                   a.max_blocks * kBlockSize);
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[slot]);
     }

@@ -22,9 +22,14 @@ struct DecodeArgs {
   int32_t num_splits;              // items per (request, head); 1 in direct mode
   int32_t split_blocks;            // blocks per split; <= 0: direct mode (whole range)
   int32_t* seg_counters;           // split mode: non-null fuses the combine (zeroed [B*Hkv])
+  float* logits;                   // optional fp32 [B][Hq][max_blocks*bs]: log2-domain logits
   float scale, softcap;
   int32_t window;
 };
+
+cudaError_t launch_key_mass(const float* logits, const float* lse, const int32_t* seq_lens,
+                            int32_t B, int32_t Hq, int32_t Hkv, int32_t max_keys, int32_t window,
+                            float* key_mass, cudaStream_t stream);
 
 cudaError_t launch_decode(const DecodeArgs& a, int head_dim, int group, int grid,
                           cudaStream_t stream);

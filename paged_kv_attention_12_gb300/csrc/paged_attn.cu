@@ -162,11 +162,13 @@ size_t paged_decode_splitk_workspace_bytes(int32_t B, int32_t Hq, int32_t D, int
   return static_cast<size_t>(B) * Hq * num_splits * (static_cast<size_t>(D) + 1) * sizeof(float);
 }
 
-int paged_decode_splitk(const void* q, float* partial_o, float* partial_lse,
-                        const pka_kv_pool* kv, const int32_t* block_tables, int32_t max_blocks,
-                        const int32_t* seq_lens, int32_t B, int32_t Hq, int32_t max_seq_len,
-                        int32_t num_splits, int32_t split_blocks,
-                        const pka_attn_params* params, void* stream) {
+namespace {
+
+int splitk_impl(const void* q, float* partial_o, float* partial_lse, float* logits,
+                const pka_kv_pool* kv, const int32_t* block_tables, int32_t max_blocks,
+                const int32_t* seq_lens, int32_t B, int32_t Hq, int32_t max_seq_len,
+                int32_t num_splits, int32_t split_blocks, const pka_attn_params* params,
+                void* stream) {
   if (partial_o == nullptr || partial_lse == nullptr) return PKA_ERR_NULL;
   int st = check_common(q, kv, block_tables, max_blocks, seq_lens, B, Hq, max_seq_len, params);
   if (st != PKA_OK) return st;
@@ -182,6 +184,7 @@ int paged_decode_splitk(const void* q, float* partial_o, float* partial_lse,
   a.partial_lse = partial_lse;
   a.num_splits = num_splits;
   a.split_blocks = split_blocks;
+  a.logits = logits;
   if (static_cast<int64_t>(B) * Hq * num_splits > 0x7fffffffLL) return PKA_ERR_SHAPE;
   const int sms = pka::device_sm_count();
   if (sms <= 0) return PKA_ERR_CUDA;
@@ -189,6 +192,44 @@ int paged_decode_splitk(const void* q, float* partial_o, float* partial_lse,
   const int grid = sms;
   cudaError_t e = pka::launch_decode(a, kv->head_dim, Hq / kv->num_kv_heads, grid,
                                      static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? PKA_OK : PKA_ERR_CUDA;
+}
+
+}  // namespace
+
+int paged_decode_splitk(const void* q, float* partial_o, float* partial_lse,
+                        const pka_kv_pool* kv, const int32_t* block_tables, int32_t max_blocks,
+                        const int32_t* seq_lens, int32_t B, int32_t Hq, int32_t max_seq_len,
+                        int32_t num_splits, int32_t split_blocks,
+                        const pka_attn_params* params, void* stream) {
+  return splitk_impl(q, partial_o, partial_lse, nullptr, kv, block_tables, max_blocks, seq_lens,
+                     B, Hq, max_seq_len, num_splits, split_blocks, params, stream);
+}
+
+int paged_decode_splitk_logits(const void* q, float* partial_o, float* partial_lse,
+                               float* logits, const pka_kv_pool* kv,
+                               const int32_t* block_tables, int32_t max_blocks,
+                               const int32_t* seq_lens, int32_t B, int32_t Hq,
+                               int32_t max_seq_len, int32_t num_splits, int32_t split_blocks,
+                               const pka_attn_params* params, void* stream) {
+  if (logits == nullptr) return PKA_ERR_NULL;
+  if (static_cast<int64_t>(B) * Hq * max_blocks * 16 > (1LL << 40)) return PKA_ERR_SHAPE;
+  return splitk_impl(q, partial_o, partial_lse, logits, kv, block_tables, max_blocks, seq_lens,
+                     B, Hq, max_seq_len, num_splits, split_blocks, params, stream);
+}
+
+int paged_decode_key_mass(const float* logits, const float* lse, const int32_t* seq_lens,
+                          int32_t B, int32_t Hq, int32_t num_kv_heads, int32_t max_blocks,
+                          int32_t block_size, int32_t window, float* key_mass, void* stream) {
+  if (B < 0 || Hq <= 0 || num_kv_heads <= 0 || max_blocks <= 0) return PKA_ERR_SHAPE;
+  if (Hq % num_kv_heads != 0 || !supported_group(Hq / num_kv_heads)) return PKA_ERR_SHAPE;
+  if (block_size != 16) return PKA_ERR_UNSUPPORTED;
+  if (B == 0) return PKA_OK;
+  if (logits == nullptr || lse == nullptr || seq_lens == nullptr || key_mass == nullptr)
+    return PKA_ERR_NULL;
+  const cudaError_t e =
+      pka::launch_key_mass(logits, lse, seq_lens, B, Hq, num_kv_heads, max_blocks * block_size,
+                           window, key_mass, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? PKA_OK : PKA_ERR_CUDA;
 }
 

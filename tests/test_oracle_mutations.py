@@ -71,3 +71,29 @@ def test_append_pins_catch_planted_mistake(tmp_path, name, old, new):
                        capture_output=True, text=True, timeout=600)
     assert r.returncode == 1, f"pins did not catch {name!r}:\n{r.stdout[-2000:]}"
     assert "failed" in r.stdout
+
+
+MASS_MUTATIONS = [
+    ("unnormalised probabilities", "mass[b, kvh, keys] += p / p.sum()", "mass[b, kvh, keys] += p"),
+    ("cap ignored", "s = softcap * np.tanh(s / softcap)", "s = s"),
+    ("window ignored", "keys = visible_keys(L - 1, L, window)", "keys = visible_keys(L - 1, L, 0)"),
+    ("heads grouped by stride", "q[b, kvh * G + g]", "q[b, kvh + g * Hkv]"),
+]
+
+
+@pytest.mark.parametrize("name,old,new", MASS_MUTATIONS, ids=[m[0] for m in MASS_MUTATIONS])
+def test_key_mass_pins_catch_planted_mistake(tmp_path, name, old, new):
+    shutil.copytree(os.path.join(ROOT, "oracle"), tmp_path / "oracle",
+                    ignore=shutil.ignore_patterns("__pycache__", "*.so", "*.o"))
+    (tmp_path / "tests").mkdir()
+    for f in ("conftest.py", "test_oracle_key_mass.py"):
+        shutil.copy(os.path.join(ROOT, "tests", f), tmp_path / "tests" / f)
+    src = (tmp_path / "oracle" / "key_mass.py").read_text()
+    assert src.count(old) >= 1, f"mutation site for {name!r} not found"
+    (tmp_path / "oracle" / "key_mass.py").write_text(src.replace(old, new))
+    env = dict(os.environ, PYTHONPATH=str(tmp_path), PYTHONDONTWRITEBYTECODE="1")
+    r = subprocess.run([sys.executable, "-m", "pytest", "-q", "-x", "-p", "no:cacheprovider",
+                        "tests/test_oracle_key_mass.py"], cwd=tmp_path, env=env,
+                       capture_output=True, text=True, timeout=600)
+    assert r.returncode == 1, f"pins did not catch {name!r}:\n{r.stdout[-2000:]}"
+    assert "failed" in r.stdout
