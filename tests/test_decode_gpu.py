@@ -332,3 +332,33 @@ def test_repeated_launches_are_deterministic_and_never_time_out():
     assert err.item() == 0
     for r, ref in zip(runners, first):
         assert torch.equal(r.out, ref)
+
+
+# ------------------------------------------------------------- maximum sizes
+def test_many_requests_and_table_capacity():
+    """A wide batch (512 requests, G = 4, D = 128) where some requests fill
+    their table to the last slot (seq_len = max_blocks * 16 = 65536) and
+    others have one token; split-K, fused and direct paths agree and a
+    sample matches the oracle."""
+    rng = np.random.default_rng(5)
+    B, max_blocks = 512, 4096
+    L = rng.integers(1, 3000, size=B)
+    L[[0, 7, 300]] = max_blocks * 16
+    L[[1, 2]] = 1
+    batch = workload.make_batch(seq_lens=L.tolist(), q_lens=[1] * B, num_q_heads=32,
+                                num_kv_heads=8, head_dim=128,
+                                num_blocks=int(sum(-(-x // 16) for x in L)) + 16, device=DEV,
+                                cfg_id=41, seed=5, poison=True, max_blocks=max_blocks)
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    out, _ = run_splitk(batch, err=err)
+    outf = binding.DecodeFused(batch).run()
+    assert torch.equal(out, outf)
+    direct = torch.empty_like(batch.q)
+    binding.paged_decode_attn(batch.q, direct, batch.k_pool, batch.v_pool, batch.block_tables,
+                              batch.seq_lens, batch.max_seq_len, scale=batch.scale, err=err)
+    reqs = [0, 1, 7, 300, 511]
+    ref, _, _ = oracle_decode(batch, reqs)
+    assert_close(to_f64(out[reqs]), ref, "wide batch split-K")
+    assert_close(to_f64(direct[reqs]), ref, "wide batch direct")
+    torch.cuda.synchronize()
+    assert err.item() == 0

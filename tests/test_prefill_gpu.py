@@ -190,3 +190,31 @@ def test_long_chunks_with_decode_rows_and_empty_requests():
     in the same launch."""
     check(long_chunk_batch(256, 4, Hkv=2, extra_q=(1, 0, 300), extra_L=(900, 40, 333), seed=3),
           "long chunks + decode rows")
+
+
+def test_long_chunk_max_sizes():
+    """One 8192-token chunk on an 8192-token prefix (G = 1: 64 query tiles of
+    128 rows, 128 key tiles each at the end) next to a one-token request and a
+    short chunk; rows sampled across the long chunk are checked."""
+    batch = small([16384, 300, 5000], [8192, 1, 333], D=128, G=1, Hkv=4, seed=11, cfg_id=42)
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    out = run(batch, err)
+    arr = workload.to_numpy_f64(batch, [0])
+    rows = [0, 1, 127, 128, 4095, 8190, 8191]
+    q_rows = arr["q_rows"]
+    # reference on the sampled rows only: their keys gathered through the
+    # request's table, textbook softmax attention per row and head
+    Lr, n = 16384, 8192
+    keys = np.asarray(arr["block_tables"][0])
+    kc = oracle.gather_request_kv(arr["k_pool"], keys, Lr, 16)
+    vc = oracle.gather_request_kv(arr["v_pool"], keys, Lr, 16)
+    got = to_f64(out[[q_rows[r] for r in rows]])
+    for i, r in enumerate(rows):
+        pos = Lr - n + r
+        vis = oracle.visible_keys(pos, Lr, 0)
+        for h in range(4):
+            o, _ = oracle.softmax_attention(arr["q"][r, h:h + 1], kc[vis, h], vc[vis, h],
+                                            batch.scale, 0.0)
+            assert_close(got[i, h:h + 1], o, f"long chunk row {r} head {h}")
+    torch.cuda.synchronize()
+    assert err.item() == 0
