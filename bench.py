@@ -328,6 +328,24 @@ def time_append(dev, flush, iters, warmup):
         out[name] = {"ms": ms, "bytes": nbytes, "gbs": nbytes / (ms * 1e-3) / 1e9,
                      "roofline": {"bound": "hbm", "peak": hbm, "peak_kind": hbm_kind,
                                   "frac": nbytes / (ms * 1e-3) / 1e9 / hbm}}
+    # the same prefill tick with RMS norm of q, k, v and RoPE of q, k fused in
+    # (Hq = 8: q rows are read and written too)
+    T, hq = 4096, 8
+    q = torch.randn((T, hq, d), generator=g, device=dev).to(torch.bfloat16)
+    k_new = torch.randn((T, hkv, d), generator=g, device=dev).to(torch.bfloat16)
+    v_new = torch.randn((T, hkv, d), generator=g, device=dev).to(torch.bfloat16)
+    slots = torch.randperm(nb * bs, generator=torch.Generator().manual_seed(T))[:T]
+    slots = slots.to(torch.int32).to(dev)
+    pos = torch.arange(T, dtype=torch.int32, device=dev) + 8000
+    w = torch.ones(d, device=dev)
+    ms = time_launches(lambda: binding.paged_kv_append_rope(
+        q, k_new, v_new, k_pool, v_pool, slots, pos, q_norm_weight=w, k_norm_weight=w,
+        v_norm=True, rope_theta=1e6), flush, iters, warmup)
+    nbytes = 2.0 * T * (hq + 2 * hkv) * d * 2
+    out["prefill tick, 4096 tokens, norms + RoPE"] = {
+        "ms": ms, "bytes": nbytes, "gbs": nbytes / (ms * 1e-3) / 1e9,
+        "roofline": {"bound": "hbm", "peak": hbm, "peak_kind": hbm_kind,
+                     "frac": nbytes / (ms * 1e-3) / 1e9 / hbm}}
     return out
 
 

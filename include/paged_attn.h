@@ -246,6 +246,33 @@ int paged_kv_append(const void* k_new, const void* v_new, void* k_pool, void* v_
                     int32_t head_dim, const int32_t* slot_mapping, int32_t T, int32_t* err,
                     void* stream);
 
+/* paged_kv_append with the per-head math before attention fused in
+ * ("Custom Gemma 4 forward -- Dual-RoPE, GQA with QK/V-norm + KV sharing",
+ * github README, "What's inside").  For each token t (position positions[t],
+ * slot slot_mapping[t] as in paged_kv_append), in this order:
+ *   RMS norm   x <- x / sqrt(mean_c(x_c^2) + eps) * w_c over the D channels of
+ *              each head: q with q_norm_weight, k with k_norm_weight (fp32 [D],
+ *              device; NULL = no norm for that tensor), v with unit weight when
+ *              v_norm != 0;
+ *   RoPE       q and k, rotate-half form: with r = rotary_dim and
+ *              a_i = positions[t] * rope_theta^(-2i/r), for i < r/2:
+ *              (x_i, x_{i+r/2}) <- (x_i cos a_i - x_{i+r/2} sin a_i,
+ *                                   x_{i+r/2} cos a_i + x_i sin a_i);
+ *              channels >= r unchanged; rotary_dim = 0 turns it off (the two
+ *              RoPE variants of a dual scheme are two calls).
+ * Then k and v rows go to the pool slots and q (bf16 [T][Hq][D], may be NULL)
+ * is overwritten in place; everything is computed in fp32 from the bf16
+ * inputs and stored bf16 (round to nearest even).
+ * rotary_dim in [0, D], a multiple of 16; rope_theta > 1 when rotary_dim > 0;
+ * eps >= 0.  Errors as paged_kv_append. */
+int paged_kv_append_rope(void* q, const void* k_new, const void* v_new, void* k_pool,
+                         void* v_pool, int32_t num_blocks, int32_t num_q_heads,
+                         int32_t num_kv_heads, int32_t block_size, int32_t head_dim,
+                         const int32_t* slot_mapping, const int32_t* positions, int32_t T,
+                         const float* q_norm_weight, const float* k_norm_weight, int32_t v_norm,
+                         float eps, float rope_theta, int32_t rotary_dim, int32_t* err,
+                         void* stream);
+
 /* Decode for callers that cannot allocate device memory.  The pages have no
  * counterpart: this is a service of this library.  Some callers cannot call
  * cudaMalloc -- a plugin running while another allocator owns all device

@@ -12,3 +12,4 @@ from .paged_attention import (  # noqa: F401
 from .brute_force import brute_force_attention  # noqa: F401
 from .kv_append import kv_append  # noqa: F401
 from .key_mass import key_mass  # noqa: F401
+from .rope_norm import rms_norm, rope, kv_append_rope  # noqa: F401

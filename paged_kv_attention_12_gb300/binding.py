@@ -34,6 +34,7 @@ EXPORTS = [
     "paged_decode_splitk_combine", "paged_prefill_attn", "paged_attn_check_tables",
     "paged_decode_attn_noalloc", "paged_decode_attn_ws_bytes", "paged_decode_attn_ws",
     "paged_kv_append", "paged_decode_splitk_logits", "paged_decode_key_mass",
+    "paged_kv_append_rope",
 ]
 
 
@@ -101,6 +102,9 @@ def lib() -> ctypes.CDLL:
                                              I32, I32, I32, P(PkaAttnParams), VP]
     L.paged_decode_key_mass.restype = ctypes.c_int
     L.paged_decode_key_mass.argtypes = [VP, VP, VP, I32, I32, I32, I32, I32, I32, VP, VP]
+    L.paged_kv_append_rope.restype = ctypes.c_int
+    L.paged_kv_append_rope.argtypes = [VP, VP, VP, VP, VP, I32, I32, I32, I32, I32, VP, VP, I32,
+                                       VP, VP, I32, ctypes.c_float, ctypes.c_float, I32, VP, VP]
     L.paged_kv_append.restype = ctypes.c_int
     L.paged_kv_append.argtypes = [VP, VP, VP, VP, I32, I32, I32, I32, VP, I32, VP, VP]
     _lib = L
@@ -264,6 +268,22 @@ def paged_kv_append(k_new, v_new, k_pool, v_pool, slot_mapping, err=None, stream
                                slot_mapping.shape[0], err.data_ptr() if err is not None else None,
                                _stream(stream))
     _check("paged_kv_append", st)
+
+
+def paged_kv_append_rope(q, k_new, v_new, k_pool, v_pool, slot_mapping, positions, *,
+                         q_norm_weight=None, k_norm_weight=None, v_norm=False, eps=1e-6,
+                         rope_theta=10000.0, rotary_dim=None, err=None, stream=None):
+    """RMS-norm q / k / v, rotate q and k (rotate-half RoPE over the first
+    ``rotary_dim`` channels, default all), append k / v at their slots and
+    overwrite q (or skip it when ``q`` is None)."""
+    nb, hkv, bs, d = k_pool.shape
+    rd = d if rotary_dim is None else int(rotary_dim)
+    st = lib().paged_kv_append_rope(
+        _ptr(q), k_new.data_ptr(), v_new.data_ptr(), k_pool.data_ptr(), v_pool.data_ptr(), nb,
+        q.shape[1] if q is not None else 0, hkv, bs, d, slot_mapping.data_ptr(),
+        _ptr(positions), slot_mapping.shape[0], _ptr(q_norm_weight), _ptr(k_norm_weight),
+        1 if v_norm else 0, float(eps), float(rope_theta), rd, _ptr(err), _stream(stream))
+    _check("paged_kv_append_rope", st)
 
 
 # ------------------------------------------------------------ batch runners

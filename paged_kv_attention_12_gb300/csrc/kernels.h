@@ -84,6 +84,28 @@ struct AppendArgs {
 
 cudaError_t launch_kv_append(const AppendArgs& a, int sm_count, cudaStream_t stream);
 
+// Append with RMS norm and rotary embedding fused in.
+struct AppendRopeArgs {
+  uint16_t* q;                  // bf16 [T][Hq][D], normalised and rotated in place (or null)
+  const uint16_t* k_new;        // bf16 [T][Hkv][D]
+  const uint16_t* v_new;
+  uint16_t* k_pool;             // bf16 [num_blocks][Hkv][bs][D]
+  uint16_t* v_pool;
+  const int32_t* slot_mapping;  // [T]
+  const int32_t* positions;     // [T]: absolute position of token t
+  const float* q_norm_w;        // [D] or null: no q norm
+  const float* k_norm_w;        // [D] or null: no k norm
+  int32_t* err;
+  int32_t T, Hq, Hkv, head_dim, block_size, num_blocks;
+  int32_t v_norm;               // nonzero: RMS-normalise v (no weight)
+  int32_t rotary_dim;           // 0: no rotary embedding
+  float eps, rope_theta;
+  // freq_i / (2 pi) as a 64-bit fraction, freq_i = rope_theta^(-2i/rotary_dim)
+  unsigned long long gfrac[128];
+};
+
+cudaError_t launch_kv_append_rope(const AppendRopeArgs& a, int sm_count, cudaStream_t stream);
+
 int device_sm_count();
 
 }  // namespace pka

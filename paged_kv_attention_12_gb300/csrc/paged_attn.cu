@@ -5,6 +5,8 @@
 // (table ids, sequence lengths) and report those through the device error
 // word.  Nothing here allocates or synchronises.
 #include <cuda_runtime.h>
+
+#include <cmath>
 #include <stdint.h>
 
 #include "kernels.h"
@@ -374,6 +376,62 @@ int paged_kv_append(const void* k_new, const void* v_new, void* k_pool, void* v_
   a.num_blocks = num_blocks;
   const cudaError_t e =
       pka::launch_kv_append(a, pka::device_sm_count(), static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? PKA_OK : PKA_ERR_CUDA;
+}
+
+int paged_kv_append_rope(void* q, const void* k_new, const void* v_new, void* k_pool,
+                         void* v_pool, int32_t num_blocks, int32_t num_q_heads,
+                         int32_t num_kv_heads, int32_t block_size, int32_t head_dim,
+                         const int32_t* slot_mapping, const int32_t* positions, int32_t T,
+                         const float* q_norm_weight, const float* k_norm_weight, int32_t v_norm,
+                         float eps, float rope_theta, int32_t rotary_dim, int32_t* err,
+                         void* stream) {
+  if (T < 0 || num_blocks <= 0 || num_kv_heads <= 0) return PKA_ERR_SHAPE;
+  if (q != nullptr && (num_q_heads <= 0 || num_q_heads % num_kv_heads != 0)) return PKA_ERR_SHAPE;
+  if (block_size != 16) return PKA_ERR_UNSUPPORTED;
+  if (!supported_dim(head_dim)) return PKA_ERR_UNSUPPORTED;
+  if (rotary_dim < 0 || rotary_dim > head_dim || rotary_dim % 16 != 0) return PKA_ERR_SHAPE;
+  if (rotary_dim > 0 && !(rope_theta > 1.f)) return PKA_ERR_SHAPE;
+  if (!(eps >= 0.f)) return PKA_ERR_SHAPE;
+  if (T == 0) return PKA_OK;
+  if (k_new == nullptr || v_new == nullptr || k_pool == nullptr || v_pool == nullptr ||
+      slot_mapping == nullptr || (rotary_dim > 0 && positions == nullptr))
+    return PKA_ERR_NULL;
+  if (!aligned16(k_new) || !aligned16(v_new) || !aligned16(k_pool) || !aligned16(v_pool) ||
+      (q != nullptr && !aligned16(q)))
+    return PKA_ERR_ALIGN;
+  if (static_cast<long long>(num_blocks) * block_size > 0x7fffffffLL) return PKA_ERR_SHAPE;
+  pka::AppendRopeArgs a;
+  a.q = static_cast<uint16_t*>(q);
+  a.k_new = static_cast<const uint16_t*>(k_new);
+  a.v_new = static_cast<const uint16_t*>(v_new);
+  a.k_pool = static_cast<uint16_t*>(k_pool);
+  a.v_pool = static_cast<uint16_t*>(v_pool);
+  a.slot_mapping = slot_mapping;
+  a.positions = positions;
+  a.q_norm_w = q_norm_weight;
+  a.k_norm_w = k_norm_weight;
+  a.err = err;
+  a.T = T;
+  a.Hq = (q != nullptr) ? num_q_heads : 0;
+  a.Hkv = num_kv_heads;
+  a.head_dim = head_dim;
+  a.block_size = block_size;
+  a.num_blocks = num_blocks;
+  a.v_norm = v_norm;
+  a.rotary_dim = rotary_dim;
+  a.eps = eps;
+  a.rope_theta = rope_theta;
+  for (int i = 0; i < 128; ++i) {
+    a.gfrac[i] = 0;
+    if (i < rotary_dim / 2) {
+      const double f = std::pow(static_cast<double>(rope_theta), -2.0 * i / rotary_dim);
+      a.gfrac[i] = static_cast<unsigned long long>(
+          f * (18446744073709551616.0 / 6.283185307179586476925286766559));  // f / 2pi < 1
+    }
+  }
+  const cudaError_t e =
+      pka::launch_kv_append_rope(a, pka::device_sm_count(), static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? PKA_OK : PKA_ERR_CUDA;
 }
 

@@ -138,3 +138,19 @@ def test_kv_append_host_errors(L):
     assert _append(L, slots=0) == -1
     assert _append(L, v_pool=72) == -3              # not 16-byte aligned
     assert _append(L, k_new=40) == -3
+
+
+def test_kv_append_rope_host_errors(L):
+    def call(q=32, T=4, rd=128, theta=10000.0, eps=1e-6, d=128, bs=16, hq=8, hkv=2, pos=256):
+        return L.paged_kv_append_rope(q, 64, 96, 128, 160, 8, hq, hkv, bs, d, 192, pos, T, None,
+                                      None, 0, eps, theta, rd, None, None)
+    assert call(T=0) == 0
+    assert call(rd=24) == -2        # not a multiple of 16
+    assert call(rd=256) == -2       # wider than D
+    assert call(theta=1.0) == -2
+    assert call(eps=-1.0) == -2
+    assert call(bs=8) == -4
+    assert call(d=96) == -4
+    assert call(hq=7) == -2         # not a multiple of Hkv
+    assert call(pos=0) == -1        # RoPE needs positions
+    assert call(q=40) == -3

@@ -97,3 +97,31 @@ def test_key_mass_pins_catch_planted_mistake(tmp_path, name, old, new):
                        capture_output=True, text=True, timeout=600)
     assert r.returncode == 1, f"pins did not catch {name!r}:\n{r.stdout[-2000:]}"
     assert "failed" in r.stdout
+
+
+ROPE_MUTATIONS = [
+    ("pairs adjacent instead of halves", "x1, x2 = x[..., :half], x[..., half:rotary_dim]",
+     "x1, x2 = x[..., 0:rotary_dim:2], x[..., 1:rotary_dim:2]"),
+    ("sine sign flipped", "out[..., :half] = x1 * c - x2 * s", "out[..., :half] = x1 * c + x2 * s"),
+    ("frequency exponent over D/2", "theta ** (-2.0 * i / rotary_dim)", "theta ** (-1.0 * i / rotary_dim)"),
+    ("norm by mean absolute value", "np.mean(x * x, axis=-1, keepdims=True)",
+     "np.mean(np.abs(x), axis=-1, keepdims=True) ** 2"),
+]
+
+
+@pytest.mark.parametrize("name,old,new", ROPE_MUTATIONS, ids=[m[0] for m in ROPE_MUTATIONS])
+def test_rope_norm_pins_catch_planted_mistake(tmp_path, name, old, new):
+    shutil.copytree(os.path.join(ROOT, "oracle"), tmp_path / "oracle",
+                    ignore=shutil.ignore_patterns("__pycache__", "*.so", "*.o"))
+    (tmp_path / "tests").mkdir()
+    for f in ("conftest.py", "test_oracle_rope_norm.py"):
+        shutil.copy(os.path.join(ROOT, "tests", f), tmp_path / "tests" / f)
+    src = (tmp_path / "oracle" / "rope_norm.py").read_text()
+    assert src.count(old) >= 1, f"mutation site for {name!r} not found"
+    (tmp_path / "oracle" / "rope_norm.py").write_text(src.replace(old, new))
+    env = dict(os.environ, PYTHONPATH=str(tmp_path), PYTHONDONTWRITEBYTECODE="1")
+    r = subprocess.run([sys.executable, "-m", "pytest", "-q", "-x", "-p", "no:cacheprovider",
+                        "tests/test_oracle_rope_norm.py"], cwd=tmp_path, env=env,
+                       capture_output=True, text=True, timeout=600)
+    assert r.returncode == 1, f"pins did not catch {name!r}:\n{r.stdout[-2000:]}"
+    assert "failed" in r.stdout
