@@ -191,14 +191,17 @@ def splitk_partials(q, k_pool, v_pool, block_tables, seq_lens, scale, softcap,
     return po, pl
 
 
-def balanced_split_ranges(seq_lens, window, block_size, num_kv_heads, grid, min_chunk):
+def balanced_split_ranges(seq_lens, window, block_size, num_kv_heads, grid, min_chunk,
+                          piece_cost=2):
     """The library's split-K work partition, as plain integer arithmetic.
 
-    Segments (request, KV head) of n_b visible blocks each are laid end to
-    end, ``T = Hkv * sum(n_b)`` tiles, cut into chunks of
-    ``q = max(min_chunk, ceil(T / grid))``; the part of a segment starting at
-    tile ``A`` inside chunk ``c`` is split ``c - A // q``.  Returns
-    ``ranges[b][kvh]`` = list of (j0, j1) per split (None where unused).
+    Segments (request, KV head) are laid end to end on a line of work units:
+    a segment of n > 0 visible blocks takes ``piece_cost`` units (the fixed
+    cost of one more partial) followed by one unit per block, an empty one
+    none.  The ``T`` units are cut into chunks of
+    ``q = max(min_chunk, ceil(T / grid))``; the blocks of a segment whose
+    first block sits at unit ``A`` that fall inside chunk ``c`` form split
+    ``c - A // q``.  Returns ``ranges[b][kvh]`` = list of (j0, j1) per split.
     """
     nb = []
     jl = []
@@ -206,24 +209,26 @@ def balanced_split_ranges(seq_lens, window, block_size, num_kv_heads, grid, min_
         j0, j1 = visible_block_range(int(L), window, block_size)
         nb.append(j1 - j0)
         jl.append(j0)
-    T = num_kv_heads * sum(nb)
+    units = [n + piece_cost if n > 0 else 0 for n in nb]
+    T = num_kv_heads * sum(units)
     q = max(min_chunk, -(-T // grid)) if T > 0 else max(min_chunk, 1)
     out = []
-    A = 0
+    pos = 0  # unit where the current segment starts
     for b, n in enumerate(nb):
         per_head = []
         for kvh in range(num_kv_heads):
             splits = []
             if n > 0:
-                c0 = A // q
-                for c in range(c0, (A + n - 1) // q + 1):
+                A = pos + piece_cost
+                for c in range(A // q, (A + n - 1) // q + 1):
                     t0 = max(A, c * q)
                     t1 = min(A + n, (c + 1) * q)
                     splits.append((jl[b] + t0 - A, jl[b] + t1 - A))
             per_head.append(splits)
-            A += n
+            pos += units[b]
         out.append(per_head)
     return out
+
 
 def lse_combine(partial_o, partial_lse):
     """Log-sum-exp merge of split partials over the split axis.

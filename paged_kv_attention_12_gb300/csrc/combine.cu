@@ -13,10 +13,11 @@ namespace pka {
 namespace {
 
 // One warp per (row, 128-column segment): each lane owns one float4 of the
-// output.  Split weights are computed 32 at a time (one split per lane);
-// only splits with a non-zero weight are read, and the loads of eight of them
-// are issued before any is used, so the loop is bound by bandwidth, not by
-// the latency of one load after another.
+// output.  The row's LSE values are read 32 at a time (one split per lane);
+// the partial rows of eight splits are loaded together (splits with
+// LSE = -inf, which no CTA wrote, are not touched) and merged four at a time
+// with a running maximum, in the same groups as the decode kernel's fused
+// combine.
 template <int D>
 __global__ void __launch_bounds__(128) combine_kernel(const CombineArgs a) {
   constexpr int SEGS = D / 128;
@@ -29,47 +30,25 @@ __global__ void __launch_bounds__(128) combine_kernel(const CombineArgs a) {
   const float* lse = a.partial_lse + static_cast<size_t>(row) * S;
   const float* po = a.partial_o + static_cast<size_t>(row) * S * D + seg * 128 + lane * 4;
 
-  float M = -INFINITY;
-  for (int s = lane; s < S; s += 32) M = fmaxf(M, lse[s]);
-#pragma unroll
-  for (int o = 16; o >= 1; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-  const float Ms = (M == -INFINITY) ? 0.f : M;
-
+  float M = -INFINITY, den = 0.f;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  float den = 0.f;
   for (int base = 0; base < S; base += 32) {
+    const float lreg = (base + lane < S) ? lse[base + lane] : -INFINITY;
     const int n = min(32, S - base);
-    // exp(-inf) = 0: a split with no keys (or a slot no CTA wrote) is skipped
-    // without touching its partial output
-    const float wl = (lane < n) ? fast_exp2((lse[base + lane] - Ms) * kLog2e) : 0.f;
-    den += wl;
-    const unsigned live = __ballot_sync(0xffffffffu, wl != 0.f);
-    const int cnt = __popc(live);
-    for (int k = 0; k < cnt; k += 8) {
+    for (int c = 0; c < n; c += 8) {
+      float lv[8];
       float4 x[8];
-      float w[8];
 #pragma unroll
       for (int u = 0; u < 8; ++u) {
-        if (k + u < cnt) {  // uniform across the warp
-          const int sb = static_cast<int>(__fns(live, 0, k + u + 1));
-          w[u] = __shfl_sync(0xffffffffu, wl, sb);
-          x[u] = *reinterpret_cast<const float4*>(po + static_cast<size_t>(base + sb) * D);
-        } else {
-          w[u] = 0.f;
-          x[u] = make_float4(0.f, 0.f, 0.f, 0.f);
-        }
+        lv[u] = __shfl_sync(0xffffffffu, lreg, (c + u) & 31);  // -inf past the row's end
+        x[u] = (lv[u] != -INFINITY)
+                   ? *reinterpret_cast<const float4*>(po + static_cast<size_t>(base + c + u) * D)
+                   : make_float4(0.f, 0.f, 0.f, 0.f);
       }
-#pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        acc.x = fmaf(w[u], x[u].x, acc.x);
-        acc.y = fmaf(w[u], x[u].y, acc.y);
-        acc.z = fmaf(w[u], x[u].z, acc.z);
-        acc.w = fmaf(w[u], x[u].w, acc.w);
-      }
+      lse_merge4(M, den, acc, lv, x);
+      lse_merge4(M, den, acc, lv + 4, x + 4);
     }
   }
-#pragma unroll
-  for (int o = 16; o >= 1; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
   const float inv = den > 0.f ? 1.f / den : 0.f;
   uint16_t* dst = a.out + static_cast<size_t>(row) * D + seg * 128 + lane * 4;
   *reinterpret_cast<uint2*>(dst) =

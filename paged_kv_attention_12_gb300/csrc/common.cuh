@@ -113,6 +113,36 @@ __device__ __forceinline__ float fast_exp2(float x) {
   return y;
 }
 
+// One step of the split-K log-sum-exp merge: folds four pieces (natural-log
+// LSE lv[u], normalised partial row x[u]) into a running state (max M,
+// denominator den, numerator acc) taken relative to M.  Pieces with
+// lv = -inf must come with x = 0; a group of four such pieces leaves the
+// state untouched.  The split-K combine launch and the decode kernel's fused
+// combine both merge groups [0, 4), [4, 8), ... of a row's pieces with this
+// step, so the two paths give identical results.
+__device__ __forceinline__ void lse_merge4(float& M, float& den, float4& acc, const float* lv,
+                                          const float4* x) {
+  const float gm = fmaxf(fmaxf(lv[0], lv[1]), fmaxf(lv[2], lv[3]));
+  if (gm == -INFINITY) return;
+  const float nm = fmaxf(M, gm);
+  const float r = fast_exp2((M - nm) * 1.4426950408889634f);  // 0 while M = -inf
+  den *= r;
+  acc.x *= r;
+  acc.y *= r;
+  acc.z *= r;
+  acc.w *= r;
+#pragma unroll
+  for (int u = 0; u < 4; ++u) {
+    const float w = fast_exp2((lv[u] - nm) * 1.4426950408889634f);
+    den += w;
+    acc.x = fmaf(w, x[u].x, acc.x);
+    acc.y = fmaf(w, x[u].y, acc.y);
+    acc.z = fmaf(w, x[u].z, acc.z);
+    acc.w = fmaf(w, x[u].w, acc.w);
+  }
+  M = nm;
+}
+
 // bf16 pair (packed in a 32-bit word) -> two fp32, exact.
 __device__ __forceinline__ void bf16x2_to_f32(uint32_t w, float& lo, float& hi) {
   lo = __uint_as_float(w << 16);

@@ -102,6 +102,15 @@ struct Piece {
 // Enumerates the pieces of one CTA.  Every lane of a warp runs it in
 // lockstep (it uses warp scans), and every warp of the CTA sees the same
 // sequence.
+//
+// Split mode: the segments (request, KV head) are laid end to end in a line
+// of work units, each segment taking kPieceCost units followed by one unit
+// per tile, and CTA c takes units [c q, (c+1) q).  The kPieceCost units stand
+// for the fixed cost of a piece (merging the warps' states, writing the
+// partial row): a CTA whose range starts a new segment gets that many fewer
+// tiles, so CTAs with two pieces finish with the others.
+constexpr int kPieceCost = 2;
+
 struct PieceIter {
   const DecodeArgs* a;
   bool direct;
@@ -111,7 +120,7 @@ struct PieceIter {
   long long lo, hi, q;
   bool last;
   int b, kvh;
-  long long prefix;  // sum of nb over requests before b
+  long long prefix;  // work units of one segment, summed over requests before b
   ReqGeo geo;
   bool done;
 
@@ -123,14 +132,16 @@ struct PieceIter {
       item = blockIdx.x;
       return;
     }
-    // total tiles T = Hkv * sum_b nb_b (the first 32 requests' counts stay in
-    // a register, so batches of up to 32 requests read seq_lens once)
+    // total work units T = Hkv * sum_b u_b, u_b = nb_b + kPieceCost for a
+    // request with visible keys (the first 32 requests' counts stay in a
+    // register, so batches of up to 32 requests read seq_lens once)
+    auto units = [](int nb) { return nb > 0 ? nb + kPieceCost : 0; };
     long long T = 0;
-    const int nb0 = (lane < args.batch) ? req_geo(args, lane).nb : 0;
+    const int u0 = units((lane < args.batch) ? req_geo(args, lane).nb : 0);
     for (int base = 0; base < args.batch; base += 32) {
       const int bb = base + lane;
-      const int nb = (base == 0) ? nb0 : ((bb < args.batch) ? req_geo(args, bb).nb : 0);
-      T += __shfl_sync(0xffffffffu, warp_incl_scan(nb, lane), 31);
+      const int u = (base == 0) ? u0 : units((bb < args.batch) ? req_geo(args, bb).nb : 0);
+      T += __shfl_sync(0xffffffffu, warp_incl_scan(u, lane), 31);
     }
     T *= args.Hkv;
     const long long grid = gridDim.x;
@@ -145,17 +156,17 @@ struct PieceIter {
     hi = min(T, lo + q);
     last = (c == weff - 1);
     // first request holding a segment this CTA touches: the first b with
-    // Hkv*(prefix_b + nb_b) + (nb_b == 0) > lo
+    // Hkv*(prefix_b + u_b) + (u_b == 0) > lo
     long long run = 0;
     b = args.batch;
     prefix = run;
     for (int base = 0; base < args.batch; base += 32) {
       const int bb = base + lane;
-      const int nb = (base == 0) ? nb0 : ((bb < args.batch) ? req_geo(args, bb).nb : 0);
-      const int incl = warp_incl_scan(nb, lane);
-      const long long pre = run + incl - nb;
+      const int u = (base == 0) ? u0 : units((bb < args.batch) ? req_geo(args, bb).nb : 0);
+      const int incl = warp_incl_scan(u, lane);
+      const long long pre = run + incl - u;
       const bool hit = (bb < args.batch) &&
-                       (static_cast<long long>(args.Hkv) * (pre + nb) + (nb == 0 ? 1 : 0) > lo);
+                       (static_cast<long long>(args.Hkv) * (pre + u) + (u == 0 ? 1 : 0) > lo);
       const unsigned m = __ballot_sync(0xffffffffu, hit);
       if (m) {
         const int first = __ffs(m) - 1;
@@ -195,10 +206,12 @@ struct PieceIter {
           done = true;
           return false;
         }
-        const long long seg = static_cast<long long>(A.Hkv) * prefix +
-                              static_cast<long long>(kvh) * geo.nb;  // segment start
         const int n = geo.nb;
-        const bool before = seg + (n > 0 ? n : 1) <= lo;  // wholly before this chunk
+        const int u = n > 0 ? n + kPieceCost : 0;
+        const long long seg = static_cast<long long>(A.Hkv) * prefix +
+                              static_cast<long long>(kvh) * u;  // segment start
+        const long long s0 = seg + (n > 0 ? kPieceCost : 0);  // unit of its first tile
+        const bool before = (n > 0 ? s0 + n : seg + 1) <= lo;  // wholly before this chunk
         const bool after = !last && seg >= hi;
         if (after) {
           done = true;
@@ -209,23 +222,26 @@ struct PieceIter {
         // advance to the next segment
         if (++kvh == A.Hkv) {
           kvh = 0;
-          prefix += geo.nb;
+          prefix += u;
           ++b;
           if (b < A.batch) geo = req_geo(A, b);
         }
         if (before) continue;
-        const long long t0 = max(seg, lo);
-        const long long t1 = min(seg + n, hi);
+        const long long t0 = max(s0, lo);
+        const long long t1 = min(s0 + n, hi);
         p.b = cur_b;
         p.kvh = cur_kvh;
-        p.j0 = g.jlo + static_cast<int>(t0 - seg);
+        p.j0 = g.jlo + static_cast<int>(t0 - s0);
         p.ntiles = static_cast<int>(max(0LL, t1 - t0));
         p.t_lo = g.t_lo;
         p.pos = g.pos;
-        const long long cfirst = seg / q;
+        // slots: the CTA holding the first tile writes slot 0; a CTA whose
+        // range holds only the segment's piece-cost units gets a negative
+        // slot and no piece
+        const long long cfirst = s0 / q;
         p.slot = static_cast<int>(static_cast<long long>(blockIdx.x) - cfirst);
         p.fill_from = -1;
-        p.npieces = (n == 0) ? 0 : static_cast<int>((seg + n - 1) / q - cfirst + 1);
+        p.npieces = (n == 0) ? 0 : static_cast<int>((s0 + n - 1) / q - cfirst + 1);
         if (n == 0) {
           p.fill_from = 0;
         } else if (p.slot == 0) {
@@ -600,32 +616,42 @@ __global__ void __launch_bounds__((NW + 1) * 32, 2)
         }
       consumer_sync(NW * 32);
 
-      // ---- merge the warps' states and write this piece's result
-      for (int idx = threadIdx.x; idx < G * D; idx += NW * 32) {
-        const int h = idx / D;
-        const int d = idx % D;
+      // ---- merge the warps' states and write this piece's result, four
+      // consecutive columns of one head per thread (vector loads and stores,
+      // the heads' scale factors taken once per four columns)
+      for (int idx = threadIdx.x; idx < G * (D / 4); idx += NW * 32) {
+        const int h = idx / (D / 4);
+        const int d = (idx % (D / 4)) * 4;
         float M = -INFINITY;
 #pragma unroll
         for (int w = 0; w < NW; ++w) M = fmaxf(M, mrg_m[w * G + h]);
         const float Ms = (M == -INFINITY) ? 0.f : M;
-        float den = 0.f, num = 0.f;
+        float den = 0.f;
+        float4 num = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
         for (int w = 0; w < NW; ++w) {
           const float sc = fast_exp2(mrg_m[w * G + h] - Ms);
           den = fmaf(sc, mrg_l[w * G + h], den);
-          num = fmaf(sc, mrg_acc[(w * G + h) * D + d], num);
+          const float4 v = *reinterpret_cast<const float4*>(&mrg_acc[(w * G + h) * D + d]);
+          num.x = fmaf(sc, v.x, num.x);
+          num.y = fmaf(sc, v.y, num.y);
+          num.z = fmaf(sc, v.z, num.z);
+          num.w = fmaf(sc, v.w, num.w);
         }
-        const float ov = (den > 0.f) ? num / den : 0.f;
+        const float inv = (den > 0.f) ? 1.f / den : 0.f;
+        const float4 ov = make_float4(num.x * inv, num.y * inv, num.z * inv, num.w * inv);
         const int hq = pc.kvh * G + h;
         if (split) {
           if (pc.slot < a.num_splits) {
             const size_t ph = (static_cast<size_t>(pc.b) * a.Hq + hq) * a.num_splits + pc.slot;
-            a.partial_o[ph * D + d] = ov;
+            *reinterpret_cast<float4*>(a.partial_o + ph * D + d) = ov;
             if (d == 0) a.partial_lse[ph] = (den > 0.f) ? (M + log2f(den)) * kLn2 : -INFINITY;
           }
         } else {
-          reinterpret_cast<uint16_t*>(a.out)[(static_cast<size_t>(pc.qrow) * a.Hq + hq) * D + d] =
-              f32_to_bf16_rn(ov);
+          uint16_t* dst =
+              reinterpret_cast<uint16_t*>(a.out) + (static_cast<size_t>(pc.qrow) * a.Hq + hq) * D + d;
+          *reinterpret_cast<uint2*>(dst) =
+              make_uint2(pack_bf16x2(ov.x, ov.y), pack_bf16x2(ov.z, ov.w));
         }
       }
       consumer_sync(NW * 32);
@@ -666,73 +692,45 @@ __global__ void __launch_bounds__((NW + 1) * 32, 2)
       }
       if (last) {
         __threadfence();  // every other piece's partials are visible now
-        // weights of the pieces, per head, into the (free) merge area
-        float* wts = mrg_acc;  // [G][np]
-        float* dens = mrg_m;   // [G]
-        for (int h = warp; h < G; h += NW) {
-          const size_t ph0 = (static_cast<size_t>(pc.b) * a.Hq + pc.kvh * G + h) * a.num_splits;
-          float M = -INFINITY;
-          for (int sl = lane; sl < np; sl += 32) M = fmaxf(M, __ldcg(a.partial_lse + ph0 + sl));
+        // One pass over the pieces (read from L2): four consecutive columns
+        // of one head per item, the pieces' LSE and partial rows of four
+        // pieces loaded together, merged with a running maximum.  The item
+        // loop is unrolled so that the loads of all of a thread's items are
+        // in flight together.
+        constexpr int kItems = G * (D / 4);
+        constexpr int kPerThread = (kItems + NW * 32 - 1) / (NW * 32);
 #pragma unroll
-          for (int off = 16; off >= 1; off >>= 1)
-            M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
-          const float Ms = (M == -INFINITY) ? 0.f : M;
-          float den = 0.f;
-          for (int sl = lane; sl < np; sl += 32) {
-            const float w = fast_exp2((__ldcg(a.partial_lse + ph0 + sl) - Ms) * kLog2e);
-            wts[h * np + sl] = w;
-            den += w;
-          }
+        for (int k = 0; k < kPerThread; ++k) {
+          const int item = threadIdx.x + k * NW * 32;
+          if (item < kItems) {
+            const int h = item / (D / 4);
+            const int d0 = (item % (D / 4)) * 4;
+            const size_t ph0 =
+                (static_cast<size_t>(pc.b) * a.Hq + pc.kvh * G + h) * a.num_splits;
+            float M = -INFINITY, den = 0.f;
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int s0 = 0; s0 < np; s0 += 4) {
+              float lv[4];
+              float4 x[4];
 #pragma unroll
-          for (int off = 16; off >= 1; off >>= 1) den += __shfl_xor_sync(0xffffffffu, den, off);
-          if (lane == 0) dens[h] = den;
-        }
-        consumer_sync(NW * 32);
-        // one (head, 8-column chunk) per thread; the partials of four pieces
-        // are in flight at a time
-        for (int item = threadIdx.x; item < G * (D / 8); item += NW * 32) {
-          const int h = item / (D / 8);
-          const int d0 = (item % (D / 8)) * 8;
-          const size_t ph0 = (static_cast<size_t>(pc.b) * a.Hq + pc.kvh * G + h) * a.num_splits;
-          float acc8[8];
-#pragma unroll
-          for (int e = 0; e < 8; ++e) acc8[e] = 0.f;
-          for (int s0 = 0; s0 < np; s0 += 4) {
-            float4 x[4][2];
-            float w[4];
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-              w[u] = (s0 + u < np) ? wts[h * np + s0 + u] : 0.f;
-              if (w[u] != 0.f) {
-                const float4* src =
-                    reinterpret_cast<const float4*>(a.partial_o + (ph0 + s0 + u) * D + d0);
-                x[u][0] = __ldcg(src);
-                x[u][1] = __ldcg(src + 1);
-              } else {
-                x[u][0] = x[u][1] = make_float4(0.f, 0.f, 0.f, 0.f);
+              for (int u = 0; u < 4; ++u) {
+                if (s0 + u < np) {
+                  lv[u] = __ldcg(a.partial_lse + ph0 + s0 + u);
+                  x[u] = __ldcg(reinterpret_cast<const float4*>(a.partial_o +
+                                                                (ph0 + s0 + u) * D + d0));
+                } else {
+                  lv[u] = -INFINITY;
+                  x[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+                }
               }
+              lse_merge4(M, den, acc, lv, x);
             }
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-              acc8[0] = fmaf(w[u], x[u][0].x, acc8[0]);
-              acc8[1] = fmaf(w[u], x[u][0].y, acc8[1]);
-              acc8[2] = fmaf(w[u], x[u][0].z, acc8[2]);
-              acc8[3] = fmaf(w[u], x[u][0].w, acc8[3]);
-              acc8[4] = fmaf(w[u], x[u][1].x, acc8[4]);
-              acc8[5] = fmaf(w[u], x[u][1].y, acc8[5]);
-              acc8[6] = fmaf(w[u], x[u][1].z, acc8[6]);
-              acc8[7] = fmaf(w[u], x[u][1].w, acc8[7]);
-            }
+            const float inv = den > 0.f ? 1.f / den : 0.f;
+            uint16_t* dst = reinterpret_cast<uint16_t*>(a.out) +
+                            (static_cast<size_t>(pc.qrow) * a.Hq + pc.kvh * G + h) * D + d0;
+            *reinterpret_cast<uint2*>(dst) = make_uint2(pack_bf16x2(acc.x * inv, acc.y * inv),
+                                                        pack_bf16x2(acc.z * inv, acc.w * inv));
           }
-          const float den = dens[h];
-          const float inv = den > 0.f ? 1.f / den : 0.f;
-          uint16_t* dst = reinterpret_cast<uint16_t*>(a.out) +
-                          (static_cast<size_t>(pc.qrow) * a.Hq + pc.kvh * G + h) * D + d0;
-          *reinterpret_cast<uint4*>(dst) =
-              make_uint4(pack_bf16x2(acc8[0] * inv, acc8[1] * inv),
-                         pack_bf16x2(acc8[2] * inv, acc8[3] * inv),
-                         pack_bf16x2(acc8[4] * inv, acc8[5] * inv),
-                         pack_bf16x2(acc8[6] * inv, acc8[7] * inv));
         }
         if (threadIdx.x == 0) a.seg_counters[pc.b * a.Hkv + pc.kvh] = 0;
         consumer_sync(NW * 32);

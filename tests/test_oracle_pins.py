@@ -374,8 +374,9 @@ def test_splitk_combine_equals_full(window):
     assert np.isneginf(pl[1, :, 1:]).all()  # L=3 -> one block
 
 
+@pytest.mark.parametrize("piece_cost", [0, 2, 5])
 @pytest.mark.parametrize("grid,min_chunk", [(1, 1), (3, 2), (7, 4), (64, 1)])
-def test_balanced_partition_covers_and_combines(grid, min_chunk):
+def test_balanced_partition_covers_and_combines(grid, min_chunk, piece_cost):
     """The library's split partition: ranges of each (request, head) are
     disjoint, contiguous and cover exactly the visible blocks; combining the
     partials over them gives full attention."""
@@ -385,8 +386,13 @@ def test_balanced_partition_covers_and_combines(grid, min_chunk):
     p = problem(rng, L, [1 if x else 0 for x in L], Hq=4, Hkv=2, D=8, bs=4)
     q = rng.standard_normal((len(L), 4, 8))
     for window in (0, 9):
-        ranges = balanced_split_ranges(L, window, 4, 2, grid, min_chunk)
+        ranges = balanced_split_ranges(L, window, 4, 2, grid, min_chunk, piece_cost)
         S = max(len(r) for per in ranges for r in per) or 1
+        # a segment's splits never outnumber ceil(n / min_chunk) + 1
+        for b, per in enumerate(ranges):
+            jlo, jhi = visible_block_range(L[b], window, 4)
+            for splits in per:
+                assert len(splits) <= -(-(jhi - jlo) // min_chunk) + 1
         for b, per in enumerate(ranges):
             jlo, jhi = visible_block_range(L[b], window, 4)
             for splits in per:
