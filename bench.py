@@ -12,7 +12,12 @@ Each layer is one split-K decode launch followed by one LSE-combine launch
 
 Metric: paged-decode KV GB/s, counting algorithmic bytes (K/V rows of every
 visible key plus the query rows) per step over the device time of the step.
-The L2 is flushed (a 512 MiB write) before every timed step; the flush is
+The L2 is flushed before every timed step by a 512 MiB write followed by a
+256 MiB read of the written buffer: the write evicts every line the step
+could reuse, and the read evicts the flush's own dirty lines, whose
+write-back would otherwise land inside the next step (a decode step is
+preceded in a real engine by kernels that leave a few MB dirty, not 100+ MB).
+The step is also timed after the write alone (``dirty_l2``).  The flush is
 outside the per-step CUDA-event window.
 
 ``--impl reference`` times the fp64 CPU oracle on a bounded sample of the
@@ -240,6 +245,25 @@ def batch_kv_bytes(batch) -> float:
     return float(total + batch.q.numel() * 2)
 
 
+class L2Flush:
+    """Evicts the L2 before a timed region: a write of a 512 MiB buffer (four
+    times the L2), then, unless ``dirty``, a read of its first 256 MiB, which
+    evicts the dirty lines the write left so that their write-back does not
+    fall into the timed region."""
+
+    def __init__(self, dev):
+        import torch
+        self.buf = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+        self.acc = torch.empty((), dtype=torch.float32, device=dev)
+        self.dirty = False
+
+    def __call__(self, value: float = 1.0, dirty: bool = None):
+        import torch
+        self.buf.fill_(value)
+        if not (self.dirty if dirty is None else dirty):
+            torch.sum(self.buf[: self.buf.numel() // 2], dim=0, out=self.acc)
+
+
 def time_launches(fn, flush, iters, warmup):
     """Median CUDA-event time (ms) of fn(), L2 flushed before every call.
     fn() is captured once as a CUDA graph and replayed, as in the main step,
@@ -247,18 +271,18 @@ def time_launches(fn, flush, iters, warmup):
     import torch
     stream = torch.cuda.current_stream()
     for _ in range(warmup):
-        flush.fill_(1.0)
+        flush(1.0)
         fn()
     torch.cuda.synchronize()
     graph = torch.cuda.CUDAGraph()
     with torch.cuda.graph(graph):
         fn()
-    flush.fill_(1.0)
+    flush(1.0)
     graph.replay()
     torch.cuda.synchronize()
     ts = []
     for i in range(iters):
-        flush.fill_(float(i))
+        flush(float(i))
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
         graph.replay()
@@ -444,7 +468,7 @@ def main():
     binding.lib()
 
     if args.workload is not None:
-        flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+        flush = L2Flush(dev)
         entry = other_workloads(dev, flush, iters=args.steps, warmup=max(args.warmup, 1),
                                 cfgs=(args.workload,))[str(args.workload)]
         if rank == 0:
@@ -458,7 +482,7 @@ def main():
     else:
         runners = [binding.DecodeSplitK(b) for b in calls]
     bytes_step = step_bytes(calls)
-    flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+    flush = L2Flush(dev)
     stream = torch.cuda.current_stream()
 
     # A step's per-call inputs (q, block tables, seq_lens of both layers) live
@@ -505,7 +529,7 @@ def main():
                 binding.paged_decode_splitk_combine(r.partial_o, r.partial_lse, r.out)
 
     for _ in range(args.warmup):
-        flush.fill_(1.0)
+        flush(1.0)
         step()
     torch.cuda.synchronize()
     # One step as a CUDA graph: the launches of a step run back to back on the
@@ -514,7 +538,7 @@ def main():
     with torch.cuda.graph(graph):
         step()
     for _ in range(2):
-        flush.fill_(1.0)
+        flush(1.0)
         graph.replay()
     torch.cuda.synchronize()
 
@@ -527,7 +551,7 @@ def main():
     torch.cuda.synchronize()
     t_wall = time.perf_counter()
     for s_ in range(args.steps):
-        flush.fill_(float(s_))
+        flush(float(s_))
         ev[s_][0].record(stream)
         graph.replay()
         ev[s_][1].record(stream)
@@ -541,6 +565,24 @@ def main():
     ms_per_step = total_ms / args.steps
     value = world * bytes_step / (ms_per_step * 1e-3) / 1e9
 
+    # the same steps after the write alone: the flush's dirty lines are
+    # written back while the step runs
+    dev_ev = []
+    barrier(world)
+    for s_ in range(args.steps):
+        flush(float(s_), dirty=True)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        graph.replay()
+        e1.record(stream)
+        dev_ev.append((e0, e1))
+    torch.cuda.synchronize()
+    dirty_ms = max_over_ranks(sum(a.elapsed_time(b) for a, b in dev_ev), world) / args.steps
+    dirty_l2 = {"value": world * bytes_step / (dirty_ms * 1e-3) / 1e9, "unit": "GB/s",
+                "ms_per_step": dirty_ms,
+                "l2": "512 MiB write only before every step (its dirty lines are written "
+                      "back during the step)"}
+
     # the dominant kernel alone: each decode launch (one CUDA graph per call)
     # timed by CUDA events on its stream, the L2 flushed before it
     kgraphs = []
@@ -553,7 +595,7 @@ def main():
     kern_ms = []
     for s_ in range(args.steps):
         for i in range(len(calls)):
-            flush.fill_(float(s_))
+            flush(float(s_))
             k0, k1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             k0.record(stream)
             kgraphs[i].replay()
@@ -571,7 +613,7 @@ def main():
         d2h = host_out.numel()
         e_ms = []
         for s in range(args.warmup + args.steps):
-            flush.fill_(float(s))
+            flush(float(s))
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             e0.record(stream)
             in_buf.copy_(host_in, non_blocking=True)
@@ -599,7 +641,9 @@ def main():
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic",
-        "config": {"workload": WORKLOAD_NAME, "l2": "flushed before every step (512 MiB write)",
+        "config": {"workload": WORKLOAD_NAME,
+                   "l2": "flushed before every step: 512 MiB write, then a 256 MiB read of "
+                         "the written buffer (evicts the flush's dirty lines)",
                    "path": ("paged_decode_attn_ws (split-K, combine fused)" if args.path == "fused"
                             else "paged_decode_splitk + paged_decode_splitk_combine"),
                    "timing": "each step one CUDA-graph replay, CUDA events around it",
@@ -611,6 +655,7 @@ def main():
         "gpu_launches": args.steps * len(calls) * (1 if args.path == "fused" else 2),
         "wall_s": wall,
     }
+    line["dirty_l2"] = dirty_l2
     if e2e:
         line["e2e"] = e2e
     if clocks:

@@ -192,7 +192,7 @@ def splitk_partials(q, k_pool, v_pool, block_tables, seq_lens, scale, softcap,
 
 
 def balanced_split_ranges(seq_lens, window, block_size, num_kv_heads, grid, min_chunk,
-                          piece_cost=2):
+                          piece_cost=4):
     """The library's split-K work partition, as plain integer arithmetic.
 
     Segments (request, KV head) are laid end to end on a line of work units:

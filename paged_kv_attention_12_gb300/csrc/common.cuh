@@ -106,6 +106,12 @@ __device__ __forceinline__ uint64_t policy_evict_first() {
   return p;
 }
 
+// GPU-scope acquire-release fence: with a relaxed atomic after it, the
+// release half of a flag handshake; after an atomic, the acquire half.
+__device__ __forceinline__ void fence_acq_rel_gpu() {
+  asm volatile("fence.acq_rel.gpu;" ::: "memory");
+}
+
 // ------------------------------------------------------------ arithmetic
 __device__ __forceinline__ float fast_exp2(float x) {
   float y;

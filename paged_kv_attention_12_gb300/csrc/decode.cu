@@ -108,8 +108,10 @@ struct Piece {
 // per tile, and CTA c takes units [c q, (c+1) q).  The kPieceCost units stand
 // for the fixed cost of a piece (merging the warps' states, writing the
 // partial row): a CTA whose range starts a new segment gets that many fewer
-// tiles, so CTAs with two pieces finish with the others.
-constexpr int kPieceCost = 2;
+// tiles, so CTAs with two pieces finish with the others.  (Of 0, 2, 4 and 6
+// units, 4 gave the shortest serving and long-context decode steps: a piece
+// costs about as much as streaming four 16 KB tiles.)
+constexpr int kPieceCost = 4;
 
 struct PieceIter {
   const DecodeArgs* a;
@@ -683,7 +685,7 @@ __global__ void __launch_bounds__((NW + 1) * 32, 2)
       bool last = false;
       if (pc.ntiles > 0 && pc.slot < a.num_splits) {
         if (threadIdx.x == 0) {
-          __threadfence();  // this CTA's partials before its arrival
+          fence_acq_rel_gpu();  // the CTA's partials (ordered by the barrier) before its arrival
           const int old = atomicAdd(&a.seg_counters[pc.b * a.Hkv + pc.kvh], 1);
           *last_flag = (old == np - 1) ? 1 : 0;
         }
@@ -691,7 +693,7 @@ __global__ void __launch_bounds__((NW + 1) * 32, 2)
         last = *last_flag != 0;
       }
       if (last) {
-        __threadfence();  // every other piece's partials are visible now
+        fence_acq_rel_gpu();  // every other piece's partials are visible now
         // One pass over the pieces (read from L2): four consecutive columns
         // of one head per item, the pieces' LSE and partial rows of four
         // pieces loaded together, merged with a running maximum.  The item
