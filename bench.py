@@ -307,6 +307,10 @@ def other_workloads(dev, flush, iters=10, warmup=3, cfgs=(1, 3, 4, 5)):
         if cfg in (1, 3):
             r = binding.DecodeFused(batch)
             fn, path = r.run, "paged_decode_attn_ws (split-K, combine fused)"
+        elif cfg == 5:
+            r = binding.MixedBatch(batch)
+            fn, path = r.run, ("paged_prefill_attn_ws (one launch: decode rows on split-K "
+                               "decode pipelines, chunks on the tcgen05 prefill pipeline)")
         else:
             out = torch.empty_like(batch.q)
             fn, path = (lambda b=batch, o=out: binding.run_batch(b, o)), "paged_prefill_attn"

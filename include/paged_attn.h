@@ -190,6 +190,28 @@ int paged_prefill_attn(const void* q, void* out, const pka_kv_pool* kv,
                        int32_t max_seq_len, const pka_attn_params* params,
                        void* stream);
 
+/* Mixed batch in one launch with a workspace (mixed-batch chunked prefill,
+ * architecture page "Phase status"): same arguments, result and errors as
+ * paged_prefill_attn, but requests with exactly one query token (decode rows)
+ * go to decode pipelines in the same launch -- split-K over their keys with
+ * the log-sum-exp merge fused in, as paged_decode_attn_ws -- instead of
+ * filling G of the 128 rows of a tensor-core tile; requests with more tokens
+ * run the tensor-core prefill pipeline.
+ * workspace: device, 16-byte aligned, at least paged_prefill_attn_ws_bytes()
+ * bytes (the layout of paged_decode_attn_ws for B requests); its B*Hkv int32
+ * counters must be zero before the first call and are left zero by every
+ * call that completes (zero them again after a PKA_DEVERR_TIMEOUT).  Calls
+ * sharing one workspace must not overlap on the GPU.  PKA_ERR_WORKSPACE if
+ * workspace_bytes is too small. */
+size_t paged_prefill_attn_ws_bytes(int32_t B, int32_t Hq, int32_t Hkv, int32_t D,
+                                   int32_t max_seq_len, int32_t window);
+int paged_prefill_attn_ws(const void* q, void* out, const pka_kv_pool* kv,
+                          const int32_t* block_tables, int32_t max_blocks,
+                          const int32_t* query_start_loc, const int32_t* seq_lens,
+                          int32_t B, int32_t Hq, int32_t total_q, int32_t max_query_len,
+                          int32_t max_seq_len, const pka_attn_params* params,
+                          void* workspace, size_t workspace_bytes, void* stream);
+
 /* Checked mode: validates, on the device, every table entry a call would
  * dereference (j < ceil(seq_len/bs)) against [0, num_blocks), and seq_len
  * against [0, max_blocks*bs]; OR-s PKA_DEVERR_* bits into *err (device int32,

@@ -34,7 +34,7 @@ EXPORTS = [
     "paged_decode_splitk_combine", "paged_prefill_attn", "paged_attn_check_tables",
     "paged_decode_attn_noalloc", "paged_decode_attn_ws_bytes", "paged_decode_attn_ws",
     "paged_kv_append", "paged_decode_splitk_logits", "paged_decode_key_mass",
-    "paged_kv_append_rope",
+    "paged_kv_append_rope", "paged_prefill_attn_ws_bytes", "paged_prefill_attn_ws",
 ]
 
 
@@ -105,6 +105,11 @@ def lib() -> ctypes.CDLL:
     L.paged_kv_append_rope.restype = ctypes.c_int
     L.paged_kv_append_rope.argtypes = [VP, VP, VP, VP, VP, I32, I32, I32, I32, I32, VP, VP, I32,
                                        VP, VP, I32, ctypes.c_float, ctypes.c_float, I32, VP, VP]
+    L.paged_prefill_attn_ws_bytes.restype = ctypes.c_size_t
+    L.paged_prefill_attn_ws_bytes.argtypes = [I32, I32, I32, I32, I32, I32]
+    L.paged_prefill_attn_ws.restype = ctypes.c_int
+    L.paged_prefill_attn_ws.argtypes = [VP, VP, P(PkaKvPool), VP, I32, VP, VP, I32, I32, I32, I32,
+                                        I32, P(PkaAttnParams), VP, ctypes.c_size_t, VP]
     L.paged_kv_append.restype = ctypes.c_int
     L.paged_kv_append.argtypes = [VP, VP, VP, VP, I32, I32, I32, I32, VP, I32, VP, VP]
     _lib = L
@@ -251,6 +256,27 @@ def paged_prefill_attn(q, out, k_pool, v_pool, block_tables, query_start_loc, se
     _check("paged_prefill_attn", st)
 
 
+def paged_prefill_attn_ws_bytes(B, Hq, Hkv, D, max_seq_len, window=0) -> int:
+    return int(lib().paged_prefill_attn_ws_bytes(B, Hq, Hkv, D, int(max_seq_len), int(window)))
+
+
+def paged_prefill_attn_ws(q, out, k_pool, v_pool, block_tables, query_start_loc, seq_lens,
+                          max_query_len, max_seq_len, workspace, *, scale, softcap=0.0, window=0,
+                          err=None, stream=None):
+    """Mixed batch in one launch: decode rows on decode pipelines, chunks on
+    the tensor-core prefill pipeline.  ``workspace``: zero-initialised device
+    bytes, at least ``paged_prefill_attn_ws_bytes``; left zeroed."""
+    pool = kv_pool(k_pool, v_pool)
+    par = attn_params(scale, softcap, window, err)
+    st = lib().paged_prefill_attn_ws(q.data_ptr(), out.data_ptr(), ctypes.byref(pool),
+                                     block_tables.data_ptr(), block_tables.shape[1],
+                                     query_start_loc.data_ptr(), seq_lens.data_ptr(),
+                                     seq_lens.shape[0], q.shape[1], q.shape[0],
+                                     int(max_query_len), int(max_seq_len), ctypes.byref(par),
+                                     workspace.data_ptr(), workspace.numel(), _stream(stream))
+    _check("paged_prefill_attn_ws", st)
+
+
 def paged_attn_check_tables(block_tables, seq_lens, num_blocks, err, block_size=16, stream=None):
     st = lib().paged_attn_check_tables(block_tables.data_ptr(), block_tables.shape[1],
                                        seq_lens.data_ptr(), seq_lens.shape[0], int(num_blocks),
@@ -333,6 +359,28 @@ class DecodeFused:
         paged_decode_attn_ws(b.q, self.out, b.k_pool, b.v_pool, b.block_tables, b.seq_lens,
                              b.max_seq_len, self.workspace, scale=b.scale, softcap=b.softcap,
                              window=b.window, err=err)
+        return self.out
+
+
+class MixedBatch:
+    """A varlen batch (decode rows and prefill chunks) in one launch through
+    ``paged_prefill_attn_ws``.  Owns a zero-initialised workspace."""
+
+    def __init__(self, batch):
+        import torch
+        self.batch = batch
+        nbytes = paged_prefill_attn_ws_bytes(batch.num_requests, batch.num_q_heads,
+                                             batch.num_kv_heads, batch.head_dim,
+                                             batch.max_seq_len, batch.window)
+        self.workspace = torch.zeros(max(nbytes, 16), dtype=torch.uint8, device=batch.q.device)
+        self.out = torch.empty_like(batch.q)
+
+    def run(self, err=None):
+        b = self.batch
+        paged_prefill_attn_ws(b.q, self.out, b.k_pool, b.v_pool, b.block_tables,
+                              b.query_start_loc, b.seq_lens, b.max_query_len, b.max_seq_len,
+                              self.workspace, scale=b.scale, softcap=b.softcap, window=b.window,
+                              err=err)
         return self.out
 
 

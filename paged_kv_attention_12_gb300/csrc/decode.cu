@@ -1,753 +1,21 @@
-// Paged decode attention, direct and split-K (sm_103a: TMA tensor tiles,
-// mbarrier ring, warp-level tensor-core MMA, shuffle online softmax).
-//
-// One query token per request attends over its visible keys, read block by
-// block through the request's block table ("Triton paged decode ... kernels
-// reading K/V through block tables; split-K decode variant", inference-server
-// README, engine feature list).  Decode is bound by HBM: every K/V byte is
-// read once, so the design is about keeping enough bytes in flight, spreading
-// them evenly over the SMs, and keeping the per-byte arithmetic far below the
-// copy time.
-//
-// Work.  A segment is one (request, KV head): its visible blocks, each a
-// 16-key "tile".  The kernel is persistent (one CTA per SM).
-//  * split-K: the segments' tiles, laid end to end, are cut into equal
-//    contiguous chunks of q = max(min_chunk, ceil(total / grid)) tiles, one
-//    chunk per CTA.  Each piece of a segment inside a chunk gives one partial
-//    (normalised output, LSE) in slot (CTA index - CTA index of the
-//    segment's first tile); the CTA holding a segment's first tile also
-//    writes LSE = -inf into the slots the segment does not use, so the LSE
-//    combine needs nothing but the partials.  Every CTA streams the same
-//    number of tiles whatever the mix of lengths.
-//  * direct: CTA c takes whole segments c, c + grid, ... and writes bf16.
-//
-// Inside a CTA:
-//  * one producer warp walks the pieces' block tables (32 ids per coalesced
-//    load) and loads, per tile, the (block, head) K and V tiles with one
-//    3-D TMA copy each (D / 64 boxes of 16 rows x 64 columns, 128-byte
-//    swizzle) into a ring of
-//    shared-memory slots, completion counted on a "full" mbarrier;
-//  * NW consumer warps take the ring's tiles round robin; every slot has one
-//    owner warp, so each slot's mbarrier phases are consumed in order.  A
-//    warp computes S^T = K q^T and O^T += V^T P^T with m16n8k16 MMAs (keys
-//    or head-dim rows on M, the G <= 8 query heads of the KV group on N, so
-//    every K/V byte feeds all G heads), operands by conflict-free ldmatrix
-//    from the swizzled tiles; the online softmax runs in the exp2 domain on
-//    the accumulator fragments with shuffles; P goes to the PV operand
-//    layout through shuffles, in bf16;
-//  * at the end of a piece the consumer warps merge their (max, sum, acc)
-//    states through shared memory and write the piece's result, while the
-//    producer already streams the next piece's tiles.
-//
-// Tiles with keys outside [first visible, query position] (window start,
-// ragged tail) are masked on the fragments; V rows past the sequence end
-// (stale slots that may hold NaN) are zeroed in shared memory before P V.
-#include <cuda.h>
-#include <cudaTypedefs.h>
-
-#include "common.cuh"
-#include "kernels.h"
-#include "tcgen05.cuh"
+// Paged decode attention launch (sm_103a): one decode pipeline per CTA,
+// two persistent CTAs per SM.  The pipeline itself (work partition, TMA ring,
+// warp-level MMA, online softmax, split-K epilogue and fused combine) is in
+// decode_body.cuh.
+#include "decode_body.cuh"
+#include "tmaps.cuh"
 
 namespace pka {
-
-namespace {
-
-__device__ __forceinline__ int warp_incl_scan(int x, int lane) {
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int y = __shfl_up_sync(0xffffffffu, x, o);
-    if (lane >= o) x += y;
-  }
-  return x;
-}
-
-// Named barrier over the consumer warps only (the producer keeps streaming).
-__device__ __forceinline__ void consumer_sync(int nthreads) {
-  asm volatile("bar.sync 1, %0;" ::"r"(nthreads) : "memory");
-}
-
-// Visible keys of request b's decode query: positions [t_lo, pos], blocks
-// [jlo, jlo + nb).
-struct ReqGeo {
-  int jlo, nb, t_lo, pos;
-};
-
-__device__ __forceinline__ ReqGeo req_geo(const DecodeArgs& a, int b) {
-  ReqGeo g;
-  int L = a.seq_lens[b];
-  if (L > a.max_blocks * kBlockSize || L < 0) {
-    report(a.err, PKA_DEVERR_SEQ_LEN);  // error path only: tables cannot hold it
-    L = max(0, min(L, a.max_blocks * kBlockSize));
-  }
-  g.pos = L - 1;
-  g.t_lo = (a.window > 0) ? max(0, g.pos - a.window + 1) : 0;
-  g.jlo = g.t_lo / kBlockSize;
-  g.nb = (L > 0) ? (L + kBlockSize - 1) / kBlockSize - g.jlo : 0;
-  return g;
-}
-
-// One piece of work: tiles [first, first + ntiles) of segment (b, kvh).
-struct Piece {
-  int b, kvh;
-  int j0;        // logical block of the first tile
-  int ntiles;
-  int t_lo, pos;
-  int qrow;      // query row of the request
-  int slot;      // split-K partial slot (direct mode: unused)
-  int fill_from; // >= 0: also write LSE=-inf into slots [fill_from, num_splits)
-  int npieces;   // split-K: pieces (slots used) of this segment
-};
-
-// Enumerates the pieces of one CTA.  Every lane of a warp runs it in
-// lockstep (it uses warp scans), and every warp of the CTA sees the same
-// sequence.
-//
-// Split mode: the segments (request, KV head) are laid end to end in a line
-// of work units, each segment taking kPieceCost units followed by one unit
-// per tile, and CTA c takes units [c q, (c+1) q).  The kPieceCost units stand
-// for the fixed cost of a piece (merging the warps' states, writing the
-// partial row): a CTA whose range starts a new segment gets that many fewer
-// tiles, so CTAs with two pieces finish with the others.  (Of 0, 2, 4 and 6
-// units, 4 gave the shortest serving and long-context decode steps: a piece
-// costs about as much as streaming four 16 KB tiles.)
-constexpr int kPieceCost = 4;
-
-struct PieceIter {
-  const DecodeArgs* a;
-  bool direct;
-  // direct mode
-  int item;
-  // split mode
-  long long lo, hi, q;
-  bool last;
-  int b, kvh;
-  long long prefix;  // work units of one segment, summed over requests before b
-  ReqGeo geo;
-  bool done;
-
-  __device__ void init(const DecodeArgs& args, int lane) {
-    a = &args;
-    direct = args.split_blocks <= 0;
-    done = false;
-    if (direct) {
-      item = blockIdx.x;
-      return;
-    }
-    // total work units T = Hkv * sum_b u_b, u_b = nb_b + kPieceCost for a
-    // request with visible keys (the first 32 requests' counts stay in a
-    // register, so batches of up to 32 requests read seq_lens once)
-    auto units = [](int nb) { return nb > 0 ? nb + kPieceCost : 0; };
-    long long T = 0;
-    const int u0 = units((lane < args.batch) ? req_geo(args, lane).nb : 0);
-    for (int base = 0; base < args.batch; base += 32) {
-      const int bb = base + lane;
-      const int u = (base == 0) ? u0 : units((bb < args.batch) ? req_geo(args, bb).nb : 0);
-      T += __shfl_sync(0xffffffffu, warp_incl_scan(u, lane), 31);
-    }
-    T *= args.Hkv;
-    const long long grid = gridDim.x;
-    q = max(static_cast<long long>(args.split_blocks), (T + grid - 1) / grid);
-    const long long weff = T > 0 ? (T + q - 1) / q : 1;
-    const long long c = blockIdx.x;
-    if (c >= weff) {
-      done = true;
-      return;
-    }
-    lo = c * q;
-    hi = min(T, lo + q);
-    last = (c == weff - 1);
-    // first request holding a segment this CTA touches: the first b with
-    // Hkv*(prefix_b + u_b) + (u_b == 0) > lo
-    long long run = 0;
-    b = args.batch;
-    prefix = run;
-    for (int base = 0; base < args.batch; base += 32) {
-      const int bb = base + lane;
-      const int u = (base == 0) ? u0 : units((bb < args.batch) ? req_geo(args, bb).nb : 0);
-      const int incl = warp_incl_scan(u, lane);
-      const long long pre = run + incl - u;
-      const bool hit = (bb < args.batch) &&
-                       (static_cast<long long>(args.Hkv) * (pre + u) + (u == 0 ? 1 : 0) > lo);
-      const unsigned m = __ballot_sync(0xffffffffu, hit);
-      if (m) {
-        const int first = __ffs(m) - 1;
-        b = base + first;
-        prefix = __shfl_sync(0xffffffffu, pre, first);
-        break;
-      }
-      run += __shfl_sync(0xffffffffu, incl, 31);
-    }
-    kvh = 0;
-    if (b < args.batch) geo = req_geo(args, b);
-  }
-
-  __device__ bool next(Piece& p) {
-    if (done) return false;
-    const DecodeArgs& A = *a;
-    if (direct) {
-      const int nseg = A.batch * A.Hkv;
-      if (item >= nseg) {
-        done = true;
-        return false;
-      }
-      p.b = item / A.Hkv;
-      p.kvh = item % A.Hkv;
-      const ReqGeo g = req_geo(A, p.b);
-      p.j0 = g.jlo;
-      p.ntiles = g.nb;
-      p.t_lo = g.t_lo;
-      p.pos = g.pos;
-      p.slot = 0;
-      p.fill_from = -1;
-      p.npieces = 1;
-      item += gridDim.x;
-    } else {
-      while (true) {
-        if (b >= A.batch) {
-          done = true;
-          return false;
-        }
-        const int n = geo.nb;
-        const int u = n > 0 ? n + kPieceCost : 0;
-        const long long seg = static_cast<long long>(A.Hkv) * prefix +
-                              static_cast<long long>(kvh) * u;  // segment start
-        const long long s0 = seg + (n > 0 ? kPieceCost : 0);  // unit of its first tile
-        const bool before = (n > 0 ? s0 + n : seg + 1) <= lo;  // wholly before this chunk
-        const bool after = !last && seg >= hi;
-        if (after) {
-          done = true;
-          return false;
-        }
-        const int cur_b = b, cur_kvh = kvh;
-        const ReqGeo g = geo;
-        // advance to the next segment
-        if (++kvh == A.Hkv) {
-          kvh = 0;
-          prefix += u;
-          ++b;
-          if (b < A.batch) geo = req_geo(A, b);
-        }
-        if (before) continue;
-        const long long t0 = max(s0, lo);
-        const long long t1 = min(s0 + n, hi);
-        p.b = cur_b;
-        p.kvh = cur_kvh;
-        p.j0 = g.jlo + static_cast<int>(t0 - s0);
-        p.ntiles = static_cast<int>(max(0LL, t1 - t0));
-        p.t_lo = g.t_lo;
-        p.pos = g.pos;
-        // slots: the CTA holding the first tile writes slot 0; a CTA whose
-        // range holds only the segment's piece-cost units gets a negative
-        // slot and no piece
-        const long long cfirst = s0 / q;
-        p.slot = static_cast<int>(static_cast<long long>(blockIdx.x) - cfirst);
-        p.fill_from = -1;
-        p.npieces = (n == 0) ? 0 : static_cast<int>((s0 + n - 1) / q - cfirst + 1);
-        if (n == 0) {
-          p.fill_from = 0;
-        } else if (p.slot == 0) {
-          p.fill_from = p.npieces;
-        }
-        if (p.ntiles == 0 && p.fill_from < 0) continue;
-        break;
-      }
-    }
-    p.qrow = p.b;
-    if (A.query_start_loc != nullptr) p.qrow = A.query_start_loc[p.b + 1] - 1;
-    return true;
-  }
-};
-
-}  // namespace
-
-// ------------------------------------------------------ warp-level MMA
-// mma.sync m16n8k16 (bf16 in, fp32 accumulate) and ldmatrix, as inline PTX.
-__device__ __forceinline__ void mma_bf16_16816(float (&d)[4], const uint32_t (&a)[4],
-                                               uint32_t b0, uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
-      "{%8, %9}, {%0, %1, %2, %3};"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
-
-__device__ __forceinline__ void ldmatrix_x4(uint32_t (&r)[4], uint32_t addr) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
-               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-               : "r"(addr)
-               : "memory");
-}
-
-__device__ __forceinline__ void ldmatrix_x4_trans(uint32_t (&r)[4], uint32_t addr) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
-               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-               : "r"(addr)
-               : "memory");
-}
-
-__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
-  uint32_t r;
-  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(sel));
-  return r;
-}
-
-template <int D, int G, int NW, int NSLOT>
-struct DecodeShape {
-  static constexpr int DC = D / 64;                        // 64-column boxes of a key row
-  static constexpr int kBoxBytes = kBlockSize * 128;       // one 16-row x 64-column box
-  static constexpr int kTileBytes = kBlockSize * D * 2;    // one block's K (or V) tile
-  static constexpr int KSTEPS = D / 16;                    // k-steps of S = K q^T
-  static constexpr int MTILES = D / 16;                    // 16-row tiles of O^T = V^T P^T
-  static constexpr int kRingBytes = NSLOT * 2 * kTileBytes;
-  static constexpr int kBarBytes = (2 * NSLOT * 8 + 15) / 16 * 16;
-  static constexpr int kMergeMLFloats = (2 * NW * G + 3) / 4 * 4;
-  static constexpr int kMergeBytes = (kMergeMLFloats + NW * G * D) * 4;
-  // + 1 KiB so the ring can start on a 1024-byte boundary (128B swizzle),
-  // + 16 bytes for the fused combine's "last piece" flag
-  static constexpr int kSmemBytes = 1024 + kRingBytes + kBarBytes + kMergeBytes + 16;
-  static_assert(G >= 1 && G <= 8, "the query heads of a group are the MMA's N = 8 columns");
-  static_assert(kSmemBytes <= 232448 / 2 - 1024, "two CTAs per SM");
-  static_assert(NSLOT % NW == 0, "each ring slot must have exactly one owner warp");
-};
-
-// One ring slot (a block's 16 keys) for one consumer warp, on the tensor
-// cores at warp level: S^T[16 keys x 8] = K[16 x D] q^T[D x 8] (the G query
-// heads are the N columns, the rest zero), online softmax on the fragments
-// with shuffles, then O^T[D x 8] += V^T[D x 16] P^T[16 x 8].  K and V come
-// from 128B-swizzled boxes, so every ldmatrix is bank-conflict free.
-// Fragment roles (g = lane / 4, t = lane % 4): S^T holds keys g and g+8 of
-// heads 2t and 2t+1; O^T tile mt holds rows mt*16 + g (+8) of heads 2t, 2t+1.
-template <int D, int G, int NW, int NSLOT>
-__device__ __forceinline__ void decode_slot(
-    const bool edge, uint32_t k_addr, uint8_t* v_ptr, const uint32_t (&bq)[D / 16][2],
-    float (&o)[D / 16][4], float (&m)[2], float (&l)[2], int lane, int tok0, int t_lo, int pos,
-    float qscale, float softcap, float inv_cap, float* logits, int logit_stride) {
-  using S = DecodeShape<D, G, NW, NSLOT>;
-  const int g = lane >> 2, t = lane & 3;
-
-  // ---- S^T = K q^T (even and odd k-steps in two accumulators: two
-  // dependent MMA chains of half the length)
-  float s[4] = {0.f, 0.f, 0.f, 0.f};
-  float s2[4] = {0.f, 0.f, 0.f, 0.f};
-  {
-    const int row = (lane & 7) + ((lane >> 3) & 1) * 8;
-    const int hi = lane >> 4;
-    const uint32_t rbase = k_addr + row * 128;
-#pragma unroll
-    for (int kk = 0; kk < S::KSTEPS; ++kk) {
-      uint32_t a[4];
-      const int j = (kk & 3) * 2 + hi;
-      ldmatrix_x4(a, rbase + (kk >> 2) * S::kBoxBytes + ((j ^ (row & 7)) << 4));
-      if (kk & 1)
-        mma_bf16_16816(s2, a, bq[kk][0], bq[kk][1]);
-      else
-        mma_bf16_16816(s, a, bq[kk][0], bq[kk][1]);
-    }
-#pragma unroll
-    for (int i = 0; i < 4; ++i) s[i] += s2[i];
-  }
-  // ---- logits (log2 domain), mask, online softmax on the fragment
-  const bool head_ok0 = (2 * t) < G, head_ok1 = (2 * t + 1) < G;
-  bool key_ok_lo = true, key_ok_hi = true;
-  if (edge) {
-    key_ok_lo = (tok0 + g >= t_lo) && (tok0 + g <= pos);
-    key_ok_hi = (tok0 + g + 8 >= t_lo) && (tok0 + g + 8 <= pos);
-  }
-  float x[4];
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    float v = s[i];
-    if (softcap > 0.f) {
-      // tanh(y) = 1 - 2 / (e^{2y} + 1); absolute error ~1e-7
-      const float e = fast_exp2(fminf(2.f * kLog2e * (v * qscale * inv_cap), 126.f));
-      v = softcap * (1.f - __fdividef(2.f, e + 1.f)) * kLog2e;
-    }
-    else v *= qscale;
-    const bool ok = ((i & 1) ? head_ok1 : head_ok0) && ((i & 2) ? key_ok_hi : key_ok_lo);
-    x[i] = ok ? v : -INFINITY;
-    // optional: the visible keys' log2-domain logits of the G heads
-    // (logits points at head kvh * G, key 0 of the request)
-    if (logits != nullptr && ok)
-      logits[(2 * t + (i & 1)) * logit_stride + tok0 + g + ((i & 2) ? 8 : 0)] = v;
-  }
-  float alpha[2], ms[2];
-#pragma unroll
-  for (int j = 0; j < 2; ++j) {
-    float mx = fmaxf(x[j], x[j + 2]);
-#pragma unroll
-    for (int off = 4; off < 32; off <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-    const float mn = fmaxf(m[j], mx);
-    ms[j] = (mn == -INFINITY) ? 0.f : mn;
-    alpha[j] = fast_exp2(m[j] - ms[j]);
-    m[j] = mn;
-  }
-  float p[4];
-#pragma unroll
-  for (int i = 0; i < 4; ++i) p[i] = fast_exp2(x[i] - ms[i & 1]);
-  l[0] = l[0] * alpha[0] + p[0] + p[2];
-  l[1] = l[1] * alpha[1] + p[1] + p[3];
-  if (__any_sync(0xffffffffu, alpha[0] != 1.f || alpha[1] != 1.f)) {
-#pragma unroll
-    for (int mt = 0; mt < S::MTILES; ++mt) {
-      o[mt][0] *= alpha[0];
-      o[mt][1] *= alpha[1];
-      o[mt][2] *= alpha[0];
-      o[mt][3] *= alpha[1];
-    }
-  }
-  // ---- P^T as the B fragment: this thread needs keys 2t, 2t+1 (+8) of head g
-  const uint32_t wlo = pack_bf16x2(p[0], p[1]);  // key g,   heads 2t, 2t+1
-  const uint32_t whi = pack_bf16x2(p[2], p[3]);  // key g+8, heads 2t, 2t+1
-  const int src0 = 8 * t + (g >> 1), src1 = src0 + 4;
-  const uint32_t a0 = __shfl_sync(0xffffffffu, wlo, src0);
-  const uint32_t a1 = __shfl_sync(0xffffffffu, wlo, src1);
-  const uint32_t c0 = __shfl_sync(0xffffffffu, whi, src0);
-  const uint32_t c1 = __shfl_sync(0xffffffffu, whi, src1);
-  const uint32_t sel = (g & 1) ? 0x7632u : 0x5410u;
-  const uint32_t pb0 = prmt(a0, a1, sel);
-  const uint32_t pb1 = prmt(c0, c1, sel);
-  // ---- stale slots past the sequence end may hold NaN: zero those V rows
-  if (edge && tok0 + kBlockSize - 1 > pos) {
-    const int z0 = max(0, pos - tok0 + 1);
-    const int nz = (kBlockSize - z0) * S::DC * 8;
-    for (int idx = lane; idx < nz; idx += 32) {
-      const int r = z0 + idx / (S::DC * 8);
-      const int c = (idx / 8) % S::DC;
-      const int q = idx % 8;
-      *reinterpret_cast<uint4*>(v_ptr + c * S::kBoxBytes + r * 128 + q * 16) =
-          make_uint4(0u, 0u, 0u, 0u);
-    }
-    // the slot is refilled by TMA later: order these writes before it
-    fence_proxy_async_smem();
-    __syncwarp();
-  }
-  // ---- O^T += V^T P^T
-  {
-    const int mi = lane >> 3, rr = lane & 7;
-    const int key = rr + 8 * (mi >> 1);
-    const uint32_t vbase = smem_u32(v_ptr) + key * 128;
-#pragma unroll
-    for (int mt = 0; mt < S::MTILES; ++mt) {
-      const int dch = mt * 2 + (mi & 1);  // 16-byte chunk along D
-      uint32_t a[4];
-      ldmatrix_x4_trans(a, vbase + (dch >> 3) * S::kBoxBytes + (((dch & 7) ^ (key & 7)) << 4));
-      mma_bf16_16816(o[mt], a, pb0, pb1);
-    }
-  }
-}
 
 template <int D, int G, int NW, int NSLOT>
 __global__ void __launch_bounds__((NW + 1) * 32, 2)
     paged_decode_kernel(const __grid_constant__ DecodeArgs a,
                         const __grid_constant__ CUtensorMap tm_k,
                         const __grid_constant__ CUtensorMap tm_v) {
-  using S = DecodeShape<D, G, NW, NSLOT>;
-
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                             ~static_cast<uintptr_t>(1023));
-  uint8_t* ring = smem;
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + S::kRingBytes);
-  uint64_t* empty = full + NSLOT;
-  float* merge = reinterpret_cast<float*>(smem + S::kRingBytes + S::kBarBytes);
-  float* mrg_m = merge;                        // [NW][G]
-  float* mrg_l = merge + NW * G;               // [NW][G]
-  float* mrg_acc = merge + S::kMergeMLFloats;  // [NW][G][D]
-  volatile int* last_flag =
-      reinterpret_cast<volatile int*>(smem + S::kRingBytes + S::kBarBytes + S::kMergeBytes);
-
-  const int warp = threadIdx.x / 32;
-  const int lane = threadIdx.x % 32;
-
-  if (threadIdx.x == 0) {
-    for (int i = 0; i < NSLOT; ++i) {
-      mbar_init(&full[i], 1);
-      mbar_init(&empty[i], 1);
-    }
-    mbar_fence_init();
-  }
-  __syncthreads();
-
-  PieceIter iter;
-  iter.init(a, lane);
-  Piece pc;
-
-  if (warp == NW) {
-    // ============================ producer warp ============================
-    if (lane == 0) {
-      prefetch_tensormap(&tm_k);
-      prefetch_tensormap(&tm_v);
-    }
-    const uint32_t oob_row = static_cast<uint32_t>(a.num_blocks) * a.Hkv * kBlockSize;
-    long long issued = 0;
-    bool ok = true;
-    while (ok && iter.next(pc)) {
-      const int32_t* trow = a.tables + static_cast<size_t>(pc.b) * a.max_blocks + pc.j0;
-      for (int base = 0; base < pc.ntiles && ok; base += 32) {
-        uint32_t row = oob_row;  // a bad id reads zeros (reported) instead of faulting
-        if (base + lane < pc.ntiles) {
-          const int id = trow[base + lane];
-          if (static_cast<unsigned>(id) < static_cast<unsigned>(a.num_blocks))
-            row = (static_cast<uint32_t>(id) * a.Hkv + pc.kvh) * kBlockSize;
-          else
-            report(a.err, PKA_DEVERR_BAD_TABLE);
-        }
-        const int cnt = min(32, pc.ntiles - base);
-        for (int k = 0; k < cnt; ++k) {
-          const uint32_t r0 = __shfl_sync(0xffffffffu, row, k);
-          const int slot = static_cast<int>(issued % NSLOT);
-          const long long round = issued / NSLOT;
-          int good = 1;
-          if (lane == 0) {
-            if (round > 0)
-              good = mbar_wait(&empty[slot], static_cast<uint32_t>((round - 1) & 1), a.err);
-            if (good) mbar_arrive_expect_tx(&full[slot], 2 * S::kTileBytes);
-          }
-          good = __shfl_sync(0xffffffffu, good, 0);
-          if (!good) {
-            ok = false;
-            break;
-          }
-          // one copy per tensor (the whole 16 x D block as DC boxes of 16 rows
-          // x 64 columns), K from lane 0 and V from lane 1: one thread's
-          // copies are processed one after another
-          if (lane < 2) {
-            uint8_t* dst =
-                ring + static_cast<size_t>(slot) * 2 * S::kTileBytes + lane * S::kTileBytes;
-            tma_load_3d(dst, lane == 0 ? &tm_k : &tm_v, 0, static_cast<int>(r0), 0, &full[slot]);
-          }
-          ++issued;
-        }
-      }
-    }
-    // Every issued copy must have landed before the CTA may exit.
-    if (lane == 0) {
-      const long long first = issued > NSLOT ? issued - NSLOT : 0;
-      for (long long i = first; i < issued; ++i)
-        mbar_wait(&full[i % NSLOT], static_cast<uint32_t>((i / NSLOT) & 1), a.err);
-    }
-    return;
-  }
-
-  // ============================ consumer warps ============================
-  const int g = lane >> 2, t = lane & 3;
-  const float inv_cap = a.softcap > 0.f ? 1.f / a.softcap : 0.f;
-  const float qscale = a.scale * (a.softcap > 0.f ? 1.f : kLog2e);
-  long long tile_base = 0;
-  bool ok = true;
-
-  // q^T as B fragments: head g (zero for g >= G), elements 2t, 2t+1 (+8) of
-  // every k-step.  The next piece's fragments are loaded during the merge.
-  auto load_q = [&](const Piece& P, uint32_t (&bq)[D / 16][2]) {
-    const uint32_t* qp = reinterpret_cast<const uint32_t*>(
-        a.q + (static_cast<size_t>(P.qrow) * a.Hq + P.kvh * G + (g < G ? g : 0)) * D);
-#pragma unroll
-    for (int kk = 0; kk < D / 16; ++kk) {
-      bq[kk][0] = (g < G) ? qp[kk * 8 + t] : 0u;
-      bq[kk][1] = (g < G) ? qp[kk * 8 + 4 + t] : 0u;
-    }
-  };
-
-  uint32_t bq[D / 16][2];
-  bool have = iter.next(pc);
-  if (have) load_q(pc, bq);
-  while (have) {
-    float o[D / 16][4];
-#pragma unroll
-    for (int mt = 0; mt < D / 16; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
-    float m[2] = {-INFINITY, -INFINITY};
-    float l[2] = {0.f, 0.f};
-
-    // Tile T of the CTA's stream lives in slot T % NSLOT and belongs to warp
-    // T % NW; NSLOT is a multiple of NW, so every slot has one owner warp that
-    // consumes its phases in order (a phase-parity wait can never alias an
-    // older phase of the same slot).
-    const int i0 = static_cast<int>((warp - tile_base % NW + NW) % NW);
-    float* lg = (a.logits == nullptr)
-                    ? nullptr
-                    : a.logits + (static_cast<size_t>(pc.b) * a.Hq + pc.kvh * G) *
-                                     (static_cast<size_t>(a.max_blocks) * kBlockSize);
-    for (int i = i0; i < pc.ntiles && ok; i += NW) {
-      const long long T = tile_base + i;
-      const int slot = static_cast<int>(T % NSLOT);
-      const bool got = mbar_wait(&full[slot], static_cast<uint32_t>((T / NSLOT) & 1), a.err);
-      if (!__all_sync(0xffffffffu, got)) {
-        ok = false;
-        break;
-      }
-      uint8_t* kp = ring + static_cast<size_t>(slot) * 2 * S::kTileBytes;
-      const int tok0 = (pc.j0 + i) * kBlockSize;
-      const bool edge = (tok0 < pc.t_lo || tok0 + kBlockSize - 1 > pc.pos);
-      decode_slot<D, G, NW, NSLOT>(edge, smem_u32(kp), kp + S::kTileBytes, bq, o, m, l, lane,
-                                   tok0, pc.t_lo, pc.pos, qscale, a.softcap, inv_cap, lg,
-                                   a.max_blocks * kBlockSize);
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&empty[slot]);
-    }
-    tile_base += pc.ntiles;
-
-    Piece nx;
-    const bool have_next = iter.next(nx);
-    if (have_next) load_q(nx, bq);
-
-    const bool split = a.split_blocks > 0;
-    if (pc.ntiles > 0) {
-      // ---- per-warp totals: sums over the 8 key rows held by lanes g
-#pragma unroll
-      for (int j = 0; j < 2; ++j)
-#pragma unroll
-        for (int off = 4; off < 32; off <<= 1) l[j] += __shfl_xor_sync(0xffffffffu, l[j], off);
-      if (g == 0) {
-#pragma unroll
-        for (int j = 0; j < 2; ++j) {
-          const int h = 2 * t + j;
-          if (h < G) {
-            mrg_m[warp * G + h] = m[j];
-            mrg_l[warp * G + h] = l[j];
-          }
-        }
-      }
-#pragma unroll
-      for (int mt = 0; mt < D / 16; ++mt)
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const int h = 2 * t + (i & 1);
-          const int d = mt * 16 + g + ((i & 2) ? 8 : 0);
-          if (h < G) mrg_acc[(warp * G + h) * D + d] = o[mt][i];
-        }
-      consumer_sync(NW * 32);
-
-      // ---- merge the warps' states and write this piece's result, four
-      // consecutive columns of one head per thread (vector loads and stores,
-      // the heads' scale factors taken once per four columns)
-      for (int idx = threadIdx.x; idx < G * (D / 4); idx += NW * 32) {
-        const int h = idx / (D / 4);
-        const int d = (idx % (D / 4)) * 4;
-        float M = -INFINITY;
-#pragma unroll
-        for (int w = 0; w < NW; ++w) M = fmaxf(M, mrg_m[w * G + h]);
-        const float Ms = (M == -INFINITY) ? 0.f : M;
-        float den = 0.f;
-        float4 num = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-        for (int w = 0; w < NW; ++w) {
-          const float sc = fast_exp2(mrg_m[w * G + h] - Ms);
-          den = fmaf(sc, mrg_l[w * G + h], den);
-          const float4 v = *reinterpret_cast<const float4*>(&mrg_acc[(w * G + h) * D + d]);
-          num.x = fmaf(sc, v.x, num.x);
-          num.y = fmaf(sc, v.y, num.y);
-          num.z = fmaf(sc, v.z, num.z);
-          num.w = fmaf(sc, v.w, num.w);
-        }
-        const float inv = (den > 0.f) ? 1.f / den : 0.f;
-        const float4 ov = make_float4(num.x * inv, num.y * inv, num.z * inv, num.w * inv);
-        const int hq = pc.kvh * G + h;
-        if (split) {
-          if (pc.slot < a.num_splits) {
-            const size_t ph = (static_cast<size_t>(pc.b) * a.Hq + hq) * a.num_splits + pc.slot;
-            *reinterpret_cast<float4*>(a.partial_o + ph * D + d) = ov;
-            if (d == 0) a.partial_lse[ph] = (den > 0.f) ? (M + log2f(den)) * kLn2 : -INFINITY;
-          }
-        } else {
-          uint16_t* dst =
-              reinterpret_cast<uint16_t*>(a.out) + (static_cast<size_t>(pc.qrow) * a.Hq + hq) * D + d;
-          *reinterpret_cast<uint2*>(dst) =
-              make_uint2(pack_bf16x2(ov.x, ov.y), pack_bf16x2(ov.z, ov.w));
-        }
-      }
-      consumer_sync(NW * 32);
-    } else if (!split) {
-      // a request with no visible key: output 0
-      for (int idx = threadIdx.x; idx < G * D; idx += NW * 32) {
-        const int hq = pc.kvh * G + idx / D;
-        reinterpret_cast<uint16_t*>(a.out)[(static_cast<size_t>(pc.qrow) * a.Hq + hq) * D +
-                                           idx % D] = 0;
-      }
-    }
-    const bool fused = split && a.seg_counters != nullptr;
-    // ---- split-K: slots of this segment no CTA fills get LSE = -inf
-    if (split && !fused && pc.fill_from >= 0) {
-      if (pc.fill_from > a.num_splits && threadIdx.x == 0) report(a.err, PKA_DEVERR_SEQ_LEN);
-      const int nfill = a.num_splits - min(pc.fill_from, a.num_splits);
-      for (int idx = threadIdx.x; idx < G * nfill; idx += NW * 32) {
-        const int hq = pc.kvh * G + idx / nfill;
-        const int sl = pc.fill_from + idx % nfill;
-        a.partial_lse[(static_cast<size_t>(pc.b) * a.Hq + hq) * a.num_splits + sl] = -INFINITY;
-      }
-    }
-    // ---- fused LSE combine: the CTA that writes a segment's last piece
-    // merges all of its pieces (the other CTAs' partials are read from L2)
-    // and resets the segment's arrival counter for the next call.
-    if (fused) {
-      if (pc.npieces > a.num_splits && threadIdx.x == 0) report(a.err, PKA_DEVERR_SEQ_LEN);
-      const int np = min(pc.npieces, a.num_splits);
-      bool last = false;
-      if (pc.ntiles > 0 && pc.slot < a.num_splits) {
-        if (threadIdx.x == 0) {
-          fence_acq_rel_gpu();  // the CTA's partials (ordered by the barrier) before its arrival
-          const int old = atomicAdd(&a.seg_counters[pc.b * a.Hkv + pc.kvh], 1);
-          *last_flag = (old == np - 1) ? 1 : 0;
-        }
-        consumer_sync(NW * 32);
-        last = *last_flag != 0;
-      }
-      if (last) {
-        fence_acq_rel_gpu();  // every other piece's partials are visible now
-        // One pass over the pieces (read from L2): four consecutive columns
-        // of one head per item, the pieces' LSE and partial rows of four
-        // pieces loaded together, merged with a running maximum.  The item
-        // loop is unrolled so that the loads of all of a thread's items are
-        // in flight together.
-        constexpr int kItems = G * (D / 4);
-        constexpr int kPerThread = (kItems + NW * 32 - 1) / (NW * 32);
-#pragma unroll
-        for (int k = 0; k < kPerThread; ++k) {
-          const int item = threadIdx.x + k * NW * 32;
-          if (item < kItems) {
-            const int h = item / (D / 4);
-            const int d0 = (item % (D / 4)) * 4;
-            const size_t ph0 =
-                (static_cast<size_t>(pc.b) * a.Hq + pc.kvh * G + h) * a.num_splits;
-            float M = -INFINITY, den = 0.f;
-            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-            for (int s0 = 0; s0 < np; s0 += 4) {
-              float lv[4];
-              float4 x[4];
-#pragma unroll
-              for (int u = 0; u < 4; ++u) {
-                if (s0 + u < np) {
-                  lv[u] = __ldcg(a.partial_lse + ph0 + s0 + u);
-                  x[u] = __ldcg(reinterpret_cast<const float4*>(a.partial_o +
-                                                                (ph0 + s0 + u) * D + d0));
-                } else {
-                  lv[u] = -INFINITY;
-                  x[u] = make_float4(0.f, 0.f, 0.f, 0.f);
-                }
-              }
-              lse_merge4(M, den, acc, lv, x);
-            }
-            const float inv = den > 0.f ? 1.f / den : 0.f;
-            uint16_t* dst = reinterpret_cast<uint16_t*>(a.out) +
-                            (static_cast<size_t>(pc.qrow) * a.Hq + pc.kvh * G + h) * D + d0;
-            *reinterpret_cast<uint2*>(dst) = make_uint2(pack_bf16x2(acc.x * inv, acc.y * inv),
-                                                        pack_bf16x2(acc.z * inv, acc.w * inv));
-          }
-        }
-        if (threadIdx.x == 0) a.seg_counters[pc.b * a.Hkv + pc.kvh] = 0;
-        consumer_sync(NW * 32);
-      } else if (pc.ntiles == 0 && pc.fill_from == 0) {
-        // a request with no visible key: output 0
-        for (int idx = threadIdx.x; idx < G * D; idx += NW * 32) {
-          const int hq = pc.kvh * G + idx / D;
-          reinterpret_cast<uint16_t*>(a.out)[(static_cast<size_t>(pc.qrow) * a.Hq + hq) * D +
-                                             idx % D] = 0;
-        }
-      }
-    }
-    pc = nx;
-    have = have_next;
-  }
+  const DecodeCtx cx{static_cast<int>(blockIdx.x), static_cast<int>(gridDim.x),
+                     static_cast<int>(threadIdx.x), 0, 1};
+  decode_body<D, G, NW, NSLOT>(a, &tm_k, &tm_v, smem_raw, cx);
 }
 
 // ------------------------------------------------------------- launchers
@@ -769,39 +37,6 @@ struct DecodeTuning {
   static constexpr int NSLOT = NW * SPW;
 };
 
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  if (fn == nullptr) {
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
-                                         &q) != cudaSuccess ||
-        q != cudaDriverEntryPointSuccess)
-      return nullptr;
-    fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-  }
-  return fn;
-}
-
-// A pool viewed as a 3-D tensor (64 columns, num_blocks * Hkv * 16 rows,
-// D / 64 column chunks) with strides (2, 2 D, 128) bytes, read in boxes of
-// (64, 16, D / 64) with the 128-byte swizzle: one copy brings a block's
-// 16 x D tile as D / 64 consecutive 16-row x 64-column boxes, the layout the
-// consumers' ldmatrix addressing expects.  Fewer, larger copies keep the
-// TMA unit's per-copy cost off the critical path.
-bool pool_map(CUtensorMap* m, const void* base, int D, long long rows) {
-  auto fn = encode_fn();
-  if (fn == nullptr) return false;
-  const cuuint64_t dims[3] = {64, static_cast<cuuint64_t>(rows), static_cast<cuuint64_t>(D / 64)};
-  const cuuint64_t str[2] = {static_cast<cuuint64_t>(D) * 2, 128};
-  const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(kBlockSize),
-                             static_cast<cuuint32_t>(D / 64)};
-  const cuuint32_t estr[3] = {1, 1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, str, box, estr,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 template <int D, int G>
 cudaError_t launch_decode_t(const DecodeArgs& a, int grid, cudaStream_t stream) {
   constexpr int NW = DecodeTuning<D, G>::NW;
@@ -809,7 +44,8 @@ cudaError_t launch_decode_t(const DecodeArgs& a, int grid, cudaStream_t stream) 
   using S = DecodeShape<D, G, NW, NSLOT>;
   CUtensorMap tk, tv;
   const long long rows = static_cast<long long>(a.num_blocks) * a.Hkv * kBlockSize;
-  if (!pool_map(&tk, a.k, D, rows) || !pool_map(&tv, a.v, D, rows)) return cudaErrorInvalidValue;
+  if (!tmap_pool_tiles(&tk, a.k, D, rows) || !tmap_pool_tiles(&tv, a.v, D, rows))
+    return cudaErrorInvalidValue;
   auto kern = paged_decode_kernel<D, G, NW, NSLOT>;
   cudaError_t e = set_smem_once(reinterpret_cast<const void*>(kern), S::kSmemBytes);
   if (e != cudaSuccess) return e;

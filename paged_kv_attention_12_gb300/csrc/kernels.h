@@ -25,6 +25,8 @@ struct DecodeArgs {
   float* logits;                   // optional fp32 [B][Hq][max_blocks*bs]: log2-domain logits
   float scale, softcap;
   int32_t window;
+  int32_t decode_rows_only;        // nonzero: requests whose query_start_loc span is not
+                                   // one token are skipped (no output written for them)
 };
 
 cudaError_t launch_key_mass(const float* logits, const float* lse, const int32_t* seq_lens,
@@ -66,10 +68,20 @@ struct PrefillArgs {
   int32_t batch, Hq, Hkv, num_blocks, max_blocks, total_q, max_query_len, max_seq_len;
   float scale, softcap;
   int32_t window;
+  int32_t skip_decode_rows;        // nonzero: requests with one query token are left out
 };
 
 cudaError_t launch_prefill(const PrefillArgs& a, int head_dim, int group, int sm_count,
                            cudaStream_t stream);
+
+// Mixed batch in one launch: the prefill items of `pa` (skip_decode_rows set)
+// on prefill CTAs, the decode rows of `da` (decode_rows_only set, split-K
+// with the fused combine) on `decode_ctas` CTAs of two decode pipelines each.
+cudaError_t launch_mixed(const PrefillArgs& pa, const DecodeArgs& da, int head_dim, int group,
+                         int decode_ctas, cudaStream_t stream);
+
+// Query tokens per 128-row prefill tile (0: unsupported shape).
+int mixed_query_tile(int head_dim, int group);
 
 // Append of new tokens' K/V rows into a pool.
 struct AppendArgs {

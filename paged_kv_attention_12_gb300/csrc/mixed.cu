@@ -1,0 +1,129 @@
+// Mixed batch -- decode rows and chunked-prefill chunks -- in one launch
+// (sm_103a).  Decode tokens and prefill chunks of the same engine tick go
+// through one attention call ("mixed-batch chunked prefill", architecture
+// page, "Phase status"), and the two kinds of rows want different machines:
+// a prefill chunk is a dense contraction for the tcgen05 pipeline, while a
+// decode row (one token, G query heads) would fill 4 of the 128 rows of a
+// tensor-core tile and is bound by streaming its keys.
+//
+// So the launch has two kinds of CTAs, 256 threads each:
+//  * CTAs [0, n_decode): two decode pipelines each (decode_body.cuh: a
+//    producer warp and three consumer warps over half the shared memory),
+//    which split the decode rows' keys in the balanced split-K partition and
+//    merge the pieces in the launch (fused LSE combine: the last piece of a
+//    segment to finish merges it, counted in the workspace);
+//  * the CTAs after them: the tcgen05 prefill pipeline (prefill_body.cuh),
+//    one (request, KV head, query tile) item each, heaviest first; requests
+//    with one query token are left out.
+// The hardware starts CTAs in index order: the decode pipelines start at
+// once on n_decode SMs and the prefill items take the others.  The host
+// sizes n_decode from the number of prefill tokens.
+#include "decode_body.cuh"
+#include "prefill_body.cuh"
+#include "tmaps.cuh"
+
+namespace pka {
+
+namespace {
+
+// Decode pipelines of the mixed launch: two per CTA of the prefill's 256
+// threads, each a producer warp and three consumer warps, each ring in half
+// of the prefill's shared memory.
+template <int D, int G>
+struct MixedDecodeTuning {
+  static constexpr int NW = 3;
+  static constexpr int NSLOT = (D == 256) ? ((G == 8) ? 3 : 6) : 12;
+  static constexpr int kPipeThreads = (NW + 1) * 32;
+  static constexpr int kPipeBytes = DecodeShape<D, G, NW, NSLOT>::kSmemBytes;
+  static_assert(2 * kPipeThreads == PrefillShape<D, G>::kThreads, "two pipelines per CTA");
+  static constexpr int kSmemBytes = (2 * kPipeBytes > PrefillShape<D, G>::kSmemBytes)
+                                        ? 2 * kPipeBytes
+                                        : PrefillShape<D, G>::kSmemBytes;
+};
+
+}  // namespace
+
+template <int D, int G>
+__global__ void __launch_bounds__(PrefillShape<D, G>::kThreads, 1)
+    paged_mixed_kernel(const __grid_constant__ PrefillArgs pa,
+                       const __grid_constant__ DecodeArgs da, const int n_decode,
+                       const __grid_constant__ CUtensorMap tm_q,
+                       const __grid_constant__ CUtensorMap tm_k_rows,
+                       const __grid_constant__ CUtensorMap tm_k_tiles,
+                       const __grid_constant__ CUtensorMap tm_v_tiles) {
+  extern __shared__ uint8_t smem_raw[];
+  if (static_cast<int>(blockIdx.x) >= n_decode) {
+    prefill_body<D, G>(pa, &tm_q, &tm_k_rows, &tm_v_tiles, smem_raw,
+                       static_cast<int>(blockIdx.x) - n_decode);
+    return;
+  }
+  using T = MixedDecodeTuning<D, G>;
+  const int pipe = static_cast<int>(threadIdx.x) / T::kPipeThreads;  // 0 or 1
+  // named barriers 1, 2 (pipeline 0) and 3, 4 (pipeline 1)
+  const DecodeCtx cx{static_cast<int>(blockIdx.x) * 2 + pipe, n_decode * 2,
+                     static_cast<int>(threadIdx.x) % T::kPipeThreads, 1 + 2 * pipe, 2 + 2 * pipe};
+  decode_body<D, G, T::NW, T::NSLOT>(da, &tm_k_tiles, &tm_v_tiles,
+                                     smem_raw + pipe * T::kPipeBytes, cx);
+}
+
+namespace {
+
+template <int D, int G>
+cudaError_t launch_mixed_t(const PrefillArgs& pa, const DecodeArgs& da, int decode_ctas,
+                           cudaStream_t stream) {
+  using S = PrefillShape<D, G>;
+  using T = MixedDecodeTuning<D, G>;
+  CUtensorMap tq, tkr, tkt, tvt;
+  const long long rows = static_cast<long long>(pa.num_blocks) * pa.Hkv * kBlockSize;
+  if (!tmap_query_tiles(&tq, pa.q, D, pa.Hq, pa.total_q, G, S::TQ) ||
+      !tmap_pool_rows(&tkr, pa.k, D, rows) || !tmap_pool_tiles(&tkt, pa.k, D, rows) ||
+      !tmap_pool_tiles(&tvt, pa.v, D, rows))
+    return cudaErrorInvalidValue;
+  auto kern = paged_mixed_kernel<D, G>;
+  cudaError_t e = set_smem_once(reinterpret_cast<const void*>(kern), T::kSmemBytes);
+  if (e != cudaSuccess) return e;
+  const long long ctas = static_cast<long long>(decode_ctas) + prefill_ranks(pa, S::TQ);
+  if (ctas > 0x7fffffffLL || decode_ctas <= 0) return cudaErrorInvalidValue;
+  kern<<<static_cast<unsigned>(ctas), S::kThreads, T::kSmemBytes, stream>>>(
+      pa, da, decode_ctas, tq, tkr, tkt, tvt);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+int mixed_query_tile(int head_dim, int group) {
+  if (head_dim == 128) {
+    switch (group) {
+      case 1: return PrefillShape<128, 1>::TQ;
+      case 2: return PrefillShape<128, 2>::TQ;
+      case 4: return PrefillShape<128, 4>::TQ;
+      case 8: return PrefillShape<128, 8>::TQ;
+    }
+  } else if (head_dim == 256) {
+    switch (group) {
+      case 1: return PrefillShape<256, 1>::TQ;
+      case 2: return PrefillShape<256, 2>::TQ;
+      case 4: return PrefillShape<256, 4>::TQ;
+      case 8: return PrefillShape<256, 8>::TQ;
+    }
+  }
+  return 0;
+}
+
+cudaError_t launch_mixed(const PrefillArgs& pa, const DecodeArgs& da, int head_dim, int group,
+                         int decode_ctas, cudaStream_t stream) {
+#define PKA_MIX(D_, G_) \
+  if (head_dim == D_ && group == G_) return launch_mixed_t<D_, G_>(pa, da, decode_ctas, stream);
+  PKA_MIX(128, 1)
+  PKA_MIX(128, 2)
+  PKA_MIX(128, 4)
+  PKA_MIX(128, 8)
+  PKA_MIX(256, 1)
+  PKA_MIX(256, 2)
+  PKA_MIX(256, 4)
+  PKA_MIX(256, 8)
+#undef PKA_MIX
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace pka

@@ -309,17 +309,13 @@ int paged_decode_splitk_combine(const float* partial_o, const float* partial_lse
   return e == cudaSuccess ? PKA_OK : PKA_ERR_CUDA;
 }
 
-int paged_prefill_attn(const void* q, void* out, const pka_kv_pool* kv,
-                       const int32_t* block_tables, int32_t max_blocks,
-                       const int32_t* query_start_loc, const int32_t* seq_lens, int32_t B,
-                       int32_t Hq, int32_t total_q, int32_t max_query_len, int32_t max_seq_len,
-                       const pka_attn_params* params, void* stream) {
-  if (out == nullptr || query_start_loc == nullptr) return PKA_ERR_NULL;
-  int st = check_common(q, kv, block_tables, max_blocks, seq_lens, B, Hq, max_seq_len, params);
-  if (st != PKA_OK) return st;
-  if (total_q < 0 || max_query_len < 0 || max_query_len > max_seq_len) return PKA_ERR_SHAPE;
-  if (!aligned16(out)) return PKA_ERR_ALIGN;
-  if (B == 0 || total_q == 0) return PKA_OK;
+namespace {
+
+pka::PrefillArgs prefill_args(const void* q, void* out, const pka_kv_pool* kv,
+                              const int32_t* block_tables, int32_t max_blocks,
+                              const int32_t* query_start_loc, const int32_t* seq_lens, int32_t B,
+                              int32_t Hq, int32_t total_q, int32_t max_query_len,
+                              int32_t max_seq_len, const pka_attn_params* params) {
   pka::PrefillArgs a{};
   a.q = static_cast<const uint16_t*>(q);
   a.out = static_cast<uint16_t*>(out);
@@ -340,10 +336,91 @@ int paged_prefill_attn(const void* q, void* out, const pka_kv_pool* kv,
   a.scale = params->scale;
   a.softcap = params->softcap;
   a.window = params->window;
+  return a;
+}
+
+int check_prefill(const void* q, void* out, const pka_kv_pool* kv, const int32_t* block_tables,
+                  int32_t max_blocks, const int32_t* query_start_loc, const int32_t* seq_lens,
+                  int32_t B, int32_t Hq, int32_t total_q, int32_t max_query_len,
+                  int32_t max_seq_len, const pka_attn_params* params) {
+  if (out == nullptr || query_start_loc == nullptr) return PKA_ERR_NULL;
+  int st = check_common(q, kv, block_tables, max_blocks, seq_lens, B, Hq, max_seq_len, params);
+  if (st != PKA_OK) return st;
+  if (total_q < 0 || max_query_len < 0 || max_query_len > max_seq_len) return PKA_ERR_SHAPE;
+  if (!aligned16(out)) return PKA_ERR_ALIGN;
+  return PKA_OK;
+}
+
+}  // namespace
+
+int paged_prefill_attn(const void* q, void* out, const pka_kv_pool* kv,
+                       const int32_t* block_tables, int32_t max_blocks,
+                       const int32_t* query_start_loc, const int32_t* seq_lens, int32_t B,
+                       int32_t Hq, int32_t total_q, int32_t max_query_len, int32_t max_seq_len,
+                       const pka_attn_params* params, void* stream) {
+  int st = check_prefill(q, out, kv, block_tables, max_blocks, query_start_loc, seq_lens, B, Hq,
+                         total_q, max_query_len, max_seq_len, params);
+  if (st != PKA_OK) return st;
+  if (B == 0 || total_q == 0) return PKA_OK;
+  const pka::PrefillArgs a = prefill_args(q, out, kv, block_tables, max_blocks, query_start_loc,
+                                          seq_lens, B, Hq, total_q, max_query_len, max_seq_len,
+                                          params);
   const int sms = pka::device_sm_count();
   if (sms <= 0) return PKA_ERR_CUDA;
   cudaError_t e = pka::launch_prefill(a, kv->head_dim, Hq / kv->num_kv_heads, sms,
                                       static_cast<cudaStream_t>(stream));
+  if (e == cudaErrorNotSupported) return PKA_ERR_UNSUPPORTED;
+  return e == cudaSuccess ? PKA_OK : PKA_ERR_CUDA;
+}
+
+size_t paged_prefill_attn_ws_bytes(int32_t B, int32_t Hq, int32_t Hkv, int32_t D,
+                                   int32_t max_seq_len, int32_t window) {
+  return paged_decode_attn_ws_bytes(B, Hq, Hkv, D, max_seq_len, window);
+}
+
+int paged_prefill_attn_ws(const void* q, void* out, const pka_kv_pool* kv,
+                          const int32_t* block_tables, int32_t max_blocks,
+                          const int32_t* query_start_loc, const int32_t* seq_lens, int32_t B,
+                          int32_t Hq, int32_t total_q, int32_t max_query_len,
+                          int32_t max_seq_len, const pka_attn_params* params, void* workspace,
+                          size_t workspace_bytes, void* stream) {
+  int st = check_prefill(q, out, kv, block_tables, max_blocks, query_start_loc, seq_lens, B, Hq,
+                         total_q, max_query_len, max_seq_len, params);
+  if (st != PKA_OK) return st;
+  if (workspace == nullptr) return PKA_ERR_NULL;
+  if (!aligned16(workspace)) return PKA_ERR_ALIGN;
+  if (B == 0 || total_q == 0) return PKA_OK;
+  const int D = kv->head_dim, Hkv = kv->num_kv_heads, G = Hq / Hkv;
+  FusedLayout L;
+  st = fused_layout(B, Hq, Hkv, D, max_seq_len, params->window, &L);
+  if (st != PKA_OK) return st;
+  if (workspace_bytes < L.o_bytes + L.lse_bytes + L.cnt_bytes) return PKA_ERR_WORKSPACE;
+  pka::PrefillArgs pa = prefill_args(q, out, kv, block_tables, max_blocks, query_start_loc,
+                                     seq_lens, B, Hq, total_q, max_query_len, max_seq_len, params);
+  pa.skip_decode_rows = 1;
+  pka::DecodeArgs da = decode_args(q, kv, block_tables, max_blocks, seq_lens, B, Hq, params);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  da.out = out;
+  da.query_start_loc = query_start_loc;
+  da.decode_rows_only = 1;
+  da.partial_o = reinterpret_cast<float*>(ws);
+  da.partial_lse = reinterpret_cast<float*>(ws + L.o_bytes);
+  da.seg_counters = reinterpret_cast<int32_t*>(ws + L.o_bytes + L.lse_bytes);
+  da.num_splits = L.S;
+  da.split_blocks = L.C;
+  const int sms = pka::device_sm_count();
+  if (sms <= 0) return PKA_ERR_CUDA;
+  // Decode CTAs: the SMs the prefill tiles leave free, estimated from the
+  // query tokens beyond one per request (a quarter of the SMs at least).
+  const int tq = pka::mixed_query_tile(D, G);
+  if (tq <= 0) return PKA_ERR_UNSUPPORTED;
+  const long long extra = static_cast<long long>(total_q) - B;
+  const long long est_prefill = extra > 0 ? (extra + tq - 1) / tq * Hkv : 0;
+  long long decode_ctas = static_cast<long long>(sms) - est_prefill;
+  if (decode_ctas < sms / 4) decode_ctas = sms / 4;
+  if (decode_ctas < 1) decode_ctas = 1;
+  cudaError_t e = pka::launch_mixed(pa, da, D, G, static_cast<int>(decode_ctas),
+                                    static_cast<cudaStream_t>(stream));
   if (e == cudaErrorNotSupported) return PKA_ERR_UNSUPPORTED;
   return e == cudaSuccess ? PKA_OK : PKA_ERR_CUDA;
 }

@@ -1,0 +1,685 @@
+// Paged prefill and mixed-batch attention on the 5th-generation tensor cores
+// (tcgen05 + TMEM + TMA), sm_103a.
+//
+// The chunked-prefill contractions are dense: a chunk of new tokens attends,
+// causally, over its request's cached prefix and the chunk itself, K/V read
+// through the block table ("Triton paged decode and prefill kernels reading
+// K/V through block tables", inference-server README, engine feature list;
+// mixed-batch chunked prefill, architecture page, "Phase status").  Decode
+// rows (one token) may sit in the same varlen launch.
+//
+// Work item = (request, KV head, query tile).  A query tile packs TQ = 128/G
+// tokens x the G query heads of one KV group into the 128 rows of the MMA
+// (row = token * G + g), so all G heads share every K/V tile.  Per item:
+//
+//  * warps 4 and 7 (TMA): the Q tile (one 3-D box per 64-column chunk) and,
+//    per key tile, one 2-D box per (pool block, 64-column chunk) of K into a
+//    3-stage ring, each warp half of the blocks (a TMA copy costs the issuing
+//    warp ~80 cycles whatever its size, and a tile has 16 such boxes); blocks
+//    past the request's last block get an out-of-range row coordinate so TMA
+//    fills zeros; a stage is refilled once S = Q K^T of the tile it held has
+//    completed;
+//  * warp 5 (TMA): V, one 3-D copy per block (block-major stages, which the
+//    P V MMA reads one 16-key block at a time), 2 stages, refilled once P V
+//    of its tile completed;
+//  * warp 6 (MMA): allocates TMEM (2 S buffers + the O accumulator), issues
+//    S_j = Q K_j^T (K-major A and B, 128B-swizzled) two tiles ahead, then
+//    O += P_j V_j with P_j read from TMEM and V as an MN-major shared-memory
+//    operand, committing each to mbarriers; it also zeroes V rows past
+//    seq_len (stale slots of the last block, which may hold NaN) before they
+//    reach P V;
+//  * warps 0-3 (softmax): thread r owns row r.  It reads its S row from
+//    TMEM, applies scale, softcap and the causal / window mask, keeps a
+//    running max and sum in the exp2 domain, writes P (bf16 pairs) to its
+//    own TMEM columns and signals the MMA warp (P never
+//    touches shared memory, which holds Q and the K/V rings).  O is rescaled in TMEM only
+//    when the row max grows by more than 2^8 (the stale reference max keeps
+//    every P <= 256, and O and the sum share it, so the result is exact);
+//  * epilogue: O / sum from TMEM to bf16 rows of the output.
+//
+// All waits are bounded; a timeout sets PKA_DEVERR_TIMEOUT, the roles stop,
+// the CTA still frees its TMEM.
+#pragma once
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include "common.cuh"
+#include "kernels.h"
+#include "tcgen05.cuh"
+
+namespace pka {
+
+template <int D, int G>
+struct PrefillShape {
+  static constexpr int BM = 128;                    // MMA rows: tokens x heads
+  static constexpr int TQ = BM / G;                 // tokens per query tile
+  static constexpr int BN = (D == 256) ? 64 : 128;  // keys per key tile
+  static constexpr int DC = D / 64;                 // 128-byte chunks of a K/V/Q row
+  static constexpr int kBlocksPerTile = BN / kBlockSize;
+  static constexpr int kQChunk = BM * 128;
+  static constexpr int kKVChunk = BN * 128;        // K stage: [D/64 chunks][BN rows][128 B]
+  static constexpr int kVBlock = kBlockSize * D * 2;  // V stage: [BN/16 blocks][D/64 chunks][16 rows][128 B]
+  static constexpr int kQBytes = BM * D * 2;
+  static constexpr int kKVBytes = BN * D * 2;
+  static constexpr int KST = 3;                     // K ring stages
+  static constexpr int VST = 2;                     // V ring stages
+  static constexpr int oQ = 0;
+  static constexpr int oK = oQ + kQBytes;
+  static constexpr int oV = oK + KST * kKVBytes;
+  static constexpr int oBar = oV + VST * kKVBytes;
+  static constexpr int kNumBars = 15;
+  static constexpr int oMisc = oBar + kNumBars * 8;
+  static constexpr int kSmemBytes = oMisc + 16 + 1024;  // + slack to align the base to 1 KiB
+  // TMEM columns: S_j (fp32, BN columns) in buffer j % 2 at (j % 2) * BN;
+  // O (fp32) at [256, 256 + D); P_j (bf16 pairs, BN / 2 columns), the A
+  // operand of P_j V_j, in buffer j % 2 at kTmemP + (j % 2) * BN / 2.  P has
+  // columns of its own: S_{j+2} may be written while P_j V_j still reads P_j
+  // (consecutive MMAs overlap in the pipe), so P_j must not alias S_j.
+  static constexpr uint32_t kTmemO = 256;
+  static constexpr uint32_t kTmemP = (D == 256) ? 2 * BN : 256 + D;
+  static constexpr uint32_t kTmemCols = 512;
+  static constexpr int kThreads = 8 * 32;
+  // cost buckets of the heaviest-first ranking (scratch in the K stages)
+  static constexpr int kCostBuckets = 4096;
+  static_assert((kCostBuckets + 64) * 4 <= KST * kKVBytes, "ranking scratch");
+  static_assert(BN % 64 == 0, "P is stored to TMEM 32 columns (64 keys) at a time");
+  static_assert(kTmemP >= 2 * BN && (kTmemP + BN <= kTmemO || kTmemP >= kTmemO + D) &&
+                    kTmemP + BN <= kTmemCols,
+                "P buffers clear of S and O");
+  static_assert(kSmemBytes <= 232448, "shared memory");
+  static_assert(2 * BN <= 256 && D <= 256, "TMEM columns");
+};
+
+namespace {
+
+constexpr int kWarpTmaK = 4;
+constexpr int kWarpTmaV = 5;
+constexpr int kWarpMma = 6;
+constexpr int kWarpTmaK2 = 7;
+
+struct Item {
+  int b, kvh, q0, n, L, it0, it1, kbase, ntiles, nblk;
+};
+
+// bar indices
+// Every ring stage has its own "empty" barrier (K: B_KEMPTY, V: B_PV, whose
+// two barriers are the two V stages), so a producer waiting for use r - 1 of
+// a stage can never see the barrier one phase further on: use r cannot
+// complete before the producer has loaded it.
+enum { B_Q = 0, B_KFULL = 1, B_VFULL = 4, B_QK = 6, B_PV = 8, B_PRDY = 10, B_KEMPTY = 12 };
+
+__device__ __forceinline__ bool stop_requested(const volatile int* flag) { return *flag != 0; }
+
+__device__ __forceinline__ bool cta_wait(uint64_t* bar, uint32_t parity, int32_t* err,
+                                         volatile int* failed) {
+  if (mbar_wait(bar, parity, err)) return true;
+  *failed = 1;
+  return false;
+}
+
+// Every lane waits; the warp agrees on one outcome so that it never diverges.
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, int32_t* err,
+                                          volatile int* failed) {
+  const bool ok = __all_sync(0xffffffffu, mbar_wait(bar, parity, err));
+  if (!ok) *failed = 1;
+  return ok;
+}
+
+// exp2-based tanh: tanh(y) = 1 - 2 / (exp(2y) + 1); absolute error ~1e-7.
+__device__ __forceinline__ float tanh_via_exp2(float y) {
+  const float e = fast_exp2(fminf(2.f * kLog2e * y, 126.f));
+  return 1.f - __fdividef(2.f, e + 1.f);
+}
+
+// tanh(y) for |y| < 0.5 from its odd Taylor series through y^11 (the first
+// omitted term, 21844 y^13 / 6081075, is below 4.5e-7 there): FMA-pipe work
+// only, where the exp2 form needs two MUFU operations.
+__device__ __forceinline__ float tanh_taylor(float y) {
+  const float y2 = y * y;
+  float q = fmaf(y2, -1382.f / 155925.f, 62.f / 2835.f);
+  q = fmaf(y2, q, -17.f / 315.f);
+  q = fmaf(y2, q, 2.f / 15.f);
+  q = fmaf(y2, q, -1.f / 3.f);
+  return fmaf(y * y2, q, y);
+}
+
+// Cost of query tile qt of request b in key tiles (0: no query row there).
+template <int TQ, int BN>
+__device__ __forceinline__ int tile_cost(const PrefillArgs& a, int b, int qt) {
+  const int q0 = a.query_start_loc[b];
+  const int n = a.query_start_loc[b + 1] - q0;
+  const int L = min(a.seq_lens[b], a.max_blocks * kBlockSize);
+  const int it0 = qt * TQ;
+  if (n <= 0 || n > L || it0 >= n || (a.skip_decode_rows != 0 && n == 1)) return 0;
+  const int it1 = min(n, it0 + TQ) - 1;
+  const int p_first = L - n + it0;
+  const int p_last = L - n + it1;
+  const int t_lo = (a.window > 0) ? max(0, p_first - a.window + 1) : 0;
+  return (p_last + 1 - (t_lo & ~(kBlockSize - 1)) + BN - 1) / BN + 1;
+}
+
+// Block-wide exclusive scan of one int per thread (blockDim.x <= 1024).
+__device__ __forceinline__ int block_excl_scan(int x, int* warp_sums, int* total) {
+  const int lane = threadIdx.x % 32, warp = threadIdx.x / 32, nw = (blockDim.x + 31) / 32;
+  int incl = x;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  if (lane == 31) warp_sums[warp] = incl;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int run = 0;
+    for (int w = 0; w < nw; ++w) {
+      const int t = warp_sums[w];
+      warp_sums[w] = run;
+      run += t;
+    }
+    *total = run;
+  }
+  __syncthreads();
+  const int r = warp_sums[warp] + incl - x;
+  __syncthreads();
+  return r;
+}
+
+// Longest-processing-time-first order of the (request, query tile) pairs.
+// Every CTA ranks all pairs by cost (heaviest first, ties by index) with a
+// counting sort in shared memory and returns the pair of rank `rank`; the
+// hardware launches CTAs in blockIdx order, so the heaviest tiles start first
+// and the light ones fill the tail.  All CTAs compute the same order.
+template <int TQ, int BN>
+__device__ int lpt_pair(const PrefillArgs& a, int qtiles, int rank, int* scratch, int nbuck) {
+  int* hist = scratch;                  // [nbuck]
+  int* warp_sums = scratch + nbuck;     // [32]
+  int* misc = warp_sums + 32;           // [4]
+  const int npairs = a.batch * qtiles;
+  for (int k = threadIdx.x; k < nbuck; k += blockDim.x) hist[k] = 0;
+  __syncthreads();
+  for (int i = threadIdx.x; i < npairs; i += blockDim.x)
+    atomicAdd(&hist[min(tile_cost<TQ, BN>(a, i / qtiles, i % qtiles), nbuck - 1)], 1);
+  __syncthreads();
+  // start of bucket k in the descending order: pairs in buckets > k.  Each
+  // thread owns a run of buckets counted from the top.
+  const int per = (nbuck + blockDim.x - 1) / blockDim.x;
+  const int hi_k = nbuck - 1 - static_cast<int>(threadIdx.x) * per;  // first bucket of the run
+  int mine = 0;
+  for (int u = 0; u < per; ++u)
+    if (hi_k - u >= 0) mine += hist[hi_k - u];
+  int run = block_excl_scan(mine, warp_sums, &misc[0]);
+  for (int u = 0; u < per; ++u) {
+    const int k = hi_k - u;
+    if (k < 0) break;
+    const int c = hist[k];
+    if (rank >= run && rank < run + c) {  // exactly one thread matches
+      misc[1] = k;
+      misc[2] = rank - run;
+    }
+    run += c;
+  }
+  __syncthreads();
+  const int kb = misc[1], off = misc[2];
+  // the off-th pair (in index order) of bucket kb
+  const int chunk = (npairs + blockDim.x - 1) / blockDim.x;
+  const int i0 = threadIdx.x * chunk, i1 = min(npairs, i0 + chunk);
+  int cnt = 0;
+  for (int i = i0; i < i1; ++i)
+    cnt += (min(tile_cost<TQ, BN>(a, i / qtiles, i % qtiles), nbuck - 1) == kb);
+  const int before = block_excl_scan(cnt, warp_sums, &misc[0]);
+  if (off >= before && off < before + cnt) {
+    int seen = before;
+    for (int i = i0; i < i1; ++i) {
+      if (min(tile_cost<TQ, BN>(a, i / qtiles, i % qtiles), nbuck - 1) == kb) {
+        if (seen == off) {
+          misc[3] = i;
+          break;
+        }
+        ++seen;
+      }
+    }
+  }
+  __syncthreads();
+  const int pair = misc[3];
+  __syncthreads();
+  return pair;
+}
+
+}  // namespace
+
+// Ranks (CTAs) a prefill launch needs: one per (request, query tile, KV
+// head) with work.  A request of n rows has ceil(n / TQ) <= 1 + (n - 1) / TQ
+// query tiles (0 when n = 0), so B requests of total_q rows have at most
+// B + (total_q - B) / TQ, and at most B * ceil(max_query_len / TQ).
+inline long long prefill_ranks(const PrefillArgs& a, int TQ) {
+  const long long qtiles = (a.max_query_len + TQ - 1) / TQ;
+  long long pairs = static_cast<long long>(a.batch) * qtiles;
+  const long long extra = static_cast<long long>(a.total_q) - a.batch;
+  const long long bound = a.batch + (extra > 0 ? extra / TQ : 0);
+  if (bound < pairs) pairs = bound;
+  return pairs * a.Hkv;
+}
+
+// One prefill work item per CTA on the S::kSmemBytes of shared memory at
+// smem_raw: the item of rank `rank` (heaviest first; ranks past the last
+// item return at once).
+template <int D, int G>
+__device__ __forceinline__ void prefill_body(const PrefillArgs& a, const CUtensorMap* tm_q,
+                                             const CUtensorMap* tm_k, const CUtensorMap* tm_v,
+                                             uint8_t* smem_raw, int rank) {
+  using S = PrefillShape<D, G>;
+  constexpr int BN = S::BN, TQ = S::TQ, DC = S::DC;
+
+  // ---------------------------------------------------------- work item
+  // ------------------------------------------------------- shared memory
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+
+  // ---------------------------------------------------------- work item
+  // 1-D grid over (pair rank, KV head): CTA r takes the (r / Hkv)-th heaviest
+  // (request, query tile) pair, KV head r % Hkv.  The K stage buffers are
+  // free until the first TMA load, so the ranking uses them as scratch.
+  Item it;
+  const int qtiles = (a.max_query_len + TQ - 1) / TQ;
+  // Ranks past the number of (request, query tile) pairs with work leave
+  // before the ranking: a request of n query rows has ceil(n / TQ) such
+  // pairs (the ones tile_cost rates above zero).
+  {
+    int* scratch = reinterpret_cast<int*>(smem + S::oK);
+    int cnt = 0;
+    for (int b = threadIdx.x; b < a.batch; b += blockDim.x) {
+      const int n = a.query_start_loc[b + 1] - a.query_start_loc[b];
+      const int L = min(a.seq_lens[b], a.max_blocks * kBlockSize);
+      if (n > 0 && n <= L && !(a.skip_decode_rows != 0 && n == 1)) cnt += (n + TQ - 1) / TQ;
+    }
+    block_excl_scan(cnt, scratch, scratch + 32);
+    const int pairs_with_work = scratch[32];
+    __syncthreads();
+    if (rank / a.Hkv >= pairs_with_work) return;  // uniform
+  }
+  // costs are at most ceil(max_seq_len / BN) + 1 key tiles
+  const int nbuck = min(S::kCostBuckets, (a.max_seq_len + BN - 1) / BN + 2);
+  const int pair = lpt_pair<TQ, BN>(a, qtiles, rank / a.Hkv,
+                                    reinterpret_cast<int*>(smem + S::oK), nbuck);
+  it.b = pair / qtiles;
+  it.kvh = rank % a.Hkv;
+  const int qt = pair % qtiles;
+  it.q0 = a.query_start_loc[it.b];
+  it.n = a.query_start_loc[it.b + 1] - it.q0;
+  it.L = a.seq_lens[it.b];
+  if (it.L > a.max_blocks * kBlockSize) {
+    if (threadIdx.x == 0 && qt == 0 && it.kvh == 0) report(a.err, PKA_DEVERR_SEQ_LEN);
+    it.L = a.max_blocks * kBlockSize;
+  }
+  if (it.n > it.L) {
+    if (threadIdx.x == 0 && qt == 0 && it.kvh == 0) report(a.err, PKA_DEVERR_SEQ_LEN);
+    return;
+  }
+  it.it0 = qt * TQ;
+  // uniform: nothing to do for this tile (or a decode row left to the
+  // decode pipelines of a mixed launch)
+  if (it.n <= 0 || it.it0 >= it.n || (a.skip_decode_rows != 0 && it.n == 1)) return;
+  it.it1 = min(it.n, it.it0 + TQ) - 1;
+  const int p_first = it.L - it.n + it.it0;
+  const int p_last = it.L - it.n + it.it1;
+  const int t_lo = (a.window > 0) ? max(0, p_first - a.window + 1) : 0;
+  it.kbase = t_lo & ~(kBlockSize - 1);
+  it.ntiles = (p_last + 1 - it.kbase + BN - 1) / BN;
+  it.nblk = (it.L + kBlockSize - 1) / kBlockSize;
+
+  uint8_t* sQ = smem + S::oQ;
+  uint8_t* sK = smem + S::oK;
+  uint8_t* sV = smem + S::oV;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S::oBar);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + S::oMisc);
+  volatile int* failed = reinterpret_cast<volatile int*>(smem + S::oMisc + 4);
+
+  const int warp = threadIdx.x / 32;
+  const int lane = threadIdx.x % 32;
+
+  if (threadIdx.x == 0) {
+    mbar_init(&bars[B_Q], 1);
+    for (int i = 0; i < S::KST; ++i) {
+      mbar_init(&bars[B_KFULL + i], 1);
+      mbar_init(&bars[B_KEMPTY + i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&bars[B_VFULL + i], 1);
+      mbar_init(&bars[B_QK + i], 1);
+      mbar_init(&bars[B_PV + i], 1);
+      mbar_init(&bars[B_PRDY + i], 128);
+    }
+    *failed = 0;
+    mbar_fence_init();
+  }
+  if (warp == kWarpMma) tmem_alloc(tmem_slot, S::kTmemCols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  const uint32_t oob_row = static_cast<uint32_t>(a.num_blocks) * a.Hkv * kBlockSize;
+  const int32_t* trow = a.tables + static_cast<size_t>(it.b) * a.max_blocks;
+
+  if (warp == kWarpTmaK || warp == kWarpTmaK2 || warp == kWarpTmaV) {
+    // ============================ TMA producers ============================
+    // K stage j % KST is refilled once S_j = Q K_j^T has completed, V stage
+    // j % VST once P_j V_j has.  Issuing a TMA copy costs its warp ~80 cycles
+    // whatever the size, so the 16 boxes of a K tile are split over two
+    // warps and V is read with one 3-D copy per block.
+    const bool is_k = (warp != kWarpTmaV);
+    const int kpart = (warp == kWarpTmaK2) ? 1 : 0;
+    const int nst = is_k ? S::KST : S::VST;
+    uint8_t* ring = is_k ? sK : sV;
+    uint64_t* full = &bars[is_k ? B_KFULL : B_VFULL];
+    static_assert(S::VST == 2, "the two P V barriers double as the V stages' empty barriers");
+    uint64_t* freed = &bars[is_k ? B_KEMPTY : B_PV];
+    int issued = 0;
+    if (lane == 0) {
+      prefetch_tensormap(is_k ? tm_k : tm_v);
+      if (warp == kWarpTmaK) {
+        prefetch_tensormap(tm_q);
+        mbar_arrive_expect_tx(&bars[B_Q], S::kQBytes);
+#pragma unroll
+        for (int c = 0; c < DC; ++c)
+          tma_load_3d(sQ + c * S::kQChunk, tm_q, c * 64, it.kvh * G, it.q0 + it.it0, &bars[B_Q]);
+      }
+    }
+    // Pool rows of the item's blocks, read by the whole warp 32 at a time
+    // (one coalesced load) into a window of 64 blocks held one per lane in
+    // two registers (the second half is read ahead); the issuing lanes take
+    // them by shuffle.  Block b (counted from the first key tile) maps to
+    // TMA row (id * Hkv + kvh) * 16, or to an out-of-range row past the
+    // request's last block (TMA fills zeros).
+    constexpr int BPT = S::kBlocksPerTile;
+    static_assert(32 % BPT == 0, "a tile's blocks never straddle two 32-block windows");
+    const int jb0 = it.kbase / kBlockSize;
+    auto load_rows = [&](int base) -> uint32_t {
+      const int jb = jb0 + base + lane;
+      uint32_t row = oob_row;
+      if (jb < it.nblk) {
+        const int id = trow[jb];
+        if (static_cast<unsigned>(id) < static_cast<unsigned>(a.num_blocks))
+          row = (static_cast<uint32_t>(id) * a.Hkv + it.kvh) * kBlockSize;
+        else
+          report(a.err, PKA_DEVERR_BAD_TABLE);
+      }
+      return row;
+    };
+    int win = 0;  // rows_lo: blocks [win, win + 32); rows_hi: the next 32
+    uint32_t rows_lo = load_rows(0), rows_hi = load_rows(32);
+    for (int j = 0; j < it.ntiles; ++j) {
+      if (__any_sync(0xffffffffu, stop_requested(failed))) break;
+      if (j * BPT >= win + 32) {
+        rows_lo = rows_hi;
+        rows_hi = load_rows(win + 64);
+        win += 32;
+      }
+      uint32_t rl[BPT];
+#pragma unroll
+      for (int kb = 0; kb < BPT; ++kb)
+        rl[kb] = __shfl_sync(0xffffffffu, rows_lo, (j * BPT + kb - win) & 31);
+      const int st = j % nst;
+      int good = 1;
+      if (lane == 0) {
+        if (j >= nst && !cta_wait(&freed[st], (j / nst - 1) & 1, a.err, failed)) good = 0;
+        // one expect for the whole stage (the other K warp's copies count too)
+        if (good && kpart == 0) mbar_arrive_expect_tx(&full[st], S::kKVBytes);
+      }
+      if (!__shfl_sync(0xffffffffu, good, 0)) break;
+      uint8_t* dst = ring + st * S::kKVBytes;
+      if (is_k) {
+        // K: chunk-major (the S MMA reads 64 keys of one 64-column chunk as
+        // 8 uniformly strided 8-row groups), one box per (block, chunk); this
+        // warp takes blocks [kpart * BPT / 2, (kpart + 1) * BPT / 2)
+        if (lane < (BPT / 2) * DC) {
+          const int kb = kpart * (BPT / 2) + lane / DC, c = lane % DC;
+          uint32_t r = rl[0];
+#pragma unroll
+          for (int q = 1; q < BPT; ++q)
+            if (kb == q) r = rl[q];
+          tma_load_2d(dst + c * S::kKVChunk + kb * kBlockSize * 128, tm_k, c * 64,
+                      static_cast<int>(r), &full[st]);
+        }
+      } else if (lane < BPT) {
+        // V: block-major (each P V MMA reads one block's 16 keys), one 3-D
+        // copy per block
+        uint32_t r = rl[0];
+#pragma unroll
+        for (int q = 1; q < BPT; ++q)
+          if (lane == q) r = rl[q];
+        tma_load_3d(dst + lane * S::kVBlock, tm_v, 0, static_cast<int>(r), 0, &full[st]);
+      }
+      issued = j + 1;
+    }
+    if (lane == 0) {
+      // every issued copy must land before the CTA may finish
+      for (int j = issued - nst < 0 ? 0 : issued - nst; j < issued; ++j)
+        mbar_wait(&full[j % nst], (j / nst) & 1, a.err);
+      if (warp == kWarpTmaK && stop_requested(failed)) mbar_wait(&bars[B_Q], 0, a.err);
+    }
+    __syncwarp();
+  } else if (warp == kWarpMma) {
+    // ================================ MMA ================================
+    constexpr uint32_t idesc_qk = idesc_bf16_f32(128, BN, 0, 0);
+    constexpr uint32_t idesc_pv = idesc_bf16_f32(128, D, 0, 1);
+    const uint32_t aQ = smem_u32(sQ), aK = smem_u32(sK), aV = smem_u32(sV);
+    int committed_pv = 0;  // number of P V tiles issued
+    bool ok = warp_wait(&bars[B_Q], 0, a.err, failed);
+    auto issue_qk = [&](int j) -> bool {
+      const int st = j & 1;  // S buffer
+      const int ks = j % S::KST;
+      if (!warp_wait(&bars[B_KFULL + ks], (j / S::KST) & 1, a.err, failed)) return false;
+      tc_fence_after();
+      if (lane == 0) {
+        const uint32_t kst = aK + ks * S::kKVBytes;
+#pragma unroll
+        for (int c = 0; c < DC; ++c)
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+            const uint64_t da = smem_desc_sw128(aQ + c * S::kQChunk + kk * 32, 16, 1024);
+            const uint64_t db = smem_desc_sw128(kst + c * S::kKVChunk + kk * 32, 16, 1024);
+            umma_bf16(tmem + st * BN, da, db, idesc_qk, (c | kk) != 0);
+          }
+        umma_commit(&bars[B_QK + st]);
+        umma_commit(&bars[B_KEMPTY + ks]);
+      }
+      __syncwarp();
+      return true;
+    };
+    if (ok) ok = issue_qk(0);
+    if (ok && it.ntiles > 1) ok = issue_qk(1);
+    for (int j = 0; ok && j < it.ntiles; ++j) {
+      if (__any_sync(0xffffffffu, stop_requested(failed))) break;
+      const int st = j & 1;
+      const uint32_t ph = (j >> 1) & 1;
+      if (!warp_wait(&bars[B_VFULL + st], ph, a.err, failed)) break;
+      // V rows at positions >= seq_len (stale slots of the last block) -> 0
+      const int t0 = it.kbase + j * BN;
+      const int z0 = it.L - t0;
+      const int z1 = min(BN, it.nblk * kBlockSize - t0);
+      if (z0 > 0 && z0 < z1) {
+        uint8_t* vst = sV + st * S::kKVBytes;
+        const int nrows = z1 - z0;
+        for (int idx = lane; idx < nrows * DC * 8; idx += 32) {
+          const int r = z0 + idx / (DC * 8);
+          const int c = (idx / 8) % DC;
+          const int q = idx % 8;
+          *reinterpret_cast<uint4*>(vst + (r / kBlockSize) * S::kVBlock + c * (kBlockSize * 128) +
+                                    (r % kBlockSize) * 128 + q * 16) =
+              make_uint4(0u, 0u, 0u, 0u);
+        }
+        fence_proxy_async_smem();
+      }
+      __syncwarp();
+      if (!warp_wait(&bars[B_PRDY + st], ph, a.err, failed)) break;
+      tc_fence_after();
+      if (lane == 0) {
+        // A = P_j from TMEM (8 columns per 16 keys), B = V_j from the ring
+        const uint32_t vst = aV + st * S::kKVBytes;
+#pragma unroll
+        for (int k = 0; k < BN / 16; ++k) {
+          // block k of the stage: 64-column chunks 16 x 128 B apart
+          const uint64_t db = smem_desc_sw128(vst + k * S::kVBlock, kBlockSize * 128, 1024);
+          umma_bf16_ts(tmem + S::kTmemO, tmem + S::kTmemP + st * (BN / 2) + k * 8, db, idesc_pv,
+                       (j > 0 || k > 0) ? 1u : 0u);
+        }
+        umma_commit(&bars[B_PV + st]);
+      }
+      __syncwarp();
+      committed_pv = j + 1;
+      if (j + 2 < it.ntiles) ok = issue_qk(j + 2);
+    }
+    // the last P V must finish before TMEM is freed
+    if (committed_pv > 0)
+      mbar_wait(&bars[B_PV + ((committed_pv - 1) & 1)], ((committed_pv - 1) >> 1) & 1, a.err);
+  } else {
+    // ============================== softmax ==============================
+    const int r = threadIdx.x;  // row of the tile, TMEM lane
+    const int tok = r / G;
+    const int g = r % G;
+    const int qi = it.it0 + tok;
+    const bool row_valid = qi <= it.it1;
+    const int p = it.L - it.n + qi;
+    const int kmin = (a.window > 0) ? p - a.window + 1 : -0x40000000;
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+    const bool capped = a.softcap > 0.f;
+    const float sl2 = a.scale * kLog2e;
+    const float cap_in = capped ? a.scale / a.softcap : 0.f;
+    const float cap_out = a.softcap * kLog2e;
+    float m_ref = -INFINITY;
+    float l = 0.f;
+    bool ok = true;
+    for (int j = 0; j < it.ntiles; ++j) {
+      if (__any_sync(0xffffffffu, stop_requested(failed))) {
+        ok = false;
+        break;
+      }
+      const int st = j & 1;
+      const uint32_t ph = (j >> 1) & 1;
+      if (!warp_wait(&bars[B_QK + st], ph, a.err, failed)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      float s[BN];
+#pragma unroll
+      for (int c = 0; c < BN / 32; ++c) {
+        float t[32];
+        tmem_ld32(lane_base + st * BN + c * 32, t);
+#pragma unroll
+        for (int e = 0; e < 32; ++e) s[c * 32 + e] = t[e];
+      }
+      const int t0 = it.kbase + j * BN;
+      const int c_hi = row_valid ? min(BN - 1, p - t0) : -1;
+      const int c_lo = max(0, kmin - t0);
+      // Only rows on a causal diagonal or a window edge need the per-column
+      // mask; the warp takes the masked loop only if one of its rows does.
+      const bool need_mask = __any_sync(0xffffffffu, c_lo > 0 || c_hi < BN - 1);
+      if (capped) {
+        // log2-domain logits cap * tanh(s * scale / cap) * log2(e); the
+        // Taylor form when every |y| of the warp's rows is below 0.5
+        float amax = 0.f;
+#pragma unroll
+        for (int c = 0; c < BN; ++c) amax = fmaxf(amax, fabsf(s[c]));
+        if (__all_sync(0xffffffffu, amax * cap_in < 0.5f)) {
+#pragma unroll
+          for (int c = 0; c < BN; ++c) s[c] = cap_out * tanh_taylor(s[c] * cap_in);
+        } else {
+#pragma unroll
+          for (int c = 0; c < BN; ++c) s[c] = cap_out * tanh_via_exp2(s[c] * cap_in);
+        }
+      }
+      // (uncapped: s stays raw; scale > 0, so the raw max scales to the max)
+      if (need_mask) {
+#pragma unroll
+        for (int c = 0; c < BN; ++c)
+          if (!(c >= c_lo && c <= c_hi)) s[c] = -INFINITY;
+      }
+      float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+      for (int c = 0; c < BN; ++c) m4[c & 3] = fmaxf(m4[c & 3], s[c]);
+      float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+      if (!capped) mx *= sl2;
+      const float m_new = fmaxf(m_ref, mx);
+      const bool resc = (j > 0) && (m_new > m_ref + 8.f);
+      if (__any_sync(0xffffffffu, resc)) {
+        // O must hold P_{j-1} V_{j-1} before it is rescaled
+        if (!warp_wait(&bars[B_PV + ((j - 1) & 1)], ((j - 1) >> 1) & 1, a.err, failed)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const float f = resc ? fast_exp2(m_ref - m_new) : 1.f;
+#pragma unroll 1
+        for (int c = 0; c < D / 32; ++c) {
+          float o[32];
+          tmem_ld32(lane_base + S::kTmemO + c * 32, o);
+#pragma unroll
+          for (int e = 0; e < 32; ++e) o[e] *= f;
+          tmem_st32(lane_base + S::kTmemO + c * 32, o);
+        }
+      }
+      if (resc) l *= fast_exp2(m_ref - m_new);
+      if (j == 0 || resc) m_ref = m_new;
+      const float ms = (m_ref == -INFINITY) ? 0.f : m_ref;
+      // P_j (bf16 pairs) into P buffer j % 2.  Its last reader, P_{j-2}
+      // V_{j-2}, was issued before S_j, whose completion this thread has
+      // waited for (a commit covers every earlier MMA of the issuer).
+      // p = 2^(x - ms), x the log2-domain logit (uncapped: x = s * scale * log2 e,
+      // fused into one FMA)
+      const float xs = capped ? 1.f : sl2;
+      float lsum0 = 0.f, lsum1 = 0.f;
+#pragma unroll
+      for (int h = 0; h < BN / 64; ++h) {
+        uint32_t pk[32];
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+          const float p0 = fast_exp2(fmaf(s[h * 64 + 2 * e], xs, -ms));
+          const float p1 = fast_exp2(fmaf(s[h * 64 + 2 * e + 1], xs, -ms));
+          lsum0 += p0;
+          lsum1 += p1;
+          pk[e] = pack_bf16x2(p0, p1);
+        }
+        tmem_st32_u(lane_base + S::kTmemP + st * (BN / 2) + h * 32, pk);
+      }
+      l += lsum0 + lsum1;
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(&bars[B_PRDY + st]);
+    }
+    // ------------------------------------------------------------ epilogue
+    if (ok) {
+      const int jl = it.ntiles - 1;
+      ok = warp_wait(&bars[B_PV + (jl & 1)], (jl >> 1) & 1, a.err, failed);
+    }
+    if (ok) {
+      tc_fence_after();
+      const float inv = (l > 0.f) ? 1.f / l : 0.f;
+      uint16_t* orow = a.out + (static_cast<size_t>(it.q0 + qi) * a.Hq + it.kvh * G + g) * D;
+#pragma unroll 1
+      for (int c = 0; c < D / 32; ++c) {
+        float o[32];
+        tmem_ld32(lane_base + S::kTmemO + c * 32, o);
+        if (row_valid) {
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const uint4 w = make_uint4(pack_bf16x2(o[q * 8 + 0] * inv, o[q * 8 + 1] * inv),
+                                       pack_bf16x2(o[q * 8 + 2] * inv, o[q * 8 + 3] * inv),
+                                       pack_bf16x2(o[q * 8 + 4] * inv, o[q * 8 + 5] * inv),
+                                       pack_bf16x2(o[q * 8 + 6] * inv, o[q * 8 + 7] * inv));
+            *reinterpret_cast<uint4*>(orow + c * 32 + q * 8) = w;
+          }
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == kWarpMma) tmem_dealloc(tmem, S::kTmemCols);
+}
+
+}  // namespace pka

@@ -118,6 +118,27 @@ def test_combine_and_prefill_and_check_argument_errors(L):
     assert L.paged_attn_check_tables(64, 0, 64, 2, 8, 16, 32, None) == -2
 
 
+def test_mixed_workspace_argument_errors(L):
+    """paged_prefill_attn_ws: the prefill checks, then the workspace's
+    presence, alignment and size, all before any launch."""
+    pool = _pool()
+    par = binding.PkaAttnParams(0.1, 0.0, 0, None)
+    need = L.paged_prefill_attn_ws_bytes(2, 8, 2, 128, 64, 0)
+    assert need == L.paged_decode_attn_ws_bytes(2, 8, 2, 128, 64, 0) > 0
+
+    def call(qsl=80, ws=256, nbytes=None, max_query_len=5):
+        return L.paged_prefill_attn_ws(32, 32, ctypes.byref(pool), 64, 4, qsl, 64, 2, 8, 10,
+                                       max_query_len, 64, ctypes.byref(par), ws,
+                                       need if nbytes is None else nbytes, None)
+
+    assert call(qsl=None) == -1
+    assert call(max_query_len=65) == -2
+    assert call(ws=None) == -1
+    assert call(ws=264) == -3
+    assert call(nbytes=need - 1) == -5
+    assert L.paged_prefill_attn_ws_bytes(0, 8, 2, 128, 64, 0) == 0
+
+
 def test_zero_batch_is_a_no_op(L):
     assert _decode(L, B=0) == 0
 
