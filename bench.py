@@ -102,20 +102,31 @@ def hbm_peak():
     return FALLBACK_HBM_GBS, "fallback"
 
 
+DECODE_SOURCES = ("decode.cu", "decode_body.cuh", "common.cuh", "tmaps.cuh")
+
+
+def decode_source_hash() -> str:
+    """sha256[:16] over the decode kernel's source files, in a fixed order."""
+    import hashlib
+    h = hashlib.sha256()
+    for f in DECODE_SOURCES:
+        h.update(open(os.path.join(ROOT, "paged_kv_attention_12_gb300", "csrc", f), "rb").read())
+    return h.hexdigest()[:16]
+
+
 def traffic_from_profile():
     """DRAM bytes per launch from the committed ncu summary, if it was taken
     on the current decode kernel source (else None)."""
     import hashlib
     if not os.path.exists(PROFILE_SUMMARY):
         return None
-    src = os.path.join(ROOT, "paged_kv_attention_12_gb300", "csrc", "decode.cu")
-    h = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    h = decode_source_hash()
     vals = {}
     for line in open(PROFILE_SUMMARY):
-        if ":" in line and line.strip().startswith("- "):
-            k, v = line.strip()[2:].split(":", 1)
-            vals[k.strip()] = v.strip()
-    if vals.get("decode.cu sha256[:16]") != h:
+        if ": " in line and line.strip().startswith("- "):
+            k, v = line.strip()[2:].split(": ", 1)
+            vals[k.strip()] = (v.split() or [""])[0]
+    if vals.get("decode kernel source sha256[:16]") != h:
         return None
     try:
         return float(vals["dram bytes per launch (avg)"])

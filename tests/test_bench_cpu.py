@@ -47,3 +47,19 @@ def test_attention_pairs_of_a_causal_chunk():
                             head_dim=128, num_blocks=2, cfg_id=32)
     # queries at positions 6..9 see 7, 8, 9, 10 keys
     assert bench.attention_pairs(b) == 7 + 8 + 9 + 10
+
+
+def test_profile_traffic_is_read_only_for_the_current_kernel_source(tmp_path, monkeypatch):
+    """bench.py takes roofline.traffic from the committed ncu summary only if
+    the summary names the hash of the decode kernel's current source."""
+    import bench
+    h = bench.decode_source_hash()
+    assert len(h) == 16
+    p = tmp_path / "summary.md"
+    monkeypatch.setattr(bench, "PROFILE_SUMMARY", str(p))
+    p.write_text(f"# x\n\n- decode kernel source sha256[:16]: {h} (files)\n"
+                 "- dram bytes per launch (avg): 93396736\n")
+    assert bench.traffic_from_profile() == 93396736.0
+    p.write_text("- decode kernel source sha256[:16]: 0123456789abcdef\n"
+                 "- dram bytes per launch (avg): 93396736\n")
+    assert bench.traffic_from_profile() is None
