@@ -331,9 +331,12 @@ struct DecodeShape {
   static constexpr int kBarBytes = (2 * NSLOT * 8 + 15) / 16 * 16;
   static constexpr int kMergeMLFloats = (2 * NW * G + 3) / 4 * 4;
   static constexpr int kMergeBytes = (kMergeMLFloats + NW * G * D) * 4;
-  // + 1 KiB so the ring can start on a 1024-byte boundary (128B swizzle),
-  // + 16 bytes for the fused combine's "last piece" flag
-  static constexpr int kSmemBytes = 1024 + kRingBytes + kBarBytes + kMergeBytes + 16;
+  // fused combine: up to kMaxPend pieces whose arrival is deferred to the
+  // end of the CTA's work, 4 ints each, and one "last piece" flag per entry
+  static constexpr int kMaxPend = 4;
+  static constexpr int kPendBytes = kMaxPend * 5 * 4;
+  // + 1 KiB so the ring can start on a 1024-byte boundary (128B swizzle)
+  static constexpr int kSmemBytes = 1024 + kRingBytes + kBarBytes + kMergeBytes + kPendBytes;
   static_assert(G >= 1 && G <= 8, "the query heads of a group are the MMA's N = 8 columns");
   static_assert(kSmemBytes <= 232448 / 2 - 1024, "two CTAs per SM");
   static_assert(NSLOT % NW == 0, "each ring slot must have exactly one owner warp");
@@ -482,8 +485,9 @@ __device__ __forceinline__ void decode_body(const DecodeArgs& a, const CUtensorM
   float* mrg_m = merge;                        // [NW][G]
   float* mrg_l = merge + NW * G;               // [NW][G]
   float* mrg_acc = merge + S::kMergeMLFloats;  // [NW][G][D]
-  volatile int* last_flag =
-      reinterpret_cast<volatile int*>(smem + S::kRingBytes + S::kBarBytes + S::kMergeBytes);
+  int* pend = reinterpret_cast<int*>(smem + S::kRingBytes + S::kBarBytes + S::kMergeBytes);
+  volatile int* pend_last = pend + S::kMaxPend * 4;  // [kMaxPend]
+  int npend = 0;  // the same in every consumer thread
 
   const int warp = cx.tid / 32;
   const int lane = cx.tid % 32;
@@ -575,6 +579,72 @@ __device__ __forceinline__ void decode_body(const DecodeArgs& a, const CUtensorM
       bq[kk][0] = (g < G) ? qp[kk * 8 + t] : 0u;
       bq[kk][1] = (g < G) ? qp[kk * 8 + 4 + t] : 0u;
     }
+  };
+
+  // Arrivals of the pending pieces (one fence for all of them, the atomics
+  // in flight together), then the merge of every segment they complete.
+  auto flush_pending = [&]() {
+    named_sync(cx.bar_cons, NW * 32);  // the pieces' partials and pend[] written
+    if (cx.tid == 0) {
+      fence_acq_rel_gpu();  // the CTA's partials (ordered by the barrier) before its arrivals
+      int old[S::kMaxPend];
+#pragma unroll
+      for (int i = 0; i < S::kMaxPend; ++i)
+        if (i < npend) old[i] = atomicAdd(&a.seg_counters[pend[i * 4] * a.Hkv + pend[i * 4 + 1]], 1);
+#pragma unroll
+      for (int i = 0; i < S::kMaxPend; ++i)
+        if (i < npend) pend_last[i] = (old[i] == pend[i * 4 + 2] - 1) ? 1 : 0;
+    }
+    named_sync(cx.bar_cons, NW * 32);
+    for (int i = 0; i < npend; ++i) {
+      if (pend_last[i] == 0) continue;  // uniform
+      const int cb = pend[i * 4], ckvh = pend[i * 4 + 1], np = pend[i * 4 + 2];
+      const int cqrow = pend[i * 4 + 3];
+      fence_acq_rel_gpu();  // every other piece's partials are visible now
+      // One pass over the pieces (read from L2): four consecutive columns
+      // of one head per item, the pieces' LSE and partial rows of four
+      // pieces loaded together, merged with a running maximum.  The item
+      // loop is unrolled so that the loads of all of a thread's items are
+      // in flight together.
+      constexpr int kItems = G * (D / 4);
+      constexpr int kPerThread = (kItems + NW * 32 - 1) / (NW * 32);
+#pragma unroll
+      for (int k = 0; k < kPerThread; ++k) {
+        const int item = cx.tid + k * NW * 32;
+        if (item < kItems) {
+          const int h = item / (D / 4);
+          const int d0 = (item % (D / 4)) * 4;
+          const size_t ph0 =
+              (static_cast<size_t>(cb) * a.Hq + ckvh * G + h) * a.num_splits;
+          float M = -INFINITY, den = 0.f;
+          float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+          for (int s0 = 0; s0 < np; s0 += 4) {
+            float lv[4];
+            float4 x[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              if (s0 + u < np) {
+                lv[u] = __ldcg(a.partial_lse + ph0 + s0 + u);
+                x[u] = __ldcg(reinterpret_cast<const float4*>(a.partial_o +
+                                                              (ph0 + s0 + u) * D + d0));
+              } else {
+                lv[u] = -INFINITY;
+                x[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+              }
+            }
+            lse_merge4(M, den, acc, lv, x);
+          }
+          const float inv = den > 0.f ? 1.f / den : 0.f;
+          uint16_t* dst = reinterpret_cast<uint16_t*>(a.out) +
+                          (static_cast<size_t>(cqrow) * a.Hq + ckvh * G + h) * D + d0;
+          *reinterpret_cast<uint2*>(dst) = make_uint2(pack_bf16x2(acc.x * inv, acc.y * inv),
+                                                      pack_bf16x2(acc.z * inv, acc.w * inv));
+        }
+      }
+      named_sync(cx.bar_cons, NW * 32);
+      if (cx.tid == 0) a.seg_counters[cb * a.Hkv + ckvh] = 0;
+    }
+    named_sync(cx.bar_cons, NW * 32);  // pend[] and pend_last[] free again
   };
 
   uint32_t bq[D / 16][2];
@@ -704,66 +774,22 @@ __device__ __forceinline__ void decode_body(const DecodeArgs& a, const CUtensorM
         a.partial_lse[(static_cast<size_t>(pc.b) * a.Hq + hq) * a.num_splits + sl] = -INFINITY;
       }
     }
-    // ---- fused LSE combine: the CTA that writes a segment's last piece
-    // merges all of its pieces (the other CTAs' partials are read from L2)
-    // and resets the segment's arrival counter for the next call.
+    // ---- fused LSE combine: a piece's arrival on its segment's counter is
+    // deferred to the end of the CTA's work (or until kMaxPend pieces are
+    // pending), so that a CTA with several pieces never stalls between them
+    // on the fence, the atomic or a merge; the arrival that completes a
+    // segment merges all of its pieces (the other CTAs' partials are read
+    // from L2) and resets the counter for the next call.
     if (fused) {
       if (pc.npieces > a.num_splits && cx.tid == 0) report(a.err, PKA_DEVERR_SEQ_LEN);
-      const int np = min(pc.npieces, a.num_splits);
-      bool last = false;
       if (pc.ntiles > 0 && pc.slot < a.num_splits) {
         if (cx.tid == 0) {
-          fence_acq_rel_gpu();  // the CTA's partials (ordered by the barrier) before its arrival
-          const int old = atomicAdd(&a.seg_counters[pc.b * a.Hkv + pc.kvh], 1);
-          *last_flag = (old == np - 1) ? 1 : 0;
+          pend[npend * 4 + 0] = pc.b;
+          pend[npend * 4 + 1] = pc.kvh;
+          pend[npend * 4 + 2] = min(pc.npieces, a.num_splits);
+          pend[npend * 4 + 3] = pc.qrow;
         }
-        named_sync(cx.bar_cons, NW * 32);
-        last = *last_flag != 0;
-      }
-      if (last) {
-        fence_acq_rel_gpu();  // every other piece's partials are visible now
-        // One pass over the pieces (read from L2): four consecutive columns
-        // of one head per item, the pieces' LSE and partial rows of four
-        // pieces loaded together, merged with a running maximum.  The item
-        // loop is unrolled so that the loads of all of a thread's items are
-        // in flight together.
-        constexpr int kItems = G * (D / 4);
-        constexpr int kPerThread = (kItems + NW * 32 - 1) / (NW * 32);
-#pragma unroll
-        for (int k = 0; k < kPerThread; ++k) {
-          const int item = cx.tid + k * NW * 32;
-          if (item < kItems) {
-            const int h = item / (D / 4);
-            const int d0 = (item % (D / 4)) * 4;
-            const size_t ph0 =
-                (static_cast<size_t>(pc.b) * a.Hq + pc.kvh * G + h) * a.num_splits;
-            float M = -INFINITY, den = 0.f;
-            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-            for (int s0 = 0; s0 < np; s0 += 4) {
-              float lv[4];
-              float4 x[4];
-#pragma unroll
-              for (int u = 0; u < 4; ++u) {
-                if (s0 + u < np) {
-                  lv[u] = __ldcg(a.partial_lse + ph0 + s0 + u);
-                  x[u] = __ldcg(reinterpret_cast<const float4*>(a.partial_o +
-                                                                (ph0 + s0 + u) * D + d0));
-                } else {
-                  lv[u] = -INFINITY;
-                  x[u] = make_float4(0.f, 0.f, 0.f, 0.f);
-                }
-              }
-              lse_merge4(M, den, acc, lv, x);
-            }
-            const float inv = den > 0.f ? 1.f / den : 0.f;
-            uint16_t* dst = reinterpret_cast<uint16_t*>(a.out) +
-                            (static_cast<size_t>(pc.qrow) * a.Hq + pc.kvh * G + h) * D + d0;
-            *reinterpret_cast<uint2*>(dst) = make_uint2(pack_bf16x2(acc.x * inv, acc.y * inv),
-                                                        pack_bf16x2(acc.z * inv, acc.w * inv));
-          }
-        }
-        if (cx.tid == 0) a.seg_counters[pc.b * a.Hkv + pc.kvh] = 0;
-        named_sync(cx.bar_cons, NW * 32);
+        ++npend;
       } else if (pc.ntiles == 0 && pc.fill_from == 0) {
         // a request with no visible key: output 0
         for (int idx = cx.tid; idx < G * D; idx += NW * 32) {
@@ -772,6 +798,10 @@ __device__ __forceinline__ void decode_body(const DecodeArgs& a, const CUtensorM
                                              idx % D] = 0;
         }
       }
+    }
+    if (fused && npend > 0 && (npend == S::kMaxPend || !have_next)) {
+      flush_pending();
+      npend = 0;
     }
     pc = nx;
     have = have_next;
