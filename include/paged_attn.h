@@ -220,6 +220,15 @@ int paged_attn_check_tables(const int32_t* block_tables, int32_t max_blocks,
                             const int32_t* seq_lens, int32_t B, int32_t num_blocks,
                             int32_t block_size, int32_t* err, void* stream);
 
+/* Self-test of the bounded waits.  Launches one CTA whose thread waits, with
+ * the wait routine of every kernel in this library, on an mbarrier phase
+ * that nothing completes, for budget_cycles SM clock cycles (1 ..
+ * 2e9; the kernels' own budget is 2e9, about a second).  The wait runs out,
+ * PKA_DEVERR_TIMEOUT is OR-ed into *err (device int32, required) and the
+ * kernel returns: a stalled pipeline ends with an error status and a usable
+ * context instead of a hang.  PKA_ERR_NULL / PKA_ERR_SHAPE on bad arguments. */
+int pka_selftest_bounded_wait(int32_t* err, int64_t budget_cycles, void* stream);
+
 /* H2O attention mass.  The engine's cache offers an H2O eviction policy
  * ("Eviction policies -- Pluggable per-session: LRU, AttentionSink, H2O",
  * github README, "What's inside"; "H2O wiring deferred", architecture page,

@@ -35,6 +35,7 @@ EXPORTS = [
     "paged_decode_attn_noalloc", "paged_decode_attn_ws_bytes", "paged_decode_attn_ws",
     "paged_kv_append", "paged_decode_splitk_logits", "paged_decode_key_mass",
     "paged_kv_append_rope", "paged_prefill_attn_ws_bytes", "paged_prefill_attn_ws",
+    "pka_selftest_bounded_wait",
 ]
 
 
@@ -110,6 +111,8 @@ def lib() -> ctypes.CDLL:
     L.paged_prefill_attn_ws.restype = ctypes.c_int
     L.paged_prefill_attn_ws.argtypes = [VP, VP, P(PkaKvPool), VP, I32, VP, VP, I32, I32, I32, I32,
                                         I32, P(PkaAttnParams), VP, ctypes.c_size_t, VP]
+    L.pka_selftest_bounded_wait.restype = ctypes.c_int
+    L.pka_selftest_bounded_wait.argtypes = [VP, ctypes.c_int64, VP]
     L.paged_kv_append.restype = ctypes.c_int
     L.paged_kv_append.argtypes = [VP, VP, VP, VP, I32, I32, I32, I32, VP, I32, VP, VP]
     _lib = L
@@ -275,6 +278,14 @@ def paged_prefill_attn_ws(q, out, k_pool, v_pool, block_tables, query_start_loc,
                                      int(max_query_len), int(max_seq_len), ctypes.byref(par),
                                      workspace.data_ptr(), workspace.numel(), _stream(stream))
     _check("paged_prefill_attn_ws", st)
+
+
+def selftest_bounded_wait(err, budget_cycles, stream=None):
+    """A wait that can never complete, with the library's wait routine and a
+    budget of ``budget_cycles``: it must end with PKA_DEVERR_TIMEOUT in
+    ``err`` (device int32)."""
+    st = lib().pka_selftest_bounded_wait(err.data_ptr(), int(budget_cycles), _stream(stream))
+    _check("pka_selftest_bounded_wait", st)
 
 
 def paged_attn_check_tables(block_tables, seq_lens, num_blocks, err, block_size=16, stream=None):

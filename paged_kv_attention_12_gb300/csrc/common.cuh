@@ -65,17 +65,23 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 }
 
 // Wait until the phase with the given parity has completed.  Gives up after
-// kWaitBudgetCycles, reports PKA_DEVERR_TIMEOUT and returns false.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int32_t* err) {
+// `budget` SM clock cycles, reports PKA_DEVERR_TIMEOUT and returns false.
+__device__ __forceinline__ bool mbar_wait_budget(uint64_t* bar, uint32_t parity, int32_t* err,
+                                                 long long budget) {
   if (mbar_try_wait(bar, parity)) return true;
   const long long t0 = clock64();
   while (true) {
     if (mbar_try_wait(bar, parity)) return true;
-    if (clock64() - t0 > kWaitBudgetCycles) {
+    if (clock64() - t0 > budget) {
       report(err, PKA_DEVERR_TIMEOUT);
       return false;
     }
   }
+}
+
+// Every wait of the library's kernels: a budget of kWaitBudgetCycles.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int32_t* err) {
+  return mbar_wait_budget(bar, parity, err, kWaitBudgetCycles);
 }
 
 // ------------------------------------------------------- bulk copy (TMA)

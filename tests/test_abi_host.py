@@ -118,6 +118,12 @@ def test_combine_and_prefill_and_check_argument_errors(L):
     assert L.paged_attn_check_tables(64, 0, 64, 2, 8, 16, 32, None) == -2
 
 
+def test_selftest_argument_errors(L):
+    assert L.pka_selftest_bounded_wait(None, 1000, None) == -1
+    assert L.pka_selftest_bounded_wait(16, 0, None) == -2
+    assert L.pka_selftest_bounded_wait(16, 2000000001, None) == -2
+
+
 def test_mixed_workspace_argument_errors(L):
     """paged_prefill_attn_ws: the prefill checks, then the workspace's
     presence, alignment and size, all before any launch."""
