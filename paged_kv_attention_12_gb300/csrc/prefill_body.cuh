@@ -135,6 +135,14 @@ __device__ __forceinline__ float tanh_via_exp2(float y) {
 // tanh(y) for |y| < 0.5 from its odd Taylor series through y^11 (the first
 // omitted term, 21844 y^13 / 6081075, is below 4.5e-7 there): FMA-pipe work
 // only, where the exp2 form needs two MUFU operations.
+// tanh(y) for |y| < 1/8 from y - y^3/3 + 2 y^5/15 (the first omitted term,
+// 17 y^7 / 315, is below 2.6e-8 there): four FMA-pipe operations.
+__device__ __forceinline__ float tanh_taylor_short(float y) {
+  const float y2 = y * y;
+  const float q = fmaf(y2, 2.f / 15.f, -1.f / 3.f);
+  return fmaf(y * y2, q, y);
+}
+
 __device__ __forceinline__ float tanh_taylor(float y) {
   const float y2 = y * y;
   float q = fmaf(y2, -1382.f / 155925.f, 62.f / 2835.f);
@@ -578,12 +586,16 @@ __device__ __forceinline__ void prefill_body(const PrefillArgs& a, const CUtenso
       // mask; the warp takes the masked loop only if one of its rows does.
       const bool need_mask = __any_sync(0xffffffffu, c_lo > 0 || c_hi < BN - 1);
       if (capped) {
-        // log2-domain logits cap * tanh(s * scale / cap) * log2(e); the
-        // Taylor form when every |y| of the warp's rows is below 0.5
+        // log2-domain logits cap * tanh(s * scale / cap) * log2(e); a
+        // Taylor form when every |y| of the warp's rows is below 1/8 (three
+        // terms) or 0.5 (six terms), else the exp2 form
         float amax = 0.f;
 #pragma unroll
         for (int c = 0; c < BN; ++c) amax = fmaxf(amax, fabsf(s[c]));
-        if (__all_sync(0xffffffffu, amax * cap_in < 0.5f)) {
+        if (__all_sync(0xffffffffu, amax * cap_in < 0.125f)) {
+#pragma unroll
+          for (int c = 0; c < BN; ++c) s[c] = cap_out * tanh_taylor_short(s[c] * cap_in);
+        } else if (__all_sync(0xffffffffu, amax * cap_in < 0.5f)) {
 #pragma unroll
           for (int c = 0; c < BN; ++c) s[c] = cap_out * tanh_taylor(s[c] * cap_in);
         } else {

@@ -64,7 +64,8 @@ def test_group_sizes(D, G):
     check(small([150, 61], [90, 61], D=D, G=G, Hkv=2 if G < 8 else 1, seed=G), f"D={D} G={G}")
 
 
-@pytest.mark.parametrize("window,softcap", [(0, 30.0), (37, 0.0), (100, 50.0)])
+@pytest.mark.parametrize("window,softcap", [(0, 30.0), (37, 0.0), (100, 50.0), (0, 2.0),
+                                            (64, 8.0)])
 def test_window_and_softcap(window, softcap):
     check(small([400, 130, 57], [130, 1, 57], D=256, Hkv=2, window=window, softcap=softcap,
                 seed=window), f"W={window} cap={softcap}")
