@@ -152,12 +152,10 @@ __device__ __forceinline__ float tanh_taylor(float y) {
   return fmaf(y * y2, q, y);
 }
 
-// Cost of query tile qt of request b in key tiles (0: no query row there).
+// Cost in key tiles of query tile qt of a request with n query rows and
+// context length L (clamped to the table) (0: no query row there).
 template <int TQ, int BN>
-__device__ __forceinline__ int tile_cost(const PrefillArgs& a, int b, int qt) {
-  const int q0 = a.query_start_loc[b];
-  const int n = a.query_start_loc[b + 1] - q0;
-  const int L = min(a.seq_lens[b], a.max_blocks * kBlockSize);
+__device__ __forceinline__ int tile_cost_nl(const PrefillArgs& a, int n, int L, int qt) {
   const int it0 = qt * TQ;
   if (n <= 0 || n > L || it0 >= n || (a.skip_decode_rows != 0 && n == 1)) return 0;
   const int it1 = min(n, it0 + TQ) - 1;
@@ -165,6 +163,22 @@ __device__ __forceinline__ int tile_cost(const PrefillArgs& a, int b, int qt) {
   const int p_last = L - n + it1;
   const int t_lo = (a.window > 0) ? max(0, p_first - a.window + 1) : 0;
   return (p_last + 1 - (t_lo & ~(kBlockSize - 1)) + BN - 1) / BN + 1;
+}
+
+// Requests whose (n, L) the ranking keeps in shared memory (more: read from
+// global memory at every use).
+constexpr int kReqCache = 4096;
+constexpr int kReqCacheOffset = 4224;  // ints, past the ranking's own scratch
+
+// tile_cost_nl for request b, its (n, L) from the shared-memory copy when
+// rn != nullptr.
+template <int TQ, int BN>
+__device__ __forceinline__ int tile_cost(const PrefillArgs& a, const int* rn, const int* rL,
+                                         int b, int qt) {
+  if (rn != nullptr) return tile_cost_nl<TQ, BN>(a, rn[b], rL[b], qt);
+  const int n = a.query_start_loc[b + 1] - a.query_start_loc[b];
+  const int L = min(a.seq_lens[b], a.max_blocks * kBlockSize);
+  return tile_cost_nl<TQ, BN>(a, n, L, qt);
 }
 
 // Block-wide exclusive scan of one int per thread (blockDim.x <= 1024).
@@ -199,7 +213,8 @@ __device__ __forceinline__ int block_excl_scan(int x, int* warp_sums, int* total
 // hardware launches CTAs in blockIdx order, so the heaviest tiles start first
 // and the light ones fill the tail.  All CTAs compute the same order.
 template <int TQ, int BN>
-__device__ int lpt_pair(const PrefillArgs& a, int qtiles, int rank, int* scratch, int nbuck) {
+__device__ int lpt_pair(const PrefillArgs& a, int qtiles, int rank, int* scratch, int nbuck,
+                        const int* rn, const int* rL) {
   int* hist = scratch;                  // [nbuck]
   int* warp_sums = scratch + nbuck;     // [32]
   int* misc = warp_sums + 32;           // [4]
@@ -207,7 +222,7 @@ __device__ int lpt_pair(const PrefillArgs& a, int qtiles, int rank, int* scratch
   for (int k = threadIdx.x; k < nbuck; k += blockDim.x) hist[k] = 0;
   __syncthreads();
   for (int i = threadIdx.x; i < npairs; i += blockDim.x)
-    atomicAdd(&hist[min(tile_cost<TQ, BN>(a, i / qtiles, i % qtiles), nbuck - 1)], 1);
+    atomicAdd(&hist[min(tile_cost<TQ, BN>(a, rn, rL, i / qtiles, i % qtiles), nbuck - 1)], 1);
   __syncthreads();
   // start of bucket k in the descending order: pairs in buckets > k.  Each
   // thread owns a run of buckets counted from the top.
@@ -234,12 +249,12 @@ __device__ int lpt_pair(const PrefillArgs& a, int qtiles, int rank, int* scratch
   const int i0 = threadIdx.x * chunk, i1 = min(npairs, i0 + chunk);
   int cnt = 0;
   for (int i = i0; i < i1; ++i)
-    cnt += (min(tile_cost<TQ, BN>(a, i / qtiles, i % qtiles), nbuck - 1) == kb);
+    cnt += (min(tile_cost<TQ, BN>(a, rn, rL, i / qtiles, i % qtiles), nbuck - 1) == kb);
   const int before = block_excl_scan(cnt, warp_sums, &misc[0]);
   if (off >= before && off < before + cnt) {
     int seen = before;
     for (int i = i0; i < i1; ++i) {
-      if (min(tile_cost<TQ, BN>(a, i / qtiles, i % qtiles), nbuck - 1) == kb) {
+      if (min(tile_cost<TQ, BN>(a, rn, rL, i / qtiles, i % qtiles), nbuck - 1) == kb) {
         if (seen == off) {
           misc[3] = i;
           break;
@@ -293,23 +308,33 @@ __device__ __forceinline__ void prefill_body(const PrefillArgs& a, const CUtenso
   // Ranks past the number of (request, query tile) pairs with work leave
   // before the ranking: a request of n query rows has ceil(n / TQ) such
   // pairs (the ones tile_cost rates above zero).
+  // The same pass keeps every request's (n, L) in shared memory for the
+  // ranking, which would otherwise read them once per query tile.
+  int* scratch = reinterpret_cast<int*>(smem + S::oK);
+  const bool cache = a.batch <= kReqCache;
+  int* rn = cache ? scratch + kReqCacheOffset : nullptr;
+  int* rL = cache ? rn + kReqCache : nullptr;
+  static_assert((kReqCacheOffset + 2 * kReqCache) * 4 <= S::KST * S::kKVBytes,
+                "the request cache fits in the K stages");
   {
-    int* scratch = reinterpret_cast<int*>(smem + S::oK);
     int cnt = 0;
     for (int b = threadIdx.x; b < a.batch; b += blockDim.x) {
       const int n = a.query_start_loc[b + 1] - a.query_start_loc[b];
       const int L = min(a.seq_lens[b], a.max_blocks * kBlockSize);
+      if (cache) {
+        rn[b] = n;
+        rL[b] = L;
+      }
       if (n > 0 && n <= L && !(a.skip_decode_rows != 0 && n == 1)) cnt += (n + TQ - 1) / TQ;
     }
-    block_excl_scan(cnt, scratch, scratch + 32);
+    block_excl_scan(cnt, scratch, scratch + 32);  // also orders rn / rL for every thread
     const int pairs_with_work = scratch[32];
     __syncthreads();
     if (rank / a.Hkv >= pairs_with_work) return;  // uniform
   }
   // costs are at most ceil(max_seq_len / BN) + 1 key tiles
   const int nbuck = min(S::kCostBuckets, (a.max_seq_len + BN - 1) / BN + 2);
-  const int pair = lpt_pair<TQ, BN>(a, qtiles, rank / a.Hkv,
-                                    reinterpret_cast<int*>(smem + S::oK), nbuck);
+  const int pair = lpt_pair<TQ, BN>(a, qtiles, rank / a.Hkv, scratch, nbuck, rn, rL);
   it.b = pair / qtiles;
   it.kvh = rank % a.Hkv;
   const int qt = pair % qtiles;
