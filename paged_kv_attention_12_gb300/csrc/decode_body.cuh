@@ -10,18 +10,21 @@
 // copy time.
 //
 // Work.  A segment is one (request, KV head): its visible blocks, each a
-// 16-key "tile".  The kernel is persistent (one CTA per SM).
-//  * split-K: the segments' tiles, laid end to end, are cut into equal
-//    contiguous chunks of q = max(min_chunk, ceil(total / grid)) tiles, one
-//    chunk per CTA.  Each piece of a segment inside a chunk gives one partial
-//    (normalised output, LSE) in slot (CTA index - CTA index of the
-//    segment's first tile); the CTA holding a segment's first tile also
+// 16-key "tile".  The pipelines are persistent (two per SM).
+//  * split-K: the segments, laid end to end as work units (a fixed cost per
+//    piece, then one unit per tile), are cut into equal contiguous chunks of
+//    q = max(min_chunk, ceil(total / pipelines)) units, one chunk per
+//    pipeline.  Each piece of a segment inside a chunk gives one partial
+//    (normalised output, LSE) in slot (chunk index - chunk index of the
+//    segment's first tile); the pipeline holding a segment's first tile also
 //    writes LSE = -inf into the slots the segment does not use, so the LSE
-//    combine needs nothing but the partials.  Every CTA streams the same
-//    number of tiles whatever the mix of lengths.
-//  * direct: CTA c takes whole segments c, c + grid, ... and writes bf16.
+//    combine needs nothing but the partials.  With a workspace of arrival
+//    counters, the pipeline whose arrival completes a segment merges its
+//    partials in the same launch (fused combine).
+//  * direct: pipeline c takes whole segments c, c + pipelines, ... and
+//    writes bf16.
 //
-// Inside a CTA:
+// Inside a pipeline (a CTA of its own, or half of a mixed-batch CTA):
 //  * one producer warp walks the pieces' block tables (32 ids per coalesced
 //    load) and loads, per tile, the (block, head) K and V tiles with one
 //    3-D TMA copy each (D / 64 boxes of 16 rows x 64 columns, 128-byte
