@@ -219,3 +219,32 @@ def test_long_chunk_max_sizes():
             assert_close(got[i, h:h + 1], o, f"long chunk row {r} head {h}")
     torch.cuda.synchronize()
     assert err.item() == 0
+
+
+def test_many_requests_rank_from_global_memory():
+    """More requests than the ranking keeps in shared memory (4096): the
+    ranking reads (rows, length) from global memory; decode rows, short
+    chunks and empty requests mixed, checked on sampled requests through both
+    the single-pipeline and the mixed launch."""
+    rng = np.random.default_rng(12)
+    B = 4500
+    L = rng.integers(1, 40, size=B)
+    n = np.ones(B, dtype=np.int64)
+    chunks = [5, 1000, 2222, 4499]
+    n[chunks] = [33, 20, 40, 7]
+    L[chunks] = np.maximum(L[chunks], n[chunks]) + 50
+    n[[7, 3000]] = 0
+    batch = workload.make_batch(seq_lens=L.tolist(), q_lens=n.tolist(), num_q_heads=8,
+                                num_kv_heads=2, head_dim=128,
+                                num_blocks=int(sum(-(-x // 16) for x in L)) + 8, cfg_id=43,
+                                seed=12, device=DEV, poison=True)
+    reqs = [0, 5, 6, 1000, 2222, 3001, 4498, 4499]
+    arr = workload.to_numpy_f64(batch, reqs)
+    ref, _ = oracle.run_batch(arr)
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    out = run(batch, err)
+    assert_close(to_f64(out[arr["q_rows"]]), ref, "single pipeline, 4500 requests")
+    mixed = binding.MixedBatch(batch).run(err)
+    assert_close(to_f64(mixed[arr["q_rows"]]), ref, "mixed launch, 4500 requests")
+    torch.cuda.synchronize()
+    assert err.item() == 0
