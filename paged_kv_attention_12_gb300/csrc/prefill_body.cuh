@@ -598,11 +598,11 @@ __device__ __forceinline__ void prefill_body(const PrefillArgs& a, const CUtenso
       tc_fence_after();
       float s[BN];
 #pragma unroll
-      for (int c = 0; c < BN / 32; ++c) {
-        float t[32];
-        tmem_ld32(lane_base + st * BN + c * 32, t);
+      for (int c = 0; c < BN / 64; ++c) {  // 64 columns per load and wait
+        float t[64];
+        tmem_ld64(lane_base + st * BN + c * 64, t);
 #pragma unroll
-        for (int e = 0; e < 32; ++e) s[c * 32 + e] = t[e];
+        for (int e = 0; e < 64; ++e) s[c * 64 + e] = t[e];
       }
       const int t0 = it.kbase + j * BN;
       const int c_hi = row_valid ? min(BN - 1, p - t0) : -1;
@@ -696,17 +696,17 @@ __device__ __forceinline__ void prefill_body(const PrefillArgs& a, const CUtenso
       const float inv = (l > 0.f) ? 1.f / l : 0.f;
       uint16_t* orow = a.out + (static_cast<size_t>(it.q0 + qi) * a.Hq + it.kvh * G + g) * D;
 #pragma unroll 1
-      for (int c = 0; c < D / 32; ++c) {
-        float o[32];
-        tmem_ld32(lane_base + S::kTmemO + c * 32, o);
+      for (int c = 0; c < D / 64; ++c) {  // 64 columns per load and wait
+        float o[64];
+        tmem_ld64(lane_base + S::kTmemO + c * 64, o);
         if (row_valid) {
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
+          for (int q = 0; q < 8; ++q) {
             const uint4 w = make_uint4(pack_bf16x2(o[q * 8 + 0] * inv, o[q * 8 + 1] * inv),
                                        pack_bf16x2(o[q * 8 + 2] * inv, o[q * 8 + 3] * inv),
                                        pack_bf16x2(o[q * 8 + 4] * inv, o[q * 8 + 5] * inv),
                                        pack_bf16x2(o[q * 8 + 6] * inv, o[q * 8 + 7] * inv));
-            *reinterpret_cast<uint4*>(orow + c * 32 + q * 8) = w;
+            *reinterpret_cast<uint4*>(orow + c * 64 + q * 8) = w;
           }
         }
       }
