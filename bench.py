@@ -63,8 +63,8 @@ def parse():
                         "split: split-K decode launch + combine launch")
     p.add_argument("--no-other", action="store_true",
                    help="skip the per-workload measurements of the other configurations")
-    p.add_argument("--cpu-seconds", type=float, default=15.0,
-                   help="budget of the oracle sample (CPU baseline)")
+    p.add_argument("--cpu-seconds", type=float, default=6.0,
+                   help="budget of each leg of the oracle samples (CPU baseline)")
     p.add_argument("--workload", type=int, choices=[1, 3, 4, 5], default=None,
                    help="time only this other configuration (--steps launches after "
                         "--warmup) and print its entry as the JSON line")
@@ -189,35 +189,155 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
-def cpu_baseline(calls, budget_s: float):
-    """The fp64 oracle on a bounded sample (first requests of each layer)."""
-    import numpy as np  # noqa: F401
+def _oracle_task(task):
+    """One piece of the CPU baseline, run in a spawned host process: the
+    oracle on a saved sub-batch (``path``, an .npz of oracle inputs),
+    ``reps`` times.  The loaded inputs stay cached in the process."""
+    import numpy as np
     import oracle
+    path, reps = task
+    cache = _oracle_task.__dict__.setdefault("cache", {})
+    if path not in cache:
+        with np.load(path) as z:
+            arr = {k: z[k] for k in z.files}
+        for k in ("scale", "softcap"):
+            arr[k] = float(arr[k])
+        arr["window"] = int(arr["window"])
+        cache[path] = arr
+    t0 = time.perf_counter()
+    for _ in range(reps):
+        oracle.run_batch(cache[path])
+    return time.perf_counter() - t0
+
+
+def _noop(_):
+    return os.getpid()
+
+
+def _save_sub_batch(arr, path, rows=None):
+    """Writes the oracle inputs of one request (``arr`` from to_numpy_f64 with
+    one request), optionally only query rows [r0, r1) of its chunk: the rows
+    keep their positions (seq_len shortened by the rows dropped after r1)."""
+    import numpy as np
+    out = {k: v for k, v in arr.items() if k != "q_rows"}
+    if rows is not None:
+        r0, r1 = rows
+        n = int(arr["query_start_loc"][1])
+        out["q"] = arr["q"][r0:r1]
+        out["query_start_loc"] = np.array([0, r1 - r0], dtype=np.int64)
+        out["seq_lens"] = arr["seq_lens"] - (n - r1)
+    np.savez(path, **out)
+
+
+def _run_pool(tasks, procs):
+    """Wall time of the tasks over ``procs`` spawned processes (already
+    started and warmed up before the clock starts)."""
+    import multiprocessing as mp
+    ctx = mp.get_context("spawn")  # never fork a process that holds a CUDA context
+    with ctx.Pool(procs) as pool:
+        pool.map(_noop, range(4 * procs), chunksize=1)
+        t0 = time.perf_counter()
+        pool.map(_oracle_task, tasks, chunksize=1)
+        return time.perf_counter() - t0
+
+
+def cpu_baseline(calls, prefill_batch, budget_s: float):
+    """The fp64 oracle, as it stands, on bounded samples of the workloads, on
+    one host thread and on every host core (one spawned process per core,
+    BLAS at one thread each); inputs are saved beforehand, so the timings
+    cover the oracle alone.
+
+    decode: every request of both layers, each repeated to fill the budget
+    (GB/s of K/V + q, the metric's unit); prefill (the chunked-prefill
+    workload): 16-row groups of query rows spread evenly over each request's
+    chunk (TFLOP/s over the sampled rows' visible (query, key) pairs)."""
+    import shutil
+    import tempfile
+
     from paged_kv_attention_12_gb300 import workload
-    done_bytes = 0.0
-    t_used = 0.0
-    reqs_done = 0
-    per_layer = max(1, budget_s / len(calls))
-    for batch in calls:
-        t_layer = 0.0
-        for b in range(batch.num_requests):
-            if t_layer >= per_layer:
-                break
-            arr = workload.to_numpy_f64(batch, [b])
-            t0 = time.perf_counter()
-            oracle.run_batch(arr)
-            dt = time.perf_counter() - t0
-            t_layer += dt
-            L = batch.seq_lens_host[b]
-            vis = L if batch.window <= 0 else min(L, batch.window)
-            done_bytes += vis * 2 * batch.num_kv_heads * batch.head_dim * 2 + \
-                batch.num_q_heads * batch.head_dim * 2
-            reqs_done += 1
-        t_used += t_layer
-    return {"value": done_bytes / t_used / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
-            "sample": f"{reqs_done} of {sum(c.num_requests for c in calls)} decode requests "
-                      f"(first requests of each layer, same workload), fp64 numpy oracle, "
-                      f"one thread, {t_used:.1f} s"}
+    procs = max(1, os.cpu_count() or 1)
+    tmp = tempfile.mkdtemp(prefix="pka_oracle_")
+    try:
+        # ---- decode: one file per request of each layer
+        files, nbytes, t_pass = [], 0.0, 0.0
+        for li, batch in enumerate(calls):
+            for b in range(batch.num_requests):
+                arr = workload.to_numpy_f64(batch, [b])
+                path = os.path.join(tmp, f"d{li}_{b}.npz")
+                _save_sub_batch(arr, path)
+                files.append(path)
+                L = batch.seq_lens_host[b]
+                vis = L if batch.window <= 0 else min(L, batch.window)
+                nbytes += vis * 2 * batch.num_kv_heads * batch.head_dim * 2 + \
+                    batch.num_q_heads * batch.head_dim * 2
+                t_pass += _oracle_task((path, 1))  # calibration pass, in this process
+        reps1 = max(1, int(round(budget_s / max(t_pass, 1e-6))))
+        t1 = _run_pool([(f, reps1) for f in files], 1)
+        repsn = reps1 * procs
+        tn = _run_pool([(f, repsn) for f in files], procs)
+        dec1 = nbytes * reps1 / t1 / 1e9
+        decn = nbytes * repsn / tn / 1e9
+        # ---- prefill: 16-row groups spread evenly over every chunk
+        pre = {}
+        if prefill_batch is not None:
+            B = prefill_batch.num_requests
+            qsl = prefill_batch.query_start_host()
+            arrs = [workload.to_numpy_f64(prefill_batch, [b]) for b in range(B)]
+            paths = []
+            for b in range(B):
+                p = os.path.join(tmp, f"p{b}.npz")
+                _save_sub_batch(arrs[b], p)
+                paths.append(p)
+
+            def pairs(b, r0, r1):
+                L, n = prefill_batch.seq_lens_host[b], qsl[b + 1] - qsl[b]
+                return sum(L - n + i + 1 for i in range(r0, r1))  # causal, no window
+
+            # calibration: the last group of the longest request
+            bl = max(range(B), key=lambda x: prefill_batch.seq_lens_host[x])
+            n_bl = qsl[bl + 1] - qsl[bl]
+            cal = os.path.join(tmp, "pcal.npz")
+            _save_sub_batch(arrs[bl], cal, (n_bl - 16, n_bl))
+            t_pair = _oracle_task((cal, 1)) / pairs(bl, n_bl - 16, n_bl)
+            total_pairs = sum(pairs(b, 0, qsl[b + 1] - qsl[b]) for b in range(B))
+
+            def sample(frac):
+                tasks, npairs = [], 0
+                for b in range(B):
+                    n = qsl[b + 1] - qsl[b]
+                    groups = max(1, n // 16)
+                    take = max(1, min(groups, int(round(groups * frac))))
+                    for k in range(take):
+                        g = (k * groups) // take
+                        r0, r1 = g * 16, min(n, g * 16 + 16)
+                        p = os.path.join(tmp, f"p{b}_{r0}.npz")
+                        if not os.path.exists(p):
+                            _save_sub_batch(arrs[b], p, (r0, r1))
+                        tasks.append((p, 1))
+                        npairs += pairs(b, r0, r1)
+                return tasks, npairs
+
+            fl = 4.0 * prefill_batch.head_dim * prefill_batch.num_q_heads
+            frac1 = min(1.0, budget_s / max(total_pairs * t_pair, 1e-6))
+            tasks1, np1 = sample(frac1)
+            p1 = _run_pool(tasks1, 1)
+            tasksn, npn = sample(min(1.0, frac1 * procs))
+            pn = _run_pool(tasksn, procs)
+            pre = {"unit": "TFLOP/s", "single_thread": fl * np1 / p1 / 1e12,
+                   "all_cores": fl * npn / pn / 1e12, "cores": procs,
+                   "sample": f"chunked-prefill workload: {np1} of {total_pairs} visible "
+                             f"(query, key) pairs on one thread ({p1:.1f} s), {npn} on "
+                             f"{procs} processes ({pn:.1f} s); 16-row groups spread over "
+                             f"each chunk"}
+    finally:
+        shutil.rmtree(tmp, ignore_errors=True)
+    return {"value": decn, "unit": "GB/s", "cores": procs, "kind": "oracle",
+            "single_thread": {"value": dec1, "unit": "GB/s", "cores": 1},
+            "sample": f"decode serving workload, all {len(files)} requests of both layers: "
+                      f"{reps1} passes on one thread ({t1:.1f} s), {repsn} passes over "
+                      f"{procs} spawned processes ({tn:.1f} s); fp64 numpy oracle, BLAS at "
+                      f"one thread per process",
+            "prefill": pre}
 
 
 def bf16_peak():
@@ -690,7 +810,9 @@ def main():
     if not args.no_other and world == 1:
         line["other_workloads"] = other_workloads(dev, flush)
     if not args.no_cpu_baseline and world == 1:
-        line["cpu_baseline"] = cpu_baseline(calls, args.cpu_seconds)
+        pre = workload.chunked_prefill(0, dev)
+        line["cpu_baseline"] = cpu_baseline(calls, pre, args.cpu_seconds)
+        del pre
     print(json.dumps(line))
     if world > 1:
         import torch.distributed as dist

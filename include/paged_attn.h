@@ -65,7 +65,7 @@ typedef enum {
   PKA_ERR_SHAPE = -2,       /* inconsistent sizes (Hq % Hkv, negative sizes, ...) */
   PKA_ERR_ALIGN = -3,       /* q/out/pool pointer not 16-byte aligned */
   PKA_ERR_UNSUPPORTED = -4, /* head_dim, block_size or G outside the supported set */
-  PKA_ERR_WORKSPACE = -5,   /* split-K partition does not cover max_seq_len */
+  PKA_ERR_WORKSPACE = -5,   /* workspace too small (partials, slots or counters) */
   PKA_ERR_BAD_TABLE = -6,   /* (host view of PKA_DEVERR_BAD_TABLE) */
   PKA_ERR_TIMEOUT = -7,     /* (host view of PKA_DEVERR_TIMEOUT) */
   PKA_ERR_CUDA = -8         /* a CUDA runtime call or launch failed */
@@ -75,6 +75,8 @@ typedef enum {
 #define PKA_DEVERR_BAD_TABLE 1  /* a table id was outside [0, num_blocks) */
 #define PKA_DEVERR_TIMEOUT 2    /* a bounded mbarrier wait ran out */
 #define PKA_DEVERR_SEQ_LEN 4    /* seq_len beyond max_blocks*bs or the split cover */
+#define PKA_DEVERR_QUERY_LOC 8  /* query_start_loc span outside [0, total_q], negative,
+                                   or longer than max_query_len (request skipped) */
 
 /* One layer's K/V block pool.  k and v are device pointers, 16-byte aligned,
  * bf16 [num_blocks][num_kv_heads][block_size][head_dim]. */
@@ -87,10 +89,12 @@ typedef struct {
   int32_t head_dim;
 } pka_kv_pool;
 
-/* Attention parameters.  scale multiplies q.k; softcap <= 0 disables the tanh
- * cap; window <= 0 is full (causal) attention, else the W-key sliding window
- * described above.  err: optional device int32 the kernels OR error bits into
- * (never cleared by the library). */
+/* Attention parameters.  scale multiplies q.k and may be any finite value
+ * (zero or negative included; NaN or infinite: PKA_ERR_SHAPE); softcap <= 0
+ * or +infinity disables the tanh cap (NaN: PKA_ERR_SHAPE); window <= 0 is
+ * full (causal) attention, else the W-key sliding window described above.
+ * err: optional device int32 the kernels OR error bits into (never cleared by
+ * the library). */
 typedef struct {
   float scale;
   float softcap;
@@ -133,15 +137,18 @@ size_t paged_decode_splitk_workspace_bytes(int32_t B, int32_t Hq, int32_t D,
 /* Split-K decode ("split-K decode variant", engine feature list).
  * Work partition: a segment is one (request, KV head) with n_b visible
  * blocks ("tiles", blocks [jlo_b, jlo_b + n_b), jlo_b = block of the first
- * visible key).  Segments are laid end to end in (request, head) order,
- * T = Hkv * sum_b n_b tiles in all, and cut into chunks of
- * q = max(C, ceil(T / grid)) tiles, grid = twice the GPU's SM count;
- * chunk c is streamed by CTA c.  The part of a segment starting at tile A that falls
- * in chunk c is written to slot c - floor(A / q): its softmax-normalised
- * partial output partial_o fp32 [B][Hq][S][D] and its natural-log LSE
- * partial_lse fp32 [B][Hq][S].  Slots a segment does not use get LSE -inf
- * (their partial_o is left untouched).  Needs S >= ceil(T_max / C) + 1 for
- * T_max the visible blocks of max_seq_len (else PKA_ERR_WORKSPACE). */
+ * visible key).  Segments are laid end to end in (request, head) order on a
+ * line of work units: a segment with n_b > 0 takes P = 4 units (the fixed
+ * cost of one partial) followed by one unit per tile, an empty segment none.
+ * The T units of the line are cut into chunks of q = max(C, ceil(T / grid))
+ * units, grid = twice the GPU's SM count, and chunk c is streamed by CTA c.
+ * The tiles of a segment whose first tile sits at unit A that fall in chunk
+ * c form its piece c - floor(A / q), written to that slot: the piece's
+ * softmax-normalised partial output partial_o fp32 [B][Hq][S][D] and its
+ * natural-log LSE partial_lse fp32 [B][Hq][S].  Slots a segment does not use
+ * get LSE -inf (their partial_o is left untouched).  Needs
+ * S >= ceil(T_max / C) + 1 for T_max the visible blocks of max_seq_len (else
+ * PKA_ERR_WORKSPACE). */
 int paged_decode_splitk(const void* q, float* partial_o, float* partial_lse,
                         const pka_kv_pool* kv, const int32_t* block_tables,
                         int32_t max_blocks, const int32_t* seq_lens, int32_t B,
@@ -182,7 +189,11 @@ int paged_decode_splitk_combine(const float* partial_o, const float* partial_lse
  * [query_start_loc[b], query_start_loc[b+1]) of q bf16 [total_q][Hq][D]; rows
  * with one token (decode) and chunks of many tokens may be mixed in one
  * launch.  Causal over cached prefix + chunk.  out bf16 [total_q][Hq][D].
- * max_query_len / max_seq_len are host upper bounds. */
+ * max_query_len / max_seq_len are host upper bounds.  query_start_loc is
+ * device data: a request whose span is not 0 <= query_start_loc[b] <=
+ * query_start_loc[b+1] <= total_q, or is longer than max_query_len, is
+ * skipped (its rows are not written) and PKA_DEVERR_QUERY_LOC is OR-ed into
+ * the error word; nothing outside out's total_q rows is ever written. */
 int paged_prefill_attn(const void* q, void* out, const pka_kv_pool* kv,
                        const int32_t* block_tables, int32_t max_blocks,
                        const int32_t* query_start_loc, const int32_t* seq_lens,
@@ -316,7 +327,10 @@ int paged_kv_append_rope(void* q, const void* k_new, const void* v_new, void* k_
  * Limit: B*Hq*S*(D+1)*4 bytes <= 16 MiB for the S paged_decode_splitk_plan
  * gives; larger calls return PKA_ERR_WORKSPACE before launching anything.
  * The first call on each device looks up the array's device address (make
- * that first call before any stream capture).  Every GPU that loads the
+ * that first call before any stream capture) and keeps it for the life of
+ * the process: after cudaDeviceReset the library's module is loaded again at
+ * another address, so a process that resets a device must not call this
+ * entry point on that device afterwards.  Every GPU that loads the
  * library holds the array until the process exits.  All calls share the one
  * array: calls that overlap on the GPU (other streams, other threads) race
  * and must be serialised by the caller. */

@@ -6,7 +6,7 @@ and this package imports nothing from the product.
 """
 from .paged_attention import (  # noqa: F401
     gather_request_kv, visible_keys, softmax_attention, paged_attention,
-    paged_decode, visible_block_range, splitk_partials, balanced_split_ranges, lse_combine,
+    paged_decode, visible_block_range, splitk_partials, lse_combine,
     run_batch,
 )
 from .brute_force import brute_force_attention  # noqa: F401

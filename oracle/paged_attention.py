@@ -32,8 +32,8 @@ Conventions where the pages are silent (each is one reading, stated once):
   it, so the partition is an input: each split covers a contiguous range of
   the request's visible blocks; its partial is the (softmax-normalised
   output, LSE) over that range and the combine is the log-sum-exp merge of
-  the partials.  ``balanced_split_ranges`` states the partition the library
-  uses, as integer arithmetic.
+  the partials.  Which partition a GPU launch uses is the library's
+  scheduling choice and is not restated here.
 """
 from __future__ import annotations
 
@@ -191,45 +191,6 @@ def splitk_partials(q, k_pool, v_pool, block_tables, seq_lens, scale, softcap,
     return po, pl
 
 
-def balanced_split_ranges(seq_lens, window, block_size, num_kv_heads, grid, min_chunk,
-                          piece_cost=4):
-    """The library's split-K work partition, as plain integer arithmetic.
-
-    Segments (request, KV head) are laid end to end on a line of work units:
-    a segment of n > 0 visible blocks takes ``piece_cost`` units (the fixed
-    cost of one more partial) followed by one unit per block, an empty one
-    none.  The ``T`` units are cut into chunks of
-    ``q = max(min_chunk, ceil(T / grid))``; the blocks of a segment whose
-    first block sits at unit ``A`` that fall inside chunk ``c`` form split
-    ``c - A // q``.  Returns ``ranges[b][kvh]`` = list of (j0, j1) per split.
-    """
-    nb = []
-    jl = []
-    for L in seq_lens:
-        j0, j1 = visible_block_range(int(L), window, block_size)
-        nb.append(j1 - j0)
-        jl.append(j0)
-    units = [n + piece_cost if n > 0 else 0 for n in nb]
-    T = num_kv_heads * sum(units)
-    q = max(min_chunk, -(-T // grid)) if T > 0 else max(min_chunk, 1)
-    out = []
-    pos = 0  # unit where the current segment starts
-    for b, n in enumerate(nb):
-        per_head = []
-        for kvh in range(num_kv_heads):
-            splits = []
-            if n > 0:
-                A = pos + piece_cost
-                for c in range(A // q, (A + n - 1) // q + 1):
-                    t0 = max(A, c * q)
-                    t1 = min(A + n, (c + 1) * q)
-                    splits.append((jl[b] + t0 - A, jl[b] + t1 - A))
-            per_head.append(splits)
-            pos += units[b]
-        out.append(per_head)
-    return out
-
-
 def lse_combine(partial_o, partial_lse):
     """Log-sum-exp merge of split partials over the split axis.
 
@@ -260,7 +221,6 @@ def run_batch(arrays):
 
 __all__ = [
     "gather_request_kv", "visible_keys", "softmax_attention", "paged_attention",
-    "paged_decode", "visible_block_range", "splitk_partials", "balanced_split_ranges",
-    "lse_combine",
+    "paged_decode", "visible_block_range", "splitk_partials", "lse_combine",
     "run_batch",
 ]

@@ -27,6 +27,7 @@ STATUS = {
 DEVERR_BAD_TABLE = 1
 DEVERR_TIMEOUT = 2
 DEVERR_SEQ_LEN = 4
+DEVERR_QUERY_LOC = 8
 
 EXPORTS = [
     "pka_version", "pka_status_string", "paged_decode_attn", "paged_decode_splitk_plan",

@@ -91,8 +91,19 @@ struct ReqGeo {
 
 __device__ __forceinline__ ReqGeo req_geo(const DecodeArgs& a, int b) {
   ReqGeo g;
-  g.skip = a.decode_rows_only != 0 &&
-           a.query_start_loc[b + 1] - a.query_start_loc[b] != 1;
+  g.skip = false;
+  if (a.query_start_loc != nullptr) {
+    // a varlen batch: the request's query row is query_start_loc[b + 1] - 1;
+    // a span outside [0, total_q] (or longer than max_query_len) is skipped
+    // and reported, so no row outside the output is ever written
+    const int lo = a.query_start_loc[b], hi = a.query_start_loc[b + 1];
+    if (lo < 0 || hi < lo || hi > a.total_q || hi - lo > a.max_query_len) {
+      report(a.err, PKA_DEVERR_QUERY_LOC);
+      g.skip = true;
+    } else {
+      g.skip = hi - lo != 1 && a.decode_rows_only != 0;
+    }
+  }
   if (g.skip) {
     g.pos = -1;
     g.t_lo = g.jlo = g.nb = 0;

@@ -4,6 +4,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "paged_attn.h"
+
 namespace pka {
 
 // Arguments of the decode kernel (direct output or split-K partials).
@@ -27,6 +29,7 @@ struct DecodeArgs {
   int32_t window;
   int32_t decode_rows_only;        // nonzero: requests whose query_start_loc span is not
                                    // one token are skipped (no output written for them)
+  int32_t total_q, max_query_len;  // with query_start_loc: rows of q / out, longest span
 };
 
 cudaError_t launch_key_mass(const float* logits, const float* lse, const int32_t* seq_lens,
@@ -119,5 +122,11 @@ struct AppendRopeArgs {
 cudaError_t launch_kv_append_rope(const AppendRopeArgs& a, int sm_count, cudaStream_t stream);
 
 int device_sm_count();
+
+// The argument checks of paged_decode_attn (host only, nothing launched):
+// PKA_OK or the pka_status the entry points return for these arguments.
+int check_decode_call(const void* q, const void* out, const pka_kv_pool* kv,
+                      const int32_t* block_tables, int32_t max_blocks, const int32_t* seq_lens,
+                      int32_t B, int32_t Hq, int32_t max_seq_len, const pka_attn_params* params);
 
 }  // namespace pka

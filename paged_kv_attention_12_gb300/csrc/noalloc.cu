@@ -18,6 +18,7 @@
 
 #include <mutex>
 
+#include "kernels.h"
 #include "paged_attn.h"
 
 namespace {
@@ -57,13 +58,15 @@ int paged_decode_attn_noalloc(const void* q, void* out, const pka_kv_pool* kv,
                               const int32_t* seq_lens, int32_t B, int32_t Hq,
                               int32_t max_seq_len, const pka_attn_params* params,
                               void* stream) {
-  if (kv == nullptr || params == nullptr || out == nullptr) return PKA_ERR_NULL;
-  if (B < 0 || Hq <= 0) return PKA_ERR_SHAPE;
+  // the same argument checks as every other decode entry point, before the
+  // empty batch returns
+  int st = pka::check_decode_call(q, out, kv, block_tables, max_blocks, seq_lens, B, Hq,
+                                  max_seq_len, params);
+  if (st != PKA_OK) return st;
   if (B == 0) return PKA_OK;
-  if (kv->num_kv_heads <= 0) return PKA_ERR_SHAPE;
   int32_t S = 0, C = 0;
-  int st = paged_decode_splitk_plan(B, kv->num_kv_heads, max_seq_len, kv->block_size,
-                                    params->window, 0, &S, &C);
+  st = paged_decode_splitk_plan(B, kv->num_kv_heads, max_seq_len, kv->block_size,
+                                params->window, 0, &S, &C);
   if (st != PKA_OK) return st;
   // partial outputs [B][Hq][S][D] first, then the LSEs [B][Hq][S]
   const size_t n_o = static_cast<size_t>(B) * Hq * S * kv->head_dim;

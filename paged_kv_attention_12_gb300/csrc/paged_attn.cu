@@ -52,8 +52,8 @@ int check_common(const void* q, const pka_kv_pool* kv, const int32_t* block_tabl
   if (B < 0 || max_blocks <= 0 || max_seq_len < 0) return PKA_ERR_SHAPE;
   if (static_cast<int64_t>(max_seq_len) > static_cast<int64_t>(max_blocks) * kv->block_size)
     return PKA_ERR_SHAPE;
-  if (!(params->scale == params->scale) || !(params->softcap == params->softcap))
-    return PKA_ERR_SHAPE;  // NaN scale or cap
+  if (!std::isfinite(params->scale) || std::isnan(params->softcap))
+    return PKA_ERR_SHAPE;  // NaN or infinite scale, NaN cap
   if (!aligned16(q)) return PKA_ERR_ALIGN;
   return PKA_OK;
 }
@@ -75,7 +75,7 @@ pka::DecodeArgs decode_args(const void* q, const pka_kv_pool* kv, const int32_t*
   a.num_blocks = kv->num_blocks;
   a.max_blocks = max_blocks;
   a.scale = p->scale;
-  a.softcap = p->softcap;
+  a.softcap = std::isinf(p->softcap) ? 0.f : p->softcap;  // an infinite cap is no cap
   a.window = p->window;
   return a;
 }
@@ -83,6 +83,16 @@ pka::DecodeArgs decode_args(const void* q, const pka_kv_pool* kv, const int32_t*
 }  // namespace
 
 namespace pka {
+
+int check_decode_call(const void* q, const void* out, const pka_kv_pool* kv,
+                      const int32_t* block_tables, int32_t max_blocks, const int32_t* seq_lens,
+                      int32_t B, int32_t Hq, int32_t max_seq_len, const pka_attn_params* params) {
+  if (out == nullptr) return PKA_ERR_NULL;
+  const int st =
+      check_common(q, kv, block_tables, max_blocks, seq_lens, B, Hq, max_seq_len, params);
+  if (st != PKA_OK) return st;
+  return aligned16(out) ? PKA_OK : PKA_ERR_ALIGN;
+}
 
 int device_sm_count() {
   int dev = 0;
@@ -107,7 +117,8 @@ const char* pka_status_string(int status) {
     case PKA_ERR_SHAPE: return "inconsistent sizes";
     case PKA_ERR_ALIGN: return "pointer not 16-byte aligned";
     case PKA_ERR_UNSUPPORTED: return "unsupported head_dim, block_size or GQA group";
-    case PKA_ERR_WORKSPACE: return "split-K partition does not cover max_seq_len";
+    case PKA_ERR_WORKSPACE:
+      return "split-K workspace too small (partials or slots for max_seq_len)";
     case PKA_ERR_BAD_TABLE: return "block table id out of range";
     case PKA_ERR_TIMEOUT: return "bounded device wait timed out";
     case PKA_ERR_CUDA: return "CUDA launch or runtime error";
@@ -334,7 +345,7 @@ pka::PrefillArgs prefill_args(const void* q, void* out, const pka_kv_pool* kv,
   a.max_query_len = max_query_len;
   a.max_seq_len = max_seq_len;
   a.scale = params->scale;
-  a.softcap = params->softcap;
+  a.softcap = std::isinf(params->softcap) ? 0.f : params->softcap;
   a.window = params->window;
   return a;
 }
@@ -403,6 +414,8 @@ int paged_prefill_attn_ws(const void* q, void* out, const pka_kv_pool* kv,
   da.out = out;
   da.query_start_loc = query_start_loc;
   da.decode_rows_only = 1;
+  da.total_q = total_q;
+  da.max_query_len = max_query_len;
   da.partial_o = reinterpret_cast<float*>(ws);
   da.partial_lse = reinterpret_cast<float*>(ws + L.o_bytes);
   da.seg_counters = reinterpret_cast<int32_t*>(ws + L.o_bytes + L.lse_bytes);

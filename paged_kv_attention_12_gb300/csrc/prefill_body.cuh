@@ -152,6 +152,17 @@ __device__ __forceinline__ float tanh_taylor(float y) {
   return fmaf(y * y2, q, y);
 }
 
+// Query rows [*q0, *q0 + n) of request b; returns n.  A request whose span
+// is not 0 <= query_start_loc[b] <= query_start_loc[b+1] <= total_q, or is
+// longer than max_query_len, gets n = -1: it has no tile and no row of it is
+// written (the first pass over the requests reports it).
+__device__ __forceinline__ int query_span(const PrefillArgs& a, int b, int* q0) {
+  const int lo = a.query_start_loc[b], hi = a.query_start_loc[b + 1];
+  *q0 = lo;
+  if (lo < 0 || hi < lo || hi > a.total_q || hi - lo > a.max_query_len) return -1;
+  return hi - lo;
+}
+
 // Cost in key tiles of query tile qt of a request with n query rows and
 // context length L (clamped to the table) (0: no query row there).
 template <int TQ, int BN>
@@ -176,7 +187,8 @@ template <int TQ, int BN>
 __device__ __forceinline__ int tile_cost(const PrefillArgs& a, const int* rn, const int* rL,
                                          int b, int qt) {
   if (rn != nullptr) return tile_cost_nl<TQ, BN>(a, rn[b], rL[b], qt);
-  const int n = a.query_start_loc[b + 1] - a.query_start_loc[b];
+  int q0;
+  const int n = query_span(a, b, &q0);
   const int L = min(a.seq_lens[b], a.max_blocks * kBlockSize);
   return tile_cost_nl<TQ, BN>(a, n, L, qt);
 }
@@ -319,7 +331,9 @@ __device__ __forceinline__ void prefill_body(const PrefillArgs& a, const CUtenso
   {
     int cnt = 0;
     for (int b = threadIdx.x; b < a.batch; b += blockDim.x) {
-      const int n = a.query_start_loc[b + 1] - a.query_start_loc[b];
+      int q0;
+      const int n = query_span(a, b, &q0);
+      if (n < 0 && rank == 0) report(a.err, PKA_DEVERR_QUERY_LOC);
       const int L = min(a.seq_lens[b], a.max_blocks * kBlockSize);
       if (cache) {
         rn[b] = n;
@@ -338,8 +352,8 @@ __device__ __forceinline__ void prefill_body(const PrefillArgs& a, const CUtenso
   it.b = pair / qtiles;
   it.kvh = rank % a.Hkv;
   const int qt = pair % qtiles;
-  it.q0 = a.query_start_loc[it.b];
-  it.n = a.query_start_loc[it.b + 1] - it.q0;
+  it.n = query_span(a, it.b, &it.q0);
+  if (it.n < 0) return;  // uniform (reported by the first pass)
   it.L = a.seq_lens[it.b];
   if (it.L > a.max_blocks * kBlockSize) {
     if (threadIdx.x == 0 && qt == 0 && it.kvh == 0) report(a.err, PKA_DEVERR_SEQ_LEN);
@@ -579,6 +593,11 @@ __device__ __forceinline__ void prefill_body(const PrefillArgs& a, const CUtenso
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(warp * 32) << 16);
     const bool capped = a.softcap > 0.f;
     const float sl2 = a.scale * kLog2e;
+    // The uncapped path masks the raw q.k and scales the row maximum, which is
+    // the maximum of the scaled logits only for scale > 0.  For scale <= 0
+    // (uniform over the launch) the logits are scaled before the mask, as the
+    // capped path does.
+    const bool prescale = capped || !(sl2 > 0.f);
     const float cap_in = capped ? a.scale / a.softcap : 0.f;
     const float cap_out = a.softcap * kLog2e;
     float m_ref = -INFINITY;
@@ -627,8 +646,11 @@ __device__ __forceinline__ void prefill_body(const PrefillArgs& a, const CUtenso
 #pragma unroll
           for (int c = 0; c < BN; ++c) s[c] = cap_out * tanh_via_exp2(s[c] * cap_in);
         }
+      } else if (prescale) {
+#pragma unroll
+        for (int c = 0; c < BN; ++c) s[c] *= sl2;
       }
-      // (uncapped: s stays raw; scale > 0, so the raw max scales to the max)
+      // (otherwise s stays raw; scale > 0, so the raw max scales to the max)
       if (need_mask) {
 #pragma unroll
         for (int c = 0; c < BN; ++c)
@@ -638,7 +660,7 @@ __device__ __forceinline__ void prefill_body(const PrefillArgs& a, const CUtenso
 #pragma unroll
       for (int c = 0; c < BN; ++c) m4[c & 3] = fmaxf(m4[c & 3], s[c]);
       float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
-      if (!capped) mx *= sl2;
+      if (!prescale) mx *= sl2;
       const float m_new = fmaxf(m_ref, mx);
       const bool resc = (j > 0) && (m_new > m_ref + 8.f);
       if (__any_sync(0xffffffffu, resc)) {
@@ -666,7 +688,7 @@ __device__ __forceinline__ void prefill_body(const PrefillArgs& a, const CUtenso
       // waited for (a commit covers every earlier MMA of the issuer).
       // p = 2^(x - ms), x the log2-domain logit (uncapped: x = s * scale * log2 e,
       // fused into one FMA)
-      const float xs = capped ? 1.f : sl2;
+      const float xs = prescale ? 1.f : sl2;
       float lsum0 = 0.f, lsum1 = 0.f;
 #pragma unroll
       for (int h = 0; h < BN / 64; ++h) {

@@ -55,9 +55,9 @@ def _pool(**kw):
 
 
 def _decode(L, q=32, out=32, pool=None, tables=64, max_blocks=4, seq=64, B=2, Hq=8,
-            max_seq_len=64, params=True):
+            max_seq_len=64, params=True, scale=0.1, softcap=0.0):
     pool = pool or _pool()
-    par = binding.PkaAttnParams(0.1, 0.0, 0, None)
+    par = binding.PkaAttnParams(scale, softcap, 0, None)
     return L.paged_decode_attn(q, out, ctypes.byref(pool), tables, max_blocks, seq, B, Hq,
                                max_seq_len, ctypes.byref(par) if params else None, None)
 
@@ -147,6 +147,41 @@ def test_mixed_workspace_argument_errors(L):
 
 def test_zero_batch_is_a_no_op(L):
     assert _decode(L, B=0) == 0
+
+
+def test_scale_and_softcap_values(L):
+    """scale: any finite value (zero and negative included); softcap: NaN is
+    refused, +inf means no cap.  Checked with B = 0, so nothing launches."""
+    inf, nan = float("inf"), float("nan")
+    for sc in (0.0, -0.5, 1e-30, 3e38):
+        assert _decode(L, B=0, scale=sc) == 0, sc
+    for sc in (inf, -inf, nan):
+        assert _decode(L, B=0, scale=sc) == -2, sc
+    assert _decode(L, B=0, softcap=inf) == 0
+    assert _decode(L, B=0, softcap=-inf) == 0
+    assert _decode(L, B=0, softcap=nan) == -2
+    pool = _pool()
+    par = binding.PkaAttnParams(inf, 0.0, 0, None)
+    assert L.paged_prefill_attn(32, 32, ctypes.byref(pool), 64, 4, 80, 64, 0, 8, 0, 5, 64,
+                                ctypes.byref(par), None) == -2
+
+
+def test_noalloc_checks_arguments_before_the_empty_batch(L):
+    """The allocation-free decode validates like every other entry point, even
+    when B = 0 makes the call a no-op."""
+    pool = _pool()
+    par = binding.PkaAttnParams(0.1, 0.0, 0, None)
+
+    def call(q=32, B=0, Hq=8, max_seq_len=64):
+        return L.paged_decode_attn_noalloc(q, 32, ctypes.byref(pool), 64, 4, 64, B, Hq,
+                                           max_seq_len, ctypes.byref(par), None)
+
+    assert call() == 0
+    assert call(q=None) == -1
+    assert call(q=40) == -3
+    assert call(Hq=6) == -4
+    assert call(max_seq_len=65) == -2
+    assert L.pka_status_string(-5).startswith(b"split-K workspace too small")
 
 
 def _append(L, k_new=32, v_new=32, k_pool=64, v_pool=64, nb=8, hkv=2, bs=16, d=128,

@@ -10,6 +10,7 @@ import torch
 import oracle
 from paged_kv_attention_12_gb300 import _build, binding, workload
 from tests.parity import assert_close, to_f64
+from tests.splitk_partition import split_ranges
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda:0"
@@ -121,8 +122,8 @@ def test_splitk_partials_match_oracle_partials(maker):
     runner.partial_lse.fill_(float("nan"))
     runner.run()
     arr = workload.to_numpy_f64(batch)
-    ranges = oracle.balanced_split_ranges(batch.seq_lens_host, batch.window, 16,
-                                          batch.num_kv_heads, decode_grid(), runner.split_blocks)
+    ranges = split_ranges(batch.seq_lens_host, batch.window, 16, batch.num_kv_heads,
+                          decode_grid(), runner.split_blocks)
     po, pl = oracle.splitk_partials(arr["q"], arr["k_pool"], arr["v_pool"], arr["block_tables"],
                                     arr["seq_lens"], batch.scale, batch.softcap, batch.window,
                                     runner.num_splits, ranges=ranges)

@@ -130,3 +130,56 @@ def test_prefill_and_mixed_paths_write_only_their_buffers():
                                   scale=batch.scale, softcap=batch.softcap, window=batch.window)
     assert g_ws.intact() and g_o2.intact(), "mixed launch wrote outside its buffers"
     assert_close(to_f64(o2), ref, "mixed")
+
+
+def _bad_offsets_cases():
+    """(name, query_start_loc, max_query_len, requests whose spans are valid)
+    for a batch of rows [0, 40), [40, 104), [104, 161), [161, 162): each case
+    breaks one or two offsets; the rest must still be served."""
+    return [
+        ("span past total_q", [0, 40, 170, 161, 162], 64, [0, 3]),
+        ("negative start", [0, -5, 104, 161, 162], 64, [2, 3]),
+        ("span longer than max_query_len", [0, 40, 104, 161, 162], 60, [0, 2, 3]),
+        ("decode row past total_q", [0, 40, 104, 170, 171], 64, [0, 1]),
+    ]
+
+
+@pytest.mark.parametrize("case", range(4))
+@pytest.mark.parametrize("path", ["single", "mixed"])
+def test_bad_query_start_loc_is_skipped_and_reported(case, path):
+    """A malformed query_start_loc (device data the host cannot check) never
+    makes a kernel write outside out: the requests with bad spans are
+    skipped, PKA_DEVERR_QUERY_LOC is reported, and every other request's rows
+    are still right."""
+    name, qsl, mql, good = _bad_offsets_cases()[case]
+    L, n = [100, 300, 57, 20], [40, 64, 57, 1]
+    batch = workload.make_batch(seq_lens=L, q_lens=n, num_q_heads=8, num_kv_heads=2,
+                                head_dim=256, num_blocks=40, cfg_id=51, seed=case,
+                                device=DEV, poison=True)
+    arr = workload.to_numpy_f64(batch, good)
+    ref, _ = oracle.run_batch(arr)
+    bad = torch.tensor(qsl, dtype=torch.int32, device=DEV)
+    g_out = Guarded(nbytes_of(batch.q), fill=0xFF)
+    out = g_out.view(torch.bfloat16, batch.q.shape)
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    if path == "single":
+        binding.paged_prefill_attn(batch.q, out, batch.k_pool, batch.v_pool, batch.block_tables,
+                                   bad, batch.seq_lens, mql, batch.max_seq_len,
+                                   scale=batch.scale, err=err)
+    else:
+        nws = binding.paged_prefill_attn_ws_bytes(4, 8, 2, 256, batch.max_seq_len)
+        g_ws = Guarded(nws, fill=0)
+        binding.paged_prefill_attn_ws(batch.q, out, batch.k_pool, batch.v_pool,
+                                      batch.block_tables, bad, batch.seq_lens, mql,
+                                      batch.max_seq_len, g_ws.view(torch.uint8, (nws,)),
+                                      scale=batch.scale, err=err)
+        assert g_ws.intact(), f"{name}: workspace canary"
+    torch.cuda.synchronize()
+    assert g_out.intact(), f"{name}: a kernel wrote outside out"
+    assert err.item() & binding.DEVERR_QUERY_LOC, f"{name}: not reported ({err.item()})"
+    assert_close(to_f64(out[arr["q_rows"]]), ref, f"{name}: valid requests")
+    # rows that belong to no valid request keep their fill
+    untouched = torch.ones(batch.q.shape[0], dtype=torch.bool)
+    untouched[list(arr["q_rows"])] = False
+    rows = out.view(torch.int16)[untouched.to(DEV)]
+    assert bool((rows == -1).all()), f"{name}: rows of a skipped request were written"

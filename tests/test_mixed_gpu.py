@@ -76,6 +76,16 @@ def test_window_and_softcap(window, softcap):
           f"W={window} cap={softcap}")
 
 
+@pytest.mark.parametrize("scale", [0.0, -0.0625])
+@pytest.mark.parametrize("softcap", [0.0, 50.0])
+def test_zero_and_negative_scale(scale, softcap):
+    """Both pipelines of the launch take any finite scale (at 0 each row is
+    the mean of the V rows it sees)."""
+    L = [1200, 700, 90, 333, 64]
+    n = [1, 1, 1, 100, 64]
+    check(small(L, n, softcap=softcap, scale=scale, seed=8), f"scale={scale} cap={softcap}")
+
+
 def test_only_decode_rows():
     L = [int(x) for x in np.random.default_rng(3).integers(1, 2000, 40)]
     check(small(L, [1] * len(L), softcap=50.0, window=256, seed=3), "decode rows only")

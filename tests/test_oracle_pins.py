@@ -77,6 +77,40 @@ def test_identical_keys_give_mean_of_v():
             assert lse[b, h] == pytest.approx(s + math.log(L[b]), rel=1e-13)
 
 
+@pytest.mark.parametrize("softcap,window", [(0.0, 0), (30.0, 0), (0.0, 5)])
+def test_zero_scale_gives_mean_of_visible_values(softcap, window):
+    """scale = 0 makes every visible logit 0 (capped or not): each query row
+    returns the plain mean of the V rows it sees, whatever q and K are."""
+    rng = np.random.default_rng(6)
+    L = [13, 29, 1]
+    n = [1, 6, 1]
+    p = problem(rng, L, n, Hq=4, Hkv=2, D=8, bs=4)
+    out, lse = run(p, 0.0, softcap, window)
+    qs = p["query_start_loc"]
+    for b in range(3):
+        _, V = contiguous_kv(p, b)
+        for i in range(n[b]):
+            pos = L[b] - n[b] + i
+            lo = 0 if window <= 0 else max(0, pos - window + 1)
+            for h in range(4):
+                np.testing.assert_allclose(out[qs[b] + i, h], V[lo:pos + 1, h // 2].mean(axis=0),
+                                           rtol=1e-12, atol=1e-14)
+                assert lse[qs[b] + i, h] == pytest.approx(math.log(pos + 1 - lo), rel=1e-13)
+
+
+@pytest.mark.parametrize("softcap", [0.0, 4.0])
+def test_negative_scale_equals_negated_queries(softcap):
+    """s = scale * q.k and the tanh cap is odd, so a negative scale is the
+    positive one applied to -q (the keys that were least aligned win)."""
+    rng = np.random.default_rng(7)
+    p = problem(rng, [21, 40], [3, 1], Hq=4, Hkv=2, D=8, bs=4)
+    out, lse = run(p, -0.4, softcap, 0)
+    neg = dict(p, q=-p["q"])
+    out2, lse2 = run(neg, 0.4, softcap, 0)
+    np.testing.assert_allclose(out, out2, rtol=1e-13, atol=1e-14)
+    np.testing.assert_allclose(lse, lse2, rtol=1e-13, atol=1e-14)
+
+
 def test_gqa_grouping_with_constant_values():
     """V of KV head j is the constant j+1: query head h must read h // G."""
     rng = np.random.default_rng(3)
@@ -374,19 +408,20 @@ def test_splitk_combine_equals_full(window):
     assert np.isneginf(pl[1, :, 1:]).all()  # L=3 -> one block
 
 
-@pytest.mark.parametrize("piece_cost", [0, 2, 5])
+@pytest.mark.parametrize("piece_units", [0, 2, 4, 5])
 @pytest.mark.parametrize("grid,min_chunk", [(1, 1), (3, 2), (7, 4), (64, 1)])
-def test_balanced_partition_covers_and_combines(grid, min_chunk, piece_cost):
-    """The library's split partition: ranges of each (request, head) are
-    disjoint, contiguous and cover exactly the visible blocks; combining the
-    partials over them gives full attention."""
-    from oracle import balanced_split_ranges
+def test_documented_partition_covers_and_combines(grid, min_chunk, piece_units):
+    """The split partition the library documents (restated in the tests'
+    helper): ranges of each (request, head) are disjoint, contiguous and
+    cover exactly the visible blocks; combining the oracle's partials over
+    them gives full attention."""
+    from tests.splitk_partition import split_ranges
     rng = np.random.default_rng(20 + grid)
     L = [57, 0, 3, 100, 16, 1]
     p = problem(rng, L, [1 if x else 0 for x in L], Hq=4, Hkv=2, D=8, bs=4)
     q = rng.standard_normal((len(L), 4, 8))
     for window in (0, 9):
-        ranges = balanced_split_ranges(L, window, 4, 2, grid, min_chunk, piece_cost)
+        ranges = split_ranges(L, window, 4, 2, grid, min_chunk, piece_units)
         S = max(len(r) for per in ranges for r in per) or 1
         # a segment's splits never outnumber ceil(n / min_chunk) + 1
         for b, per in enumerate(ranges):

@@ -71,6 +71,16 @@ def test_window_and_softcap(window, softcap):
                 seed=window), f"W={window} cap={softcap}")
 
 
+@pytest.mark.parametrize("scale", [0.0, -0.0625, -0.25])
+@pytest.mark.parametrize("softcap", [0.0, 30.0])
+def test_zero_and_negative_scale(scale, softcap):
+    """scale may be any finite number: at 0 each row is the mean of the V rows
+    it sees, below 0 the least aligned keys win; causal diagonals, a decode
+    row and a ragged chunk are in the batch."""
+    check(small([400, 130, 57, 20], [130, 1, 57, 1], D=256, Hkv=2, softcap=softcap,
+                scale=scale, seed=17), f"scale={scale} cap={softcap}")
+
+
 def test_decode_rows_in_varlen_batch():
     check(small([33, 700, 1, 16, 17], [1, 1, 1, 16, 1], D=128, Hkv=2, seed=5), "decode rows")
 
