@@ -783,6 +783,14 @@ def main():
     peak, peak_kind = hbm_peak()
     kern_avg_s = sum(kern_ms) / len(kern_ms) * 1e-3
     achieved = (bytes_step / len(calls)) / kern_avg_s / 1e9
+    # each layer's decode launch on its own (median over the steps)
+    per_launch = []
+    for i, b in enumerate(calls):
+        ms_i = statistics.median(kern_ms[i::len(calls)])
+        gbs_i = launch_bytes(b) / (ms_i * 1e-3) / 1e9
+        per_launch.append({"call": b.name or f"call {i}", "window": b.window,
+                           "bytes": launch_bytes(b), "ms": ms_i, "achieved": gbs_i,
+                           "frac": gbs_i / peak})
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
@@ -798,7 +806,7 @@ def main():
         "roofline": {"bound": "hbm", "kernel": "paged_decode_kernel" + (" (split-K, fused combine)" if args.path == "fused" else " (split-K)"),
                      "achieved": achieved, "peak": peak, "peak_kind": peak_kind,
                      "unit": "GB/s", "frac": achieved / peak,
-                     "traffic": traffic_from_profile()},
+                     "traffic": traffic_from_profile(), "per_launch": per_launch},
         "gpu_launches": args.steps * len(calls) * (1 if args.path == "fused" else 2),
         "wall_s": wall,
     }

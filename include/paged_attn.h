@@ -148,7 +148,8 @@ size_t paged_decode_splitk_workspace_bytes(int32_t B, int32_t Hq, int32_t D,
  * natural-log LSE partial_lse fp32 [B][Hq][S].  Slots a segment does not use
  * get LSE -inf (their partial_o is left untouched).  Needs
  * S >= ceil(T_max / C) + 1 for T_max the visible blocks of max_seq_len (else
- * PKA_ERR_WORKSPACE). */
+ * PKA_ERR_WORKSPACE).  The line's arithmetic is 32-bit: PKA_ERR_SHAPE if
+ * B * Hkv * (visible blocks of a table row + 4) exceeds 2^30. */
 int paged_decode_splitk(const void* q, float* partial_o, float* partial_lse,
                         const pka_kv_pool* kv, const int32_t* block_tables,
                         int32_t max_blocks, const int32_t* seq_lens, int32_t B,
@@ -161,11 +162,13 @@ int paged_decode_splitk(const void* q, float* partial_o, float* partial_lse,
  * paged_decode_splitk with the plan's (S, C); the CTA that finishes a
  * segment's last piece merges its pieces and writes out bf16 [B][Hq][D].
  * workspace: device, 16-byte aligned, at least paged_decode_attn_ws_bytes()
- * bytes: partial outputs, partial LSEs, then B*Hkv int32 arrival counters.
- * The counters must be zero before the first call (e.g. memset once at
- * allocation); every call that completes leaves them zero again.  After a
- * call that reported PKA_DEVERR_TIMEOUT, zero them before the next call.
- * Calls sharing one workspace must not overlap on the GPU. */
+ * bytes: partial outputs fp32 [B][Hq][S][D], partial LSEs [B][Hq][S] (padded
+ * to 16 bytes), then B*Hkv int32 arrival counters.  The counters must be
+ * zero before the first call (e.g. memset once at allocation); every call
+ * that completes leaves them zero again.  After a call that reported
+ * PKA_DEVERR_TIMEOUT, zero them before the next call.  Calls sharing one
+ * workspace must not overlap on the GPU.  PKA_ERR_SHAPE if
+ * B * Hkv * (visible blocks of a table row + 4) exceeds 2^30. */
 size_t paged_decode_attn_ws_bytes(int32_t B, int32_t Hq, int32_t Hkv, int32_t D,
                                   int32_t max_seq_len, int32_t window);
 int paged_decode_attn_ws(const void* q, void* out, const pka_kv_pool* kv,
@@ -209,9 +212,9 @@ int paged_prefill_attn(const void* q, void* out, const pka_kv_pool* kv,
  * filling G of the 128 rows of a tensor-core tile; requests with more tokens
  * run the tensor-core prefill pipeline.
  * workspace: device, 16-byte aligned, at least paged_prefill_attn_ws_bytes()
- * bytes (the layout of paged_decode_attn_ws for B requests); its B*Hkv int32
- * counters must be zero before the first call and are left zero by every
- * call that completes (zero them again after a PKA_DEVERR_TIMEOUT).  Calls
+ * bytes (the layout of paged_decode_attn_ws for B requests); its counters
+ * must be zero before the first call and are left zero by every call that
+ * completes (zero them again after a PKA_DEVERR_TIMEOUT).  Calls
  * sharing one workspace must not overlap on the GPU.  PKA_ERR_WORKSPACE if
  * workspace_bytes is too small. */
 size_t paged_prefill_attn_ws_bytes(int32_t B, int32_t Hq, int32_t Hkv, int32_t D,

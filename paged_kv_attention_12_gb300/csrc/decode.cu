@@ -14,7 +14,7 @@ __global__ void __launch_bounds__((NW + 1) * 32, 2)
                         const __grid_constant__ CUtensorMap tm_v) {
   extern __shared__ uint8_t smem_raw[];
   const DecodeCtx cx{static_cast<int>(blockIdx.x), static_cast<int>(gridDim.x),
-                     static_cast<int>(threadIdx.x), 0, 1};
+                     static_cast<int>(threadIdx.x), 0, 1, 2};
   decode_body<D, G, NW, NSLOT>(a, &tm_k, &tm_v, smem_raw, cx);
 }
 

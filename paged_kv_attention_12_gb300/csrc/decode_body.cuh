@@ -38,9 +38,10 @@
 //    from the swizzled tiles; the online softmax runs in the exp2 domain on
 //    the accumulator fragments with shuffles; P goes to the PV operand
 //    layout through shuffles, in bf16;
-//  * at the end of a piece the consumer warps merge their (max, sum, acc)
-//    states through shared memory and write the piece's result, while the
-//    producer already streams the next piece's tiles.
+//  * at the end of a piece warps 1..NW-1 leave their (max, sum, acc) states
+//    in shared memory and go straight on with the next piece; warp 0 merges
+//    them in registers and writes the piece's result (through shared memory,
+//    as coalesced 16-byte stores), while the producer streams on.
 //
 // Tiles with keys outside [first visible, query position] (window start,
 // ragged tail) are masked on the fragments; V rows past the sequence end
@@ -79,8 +80,15 @@ __device__ __forceinline__ void named_sync(int id, int nthreads) {
 // pipeline's (NW + 1) warps, and bar_all / bar_cons are the named barriers of
 // the whole pipeline and of its consumer warps.
 struct DecodeCtx {
-  int vcta, vgrid, tid, bar_all, bar_cons;
+  int vcta, vgrid, tid, bar_all, bar_cons, bar_merge;
 };
+
+// Arrival on named barrier `id` without waiting (the waiting side uses
+// named_sync with the same thread count).  Memory accesses before the
+// arrival are visible to the threads that complete the barrier.
+__device__ __forceinline__ void named_arrive(int id, int nthreads) {
+  asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
 
 // Visible keys of request b's decode query: positions [t_lo, pos], blocks
 // [jlo, jlo + nb).
@@ -89,9 +97,9 @@ struct ReqGeo {
   bool skip;  // not a decode row of a mixed batch: no piece, no output
 };
 
-__device__ __forceinline__ ReqGeo req_geo(const DecodeArgs& a, int b) {
-  ReqGeo g;
-  g.skip = false;
+// The request's context length after the checks below (clamped to its
+// table row), or -1 for a request the launch skips.
+__device__ __forceinline__ int req_len(const DecodeArgs& a, int b) {
   if (a.query_start_loc != nullptr) {
     // a varlen batch: the request's query row is query_start_loc[b + 1] - 1;
     // a span outside [0, total_q] (or longer than max_query_len) is skipped
@@ -99,20 +107,26 @@ __device__ __forceinline__ ReqGeo req_geo(const DecodeArgs& a, int b) {
     const int lo = a.query_start_loc[b], hi = a.query_start_loc[b + 1];
     if (lo < 0 || hi < lo || hi > a.total_q || hi - lo > a.max_query_len) {
       report(a.err, PKA_DEVERR_QUERY_LOC);
-      g.skip = true;
-    } else {
-      g.skip = hi - lo != 1 && a.decode_rows_only != 0;
+      return -1;
     }
-  }
-  if (g.skip) {
-    g.pos = -1;
-    g.t_lo = g.jlo = g.nb = 0;
-    return g;
+    if (hi - lo != 1 && a.decode_rows_only != 0) return -1;
   }
   int L = a.seq_lens[b];
   if (L > a.max_blocks * kBlockSize || L < 0) {
     report(a.err, PKA_DEVERR_SEQ_LEN);  // error path only: tables cannot hold it
     L = max(0, min(L, a.max_blocks * kBlockSize));
+  }
+  return L;
+}
+
+// Visible blocks of a request from req_len's value (no memory access).
+__device__ __forceinline__ ReqGeo geo_of_len(const DecodeArgs& a, int L) {
+  ReqGeo g;
+  g.skip = L < 0;
+  if (g.skip) {
+    g.pos = -1;
+    g.t_lo = g.jlo = g.nb = 0;
+    return g;
   }
   g.pos = L - 1;
   g.t_lo = (a.window > 0) ? max(0, g.pos - a.window + 1) : 0;
@@ -133,36 +147,48 @@ struct Piece {
   int npieces;   // split-K: pieces (slots used) of this segment
 };
 
-// Enumerates the pieces of one CTA.  Every lane of a warp runs it in
-// lockstep (it uses warp scans), and every warp of the CTA sees the same
-// sequence.
-//
-// Split mode: the segments (request, KV head) are laid end to end in a line
-// of work units, each segment taking kPieceCost units followed by one unit
-// per tile, and CTA c takes units [c q, (c+1) q).  The kPieceCost units stand
-// for the fixed cost of a piece (merging the warps' states, writing the
-// partial row): a CTA whose range starts a new segment gets that many fewer
-// tiles, so CTAs with two pieces finish with the others.  (Of 0, 2, 4 and 6
-// units, 4 gave the shortest serving and long-context decode steps: a piece
-// costs about as much as streaming four 16 KB tiles.)
+// The split-K work line.  Segments (request, KV head) are laid end to end,
+// in that order, on a line of work units: a segment with n > 0 visible tiles
+// takes kPieceCost units followed by one unit per tile, an empty one none.
+// The kPieceCost units stand for the fixed cost of a piece (merging the
+// warps' states, writing the partial row): a pipeline whose range starts a
+// new segment gets that many fewer tiles.  The T units are cut into chunks
+// of q = max(min_chunk, ceil(T / pipelines)) units, chunk c for pipeline c;
+// the piece of a segment in chunk c goes to partial slot
+// c - floor(A / q), A the unit of the segment's first tile.  All quantities
+// fit in 31 bits (checked on the host), so the arithmetic is 32-bit.
 constexpr int kPieceCost = 4;
+// Requests whose lengths a pipeline keeps in shared memory (the partition
+// scans and the walk over segments read them there instead of going back to
+// global memory, a round trip of several hundred ns each on the path to the
+// first tile); longer batches read the rest from global memory.
+constexpr int kLenCache = 128;
 
+// Enumerates the pieces of one pipeline.  Every lane of a warp runs it in
+// lockstep (it uses warp scans), and every warp of the pipeline sees the
+// same sequence.
 struct PieceIter {
   const DecodeArgs* a;
+  const int* slen;  // req_len of the first min(B, kLenCache) requests (shared memory)
   int vcta, vgrid;  // this pipeline's index and the number of pipelines
   bool direct;
   // direct mode
   int item;
-  // split mode
-  long long lo, hi, q;
-  bool last;
+  // split mode: this pipeline's chunk [lo, hi) of the work line
+  int q, lo, hi;
+  bool last;    // the chunk holding the line's last unit: also takes the
+                // empty segments at its end
   int b, kvh;
-  long long prefix;  // work units of one segment, summed over requests before b
+  int prefix;   // units of one KV head's segments of the requests before b
   ReqGeo geo;
   bool done;
 
-  __device__ void init(const DecodeArgs& args, int lane, int vcta_, int vgrid_) {
+  __device__ static int units(int nb) { return nb > 0 ? nb + kPieceCost : 0; }
+  __device__ int len_of(int bb) const { return bb < kLenCache ? slen[bb] : req_len(*a, bb); }
+
+  __device__ void init(const DecodeArgs& args, const int* slen_, int lane, int vcta_, int vgrid_) {
     a = &args;
+    slen = slen_;
     vcta = vcta_;
     vgrid = vgrid_;
     direct = args.split_blocks <= 0;
@@ -171,41 +197,38 @@ struct PieceIter {
       item = vcta;
       return;
     }
-    // total work units T = Hkv * sum_b u_b, u_b = nb_b + kPieceCost for a
-    // request with visible keys (the first 32 requests' counts stay in a
-    // register, so batches of up to 32 requests read seq_lens once)
-    auto units = [](int nb) { return nb > 0 ? nb + kPieceCost : 0; };
-    long long T = 0;
-    const int u0 = units((lane < args.batch) ? req_geo(args, lane).nb : 0);
+    // T = Hkv * sum_b units(nb_b); the units of 32 requests per step, kept
+    // per lane for the search below when the batch has at most 32 requests
+    int T = 0;
+    int u_first = 0;
     for (int base = 0; base < args.batch; base += 32) {
       const int bb = base + lane;
-      const int u = (base == 0) ? u0 : units((bb < args.batch) ? req_geo(args, bb).nb : 0);
+      const int u = units(bb < args.batch ? geo_of_len(args, len_of(bb)).nb : 0);
+      if (base == 0) u_first = u;
       T += __shfl_sync(0xffffffffu, warp_incl_scan(u, lane), 31);
     }
     T *= args.Hkv;
-    const long long grid = vgrid;
-    q = max(static_cast<long long>(args.split_blocks), (T + grid - 1) / grid);
-    const long long weff = T > 0 ? (T + q - 1) / q : 1;
-    const long long c = vcta;
-    if (c >= weff) {
+    q = max(max(args.split_blocks, 1), (T + vgrid - 1) / vgrid);
+    const int nch = T > 0 ? (T + q - 1) / q : 1;
+    if (vcta >= nch) {
       done = true;
       return;
     }
-    lo = c * q;
+    lo = vcta * q;
     hi = min(T, lo + q);
-    last = (c == weff - 1);
-    // first request holding a segment this CTA touches: the first b with
-    // Hkv*(prefix_b + u_b) + (u_b == 0) > lo
-    long long run = 0;
+    last = (vcta == nch - 1);
+    // first request holding a segment this chunk touches: the first b with
+    // Hkv * (prefix_b + u_b) + (u_b == 0) > lo
+    int run = 0;
     b = args.batch;
-    prefix = run;
+    prefix = 0;
     for (int base = 0; base < args.batch; base += 32) {
       const int bb = base + lane;
-      const int u = (base == 0) ? u0 : units((bb < args.batch) ? req_geo(args, bb).nb : 0);
+      const int u = (base == 0) ? u_first
+                                : units(bb < args.batch ? geo_of_len(args, len_of(bb)).nb : 0);
       const int incl = warp_incl_scan(u, lane);
-      const long long pre = run + incl - u;
-      const bool hit = (bb < args.batch) &&
-                       (static_cast<long long>(args.Hkv) * (pre + u) + (u == 0 ? 1 : 0) > lo);
+      const int pre = run + incl - u;
+      const bool hit = (bb < args.batch) && (args.Hkv * (pre + u) + (u == 0 ? 1 : 0) > lo);
       const unsigned m = __ballot_sync(0xffffffffu, hit);
       if (m) {
         const int first = __ffs(m) - 1;
@@ -216,10 +239,12 @@ struct PieceIter {
       run += __shfl_sync(0xffffffffu, incl, 31);
     }
     kvh = 0;
-    if (b < args.batch) geo = req_geo(args, b);
+    if (b < args.batch) geo = geo_of_len(args, len_of(b));
   }
 
-  __device__ bool next(Piece& p) {
+  // The next piece.  `slots`: also its partial slot, the segment's number of
+  // pieces and the slots to fill (the producer needs none of them).
+  __device__ bool next(Piece& p, bool slots) {
     if (done) return false;
     const DecodeArgs& A = *a;
     if (direct) {
@@ -232,7 +257,7 @@ struct PieceIter {
         }
         p.b = item / A.Hkv;
         p.kvh = item % A.Hkv;
-        g = req_geo(A, p.b);
+        g = geo_of_len(A, len_of(p.b));
         if (!g.skip) break;
         item += vgrid;
       }
@@ -251,10 +276,9 @@ struct PieceIter {
           return false;
         }
         const int n = geo.nb;
-        const int u = n > 0 ? n + kPieceCost : 0;
-        const long long seg = static_cast<long long>(A.Hkv) * prefix +
-                              static_cast<long long>(kvh) * u;  // segment start
-        const long long s0 = seg + (n > 0 ? kPieceCost : 0);  // unit of its first tile
+        const int u = units(n);
+        const int seg = A.Hkv * prefix + kvh * u;       // segment start
+        const int s0 = seg + (n > 0 ? kPieceCost : 0);  // unit of its first tile
         const bool before = (n > 0 ? s0 + n : seg + 1) <= lo;  // wholly before this chunk
         const bool after = !last && seg >= hi;
         if (after) {
@@ -268,28 +292,27 @@ struct PieceIter {
           kvh = 0;
           prefix += u;
           ++b;
-          if (b < A.batch) geo = req_geo(A, b);
+          if (b < A.batch) geo = geo_of_len(A, len_of(b));
         }
         if (before || g.skip) continue;
-        const long long t0 = max(s0, lo);
-        const long long t1 = min(s0 + n, hi);
+        const int t0 = max(s0, lo);
+        const int t1 = min(s0 + n, hi);
         p.b = cur_b;
         p.kvh = cur_kvh;
-        p.j0 = g.jlo + static_cast<int>(t0 - s0);
-        p.ntiles = static_cast<int>(max(0LL, t1 - t0));
+        p.j0 = g.jlo + (t0 - s0);
+        p.ntiles = max(0, t1 - t0);
         p.t_lo = g.t_lo;
         p.pos = g.pos;
-        // slots: the CTA holding the first tile writes slot 0; a CTA whose
-        // range holds only the segment's piece-cost units gets a negative
-        // slot and no piece
-        const long long cfirst = s0 / q;
-        p.slot = static_cast<int>(static_cast<long long>(vcta) - cfirst);
-        p.fill_from = -1;
-        p.npieces = (n == 0) ? 0 : static_cast<int>((s0 + n - 1) / q - cfirst + 1);
-        if (n == 0) {
-          p.fill_from = 0;
-        } else if (p.slot == 0) {
-          p.fill_from = p.npieces;
+        p.slot = 0;
+        p.npieces = 0;
+        p.fill_from = (n == 0) ? 0 : -1;
+        if (n > 0 && slots) {
+          // the chunk holding the first tile writes slot 0; a chunk whose
+          // range holds only the segment's piece-cost units has no piece
+          const int cfirst = s0 / q;
+          p.slot = vcta - cfirst;
+          p.npieces = (s0 + n - 1) / q - cfirst + 1;
+          if (p.slot == 0) p.fill_from = p.npieces;
         }
         if (p.ntiles == 0 && p.fill_from < 0) continue;
         break;
@@ -342,15 +365,26 @@ struct DecodeShape {
   static constexpr int KSTEPS = D / 16;                    // k-steps of S = K q^T
   static constexpr int MTILES = D / 16;                    // 16-row tiles of O^T = V^T P^T
   static constexpr int kRingBytes = NSLOT * 2 * kTileBytes;
-  static constexpr int kBarBytes = (2 * NSLOT * 8 + 15) / 16 * 16;
-  static constexpr int kMergeMLFloats = (2 * NW * G + 3) / 4 * 4;
-  static constexpr int kMergeBytes = (kMergeMLFloats + NW * G * D) * 4;
+  static constexpr int kBarBytes = (2 * NSLOT * 8 + 8 + 15) / 16 * 16;  // + staging_free
+  // piece epilogue: warps 1..NW-1 leave their accumulator fragments (the
+  // lanes whose columns are query heads: t < TG) and their (max, sum) here
+  // for warp 0, which merges them in registers
+  static constexpr int TG = (G + 1) / 2;
+  static constexpr int kStageFrags = (NW - 1) * (D / 16) * 8 * TG;  // float4 each
+  static constexpr int kStageML = (NW - 1) * TG;                      // float4 each
+  static constexpr int kMergeBytes = (kStageFrags + kStageML) * 16;
   // fused combine: up to kMaxPend pieces whose arrival is deferred to the
   // end of the CTA's work, 4 ints each, and one "last piece" flag per entry
   static constexpr int kMaxPend = 4;
   static constexpr int kPendBytes = kMaxPend * 5 * 4;
+  // the lengths of the first kLenCache requests
+  static constexpr int kLenBytes = kLenCache * 4;
+  // a piece's result on its way out: G rows of D fp32 (bulk-copied to the
+  // partials, or converted to bf16 in place for a direct output)
+  static constexpr int kOutBytes = G * D * 4;
   // + 1 KiB so the ring can start on a 1024-byte boundary (128B swizzle)
-  static constexpr int kSmemBytes = 1024 + kRingBytes + kBarBytes + kMergeBytes + kPendBytes;
+  static constexpr int kSmemBytes =
+      1024 + kRingBytes + kBarBytes + kMergeBytes + kPendBytes + kLenBytes + kOutBytes;
   static_assert(G >= 1 && G <= 8, "the query heads of a group are the MMA's N = 8 columns");
   static_assert(kSmemBytes <= 232448 / 2 - 1024, "two CTAs per SM");
   static_assert(NSLOT % NW == 0, "each ring slot must have exactly one owner warp");
@@ -495,28 +529,32 @@ __device__ __forceinline__ void decode_body(const DecodeArgs& a, const CUtensorM
   uint8_t* ring = smem;
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + S::kRingBytes);
   uint64_t* empty = full + NSLOT;
-  float* merge = reinterpret_cast<float*>(smem + S::kRingBytes + S::kBarBytes);
-  float* mrg_m = merge;                        // [NW][G]
-  float* mrg_l = merge + NW * G;               // [NW][G]
-  float* mrg_acc = merge + S::kMergeMLFloats;  // [NW][G][D]
+  uint64_t* staging_free = empty + NSLOT;  // warp 0 has read the staging area
+  float4* stage = reinterpret_cast<float4*>(smem + S::kRingBytes + S::kBarBytes);
+  float4* stage_ml = stage + S::kStageFrags;  // [NW-1][TG]: (m0, m1, l0, l1)
   int* pend = reinterpret_cast<int*>(smem + S::kRingBytes + S::kBarBytes + S::kMergeBytes);
   volatile int* pend_last = pend + S::kMaxPend * 4;  // [kMaxPend]
   int npend = 0;  // the same in every consumer thread
+  int* slen = reinterpret_cast<int*>(smem + S::kRingBytes + S::kBarBytes + S::kMergeBytes +
+                                     S::kPendBytes);  // [kLenCache]
+  float* orow = reinterpret_cast<float*>(smem + S::kRingBytes + S::kBarBytes + S::kMergeBytes +
+                                         S::kPendBytes + S::kLenBytes);  // [G][D]
 
   const int warp = cx.tid / 32;
   const int lane = cx.tid % 32;
 
-  if (cx.tid == 0) {
-    for (int i = 0; i < NSLOT; ++i) {
-      mbar_init(&full[i], 1);
-      mbar_init(&empty[i], 1);
-    }
+  if (warp == NW) {
+    // the producer warp sets up the barriers (one lane each) and reads the
+    // requests' lengths into shared memory for the whole pipeline
+    for (int i = lane; i < 2 * NSLOT + 1; i += 32) mbar_init(full + i, 1);
     mbar_fence_init();
+    const int ncache = min(a.batch, kLenCache);
+    for (int bb = lane; bb < ncache; bb += 32) slen[bb] = req_len(a, bb);
   }
   named_sync(cx.bar_all, (NW + 1) * 32);
 
   PieceIter iter;
-  iter.init(a, lane, cx.vcta, cx.vgrid);
+  iter.init(a, slen, lane, cx.vcta, cx.vgrid);
   Piece pc;
 
   if (warp == NW) {
@@ -526,9 +564,9 @@ __device__ __forceinline__ void decode_body(const DecodeArgs& a, const CUtensorM
       prefetch_tensormap(tm_v);
     }
     const uint32_t oob_row = static_cast<uint32_t>(a.num_blocks) * a.Hkv * kBlockSize;
-    long long issued = 0;
+    int issued = 0;
     bool ok = true;
-    while (ok && iter.next(pc)) {
+    while (ok && iter.next(pc, false)) {
       const int32_t* trow = a.tables + static_cast<size_t>(pc.b) * a.max_blocks + pc.j0;
       for (int base = 0; base < pc.ntiles && ok; base += 32) {
         uint32_t row = oob_row;  // a bad id reads zeros (reported) instead of faulting
@@ -542,8 +580,8 @@ __device__ __forceinline__ void decode_body(const DecodeArgs& a, const CUtensorM
         const int cnt = min(32, pc.ntiles - base);
         for (int k = 0; k < cnt; ++k) {
           const uint32_t r0 = __shfl_sync(0xffffffffu, row, k);
-          const int slot = static_cast<int>(issued % NSLOT);
-          const long long round = issued / NSLOT;
+          const int slot = issued % NSLOT;
+          const int round = issued / NSLOT;
           int good = 1;
           if (lane == 0) {
             if (round > 0)
@@ -569,8 +607,8 @@ __device__ __forceinline__ void decode_body(const DecodeArgs& a, const CUtensorM
     }
     // Every issued copy must have landed before the CTA may exit.
     if (lane == 0) {
-      const long long first = issued > NSLOT ? issued - NSLOT : 0;
-      for (long long i = first; i < issued; ++i)
+      const int first = issued > NSLOT ? issued - NSLOT : 0;
+      for (int i = first; i < issued; ++i)
         mbar_wait(&full[i % NSLOT], static_cast<uint32_t>((i / NSLOT) & 1), a.err);
     }
     return;
@@ -580,11 +618,12 @@ __device__ __forceinline__ void decode_body(const DecodeArgs& a, const CUtensorM
   const int g = lane >> 2, t = lane & 3;
   const float inv_cap = a.softcap > 0.f ? 1.f / a.softcap : 0.f;
   const float qscale = a.scale * (a.softcap > 0.f ? 1.f : kLog2e);
-  long long tile_base = 0;
+  int tile_base = 0;
+  int nmerge = 0;  // pieces merged so far (phases of staging_free)
   bool ok = true;
 
   // q^T as B fragments: head g (zero for g >= G), elements 2t, 2t+1 (+8) of
-  // every k-step.  The next piece's fragments are loaded during the merge.
+  // every k-step.
   auto load_q = [&](const Piece& P, uint32_t (&bq)[D / 16][2]) {
     const uint32_t* qp = reinterpret_cast<const uint32_t*>(
         a.q + (static_cast<size_t>(P.qrow) * a.Hq + P.kvh * G + (g < G ? g : 0)) * D);
@@ -600,6 +639,7 @@ __device__ __forceinline__ void decode_body(const DecodeArgs& a, const CUtensorM
   auto flush_pending = [&]() {
     named_sync(cx.bar_cons, NW * 32);  // the pieces' partials and pend[] written
     if (cx.tid == 0) {
+      bulk_wait_all();      // this thread's bulk copies of the partials have completed
       fence_acq_rel_gpu();  // the CTA's partials (ordered by the barrier) before its arrivals
       int old[S::kMaxPend];
 #pragma unroll
@@ -662,7 +702,7 @@ __device__ __forceinline__ void decode_body(const DecodeArgs& a, const CUtensorM
   };
 
   uint32_t bq[D / 16][2];
-  bool have = iter.next(pc);
+  bool have = iter.next(pc, true);
   if (have) load_q(pc, bq);
   while (have) {
     float o[D / 16][4];
@@ -671,18 +711,33 @@ __device__ __forceinline__ void decode_body(const DecodeArgs& a, const CUtensorM
     float m[2] = {-INFINITY, -INFINITY};
     float l[2] = {0.f, 0.f};
 
-    // Tile T of the CTA's stream lives in slot T % NSLOT and belongs to warp
-    // T % NW; NSLOT is a multiple of NW, so every slot has one owner warp that
-    // consumes its phases in order (a phase-parity wait can never alias an
-    // older phase of the same slot).
-    const int i0 = static_cast<int>((warp - tile_base % NW + NW) % NW);
+    // Tile T of the pipeline's stream lives in slot T % NSLOT and belongs to
+    // warp T % NW; NSLOT is a multiple of NW, so every slot has one owner warp
+    // that consumes its phases in order (a phase-parity wait can never alias
+    // an older phase of the same slot), even when warps 1..NW-1 run ahead into
+    // the next piece while warp 0 merges.  Warp w takes the piece's tiles
+    // i = res (mod NW), res = (w - tile_base) mod NW; the merge adds the
+    // warps' states in the order of res, so a piece gives the same bits
+    // wherever in the stream it falls.
+    const int rho = tile_base % NW;
+    const int i0 = (warp - rho + NW) % NW;
     float* lg = (a.logits == nullptr)
                     ? nullptr
                     : a.logits + (static_cast<size_t>(pc.b) * a.Hq + pc.kvh * G) *
                                      (static_cast<size_t>(a.max_blocks) * kBlockSize);
+    // ---- split-K: slots of this segment no pipeline fills get LSE = -inf,
+    // written at the start of the piece by the last consumer warp (hidden
+    // behind the wait for the piece's first tiles)
+    if (a.split_blocks > 0 && a.seg_counters == nullptr && pc.fill_from >= 0 && warp == NW - 1) {
+      if (pc.fill_from > a.num_splits && lane == 0) report(a.err, PKA_DEVERR_SEQ_LEN);
+      for (int h = 0; h < G; ++h)
+        for (int sl = pc.fill_from + lane; sl < a.num_splits; sl += 32)
+          a.partial_lse[(static_cast<size_t>(pc.b) * a.Hq + pc.kvh * G + h) * a.num_splits + sl] =
+              -INFINITY;
+    }
     for (int i = i0; i < pc.ntiles && ok; i += NW) {
-      const long long T = tile_base + i;
-      const int slot = static_cast<int>(T % NSLOT);
+      const int T = tile_base + i;
+      const int slot = T % NSLOT;
       const bool got = mbar_wait(&full[slot], static_cast<uint32_t>((T / NSLOT) & 1), a.err);
       if (!__all_sync(0xffffffffu, got)) {
         ok = false;
@@ -700,94 +755,165 @@ __device__ __forceinline__ void decode_body(const DecodeArgs& a, const CUtensorM
     tile_base += pc.ntiles;
 
     Piece nx;
-    const bool have_next = iter.next(nx);
-    if (have_next) load_q(nx, bq);
+    const bool have_next = iter.next(nx, true);
 
     const bool split = a.split_blocks > 0;
+    const bool fused = split && a.seg_counters != nullptr;
     if (pc.ntiles > 0) {
       // ---- per-warp totals: sums over the 8 key rows held by lanes g
 #pragma unroll
       for (int j = 0; j < 2; ++j)
 #pragma unroll
         for (int off = 4; off < 32; off <<= 1) l[j] += __shfl_xor_sync(0xffffffffu, l[j], off);
-      if (g == 0) {
+      if (warp != 0) {
+        // ---- leave this warp's state for warp 0 and go on with the next
+        // piece at once: the ring keeps flowing while warp 0 merges
+        if (nmerge > 0 && ok) {
+          const bool got = mbar_wait(staging_free, static_cast<uint32_t>((nmerge - 1) & 1), a.err);
+          if (!__all_sync(0xffffffffu, got)) ok = false;
+        }
+        if (t < S::TG) {
+          float4* st = stage + ((warp - 1) * (D / 16)) * 8 * S::TG + g * S::TG + t;
 #pragma unroll
-        for (int j = 0; j < 2; ++j) {
-          const int h = 2 * t + j;
-          if (h < G) {
-            mrg_m[warp * G + h] = m[j];
-            mrg_l[warp * G + h] = l[j];
+          for (int mt = 0; mt < D / 16; ++mt)
+            st[mt * 8 * S::TG] = make_float4(o[mt][0], o[mt][1], o[mt][2], o[mt][3]);
+          if (g == 0) stage_ml[(warp - 1) * S::TG + t] = make_float4(m[0], m[1], l[0], l[1]);
+        }
+        named_arrive(cx.bar_merge, NW * 32);
+      } else {
+        // ---- warp 0: merge the other warps' states into its registers
+        named_sync(cx.bar_merge, NW * 32);
+        if (t < S::TG) {
+          // the warps' (m0, m1, l0, l1); warp 0's own are in its registers
+          const float4 own_ml = make_float4(m[0], m[1], l[0], l[1]);
+          float M0 = m[0], M1 = m[1];
+#pragma unroll
+          for (int w = 1; w < NW; ++w) {
+            const float4 x = stage_ml[(w - 1) * S::TG + t];
+            M0 = fmaxf(M0, x.x);
+            M1 = fmaxf(M1, x.y);
+          }
+          const float Ms0 = (M0 == -INFINITY) ? 0.f : M0;
+          const float Ms1 = (M1 == -INFINITY) ? 0.f : M1;
+          // residue r's state (warp (r + rho) % NW) is scaled by sc[r]
+          float sc[NW][2];
+          float den0 = 0.f, den1 = 0.f;
+#pragma unroll
+          for (int r = 0; r < NW; ++r) {
+            const int w = (r + rho) % NW;
+            const float4 x = (w == 0) ? own_ml : stage_ml[(w - 1) * S::TG + t];
+            sc[r][0] = fast_exp2(x.x - Ms0);
+            sc[r][1] = fast_exp2(x.y - Ms1);
+            den0 = (r == 0) ? sc[r][0] * x.z : fmaf(sc[r][0], x.z, den0);
+            den1 = (r == 0) ? sc[r][1] * x.w : fmaf(sc[r][1], x.w, den1);
+          }
+          m[0] = M0;
+          m[1] = M1;
+          l[0] = den0;
+          l[1] = den1;
+#pragma unroll
+          for (int mt = 0; mt < D / 16; ++mt) {
+            const float4 own = make_float4(o[mt][0], o[mt][1], o[mt][2], o[mt][3]);
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+            for (int r = 0; r < NW; ++r) {
+              const int w = (r + rho) % NW;
+              const float4 x =
+                  (w == 0) ? own : stage[(((w - 1) * (D / 16) + mt) * 8 + g) * S::TG + t];
+              if (r == 0) {
+                acc = make_float4(sc[0][0] * x.x, sc[0][1] * x.y, sc[0][0] * x.z, sc[0][1] * x.w);
+              } else {
+                acc.x = fmaf(sc[r][0], x.x, acc.x);
+                acc.y = fmaf(sc[r][1], x.y, acc.y);
+                acc.z = fmaf(sc[r][0], x.z, acc.z);
+                acc.w = fmaf(sc[r][1], x.w, acc.w);
+              }
+            }
+            o[mt][0] = acc.x;
+            o[mt][1] = acc.y;
+            o[mt][2] = acc.z;
+            o[mt][3] = acc.w;
           }
         }
-      }
-#pragma unroll
-      for (int mt = 0; mt < D / 16; ++mt)
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const int h = 2 * t + (i & 1);
-          const int d = mt * 16 + g + ((i & 2) ? 8 : 0);
-          if (h < G) mrg_acc[(warp * G + h) * D + d] = o[mt][i];
-        }
-      named_sync(cx.bar_cons, NW * 32);
-
-      // ---- merge the warps' states and write this piece's result, four
-      // consecutive columns of one head per thread (vector loads and stores,
-      // the heads' scale factors taken once per four columns)
-      for (int idx = cx.tid; idx < G * (D / 4); idx += NW * 32) {
-        const int h = idx / (D / 4);
-        const int d = (idx % (D / 4)) * 4;
-        float M = -INFINITY;
-#pragma unroll
-        for (int w = 0; w < NW; ++w) M = fmaxf(M, mrg_m[w * G + h]);
-        const float Ms = (M == -INFINITY) ? 0.f : M;
-        float den = 0.f;
-        float4 num = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-        for (int w = 0; w < NW; ++w) {
-          const float sc = fast_exp2(mrg_m[w * G + h] - Ms);
-          den = fmaf(sc, mrg_l[w * G + h], den);
-          const float4 v = *reinterpret_cast<const float4*>(&mrg_acc[(w * G + h) * D + d]);
-          num.x = fmaf(sc, v.x, num.x);
-          num.y = fmaf(sc, v.y, num.y);
-          num.z = fmaf(sc, v.z, num.z);
-          num.w = fmaf(sc, v.w, num.w);
-        }
-        const float inv = (den > 0.f) ? 1.f / den : 0.f;
-        const float4 ov = make_float4(num.x * inv, num.y * inv, num.z * inv, num.w * inv);
-        const int hq = pc.kvh * G + h;
+        // the staging area may be refilled (its reads are done)
+        __syncwarp();
+        if (lane == 0) mbar_arrive(staging_free);
+        // ---- this piece's result: each head's normalised row into the output
+        // buffer (once the previous piece's bulk copies have read it), then
+        // out through the async proxy: warp 0 does not wait for the copies to
+        // reach memory behind the K/V stream
+        if (lane == 0) bulk_wait_read_all();
+        __syncwarp();
+        const float inv0 = l[0] > 0.f ? 1.f / l[0] : 0.f;
+        const float inv1 = l[1] > 0.f ? 1.f / l[1] : 0.f;
+        const int h0 = 2 * t, h1 = 2 * t + 1;
         if (split) {
+          if (t < S::TG) {
+#pragma unroll
+            for (int mt = 0; mt < D / 16; ++mt) {
+              orow[h0 * D + mt * 16 + g] = o[mt][0] * inv0;
+              orow[h0 * D + mt * 16 + g + 8] = o[mt][2] * inv0;
+              if (h1 < G) {
+                orow[h1 * D + mt * 16 + g] = o[mt][1] * inv1;
+                orow[h1 * D + mt * 16 + g + 8] = o[mt][3] * inv1;
+              }
+            }
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
           if (pc.slot < a.num_splits) {
-            const size_t ph = (static_cast<size_t>(pc.b) * a.Hq + hq) * a.num_splits + pc.slot;
-            *reinterpret_cast<float4*>(a.partial_o + ph * D + d) = ov;
-            if (d == 0) a.partial_lse[ph] = (den > 0.f) ? (M + log2f(den)) * kLn2 : -INFINITY;
+            const size_t r0 = (static_cast<size_t>(pc.b) * a.Hq + pc.kvh * G) * a.num_splits +
+                              pc.slot;  // row of head 0 of the group
+            if (lane == 0) {
+#pragma unroll
+              for (int h = 0; h < G; ++h)
+                bulk_s2g(a.partial_o + (r0 + static_cast<size_t>(h) * a.num_splits) * D,
+                         orow + h * D, D * 4);
+              bulk_commit();
+            }
+            if (t < S::TG && g == 0) {
+              a.partial_lse[r0 + static_cast<size_t>(h0) * a.num_splits] =
+                  l[0] > 0.f ? (m[0] + log2f(l[0])) * kLn2 : -INFINITY;
+              if (h1 < G)
+                a.partial_lse[r0 + static_cast<size_t>(h1) * a.num_splits] =
+                    l[1] > 0.f ? (m[1] + log2f(l[1])) * kLn2 : -INFINITY;
+            }
           }
         } else {
-          uint16_t* dst =
-              reinterpret_cast<uint16_t*>(a.out) + (static_cast<size_t>(pc.qrow) * a.Hq + hq) * D + d;
-          *reinterpret_cast<uint2*>(dst) =
-              make_uint2(pack_bf16x2(ov.x, ov.y), pack_bf16x2(ov.z, ov.w));
+          // bf16 rows of the G heads, contiguous in out
+          uint16_t* ob16 = reinterpret_cast<uint16_t*>(orow);
+          if (t < S::TG) {
+#pragma unroll
+            for (int mt = 0; mt < D / 16; ++mt) {
+              ob16[h0 * D + mt * 16 + g] = f32_to_bf16_rn(o[mt][0] * inv0);
+              ob16[h0 * D + mt * 16 + g + 8] = f32_to_bf16_rn(o[mt][2] * inv0);
+              if (h1 < G) {
+                ob16[h1 * D + mt * 16 + g] = f32_to_bf16_rn(o[mt][1] * inv1);
+                ob16[h1 * D + mt * 16 + g + 8] = f32_to_bf16_rn(o[mt][3] * inv1);
+              }
+            }
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            bulk_s2g(reinterpret_cast<uint16_t*>(a.out) +
+                         (static_cast<size_t>(pc.qrow) * a.Hq + pc.kvh * G) * D,
+                     ob16, G * D * 2);
+            bulk_commit();
+          }
         }
       }
-      named_sync(cx.bar_cons, NW * 32);
-    } else if (!split) {
+      ++nmerge;
+    } else if (!split && warp == 0) {
       // a request with no visible key: output 0
-      for (int idx = cx.tid; idx < G * D; idx += NW * 32) {
+      for (int idx = lane; idx < G * D; idx += 32) {
         const int hq = pc.kvh * G + idx / D;
         reinterpret_cast<uint16_t*>(a.out)[(static_cast<size_t>(pc.qrow) * a.Hq + hq) * D +
                                            idx % D] = 0;
       }
     }
-    const bool fused = split && a.seg_counters != nullptr;
-    // ---- split-K: slots of this segment no CTA fills get LSE = -inf
-    if (split && !fused && pc.fill_from >= 0) {
-      if (pc.fill_from > a.num_splits && cx.tid == 0) report(a.err, PKA_DEVERR_SEQ_LEN);
-      const int nfill = a.num_splits - min(pc.fill_from, a.num_splits);
-      for (int idx = cx.tid; idx < G * nfill; idx += NW * 32) {
-        const int hq = pc.kvh * G + idx / nfill;
-        const int sl = pc.fill_from + idx % nfill;
-        a.partial_lse[(static_cast<size_t>(pc.b) * a.Hq + hq) * a.num_splits + sl] = -INFINITY;
-      }
-    }
+    // the next piece's q (after the merge, which needs the registers)
+    if (have_next) load_q(nx, bq);
     // ---- fused LSE combine: a piece's arrival on its segment's counter is
     // deferred to the end of the CTA's work (or until kMaxPend pieces are
     // pending), so that a CTA with several pieces never stalls between them
@@ -804,9 +930,9 @@ __device__ __forceinline__ void decode_body(const DecodeArgs& a, const CUtensorM
           pend[npend * 4 + 3] = pc.qrow;
         }
         ++npend;
-      } else if (pc.ntiles == 0 && pc.fill_from == 0) {
+      } else if (pc.ntiles == 0 && pc.fill_from == 0 && warp == 0) {
         // a request with no visible key: output 0
-        for (int idx = cx.tid; idx < G * D; idx += NW * 32) {
+        for (int idx = lane; idx < G * D; idx += 32) {
           const int hq = pc.kvh * G + idx / D;
           reinterpret_cast<uint16_t*>(a.out)[(static_cast<size_t>(pc.qrow) * a.Hq + hq) * D +
                                              idx % D] = 0;
@@ -820,6 +946,8 @@ __device__ __forceinline__ void decode_body(const DecodeArgs& a, const CUtensorM
     pc = nx;
     have = have_next;
   }
+  // the bulk copies of the last results complete before the pipeline ends
+  if (warp == 0 && lane == 0) bulk_wait_all();
 }
 
 }  // namespace pka

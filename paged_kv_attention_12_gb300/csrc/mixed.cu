@@ -59,9 +59,10 @@ __global__ void __launch_bounds__(PrefillShape<D, G>::kThreads, 1)
   }
   using T = MixedDecodeTuning<D, G>;
   const int pipe = static_cast<int>(threadIdx.x) / T::kPipeThreads;  // 0 or 1
-  // named barriers 1, 2 (pipeline 0) and 3, 4 (pipeline 1)
+  // named barriers 1, 2, 5 (pipeline 0) and 3, 4, 6 (pipeline 1)
   const DecodeCtx cx{static_cast<int>(blockIdx.x) * 2 + pipe, n_decode * 2,
-                     static_cast<int>(threadIdx.x) % T::kPipeThreads, 1 + 2 * pipe, 2 + 2 * pipe};
+                     static_cast<int>(threadIdx.x) % T::kPipeThreads, 1 + 2 * pipe, 2 + 2 * pipe,
+                     5 + pipe};
   decode_body<D, G, T::NW, T::NSLOT>(da, &tm_k_tiles, &tm_v_tiles,
                                      smem_raw + pipe * T::kPipeBytes, cx);
 }

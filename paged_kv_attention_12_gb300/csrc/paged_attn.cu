@@ -6,6 +6,7 @@
 // word.  Nothing here allocates or synchronises.
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cmath>
 #include <stdint.h>
 
@@ -29,6 +30,17 @@ int max_visible_blocks(int max_seq_len, int window, int bs) {
   if (window <= 0) return full;
   const int win = (window - 1) / bs + 2;
   return full < win ? full : win;
+}
+
+// The split-K work line (Hkv * sum over requests of (visible blocks + 4)
+// units) fits in 31 bits with room to spare, so the kernels' partition
+// arithmetic is 32-bit.
+// (The kernels clamp a sequence to its table row, so a row's max_blocks
+// bounds its visible blocks whatever the device lengths are.)
+bool line_fits(int32_t B, int32_t Hkv, int32_t max_blocks, int32_t window) {
+  int64_t per = max_blocks;
+  if (window > 0) per = std::min<int64_t>(per, (window - 1) / 16 + 2);
+  return static_cast<int64_t>(B) * Hkv * (per + 4) <= (int64_t(1) << 30);
 }
 
 int check_pool(const pka_kv_pool* kv, int Hq) {
@@ -199,6 +211,7 @@ int splitk_impl(const void* q, float* partial_o, float* partial_lse, float* logi
   a.split_blocks = split_blocks;
   a.logits = logits;
   if (static_cast<int64_t>(B) * Hq * num_splits > 0x7fffffffLL) return PKA_ERR_SHAPE;
+  if (!line_fits(B, kv->num_kv_heads, max_blocks, params->window)) return PKA_ERR_SHAPE;
   const int sms = pka::device_sm_count();
   if (sms <= 0) return PKA_ERR_CUDA;
   // persistent: one CTA per SM, each streaming an equal share of the tiles
@@ -251,6 +264,7 @@ int paged_decode_key_mass(const float* logits, const float* lse, const int32_t* 
 struct FusedLayout {
   int32_t S, C;
   size_t o_bytes, lse_bytes, cnt_bytes;
+  size_t total() const { return o_bytes + lse_bytes + cnt_bytes; }
 };
 
 int fused_layout(int32_t B, int32_t Hq, int32_t Hkv, int32_t D, int32_t max_seq_len,
@@ -268,7 +282,7 @@ size_t paged_decode_attn_ws_bytes(int32_t B, int32_t Hq, int32_t Hkv, int32_t D,
   if (B <= 0 || Hq <= 0 || Hkv <= 0 || D <= 0) return 0;
   FusedLayout L;
   if (fused_layout(B, Hq, Hkv, D, max_seq_len, window, &L) != PKA_OK) return 0;
-  return L.o_bytes + L.lse_bytes + L.cnt_bytes;
+  return L.total();
 }
 
 int paged_decode_attn_ws(const void* q, void* out, const pka_kv_pool* kv,
@@ -284,7 +298,8 @@ int paged_decode_attn_ws(const void* q, void* out, const pka_kv_pool* kv,
   FusedLayout L;
   st = fused_layout(B, Hq, kv->num_kv_heads, kv->head_dim, max_seq_len, params->window, &L);
   if (st != PKA_OK) return st;
-  if (workspace_bytes < L.o_bytes + L.lse_bytes + L.cnt_bytes) return PKA_ERR_WORKSPACE;
+  if (workspace_bytes < L.total()) return PKA_ERR_WORKSPACE;
+  if (!line_fits(B, kv->num_kv_heads, max_blocks, params->window)) return PKA_ERR_SHAPE;
   pka::DecodeArgs a = decode_args(q, kv, block_tables, max_blocks, seq_lens, B, Hq, params);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   a.out = out;
@@ -405,7 +420,8 @@ int paged_prefill_attn_ws(const void* q, void* out, const pka_kv_pool* kv,
   FusedLayout L;
   st = fused_layout(B, Hq, Hkv, D, max_seq_len, params->window, &L);
   if (st != PKA_OK) return st;
-  if (workspace_bytes < L.o_bytes + L.lse_bytes + L.cnt_bytes) return PKA_ERR_WORKSPACE;
+  if (workspace_bytes < L.total()) return PKA_ERR_WORKSPACE;
+  if (!line_fits(B, Hkv, max_blocks, params->window)) return PKA_ERR_SHAPE;
   pka::PrefillArgs pa = prefill_args(q, out, kv, block_tables, max_blocks, query_start_loc,
                                      seq_lens, B, Hq, total_q, max_query_len, max_seq_len, params);
   pa.skip_decode_rows = 1;

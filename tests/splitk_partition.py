@@ -51,3 +51,4 @@ def split_ranges(seq_lens, window, block_size, num_kv_heads, grid, min_chunk,
             start += u
         ranges.append(per_head)
     return ranges
+

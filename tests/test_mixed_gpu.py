@@ -20,11 +20,13 @@ def built():
 
 
 def counters(runner):
+    """Arrival counters of the workspace (the fused decode's layout)."""
     b = runner.batch
     S, _ = binding.paged_decode_splitk_plan(b.num_requests, b.num_kv_heads, b.max_seq_len, 16,
                                             b.window)
     B, Hq, D, Hkv = b.num_requests, b.num_q_heads, b.head_dim, b.num_kv_heads
     off = B * Hq * S * D * 4 + (B * Hq * S * 4 + 15) // 16 * 16
+    assert runner.workspace.numel() == off + (B * Hkv * 4 + 15) // 16 * 16
     return runner.workspace[off:off + B * Hkv * 4].view(torch.int32)
 
 
