@@ -718,26 +718,38 @@ def main():
                 "l2": "512 MiB write only before every step (its dirty lines are written "
                       "back during the step)"}
 
-    # the dominant kernel alone: each decode launch (one CUDA graph per call)
-    # timed by CUDA events on its stream, the L2 flushed before it
-    kgraphs = []
-    for i in range(len(calls)):
+    # the dominant kernel alone: each decode launch timed by CUDA events on its
+    # stream as the difference between a CUDA graph of (L2 flush, launch) and
+    # a graph of the flush alone, so that neither the flush nor the graph's
+    # own start-up latency counts as kernel time
+    def graph_of(fn):
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g):
-            launch(i)
-        kgraphs.append(g)
+            fn()
+        return g
+    fgraph = graph_of(lambda: flush(1.0))
+    kgraphs = [graph_of(lambda i=i: (flush(1.0), launch(i))) for i in range(len(calls))]
     torch.cuda.synchronize()
-    kern_ms = []
+
+    def timed(g):
+        k0, k1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        k0.record(stream)
+        g.replay()
+        k1.record(stream)
+        return (k0, k1)
+    t_flush, t_kern = [], [[] for _ in calls]
+    for s_ in range(args.steps):
+        t_flush.append(timed(fgraph))
+        for i in range(len(calls)):
+            t_kern[i].append(timed(kgraphs[i]))
+    torch.cuda.synchronize()
+    flush_med = statistics.median(a.elapsed_time(b) for a, b in t_flush)
+    kern_ms = []  # per step, per call (flattened in call order within a step)
+    kmed = [statistics.median(a.elapsed_time(b) for a, b in t_kern[i]) - flush_med
+            for i in range(len(calls))]
     for s_ in range(args.steps):
         for i in range(len(calls)):
-            flush(float(s_))
-            k0, k1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            k0.record(stream)
-            kgraphs[i].replay()
-            k1.record(stream)
-            kern_ms.append((k0, k1))
-    torch.cuda.synchronize()
-    kern_ms = [a.elapsed_time(b) for a, b in kern_ms]
+            kern_ms.append(kmed[i])
 
     # end to end through the public API with pinned host buffers
     e2e = None
@@ -786,7 +798,7 @@ def main():
     # each layer's decode launch on its own (median over the steps)
     per_launch = []
     for i, b in enumerate(calls):
-        ms_i = statistics.median(kern_ms[i::len(calls)])
+        ms_i = kmed[i]
         gbs_i = launch_bytes(b) / (ms_i * 1e-3) / 1e9
         per_launch.append({"call": b.name or f"call {i}", "window": b.window,
                            "bytes": launch_bytes(b), "ms": ms_i, "achieved": gbs_i,
@@ -801,7 +813,8 @@ def main():
                          "the written buffer (evicts the flush's dirty lines)",
                    "path": ("paged_decode_attn_ws (split-K, combine fused)" if args.path == "fused"
                             else "paged_decode_splitk + paged_decode_splitk_combine"),
-                   "timing": "each step one CUDA-graph replay, CUDA events around it",
+                   "timing": "each step one CUDA-graph replay, CUDA events around it; a "
+                             "launch alone: graph of (flush, launch) minus graph of the flush",
                    "bytes_per_step": bytes_step, "parallelism": f"replicas{world}"},
         "roofline": {"bound": "hbm", "kernel": "paged_decode_kernel" + (" (split-K, fused combine)" if args.path == "fused" else " (split-K)"),
                      "achieved": achieved, "peak": peak, "peak_kind": peak_kind,

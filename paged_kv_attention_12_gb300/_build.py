@@ -40,10 +40,10 @@ def _deps():
     return files
 
 
-def up_to_date() -> bool:
-    if not os.path.exists(LIB_PATH):
+def up_to_date(lib_path: str = LIB_PATH) -> bool:
+    if not os.path.exists(lib_path):
         return False
-    t = os.path.getmtime(LIB_PATH)
+    t = os.path.getmtime(lib_path)
     return all(os.path.getmtime(f) <= t for f in _deps())
 
 
@@ -55,26 +55,32 @@ def _compile(src: str, obj: str, extra) -> None:
         raise RuntimeError(f"nvcc failed on {os.path.basename(src)}:\n{r.stdout}\n{r.stderr}")
 
 
-def build(force: bool = False, verbose: bool = False, extra=()) -> str:
-    """Compile and link the library; returns its path."""
-    if not force and up_to_date():
-        return LIB_PATH
-    os.makedirs(OUT_DIR, exist_ok=True)
+def build(force: bool = False, verbose: bool = False, extra=(), lib_path: str = LIB_PATH) -> str:
+    """Compile and link the library; returns its path.
+
+    ``extra`` adds nvcc flags (e.g. ``-DPKA_TIMELINE`` for the instrumented
+    build); a build with extra flags goes to its own ``lib_path`` so that it
+    never replaces the product library.
+    """
+    if not force and up_to_date(lib_path):
+        return lib_path
+    out_dir = os.path.dirname(lib_path)
+    os.makedirs(out_dir, exist_ok=True)
     srcs = _sources()
-    objs = [os.path.join(OUT_DIR, os.path.basename(s)[:-3] + ".o") for s in srcs]
+    objs = [os.path.join(out_dir, os.path.basename(s)[:-3] + ".o") for s in srcs]
     with cf.ThreadPoolExecutor(max_workers=min(8, len(srcs))) as ex:
         futs = [ex.submit(_compile, s, o, list(extra)) for s, o in zip(srcs, objs)]
         for f in futs:
             f.result()
-    tmp = LIB_PATH + ".tmp"
+    tmp = lib_path + ".tmp"
     cmd = [nvcc(), *ARCH, "-shared", "-o", tmp, *objs]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB_PATH)
+    os.replace(tmp, lib_path)
     if verbose:
-        print(f"built {LIB_PATH}", file=sys.stderr)
-    return LIB_PATH
+        print(f"built {lib_path}", file=sys.stderr)
+    return lib_path
 
 
 if __name__ == "__main__":

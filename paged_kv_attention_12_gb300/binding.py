@@ -60,6 +60,15 @@ class PagedAttnError(RuntimeError):
 _lib = None
 
 
+def use_library(path: str) -> None:
+    """Load ``path`` (an instrumented build of the same library) instead of
+    the default one; only before the first call into the library."""
+    global LIB_PATH
+    if _lib is not None and os.path.abspath(path) != os.path.abspath(LIB_PATH):
+        raise RuntimeError("the library is already loaded")
+    LIB_PATH = path
+
+
 def lib() -> ctypes.CDLL:
     """Load the CUDA library (raises if it is missing)."""
     global _lib

@@ -57,6 +57,45 @@
 
 namespace pka {
 
+// ----------------------------------------------------------- timeline
+// Built with -DPKA_TIMELINE (a separate, instrumented build of the library;
+// see timeline.py beside the package), every decode pipeline records global
+// timer stamps of its phases: [layer slot: 0 = full attention, 1 = sliding
+// window][pipeline][kTimelineFields].  The default build compiles none of it.
+enum TimelineField {
+  TL_ENTRY = 0,        // pipeline starts (consumer thread 0)
+  TL_PARTITION = 1,    // producer: partition known (iterator ready)
+  TL_FIRST_ISSUE = 2,  // producer: first tile's copies issued
+  TL_FIRST_TILE = 3,   // consumer warp 0: first tile landed
+  TL_LAST_ISSUE = 4,   // producer: last tile's copies issued
+  TL_LAST_TILE = 5,    // consumer warps: last tile consumed (latest warp)
+  TL_EXIT = 6,         // consumer warps: pipeline done (latest warp)
+  TL_TILES = 7,        // tiles streamed (a count, not a time)
+  kTimelineFields = 8
+};
+constexpr int kTimelinePipes = 1024;
+#ifdef PKA_TIMELINE
+__device__ unsigned long long pka_timeline[2 * kTimelinePipes * kTimelineFields];
+__device__ __forceinline__ unsigned long long* timeline_row(const DecodeArgs& a, int vcta) {
+  return pka_timeline + ((a.window > 0 ? 1 : 0) * kTimelinePipes + vcta) * kTimelineFields;
+}
+__device__ __forceinline__ unsigned long long timeline_now() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+#define PKA_TL_SET(a, vcta, f) \
+  do { if ((vcta) < kTimelinePipes) timeline_row(a, vcta)[f] = timeline_now(); } while (0)
+#define PKA_TL_MAX(a, vcta, f) \
+  do { if ((vcta) < kTimelinePipes) atomicMax(&timeline_row(a, vcta)[f], timeline_now()); } while (0)
+#define PKA_TL_VAL(a, vcta, f, v) \
+  do { if ((vcta) < kTimelinePipes) timeline_row(a, vcta)[f] = (v); } while (0)
+#else
+#define PKA_TL_SET(a, vcta, f) do { } while (0)
+#define PKA_TL_MAX(a, vcta, f) do { } while (0)
+#define PKA_TL_VAL(a, vcta, f, v) do { } while (0)
+#endif
+
 namespace {
 
 __device__ __forceinline__ int warp_incl_scan(int x, int lane) {
@@ -542,6 +581,7 @@ __device__ __forceinline__ void decode_body(const DecodeArgs& a, const CUtensorM
 
   const int warp = cx.tid / 32;
   const int lane = cx.tid % 32;
+  if (cx.tid == 0) PKA_TL_SET(a, cx.vcta, TL_ENTRY);
 
   if (warp == NW) {
     // the producer warp sets up the barriers (one lane each) and reads the
@@ -566,6 +606,7 @@ __device__ __forceinline__ void decode_body(const DecodeArgs& a, const CUtensorM
     const uint32_t oob_row = static_cast<uint32_t>(a.num_blocks) * a.Hkv * kBlockSize;
     int issued = 0;
     bool ok = true;
+    if (lane == 0) PKA_TL_SET(a, cx.vcta, TL_PARTITION);
     while (ok && iter.next(pc, false)) {
       const int32_t* trow = a.tables + static_cast<size_t>(pc.b) * a.max_blocks + pc.j0;
       for (int base = 0; base < pc.ntiles && ok; base += 32) {
@@ -601,9 +642,14 @@ __device__ __forceinline__ void decode_body(const DecodeArgs& a, const CUtensorM
                 ring + static_cast<size_t>(slot) * 2 * S::kTileBytes + lane * S::kTileBytes;
             tma_load_3d(dst, lane == 0 ? tm_k : tm_v, 0, static_cast<int>(r0), 0, &full[slot]);
           }
+          if (lane == 0 && issued == 0) PKA_TL_SET(a, cx.vcta, TL_FIRST_ISSUE);
           ++issued;
         }
       }
+    }
+    if (lane == 0) {
+      PKA_TL_SET(a, cx.vcta, TL_LAST_ISSUE);
+      PKA_TL_VAL(a, cx.vcta, TL_TILES, static_cast<unsigned long long>(issued));
     }
     // Every issued copy must have landed before the CTA may exit.
     if (lane == 0) {
@@ -739,6 +785,7 @@ __device__ __forceinline__ void decode_body(const DecodeArgs& a, const CUtensorM
       const int T = tile_base + i;
       const int slot = T % NSLOT;
       const bool got = mbar_wait(&full[slot], static_cast<uint32_t>((T / NSLOT) & 1), a.err);
+      if (T == 0 && cx.tid == 0) PKA_TL_SET(a, cx.vcta, TL_FIRST_TILE);
       if (!__all_sync(0xffffffffu, got)) {
         ok = false;
         break;
@@ -753,6 +800,7 @@ __device__ __forceinline__ void decode_body(const DecodeArgs& a, const CUtensorM
       if (lane == 0) mbar_arrive(&empty[slot]);
     }
     tile_base += pc.ntiles;
+    if (lane == 0) PKA_TL_MAX(a, cx.vcta, TL_LAST_TILE);
 
     Piece nx;
     const bool have_next = iter.next(nx, true);
@@ -948,6 +996,7 @@ __device__ __forceinline__ void decode_body(const DecodeArgs& a, const CUtensorM
   }
   // the bulk copies of the last results complete before the pipeline ends
   if (warp == 0 && lane == 0) bulk_wait_all();
+  if (lane == 0) PKA_TL_MAX(a, cx.vcta, TL_EXIT);
 }
 
 }  // namespace pka
