@@ -13,6 +13,28 @@
 
 namespace pka {
 
+#ifdef PKA_TIMELINE
+// Instrumented builds only (-DPKA_TIMELINE): the global timer, in ns.
+__device__ __forceinline__ unsigned long long timeline_now() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+// Each translation unit has its own copy of a __device__ array; a unit
+// whose kernels record stamps exports its copy under its own names.
+#define PKA_TIMELINE_EXPORT(name, array)                                                    \
+  extern "C" int pka_timeline_copy##name(void* dst) {                                       \
+    return static_cast<int>(                                                                 \
+        cudaMemcpyFromSymbol(dst, array, sizeof(array), 0, cudaMemcpyDeviceToDevice));       \
+  }                                                                                          \
+  extern "C" int pka_timeline_clear##name(void* stream) {                                   \
+    void* p = nullptr;                                                                       \
+    if (cudaGetSymbolAddress(&p, array) != cudaSuccess) return -1;                           \
+    return static_cast<int>(cudaMemsetAsync(p, 0, sizeof(array),                              \
+                                            static_cast<cudaStream_t>(stream)));             \
+  }
+#endif
+
 constexpr int kBlockSize = 16;        // tokens per KV block (the only supported size)
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;

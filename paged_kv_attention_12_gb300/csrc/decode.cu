@@ -78,14 +78,5 @@ cudaError_t launch_decode(const DecodeArgs& a, int head_dim, int group, int grid
 #ifdef PKA_TIMELINE
 // Instrumented builds only: copy the decode timeline (device to device, into
 // dst, 2 * 1024 * 8 uint64) or zero it on the stream.
-extern "C" int pka_timeline_copy(void* dst) {
-  return static_cast<int>(cudaMemcpyFromSymbol(dst, pka::pka_timeline, sizeof(pka::pka_timeline),
-                                               0, cudaMemcpyDeviceToDevice));
-}
-extern "C" int pka_timeline_clear(void* stream) {
-  void* p = nullptr;
-  if (cudaGetSymbolAddress(&p, pka::pka_timeline) != cudaSuccess) return -1;
-  return static_cast<int>(
-      cudaMemsetAsync(p, 0, sizeof(pka::pka_timeline), static_cast<cudaStream_t>(stream)));
-}
+PKA_TIMELINE_EXPORT(, pka::pka_timeline)
 #endif

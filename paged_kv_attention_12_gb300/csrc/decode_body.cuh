@@ -79,11 +79,6 @@ __device__ unsigned long long pka_timeline[2 * kTimelinePipes * kTimelineFields]
 __device__ __forceinline__ unsigned long long* timeline_row(const DecodeArgs& a, int vcta) {
   return pka_timeline + ((a.window > 0 ? 1 : 0) * kTimelinePipes + vcta) * kTimelineFields;
 }
-__device__ __forceinline__ unsigned long long timeline_now() {
-  unsigned long long t;
-  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-  return t;
-}
 #define PKA_TL_SET(a, vcta, f) \
   do { if ((vcta) < kTimelinePipes) timeline_row(a, vcta)[f] = timeline_now(); } while (0)
 #define PKA_TL_MAX(a, vcta, f) \
@@ -137,25 +132,31 @@ struct ReqGeo {
 };
 
 // The request's context length after the checks below (clamped to its
-// table row), or -1 for a request the launch skips.
-__device__ __forceinline__ int req_len(const DecodeArgs& a, int b) {
+// table row), or -1 for a request the launch skips, from its
+// query_start_loc pair (lo, hi; ignored without query_start_loc) and its
+// seq_len L.
+__device__ __forceinline__ int req_len_of(const DecodeArgs& a, int lo, int hi, int L) {
   if (a.query_start_loc != nullptr) {
     // a varlen batch: the request's query row is query_start_loc[b + 1] - 1;
     // a span outside [0, total_q] (or longer than max_query_len) is skipped
     // and reported, so no row outside the output is ever written
-    const int lo = a.query_start_loc[b], hi = a.query_start_loc[b + 1];
     if (lo < 0 || hi < lo || hi > a.total_q || hi - lo > a.max_query_len) {
       report(a.err, PKA_DEVERR_QUERY_LOC);
       return -1;
     }
     if (hi - lo != 1 && a.decode_rows_only != 0) return -1;
   }
-  int L = a.seq_lens[b];
   if (L > a.max_blocks * kBlockSize || L < 0) {
     report(a.err, PKA_DEVERR_SEQ_LEN);  // error path only: tables cannot hold it
     L = max(0, min(L, a.max_blocks * kBlockSize));
   }
   return L;
+}
+
+__device__ __forceinline__ int req_len(const DecodeArgs& a, int b) {
+  const bool v = a.query_start_loc != nullptr;
+  return req_len_of(a, v ? a.query_start_loc[b] : 0, v ? a.query_start_loc[b + 1] : 0,
+                    a.seq_lens[b]);
 }
 
 // Visible blocks of a request from req_len's value (no memory access).
@@ -588,8 +589,24 @@ __device__ __forceinline__ void decode_body(const DecodeArgs& a, const CUtensorM
     // requests' lengths into shared memory for the whole pipeline
     for (int i = lane; i < 2 * NSLOT + 1; i += 32) mbar_init(full + i, 1);
     mbar_fence_init();
+    // every load is issued before the first check, so that the lengths
+    // take one memory round trip
     const int ncache = min(a.batch, kLenCache);
-    for (int bb = lane; bb < ncache; bb += 32) slen[bb] = req_len(a, bb);
+    const bool varlen = a.query_start_loc != nullptr;
+    int lo[kLenCache / 32], hi[kLenCache / 32], sl[kLenCache / 32];
+#pragma unroll
+    for (int k = 0; k < kLenCache / 32; ++k) {
+      const int bb = lane + 32 * k;
+      const bool in = bb < ncache;
+      lo[k] = (in && varlen) ? a.query_start_loc[bb] : 0;
+      hi[k] = (in && varlen) ? a.query_start_loc[bb + 1] : 0;
+      sl[k] = in ? a.seq_lens[bb] : 0;
+    }
+#pragma unroll
+    for (int k = 0; k < kLenCache / 32; ++k) {
+      const int bb = lane + 32 * k;
+      if (bb < ncache) slen[bb] = req_len_of(a, lo[k], hi[k], sl[k]);
+    }
   }
   named_sync(cx.bar_all, (NW + 1) * 32);
 

@@ -50,10 +50,11 @@ __global__ void __launch_bounds__(PrefillShape<D, G>::kThreads, 1)
                        const __grid_constant__ CUtensorMap tm_q,
                        const __grid_constant__ CUtensorMap tm_k_rows,
                        const __grid_constant__ CUtensorMap tm_k_tiles,
-                       const __grid_constant__ CUtensorMap tm_v_tiles) {
+                       const __grid_constant__ CUtensorMap tm_v_tiles,
+                       const __grid_constant__ CUtensorMap tm_out) {
   extern __shared__ uint8_t smem_raw[];
   if (static_cast<int>(blockIdx.x) >= n_decode) {
-    prefill_body<D, G>(pa, &tm_q, &tm_k_rows, &tm_v_tiles, smem_raw,
+    prefill_body<D, G>(pa, &tm_q, &tm_k_rows, &tm_v_tiles, &tm_out, smem_raw,
                        static_cast<int>(blockIdx.x) - n_decode);
     return;
   }
@@ -74,11 +75,12 @@ cudaError_t launch_mixed_t(const PrefillArgs& pa, const DecodeArgs& da, int deco
                            cudaStream_t stream) {
   using S = PrefillShape<D, G>;
   using T = MixedDecodeTuning<D, G>;
-  CUtensorMap tq, tkr, tkt, tvt;
+  CUtensorMap tq, tkr, tkt, tvt, to;
   const long long rows = static_cast<long long>(pa.num_blocks) * pa.Hkv * kBlockSize;
   if (!tmap_query_tiles(&tq, pa.q, D, pa.Hq, pa.total_q, G, S::TQ) ||
       !tmap_pool_rows(&tkr, pa.k, D, rows) || !tmap_pool_tiles(&tkt, pa.k, D, rows) ||
-      !tmap_pool_tiles(&tvt, pa.v, D, rows))
+      !tmap_pool_tiles(&tvt, pa.v, D, rows) ||
+      !tmap_query_tiles(&to, pa.out, D, pa.Hq, pa.total_q, G, S::TQ))
     return cudaErrorInvalidValue;
   auto kern = paged_mixed_kernel<D, G>;
   cudaError_t e = set_smem_once(reinterpret_cast<const void*>(kern), T::kSmemBytes);
@@ -86,7 +88,7 @@ cudaError_t launch_mixed_t(const PrefillArgs& pa, const DecodeArgs& da, int deco
   const long long ctas = static_cast<long long>(decode_ctas) + prefill_ranks(pa, S::TQ);
   if (ctas > 0x7fffffffLL || decode_ctas <= 0) return cudaErrorInvalidValue;
   kern<<<static_cast<unsigned>(ctas), S::kThreads, T::kSmemBytes, stream>>>(
-      pa, da, decode_ctas, tq, tkr, tkt, tvt);
+      pa, da, decode_ctas, tq, tkr, tkt, tvt, to);
   return cudaGetLastError();
 }
 
@@ -128,3 +130,10 @@ cudaError_t launch_mixed(const PrefillArgs& pa, const DecodeArgs& da, int head_d
 }
 
 }  // namespace pka
+
+#ifdef PKA_TIMELINE
+// Instrumented builds only: the stamps of the mixed launch's decode
+// pipelines and prefill CTAs.
+PKA_TIMELINE_EXPORT(_mixed, pka::pka_timeline)
+PKA_TIMELINE_EXPORT(_mixed_prefill, pka::pka_timeline_prefill)
+#endif

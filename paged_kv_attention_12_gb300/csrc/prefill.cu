@@ -11,9 +11,10 @@ __global__ void __launch_bounds__(PrefillShape<D, G>::kThreads, 1)
     paged_prefill_kernel(const __grid_constant__ PrefillArgs a,
                          const __grid_constant__ CUtensorMap tm_q,
                          const __grid_constant__ CUtensorMap tm_k,
-                         const __grid_constant__ CUtensorMap tm_v) {
+                         const __grid_constant__ CUtensorMap tm_v,
+                         const __grid_constant__ CUtensorMap tm_out) {
   extern __shared__ uint8_t smem_raw[];
-  prefill_body<D, G>(a, &tm_q, &tm_k, &tm_v, smem_raw, static_cast<int>(blockIdx.x));
+  prefill_body<D, G>(a, &tm_q, &tm_k, &tm_v, &tm_out, smem_raw, static_cast<int>(blockIdx.x));
 }
 
 // ------------------------------------------------------------- launchers
@@ -22,10 +23,11 @@ namespace {
 template <int D, int G>
 cudaError_t launch_prefill_t(const PrefillArgs& a, cudaStream_t stream) {
   using S = PrefillShape<D, G>;
-  CUtensorMap tq, tk, tv;
+  CUtensorMap tq, tk, tv, to;
   const long long rows = static_cast<long long>(a.num_blocks) * a.Hkv * kBlockSize;
   if (!tmap_query_tiles(&tq, a.q, D, a.Hq, a.total_q, G, S::TQ) ||
-      !tmap_pool_rows(&tk, a.k, D, rows) || !tmap_pool_tiles(&tv, a.v, D, rows))
+      !tmap_pool_rows(&tk, a.k, D, rows) || !tmap_pool_tiles(&tv, a.v, D, rows) ||
+      !tmap_query_tiles(&to, a.out, D, a.Hq, a.total_q, G, S::TQ))
     return cudaErrorInvalidValue;
   auto kern = paged_prefill_kernel<D, G>;
   cudaError_t e = set_smem_once(reinterpret_cast<const void*>(kern), S::kSmemBytes);
@@ -33,7 +35,7 @@ cudaError_t launch_prefill_t(const PrefillArgs& a, cudaStream_t stream) {
   const long long ctas = prefill_ranks(a, S::TQ);
   if (ctas > 0x7fffffffLL) return cudaErrorInvalidValue;
   dim3 grid(static_cast<unsigned>(ctas));
-  kern<<<grid, S::kThreads, S::kSmemBytes, stream>>>(a, tq, tk, tv);
+  kern<<<grid, S::kThreads, S::kSmemBytes, stream>>>(a, tq, tk, tv, to);
   return cudaGetLastError();
 }
 
@@ -57,3 +59,8 @@ cudaError_t launch_prefill(const PrefillArgs& a, int head_dim, int group, int /*
 }
 
 }  // namespace pka
+
+#ifdef PKA_TIMELINE
+// Instrumented builds only: the stamps of the prefill CTAs.
+PKA_TIMELINE_EXPORT(_prefill, pka::pka_timeline_prefill)
+#endif

@@ -91,12 +91,29 @@ struct PrefillShape {
   static_assert(2 * BN <= 256 && D <= 256, "TMEM columns");
 };
 
+// Built with -DPKA_TIMELINE (instrumented builds only), every prefill CTA
+// records global-timer stamps: [rank][entry, first S tile ready, last P V
+// done, exit, key tiles].  The default build compiles none of it.
+constexpr int kPrefillStampRanks = 1024;
+#ifdef PKA_TIMELINE
+__device__ unsigned long long pka_timeline_prefill[kPrefillStampRanks * 5];
+#define PKA_PF_SET(rank, f) \
+  do { if ((rank) < kPrefillStampRanks) pka_timeline_prefill[(rank) * 5 + (f)] = timeline_now(); } while (0)
+#define PKA_PF_VAL(rank, f, v) \
+  do { if ((rank) < kPrefillStampRanks) pka_timeline_prefill[(rank) * 5 + (f)] = (v); } while (0)
+#else
+#define PKA_PF_SET(rank, f) do { } while (0)
+#define PKA_PF_VAL(rank, f, v) do { } while (0)
+#endif
+
 namespace {
 
 constexpr int kWarpTmaK = 4;
 constexpr int kWarpTmaV = 5;
 constexpr int kWarpMma = 6;
 constexpr int kWarpTmaK2 = 7;
+// named barrier of the four softmax warps (the epilogue's staged stores)
+constexpr int kBarSoftmax = 1;
 
 struct Item {
   int b, kvh, q0, n, L, it0, it1, kbase, ntiles, nblk;
@@ -302,7 +319,8 @@ inline long long prefill_ranks(const PrefillArgs& a, int TQ) {
 template <int D, int G>
 __device__ __forceinline__ void prefill_body(const PrefillArgs& a, const CUtensorMap* tm_q,
                                              const CUtensorMap* tm_k, const CUtensorMap* tm_v,
-                                             uint8_t* smem_raw, int rank) {
+                                             const CUtensorMap* tm_out, uint8_t* smem_raw,
+                                             int rank) {
   using S = PrefillShape<D, G>;
   constexpr int BN = S::BN, TQ = S::TQ, DC = S::DC;
 
@@ -384,6 +402,10 @@ __device__ __forceinline__ void prefill_body(const PrefillArgs& a, const CUtenso
 
   const int warp = threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
+  if (threadIdx.x == 0) {
+    PKA_PF_SET(rank, 0);
+    PKA_PF_VAL(rank, 4, static_cast<unsigned long long>(it.ntiles));
+  }
 
   if (threadIdx.x == 0) {
     mbar_init(&bars[B_Q], 1);
@@ -614,6 +636,7 @@ __device__ __forceinline__ void prefill_body(const PrefillArgs& a, const CUtenso
         ok = false;
         break;
       }
+      if (j == 0 && threadIdx.x == 0) PKA_PF_SET(rank, 1);
       tc_fence_after();
       float s[BN];
 #pragma unroll
@@ -713,24 +736,49 @@ __device__ __forceinline__ void prefill_body(const PrefillArgs& a, const CUtenso
       const int jl = it.ntiles - 1;
       ok = warp_wait(&bars[B_PV + (jl & 1)], (jl >> 1) & 1, a.err, failed);
     }
+    if (ok && threadIdx.x == 0) PKA_PF_SET(rank, 2);
+    const bool full = (it.it1 - it.it0 + 1 == TQ);  // uniform over the CTA
     if (ok) {
       tc_fence_after();
       const float inv = (l > 0.f) ? 1.f / l : 0.f;
+      // A tile of TQ tokens of this request leaves through TMA stores from
+      // the Q tile's shared memory, which is free once the last MMA has
+      // completed (the last P V commit covers every earlier MMA): each row
+      // goes there in the 128-byte-swizzled layout the Q copies used, so the
+      // output tensor map, of the same geometry, writes back whole 2 KB runs
+      // (one token's G heads) instead of one 16-byte piece per row and
+      // store.  A tile at the end of the request's rows, whose box would
+      // cover the next request's rows, stores its valid rows one by one.
       uint16_t* orow = a.out + (static_cast<size_t>(it.q0 + qi) * a.Hq + it.kvh * G + g) * D;
 #pragma unroll 1
       for (int c = 0; c < D / 64; ++c) {  // 64 columns per load and wait
         float o[64];
         tmem_ld64(lane_base + S::kTmemO + c * 64, o);
-        if (row_valid) {
+        uint8_t* srow = sQ + c * S::kQChunk + r * 128;
 #pragma unroll
-          for (int q = 0; q < 8; ++q) {
-            const uint4 w = make_uint4(pack_bf16x2(o[q * 8 + 0] * inv, o[q * 8 + 1] * inv),
-                                       pack_bf16x2(o[q * 8 + 2] * inv, o[q * 8 + 3] * inv),
-                                       pack_bf16x2(o[q * 8 + 4] * inv, o[q * 8 + 5] * inv),
-                                       pack_bf16x2(o[q * 8 + 6] * inv, o[q * 8 + 7] * inv));
+        for (int q = 0; q < 8; ++q) {
+          const uint4 w = make_uint4(pack_bf16x2(o[q * 8 + 0] * inv, o[q * 8 + 1] * inv),
+                                     pack_bf16x2(o[q * 8 + 2] * inv, o[q * 8 + 3] * inv),
+                                     pack_bf16x2(o[q * 8 + 4] * inv, o[q * 8 + 5] * inv),
+                                     pack_bf16x2(o[q * 8 + 6] * inv, o[q * 8 + 7] * inv));
+          if (full)
+            *reinterpret_cast<uint4*>(srow + ((q ^ (r & 7)) << 4)) = w;
+          else if (row_valid)
             *reinterpret_cast<uint4*>(orow + c * 64 + q * 8) = w;
-          }
         }
+      }
+    }
+    if (full) {
+      // every softmax warp arrives, whatever its waits gave; the tile is
+      // stored only if no wait of the CTA ran out
+      fence_proxy_async_smem();
+      asm volatile("bar.sync %0, %1;" ::"r"(kBarSoftmax), "r"(128) : "memory");
+      if (threadIdx.x == 0 && !stop_requested(failed)) {
+#pragma unroll
+        for (int c = 0; c < DC; ++c)
+          tma_store_3d(tm_out, sQ + c * S::kQChunk, c * 64, it.kvh * G, it.q0 + it.it0);
+        bulk_commit();
+        bulk_wait_read_all();  // the shared memory may go once the stores have read it
       }
     }
   }
@@ -739,6 +787,7 @@ __device__ __forceinline__ void prefill_body(const PrefillArgs& a, const CUtenso
   __syncthreads();
   tc_fence_after();
   if (warp == kWarpMma) tmem_dealloc(tmem, S::kTmemCols);
+  if (threadIdx.x == 0) PKA_PF_SET(rank, 3);
 }
 
 }  // namespace pka
