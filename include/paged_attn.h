@@ -211,11 +211,32 @@ int paged_prefill_attn(const void* q, void* out, const pka_kv_pool* kv,
  * the log-sum-exp merge fused in, as paged_decode_attn_ws -- instead of
  * filling G of the 128 rows of a tensor-core tile; requests with more tokens
  * run the tensor-core prefill pipeline.
+ * SMs: the prefill side gets P of the GPU's N SMs, the decode pipelines the
+ * rest (two per SM).  P shares N in proportion to estimated SM time, from
+ * sizes only: prefill E = ceil((total_q - B) / TQ) * Hkv items (TQ = 128/G
+ * query tokens per tile) of ceil(K / BN) + 1 key tiles each at 2 us, with
+ * K = min(max_seq_len, window + TQ) (max_seq_len without window) and BN = 64
+ * at D = 256, 128 at D = 128; decode max(0, B - ceil((total_q - B) /
+ * (max_query_len - 1))) rows of Hkv * ceil(K' / 16) blocks at 64 * D bytes
+ * per block and 70 GB/s per SM, K' = min(max_seq_len, window).  With
+ * share = round(N * prefill / (prefill + decode)), P = share if share >= 2E,
+ * else E; then clamped to [1, N - N/4] (P = 0 without prefill rows).
+ * Prefill items: one per (request, query tile, KV head) with work.  When
+ * they are fewer than P (and at most 160), they are cut along their keys:
+ * with theta the smallest piece length >= 4 key tiles for which
+ * sum over items of min(8, ceil(tiles / theta)) <= min(P, 160), an item of T
+ * key tiles runs as p = min(8, ceil(T / theta)) pieces on separate CTAs,
+ * piece k taking tiles [k T / p, (k + 1) T / p); each piece leaves its
+ * normalised rows and their LSEs in the workspace and the piece that
+ * arrives last on the item's counter merges them in piece order (the same
+ * result whichever piece merges).
  * workspace: device, 16-byte aligned, at least paged_prefill_attn_ws_bytes()
- * bytes (the layout of paged_decode_attn_ws for B requests); its counters
- * must be zero before the first call and are left zero by every call that
- * completes (zero them again after a PKA_DEVERR_TIMEOUT).  Calls
- * sharing one workspace must not overlap on the GPU.  PKA_ERR_WORKSPACE if
+ * bytes: the layout of paged_decode_attn_ws for B requests, then 160 piece
+ * slots of 128 fp32 rows of D columns, their 160 * 128 fp32 LSEs and 160
+ * int32 piece counters (padded to 16 bytes).  All counters must be zero
+ * before the first call and are left zero by every call that completes
+ * (zero them again after a PKA_DEVERR_TIMEOUT).  Calls sharing one
+ * workspace must not overlap on the GPU.  PKA_ERR_WORKSPACE if
  * workspace_bytes is too small. */
 size_t paged_prefill_attn_ws_bytes(int32_t B, int32_t Hq, int32_t Hkv, int32_t D,
                                    int32_t max_seq_len, int32_t window);

@@ -72,6 +72,13 @@ struct PrefillArgs {
   float scale, softcap;
   int32_t window;
   int32_t skip_decode_rows;        // nonzero: requests with one query token are left out
+  int32_t one_wave;                // prefill CTAs that run at once: when every item fits,
+                                   // items go in index order (no ranking) and, with the
+                                   // split workspace below, are cut into pieces along keys
+  float* split_o;                  // null: no pieces; else fp32 [split_slots][D/4][128][4]
+  float* split_lse;                // fp32 [split_slots][128], log2 domain
+  int32_t* split_cnt;              // int32 [split_slots], zeroed; left zero by every call
+  int32_t split_slots;
 };
 
 cudaError_t launch_prefill(const PrefillArgs& a, int head_dim, int group, int sm_count,

@@ -85,7 +85,10 @@ cudaError_t launch_mixed_t(const PrefillArgs& pa, const DecodeArgs& da, int deco
   auto kern = paged_mixed_kernel<D, G>;
   cudaError_t e = set_smem_once(reinterpret_cast<const void*>(kern), T::kSmemBytes);
   if (e != cudaSuccess) return e;
-  const long long ctas = static_cast<long long>(decode_ctas) + prefill_ranks(pa, S::TQ);
+  long long pre = prefill_ranks(pa, S::TQ);
+  // with pieces along keys, up to one wave of units
+  if (pa.split_o != nullptr && pa.one_wave > pre) pre = min(pa.one_wave, pa.split_slots);
+  const long long ctas = static_cast<long long>(decode_ctas) + pre;
   if (ctas > 0x7fffffffLL || decode_ctas <= 0) return cudaErrorInvalidValue;
   kern<<<static_cast<unsigned>(ctas), S::kThreads, T::kSmemBytes, stream>>>(
       pa, da, decode_ctas, tq, tkr, tkt, tvt, to);

@@ -393,15 +393,30 @@ int paged_prefill_attn(const void* q, void* out, const pka_kv_pool* kv,
                                           params);
   const int sms = pka::device_sm_count();
   if (sms <= 0) return PKA_ERR_CUDA;
-  cudaError_t e = pka::launch_prefill(a, kv->head_dim, Hq / kv->num_kv_heads, sms,
+  pka::PrefillArgs a1 = a;
+  a1.one_wave = sms;  // one prefill CTA per SM
+  cudaError_t e = pka::launch_prefill(a1, kv->head_dim, Hq / kv->num_kv_heads, sms,
                                       static_cast<cudaStream_t>(stream));
   if (e == cudaErrorNotSupported) return PKA_ERR_UNSUPPORTED;
   return e == cudaSuccess ? PKA_OK : PKA_ERR_CUDA;
 }
 
+// The prefill part of the mixed launch's workspace: kPrefillSplitSlots
+// pieces of 128 rows (fp32 rows, then their LSEs), then one counter each.
+constexpr int32_t kPrefillSplitSlots = 160;
+
+size_t prefill_split_bytes(int32_t D) {
+  const size_t o = static_cast<size_t>(kPrefillSplitSlots) * 128 * D * sizeof(float);
+  const size_t lse = static_cast<size_t>(kPrefillSplitSlots) * 128 * sizeof(float);
+  const size_t cnt = (static_cast<size_t>(kPrefillSplitSlots) * sizeof(int32_t) + 15) / 16 * 16;
+  return o + lse + cnt;
+}
+
 size_t paged_prefill_attn_ws_bytes(int32_t B, int32_t Hq, int32_t Hkv, int32_t D,
                                    int32_t max_seq_len, int32_t window) {
-  return paged_decode_attn_ws_bytes(B, Hq, Hkv, D, max_seq_len, window);
+  const size_t dec = paged_decode_attn_ws_bytes(B, Hq, Hkv, D, max_seq_len, window);
+  if (dec == 0) return 0;
+  return dec + prefill_split_bytes(D);
 }
 
 int paged_prefill_attn_ws(const void* q, void* out, const pka_kv_pool* kv,
@@ -420,7 +435,7 @@ int paged_prefill_attn_ws(const void* q, void* out, const pka_kv_pool* kv,
   FusedLayout L;
   st = fused_layout(B, Hq, Hkv, D, max_seq_len, params->window, &L);
   if (st != PKA_OK) return st;
-  if (workspace_bytes < L.total()) return PKA_ERR_WORKSPACE;
+  if (workspace_bytes < L.total() + prefill_split_bytes(D)) return PKA_ERR_WORKSPACE;
   if (!line_fits(B, Hkv, max_blocks, params->window)) return PKA_ERR_SHAPE;
   pka::PrefillArgs pa = prefill_args(q, out, kv, block_tables, max_blocks, query_start_loc,
                                      seq_lens, B, Hq, total_q, max_query_len, max_seq_len, params);
@@ -439,15 +454,54 @@ int paged_prefill_attn_ws(const void* q, void* out, const pka_kv_pool* kv,
   da.split_blocks = L.C;
   const int sms = pka::device_sm_count();
   if (sms <= 0) return PKA_ERR_CUDA;
-  // Decode CTAs: the SMs the prefill tiles leave free, estimated from the
-  // query tokens beyond one per request (a quarter of the SMs at least).
+  // Decode CTAs and prefill SMs.  The host sees only sizes, so both sides'
+  // work is estimated from them: the prefill items from the query tokens
+  // beyond one per request, each streaming at most the keys a query tile
+  // can see (max_seq_len, or the window and the tile); the decode rows are
+  // the requests the chunks leave, each streaming at most as many keys.  The
+  // SMs are shared in proportion to the estimated SM time (measured rates on
+  // GB300: ~2 us per 64-key prefill tile, ~70 GB/s of decode K/V per SM),
+  // with every prefill item in one wave when a quarter of the SMs is left
+  // to the decode rows.  The prefill side cuts its items along keys when
+  // they fill less than that wave.
   const int tq = pka::mixed_query_tile(D, G);
   if (tq <= 0) return PKA_ERR_UNSUPPORTED;
   const long long extra = static_cast<long long>(total_q) - B;
-  const long long est_prefill = extra > 0 ? (extra + tq - 1) / tq * Hkv : 0;
-  long long decode_ctas = static_cast<long long>(sms) - est_prefill;
-  if (decode_ctas < sms / 4) decode_ctas = sms / 4;
+  const long long est_items = extra > 0 ? (extra + tq - 1) / tq * Hkv : 0;
+  const int window = params->window;
+  const long long keys = (window > 0) ? std::min<long long>(max_seq_len, window + tq) : max_seq_len;
+  const int bn = (D == 256) ? 64 : 128;
+  const double prefill_us = static_cast<double>(est_items) * ((keys + bn - 1) / bn + 1) * 2.0;
+  const long long chunks = (extra > 0 && max_query_len > 1) ? (extra + max_query_len - 2) /
+                                                                   (max_query_len - 1)
+                                                             : 0;
+  const long long dec_rows = std::max<long long>(0, B - chunks);
+  const long long dec_keys = (window > 0) ? std::min<long long>(max_seq_len, window) : max_seq_len;
+  const double decode_us = static_cast<double>(dec_rows) * Hkv * ((dec_keys + 15) / 16) *
+                           (64.0 * D) / 70.0e3;
+  long long prefill_sms = 0;
+  if (est_items > 0) {
+    // the proportional share, taken only when it gives every item room for
+    // two pieces or more (measured on the mixed workload: 83 prefill SMs for
+    // its 64 items of ~17 key tiles ran 59 us, 64 SMs 53 us)
+    const long long share =
+        static_cast<long long>(sms * prefill_us / (prefill_us + decode_us) + 0.5);
+    prefill_sms = (share >= 2 * est_items) ? share : est_items;
+    prefill_sms = std::min<long long>(std::max<long long>(prefill_sms, 1), sms - sms / 4);
+  }
+  long long decode_ctas = static_cast<long long>(sms) - prefill_sms;
   if (decode_ctas < 1) decode_ctas = 1;
+  // The prefill items run in the SMs the decode CTAs leave; when they fit
+  // in one wave with room to spare, they are cut along keys into pieces
+  // that fill it (the pieces' rows and counters after the decode part).
+  uint8_t* split = ws + L.total();
+  pa.one_wave = static_cast<int32_t>(sms - decode_ctas);
+  pa.split_o = reinterpret_cast<float*>(split);
+  pa.split_lse =
+      reinterpret_cast<float*>(split + static_cast<size_t>(kPrefillSplitSlots) * 128 * D * 4);
+  pa.split_cnt = reinterpret_cast<int32_t*>(split + static_cast<size_t>(kPrefillSplitSlots) * 128 *
+                                                        (D + 1) * 4);
+  pa.split_slots = kPrefillSplitSlots;
   cudaError_t e = pka::launch_mixed(pa, da, D, G, static_cast<int>(decode_ctas),
                                     static_cast<cudaStream_t>(stream));
   if (e == cudaErrorNotSupported) return PKA_ERR_UNSUPPORTED;

@@ -298,6 +298,135 @@ __device__ int lpt_pair(const PrefillArgs& a, int qtiles, int rank, int* scratch
   return pair;
 }
 
+// ------------------------------------------------ one wave, split along keys
+// When every (request, query tile, KV head) item fits in one wave of the
+// CTAs that run at once (a.one_wave), the order of the items does not
+// matter and no ranking is needed: CTA r takes unit r in index order.  With
+// a split workspace, the items' key tiles are also cut into pieces, so that
+// the units fill the wave: the smallest piece length theta (>= kMinPieceTiles
+// tiles) for which sum over items of min(kMaxPieces, ceil(tiles / theta))
+// pieces fits, found by bisection.  Piece k of an item of T tiles and P
+// pieces takes tiles [k T / P, (k + 1) T / P).
+constexpr int kMaxList = 256;         // (request, query tile) pairs the list holds
+constexpr int kListOffset = 12416;    // ints, past the request cache
+constexpr int kMinPieceTiles = 4;     // shortest piece worth a CTA of its own
+constexpr int kMaxPieces = 8;         // pieces of one item at most
+
+struct Unit {
+  int b, qt, kvh, piece, npieces, slot0;  // slot0: the unit of the item's piece 0
+};
+
+__device__ __forceinline__ int pieces_of(int tiles, int theta) {
+  return min(kMaxPieces, max(1, (tiles + theta - 1) / theta));
+}
+
+// Every thread of the CTA calls it (it uses __syncthreads); returns false
+// (uniformly) when rank has no unit.  pairs: the pairs with work (<= kMaxList).
+template <int TQ, int BN>
+__device__ bool one_wave_unit(const PrefillArgs& a, int rank, int pairs, bool split,
+                              int* scratch, const int* rn, const int* rL, Unit* u) {
+  int* list = scratch + kListOffset;        // [kMaxList][4]: b, qt, tiles, pieces
+  int* uoff = list + 4 * kMaxList;          // [kMaxList]: first unit of the pair
+  int* misc = uoff + kMaxList;              // [4]
+  const int lane = threadIdx.x % 32;
+  if (threadIdx.x < 32) {
+    // the pairs with work in index order: request-major, query tiles within
+    int run = 0;
+    for (int base = 0; base < a.batch; base += 32) {
+      const int b = base + lane;
+      int n = 0, L = 0;
+      if (b < a.batch) {
+        if (rn != nullptr) {
+          n = rn[b];
+          L = rL[b];
+        } else {
+          int q0;
+          n = query_span(a, b, &q0);
+          L = min(a.seq_lens[b], a.max_blocks * kBlockSize);
+        }
+      }
+      const int t = (n > 0 && n <= L && !(a.skip_decode_rows != 0 && n == 1)) ? (n + TQ - 1) / TQ
+                                                                              : 0;
+      int incl = t;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+      }
+      const int off = run + incl - t;
+      for (int q = 0; q < t && off + q < kMaxList; ++q) {
+        int* e = list + 4 * (off + q);
+        e[0] = b;
+        e[1] = q;
+        e[2] = tile_cost_nl<TQ, BN>(a, n, L, q) - 1;  // key tiles of the pair
+      }
+      run += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    // pieces per pair: theta by bisection over [kMinPieceTiles, longest]
+    int theta = 0x40000000;
+    if (split) {
+      int longest = 0;
+      for (int e = lane; e < pairs; e += 32) longest = max(longest, list[4 * e + 2]);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) longest = max(longest, __shfl_xor_sync(0xffffffffu, longest, o));
+      const int budget = min(a.one_wave, a.split_slots);
+      int lo = kMinPieceTiles, hi = max(kMinPieceTiles, longest);
+      while (lo < hi) {
+        const int mid = (lo + hi) / 2;
+        int units = 0;
+        for (int e = lane; e < pairs; e += 32) units += pieces_of(list[4 * e + 2], mid);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) units += __shfl_xor_sync(0xffffffffu, units, o);
+        if (units * a.Hkv <= budget)
+          hi = mid;
+        else
+          lo = mid + 1;
+      }
+      theta = hi;
+    }
+    run = 0;
+    for (int base = 0; base < pairs; base += 32) {
+      const int e = base + lane;
+      const int pc = (e < pairs) ? (split ? pieces_of(list[4 * e + 2], theta) : 1) : 0;
+      int incl = pc;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+      }
+      if (e < pairs) {
+        list[4 * e + 3] = pc;
+        uoff[e] = (run + incl - pc) * a.Hkv;
+      }
+      run += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    if (lane == 0) {
+      misc[0] = run * a.Hkv;  // units
+      misc[1] = -1;
+    }
+  }
+  __syncthreads();
+  const bool has = rank < misc[0];
+  if (has) {
+    for (int e = threadIdx.x; e < pairs; e += blockDim.x)
+      if (rank >= uoff[e] && rank < uoff[e] + list[4 * e + 3] * a.Hkv) misc[1] = e;
+  }
+  __syncthreads();
+  if (has) {
+    const int e = misc[1];
+    const int pc = list[4 * e + 3];
+    const int r = rank - uoff[e];
+    u->b = list[4 * e];
+    u->qt = list[4 * e + 1];
+    u->npieces = pc;
+    u->kvh = r / pc;
+    u->piece = r % pc;
+    u->slot0 = uoff[e] + u->kvh * pc;
+  }
+  __syncthreads();  // the scratch is free again
+  return has;
+}
+
 }  // namespace
 
 // Ranks (CTAs) a prefill launch needs: one per (request, query tile, KV
@@ -346,6 +475,10 @@ __device__ __forceinline__ void prefill_body(const PrefillArgs& a, const CUtenso
   int* rL = cache ? rn + kReqCache : nullptr;
   static_assert((kReqCacheOffset + 2 * kReqCache) * 4 <= S::KST * S::kKVBytes,
                 "the request cache fits in the K stages");
+  static_assert(kListOffset >= kReqCacheOffset + 2 * kReqCache &&
+                    (kListOffset + 5 * kMaxList + 4) * 4 <= S::KST * S::kKVBytes,
+                "the pair list fits in the K stages, past the request cache");
+  int pairs_with_work = 0;
   {
     int cnt = 0;
     for (int b = threadIdx.x; b < a.batch; b += blockDim.x) {
@@ -360,16 +493,29 @@ __device__ __forceinline__ void prefill_body(const PrefillArgs& a, const CUtenso
       if (n > 0 && n <= L && !(a.skip_decode_rows != 0 && n == 1)) cnt += (n + TQ - 1) / TQ;
     }
     block_excl_scan(cnt, scratch, scratch + 32);  // also orders rn / rL for every thread
-    const int pairs_with_work = scratch[32];
+    pairs_with_work = scratch[32];
     __syncthreads();
-    if (rank / a.Hkv >= pairs_with_work) return;  // uniform
   }
-  // costs are at most ceil(max_seq_len / BN) + 1 key tiles
-  const int nbuck = min(S::kCostBuckets, (a.max_seq_len + BN - 1) / BN + 2);
-  const int pair = lpt_pair<TQ, BN>(a, qtiles, rank / a.Hkv, scratch, nbuck, rn, rL);
-  it.b = pair / qtiles;
-  it.kvh = rank % a.Hkv;
-  const int qt = pair % qtiles;
+  // One wave: index order, and with a split workspace pieces along keys.
+  // More items than CTAs at once: heaviest first, whole items.
+  const long long items = static_cast<long long>(pairs_with_work) * a.Hkv;
+  int qt;
+  Unit un{0, 0, 0, 0, 1, 0};
+  if (items <= a.one_wave && pairs_with_work <= kMaxList) {
+    const bool split = a.split_o != nullptr && items < a.one_wave && items <= a.split_slots;
+    if (!one_wave_unit<TQ, BN>(a, rank, pairs_with_work, split, scratch, rn, rL, &un)) return;
+    it.b = un.b;
+    it.kvh = un.kvh;
+    qt = un.qt;
+  } else {
+    if (rank / a.Hkv >= pairs_with_work) return;  // uniform
+    // costs are at most ceil(max_seq_len / BN) + 1 key tiles
+    const int nbuck = min(S::kCostBuckets, (a.max_seq_len + BN - 1) / BN + 2);
+    const int pair = lpt_pair<TQ, BN>(a, qtiles, rank / a.Hkv, scratch, nbuck, rn, rL);
+    it.b = pair / qtiles;
+    it.kvh = rank % a.Hkv;
+    qt = pair % qtiles;
+  }
   it.n = query_span(a, it.b, &it.q0);
   if (it.n < 0) return;  // uniform (reported by the first pass)
   it.L = a.seq_lens[it.b];
@@ -392,6 +538,13 @@ __device__ __forceinline__ void prefill_body(const PrefillArgs& a, const CUtenso
   it.kbase = t_lo & ~(kBlockSize - 1);
   it.ntiles = (p_last + 1 - it.kbase + BN - 1) / BN;
   it.nblk = (it.L + kBlockSize - 1) / kBlockSize;
+  if (un.npieces > 1) {
+    // this piece's key tiles
+    const int j0 = un.piece * it.ntiles / un.npieces;
+    const int j1 = (un.piece + 1) * it.ntiles / un.npieces;
+    it.kbase += j0 * BN;
+    it.ntiles = j1 - j0;
+  }
 
   uint8_t* sQ = smem + S::oQ;
   uint8_t* sK = smem + S::oK;
@@ -738,9 +891,69 @@ __device__ __forceinline__ void prefill_body(const PrefillArgs& a, const CUtenso
     }
     if (ok && threadIdx.x == 0) PKA_PF_SET(rank, 2);
     const bool full = (it.it1 - it.it0 + 1 == TQ);  // uniform over the CTA
-    if (ok) {
+    // A piece of an item split along keys leaves its softmax-normalised rows
+    // (fp32) and their log2-domain LSEs in its workspace slot; the piece that
+    // arrives last on the item's counter merges every piece's slot, in piece
+    // order (the same bits whichever piece merges), and writes the output.
+    const bool split_item = un.npieces > 1;  // uniform over the CTA
+    bool write_out = true;
+    if (split_item) {
+      const int slot = un.slot0 + un.piece;
+      if (ok) {
+        tc_fence_after();
+        const float inv = (l > 0.f) ? 1.f / l : 0.f;
+        // [slot][D / 4][128 rows] float4: the 128 rows of a column group are
+        // consecutive, so each store instruction of a warp is coalesced
+        float4* po = reinterpret_cast<float4*>(a.split_o) + static_cast<size_t>(slot) * (D / 4) * 128 + r;
+#pragma unroll 1
+        for (int c = 0; c < D / 64; ++c) {
+          float o[64];
+          tmem_ld64(lane_base + S::kTmemO + c * 64, o);
+#pragma unroll
+          for (int e = 0; e < 16; ++e)
+            po[(c * 16 + e) * 128] = make_float4(o[4 * e] * inv, o[4 * e + 1] * inv,
+                                                 o[4 * e + 2] * inv, o[4 * e + 3] * inv);
+        }
+        a.split_lse[static_cast<size_t>(slot) * 128 + r] =
+            (l > 0.f) ? m_ref + log2f(l) : -INFINITY;
+      }
+      volatile int* last = reinterpret_cast<volatile int*>(smem + S::oMisc + 8);
+      asm volatile("bar.sync %0, %1;" ::"r"(kBarSoftmax), "r"(128) : "memory");
+      if (threadIdx.x == 0) {
+        fence_acq_rel_gpu();  // the CTA's rows (ordered by the barrier) before its arrival
+        const int old = atomicAdd(a.split_cnt + un.slot0, 1);
+        *last = (old == un.npieces - 1) ? 1 : 0;
+        if (old == un.npieces - 1) a.split_cnt[un.slot0] = 0;  // for the next call
+      }
+      asm volatile("bar.sync %0, %1;" ::"r"(kBarSoftmax), "r"(128) : "memory");
+      write_out = (*last != 0);
+      if (write_out) fence_acq_rel_gpu();  // every piece's rows are visible now
+    }
+    if (write_out && ok) {
       tc_fence_after();
-      const float inv = (l > 0.f) ? 1.f / l : 0.f;
+      float inv = (l > 0.f) ? 1.f / l : 0.f;
+      // split item: the pieces' weights 2^(LSE_k - max LSE)
+      float w[kMaxPieces];
+      const float4* pk = split_item ? reinterpret_cast<const float4*>(a.split_o) +
+                                          static_cast<size_t>(un.slot0) * (D / 4) * 128 + r
+                                    : nullptr;
+      if (split_item) {
+        float lk[kMaxPieces];
+        float M = -INFINITY;
+#pragma unroll
+        for (int k = 0; k < kMaxPieces; ++k) {
+          lk[k] = (k < un.npieces) ? __ldcg(a.split_lse + static_cast<size_t>(un.slot0 + k) * 128 + r)
+                                   : -INFINITY;
+          M = fmaxf(M, lk[k]);
+        }
+        float den = 0.f;
+#pragma unroll
+        for (int k = 0; k < kMaxPieces; ++k) {
+          w[k] = (M == -INFINITY) ? 0.f : fast_exp2(lk[k] - M);
+          den += w[k];
+        }
+        inv = (den > 0.f) ? 1.f / den : 0.f;
+      }
       // A tile of TQ tokens of this request leaves through TMA stores from
       // the Q tile's shared memory, which is free once the last MMA has
       // completed (the last P V commit covers every earlier MMA): each row
@@ -753,7 +966,28 @@ __device__ __forceinline__ void prefill_body(const PrefillArgs& a, const CUtenso
 #pragma unroll 1
       for (int c = 0; c < D / 64; ++c) {  // 64 columns per load and wait
         float o[64];
-        tmem_ld64(lane_base + S::kTmemO + c * 64, o);
+        if (split_item) {
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+            for (int k = 0; k < kMaxPieces; ++k) {
+              if (k < un.npieces) {
+                const float4 v = __ldcg(pk + (static_cast<size_t>(k) * (D / 4) + c * 16 + e) * 128);
+                acc.x = fmaf(w[k], v.x, acc.x);
+                acc.y = fmaf(w[k], v.y, acc.y);
+                acc.z = fmaf(w[k], v.z, acc.z);
+                acc.w = fmaf(w[k], v.w, acc.w);
+              }
+            }
+            o[4 * e] = acc.x;
+            o[4 * e + 1] = acc.y;
+            o[4 * e + 2] = acc.z;
+            o[4 * e + 3] = acc.w;
+          }
+        } else {
+          tmem_ld64(lane_base + S::kTmemO + c * 64, o);
+        }
         uint8_t* srow = sQ + c * S::kQChunk + r * 128;
 #pragma unroll
         for (int q = 0; q < 8; ++q) {
@@ -768,7 +1002,7 @@ __device__ __forceinline__ void prefill_body(const PrefillArgs& a, const CUtenso
         }
       }
     }
-    if (full) {
+    if (full && write_out) {
       // every softmax warp arrives, whatever its waits gave; the tile is
       // stored only if no wait of the CTA ran out
       fence_proxy_async_smem();

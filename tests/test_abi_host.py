@@ -130,7 +130,11 @@ def test_mixed_workspace_argument_errors(L):
     pool = _pool()
     par = binding.PkaAttnParams(0.1, 0.0, 0, None)
     need = L.paged_prefill_attn_ws_bytes(2, 8, 2, 128, 64, 0)
-    assert need == L.paged_decode_attn_ws_bytes(2, 8, 2, 128, 64, 0) > 0
+    # the decode workspace, then 160 prefill piece slots of 128 rows x D fp32,
+    # their LSEs and their counters (the header's layout)
+    dec = L.paged_decode_attn_ws_bytes(2, 8, 2, 128, 64, 0)
+    assert dec > 0
+    assert need == dec + 160 * 128 * 128 * 4 + 160 * 128 * 4 + 160 * 4
 
     def call(qsl=80, ws=256, nbytes=None, max_query_len=5):
         return L.paged_prefill_attn_ws(32, 32, ctypes.byref(pool), 64, 4, qsl, 64, 2, 8, 10,

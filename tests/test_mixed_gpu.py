@@ -19,15 +19,23 @@ def built():
     binding.lib()
 
 
+SPLIT_SLOTS = 160  # prefill pieces the workspace holds (include/paged_attn.h)
+
+
 def counters(runner):
-    """Arrival counters of the workspace (the fused decode's layout)."""
+    """Arrival counters of the workspace: the decode segments' (the fused
+    decode's layout), then the prefill pieces' after their rows and LSEs."""
     b = runner.batch
     S, _ = binding.paged_decode_splitk_plan(b.num_requests, b.num_kv_heads, b.max_seq_len, 16,
                                             b.window)
     B, Hq, D, Hkv = b.num_requests, b.num_q_heads, b.head_dim, b.num_kv_heads
     off = B * Hq * S * D * 4 + (B * Hq * S * 4 + 15) // 16 * 16
-    assert runner.workspace.numel() == off + (B * Hkv * 4 + 15) // 16 * 16
-    return runner.workspace[off:off + B * Hkv * 4].view(torch.int32)
+    dec_end = off + (B * Hkv * 4 + 15) // 16 * 16
+    poff = dec_end + SPLIT_SLOTS * 128 * (D + 1) * 4
+    assert runner.workspace.numel() == poff + (SPLIT_SLOTS * 4 + 15) // 16 * 16
+    ws = runner.workspace
+    return torch.cat([ws[off:off + B * Hkv * 4].view(torch.int32),
+                      ws[poff:poff + SPLIT_SLOTS * 4].view(torch.int32)])
 
 
 def check(batch, what, reqs=None, calls=2):
@@ -123,3 +131,84 @@ def test_full_size_mixed_sampled_requests():
     B = batch.num_requests
     reqs = [0, 17, 31, 32, 50, 63, 64, 65, 66, B - 1]
     check(batch, "cfg5 full size", reqs=reqs)
+
+
+def expected_pieces(batch):
+    """Pieces per prefill item the header's rule gives for this batch on
+    this GPU (every item's key tiles, the wave of SMs the decode CTAs leave),
+    restated from the paged_prefill_attn_ws comment."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    L = batch.seq_lens.tolist()
+    qsl = batch.query_start_loc.tolist()
+    B, Hkv, D = batch.num_requests, batch.num_kv_heads, batch.head_dim
+    G = batch.num_q_heads // Hkv
+    TQ = 128 // G
+    BN = 64 if D == 256 else 128
+    W = batch.window
+    tiles = []
+    for r in range(B):
+        n = qsl[r + 1] - qsl[r]
+        if n <= 1 or n > L[r]:
+            continue
+        for qt in range(-(-n // TQ)):
+            p_first = L[r] - n + qt * TQ
+            p_last = L[r] - n + min(n, (qt + 1) * TQ) - 1
+            t_lo = max(0, p_first - W + 1) if W > 0 else 0
+            tiles.append(-(-(p_last + 1 - (t_lo // 16) * 16) // BN))
+    # the SMs left to the prefill items (the host's split of the SMs)
+    extra = qsl[-1] - B
+    est = -(-extra // TQ) * Hkv if extra > 0 else 0
+    mql, msl = batch.max_query_len, batch.max_seq_len
+    keys = min(msl, W + TQ) if W > 0 else msl
+    prefill_us = est * (-(-keys // BN) + 1) * 2.0
+    chunks = -(-extra // (mql - 1)) if extra > 0 and mql > 1 else 0
+    dec_rows = max(0, B - chunks)
+    dec_keys = min(msl, W) if W > 0 else msl
+    decode_us = dec_rows * Hkv * (-(-dec_keys // 16)) * (64.0 * D) / 70.0e3
+    wave = 0
+    if est > 0:
+        share = int(sms * prefill_us / (prefill_us + decode_us) + 0.5)
+        wave = share if share >= 2 * est else est
+        wave = min(max(wave, 1), sms - sms // 4)
+    items = len(tiles) * Hkv
+    if not (0 < items < wave and items <= SPLIT_SLOTS):
+        return [1] * len(tiles)
+    budget = min(wave, SPLIT_SLOTS)
+
+    def pieces(t, th):
+        return min(8, max(1, -(-t // th)))
+    lo, hi = 4, max(4, max(tiles))
+    while lo < hi:
+        mid = (lo + hi) // 2
+        if sum(pieces(t, mid) for t in tiles) * Hkv <= budget:
+            hi = mid
+        else:
+            lo = mid + 1
+    return [pieces(t, hi) for t in tiles]
+
+
+@pytest.mark.parametrize("D,G,window,softcap", [(256, 4, 0, 0.0), (256, 4, 1024, 50.0),
+                                                (128, 4, 0, 30.0), (256, 8, 0, 0.0),
+                                                (128, 1, 2000, 0.0)])
+def test_prefill_tiles_split_along_keys(D, G, window, softcap):
+    """A few long-context chunk tiles next to decode rows: the items fill far
+    less than the wave of SMs left to them, so each is cut along its keys
+    into pieces on separate CTAs, merged by the piece that finishes last;
+    the result matches the oracle, repeats bit for bit, and every counter is
+    left zero."""
+    Hkv = 2 if G < 8 else 1
+    L = [3000, 40, 2500, 1, 700, 4100]
+    n = [1, 1, 40, 1, 1, 16]
+    b = small(L, n, D=D, G=G, Hkv=Hkv, window=window, softcap=softcap, seed=D + G + window)
+    assert max(expected_pieces(b)) > 1, "the case must force pieces"
+    check(b, f"split D={D} G={G} W={window} cap={softcap}")
+
+
+def test_split_pieces_short_and_ragged_tiles():
+    """Pieces of 4-8 key tiles, a chunk whose last query tile is ragged, and
+    a chunk short enough to stay whole, in one launch."""
+    L = [1, 900, 33, 2100, 520]
+    n = [1, 37, 1, 200, 3]
+    b = small(L, n, seed=77, softcap=50.0)
+    assert max(expected_pieces(b)) > 1
+    check(b, "split ragged")
