@@ -711,51 +711,72 @@ __device__ __forceinline__ void decode_body(const DecodeArgs& a, const CUtensorM
 #pragma unroll
       for (int i = 0; i < S::kMaxPend; ++i)
         if (i < npend) pend_last[i] = (old[i] == pend[i * 4 + 2] - 1) ? 1 : 0;
+      // the other CTAs' partials of every segment this CTA completes are
+      // visible to the consumer threads after this fence and the barrier
+      fence_acq_rel_gpu();
     }
     named_sync(cx.bar_cons, NW * 32);
     for (int i = 0; i < npend; ++i) {
       if (pend_last[i] == 0) continue;  // uniform
       const int cb = pend[i * 4], ckvh = pend[i * 4 + 1], np = pend[i * 4 + 2];
       const int cqrow = pend[i * 4 + 3];
-      fence_acq_rel_gpu();  // every other piece's partials are visible now
       // One pass over the pieces (read from L2): four consecutive columns
       // of one head per item, the pieces' LSE and partial rows of four
-      // pieces loaded together, merged with a running maximum.  The item
-      // loop is unrolled so that the loads of all of a thread's items are
-      // in flight together.
+      // pieces loaded together, merged with a running maximum.  Up to
+      // kBatch of a thread's items go together, group by group, so that
+      // their loads are in flight at once.
       constexpr int kItems = G * (D / 4);
       constexpr int kPerThread = (kItems + NW * 32 - 1) / (NW * 32);
+      constexpr int kBatch = kPerThread < 2 ? kPerThread : 2;
+#pragma unroll 1
+      for (int k0 = 0; k0 < kPerThread; k0 += kBatch) {
+        float M[kBatch], den[kBatch];
+        float4 acc[kBatch];
+        size_t ph0[kBatch];
 #pragma unroll
-      for (int k = 0; k < kPerThread; ++k) {
-        const int item = cx.tid + k * NW * 32;
-        if (item < kItems) {
-          const int h = item / (D / 4);
-          const int d0 = (item % (D / 4)) * 4;
-          const size_t ph0 =
-              (static_cast<size_t>(cb) * a.Hq + ckvh * G + h) * a.num_splits;
-          float M = -INFINITY, den = 0.f;
-          float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-          for (int s0 = 0; s0 < np; s0 += 4) {
-            float lv[4];
-            float4 x[4];
+        for (int k = 0; k < kBatch; ++k) {
+          const int item = cx.tid + (k0 + k) * NW * 32;
+          M[k] = -INFINITY;
+          den[k] = 0.f;
+          acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+          ph0[k] = (static_cast<size_t>(cb) * a.Hq + ckvh * G + min(item, kItems - 1) / (D / 4)) *
+                   a.num_splits;
+        }
+        for (int s0 = 0; s0 < np; s0 += 4) {
+          float lv[kBatch][4];
+          float4 x[kBatch][4];
+#pragma unroll
+          for (int k = 0; k < kBatch; ++k) {
+            const int item = cx.tid + (k0 + k) * NW * 32;
+            const int d0 = (item % (D / 4)) * 4;
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
-              if (s0 + u < np) {
-                lv[u] = __ldcg(a.partial_lse + ph0 + s0 + u);
-                x[u] = __ldcg(reinterpret_cast<const float4*>(a.partial_o +
-                                                              (ph0 + s0 + u) * D + d0));
+              if (k0 + k < kPerThread && item < kItems && s0 + u < np) {
+                lv[k][u] = __ldcg(a.partial_lse + ph0[k] + s0 + u);
+                x[k][u] = __ldcg(reinterpret_cast<const float4*>(a.partial_o +
+                                                                 (ph0[k] + s0 + u) * D + d0));
               } else {
-                lv[u] = -INFINITY;
-                x[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+                lv[k][u] = -INFINITY;
+                x[k][u] = make_float4(0.f, 0.f, 0.f, 0.f);
               }
             }
-            lse_merge4(M, den, acc, lv, x);
           }
-          const float inv = den > 0.f ? 1.f / den : 0.f;
-          uint16_t* dst = reinterpret_cast<uint16_t*>(a.out) +
-                          (static_cast<size_t>(cqrow) * a.Hq + ckvh * G + h) * D + d0;
-          *reinterpret_cast<uint2*>(dst) = make_uint2(pack_bf16x2(acc.x * inv, acc.y * inv),
-                                                      pack_bf16x2(acc.z * inv, acc.w * inv));
+#pragma unroll
+          for (int k = 0; k < kBatch; ++k) lse_merge4(M[k], den[k], acc[k], lv[k], x[k]);
+        }
+#pragma unroll
+        for (int k = 0; k < kBatch; ++k) {
+          const int item = cx.tid + (k0 + k) * NW * 32;
+          if (k0 + k < kPerThread && item < kItems) {
+            const int h = item / (D / 4);
+            const int d0 = (item % (D / 4)) * 4;
+            const float inv = den[k] > 0.f ? 1.f / den[k] : 0.f;
+            uint16_t* dst = reinterpret_cast<uint16_t*>(a.out) +
+                            (static_cast<size_t>(cqrow) * a.Hq + ckvh * G + h) * D + d0;
+            *reinterpret_cast<uint2*>(dst) =
+                make_uint2(pack_bf16x2(acc[k].x * inv, acc[k].y * inv),
+                           pack_bf16x2(acc[k].z * inv, acc[k].w * inv));
+          }
         }
       }
       named_sync(cx.bar_cons, NW * 32);
