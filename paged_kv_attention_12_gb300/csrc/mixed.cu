@@ -54,7 +54,7 @@ __global__ void __launch_bounds__(PrefillShape<D, G>::kThreads, 1)
                        const __grid_constant__ CUtensorMap tm_out) {
   extern __shared__ uint8_t smem_raw[];
   if (static_cast<int>(blockIdx.x) >= n_decode) {
-    prefill_body<D, G>(pa, &tm_q, &tm_k_rows, &tm_v_tiles, &tm_out, smem_raw,
+    prefill_body<D, G, true>(pa, &tm_q, &tm_k_rows, &tm_v_tiles, &tm_out, smem_raw,
                        static_cast<int>(blockIdx.x) - n_decode);
     return;
   }

@@ -14,7 +14,7 @@ __global__ void __launch_bounds__(PrefillShape<D, G>::kThreads, 1)
                          const __grid_constant__ CUtensorMap tm_v,
                          const __grid_constant__ CUtensorMap tm_out) {
   extern __shared__ uint8_t smem_raw[];
-  prefill_body<D, G>(a, &tm_q, &tm_k, &tm_v, &tm_out, smem_raw, static_cast<int>(blockIdx.x));
+  prefill_body<D, G, false>(a, &tm_q, &tm_k, &tm_v, &tm_out, smem_raw, static_cast<int>(blockIdx.x));
 }
 
 // ------------------------------------------------------------- launchers

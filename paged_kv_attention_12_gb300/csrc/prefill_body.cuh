@@ -445,7 +445,9 @@ inline long long prefill_ranks(const PrefillArgs& a, int TQ) {
 // One prefill work item per CTA on the S::kSmemBytes of shared memory at
 // smem_raw: the item of rank `rank` (heaviest first; ranks past the last
 // item return at once).
-template <int D, int G>
+// kSplit: the body can run pieces of items split along keys (the mixed
+// launch); without it the merge code is not compiled in.
+template <int D, int G, bool kSplit>
 __device__ __forceinline__ void prefill_body(const PrefillArgs& a, const CUtensorMap* tm_q,
                                              const CUtensorMap* tm_k, const CUtensorMap* tm_v,
                                              const CUtensorMap* tm_out, uint8_t* smem_raw,
@@ -502,7 +504,8 @@ __device__ __forceinline__ void prefill_body(const PrefillArgs& a, const CUtenso
   int qt;
   Unit un{0, 0, 0, 0, 1, 0};
   if (items <= a.one_wave && pairs_with_work <= kMaxList) {
-    const bool split = a.split_o != nullptr && items < a.one_wave && items <= a.split_slots;
+    const bool split =
+        kSplit && a.split_o != nullptr && items < a.one_wave && items <= a.split_slots;
     if (!one_wave_unit<TQ, BN>(a, rank, pairs_with_work, split, scratch, rn, rL, &un)) return;
     it.b = un.b;
     it.kvh = un.kvh;
@@ -895,7 +898,7 @@ __device__ __forceinline__ void prefill_body(const PrefillArgs& a, const CUtenso
     // (fp32) and their log2-domain LSEs in its workspace slot; the piece that
     // arrives last on the item's counter merges every piece's slot, in piece
     // order (the same bits whichever piece merges), and writes the output.
-    const bool split_item = un.npieces > 1;  // uniform over the CTA
+    const bool split_item = kSplit && un.npieces > 1;  // uniform over the CTA
     bool write_out = true;
     if (split_item) {
       const int slot = un.slot0 + un.piece;
