@@ -461,6 +461,34 @@ def other_workloads(dev, flush, iters=10, warmup=3, cfgs=(1, 3, 4, 5)):
         torch.cuda.empty_cache()
     if cfgs == (1, 3, 4, 5):
         res["append"] = time_append(dev, flush, iters, warmup)
+        res["long_chunk"] = time_long_chunk(dev, flush, iters, warmup, tc, tc_kind)
+    return res
+
+
+def time_long_chunk(dev, flush, iters, warmup, tc, tc_kind):
+    """One 512-token chunk at a 16K-token prefix beside 32 decode rows of 2K
+    tokens (Hq=8, Hkv=2, D=256, softcap 50): through paged_prefill_attn_ws,
+    whose 32 query-tile items fill far less than their SMs and are cut along
+    their keys, and through paged_prefill_attn, whole tiles."""
+    import torch
+    from paged_kv_attention_12_gb300 import binding, workload
+    L = [16896] + [2048] * 32
+    n = [512] + [1] * 32
+    batch = workload.make_batch(seq_lens=L, q_lens=n, num_q_heads=8, num_kv_heads=2,
+                                head_dim=256, num_blocks=sum(-(-x // 16) for x in L) + 8,
+                                device=dev, poison=False, cfg_id=42, seed=0, softcap=50.0)
+    flops = 4.0 * batch.head_dim * batch.num_q_heads * attention_pairs(batch)
+    mixed = binding.MixedBatch(batch)
+    out = torch.empty_like(batch.q)
+    res = {"workload": "one 512-token chunk at a 16384-token prefix + 32 decode rows of 2048 "
+                       "tokens, Hq=8, Hkv=2, D=256, softcap 50", "flops": flops}
+    for key, fn in (("ws_key_pieces", mixed.run),
+                    ("whole_tiles", lambda: binding.run_batch(batch, out))):
+        ms = time_launches(fn, flush, iters, warmup)
+        res[key] = {"ms": ms, "tflops": flops / (ms * 1e-3) / 1e12,
+                    "frac": flops / (ms * 1e-3) / 1e12 / tc, "peak_kind": tc_kind}
+    del batch, mixed, out
+    torch.cuda.empty_cache()
     return res
 
 
