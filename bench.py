@@ -332,12 +332,27 @@ def cpu_baseline(calls, prefill_batch, budget_s: float):
     finally:
         shutil.rmtree(tmp, ignore_errors=True)
     return {"value": decn, "unit": "GB/s", "cores": procs, "kind": "oracle",
+            "cpu_model": cpu_model(),
             "single_thread": {"value": dec1, "unit": "GB/s", "cores": 1},
             "sample": f"decode serving workload, all {len(files)} requests of both layers: "
                       f"{reps1} passes on one thread ({t1:.1f} s), {repsn} passes over "
                       f"{procs} spawned processes ({tn:.1f} s); fp64 numpy oracle, BLAS at "
                       f"one thread per process",
             "prefill": pre}
+
+
+def cpu_model() -> str:
+    """The host CPU's model name (/proc/cpuinfo), or the platform's machine."""
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                key, _, val = line.partition(":")
+                if key.strip() in ("model name", "CPU part", "Model"):
+                    return val.strip()
+    except OSError:
+        pass
+    import platform
+    return platform.machine()
 
 
 def bf16_peak():
@@ -456,12 +471,49 @@ def other_workloads(dev, flush, iters=10, warmup=3, cfgs=(1, 3, 4, 5)):
         else:
             entry["roofline"] = {"bound": "hbm", "achieved": gbs, "peak": hbm,
                                  "peak_kind": hbm_kind, "unit": "GB/s", "frac": gbs / hbm}
+        if cfg == 3:
+            entry["split_sweep"] = split_sweep(batch, flush, iters, warmup, hbm)
         res[str(cfg)] = entry
         del batch, fn
         torch.cuda.empty_cache()
     if cfgs == (1, 3, 4, 5):
         res["append"] = time_append(dev, flush, iters, warmup)
         res["long_chunk"] = time_long_chunk(dev, flush, iters, warmup, tc, tc_kind)
+    return res
+
+
+def split_sweep(batch, flush, iters, warmup, hbm):
+    """The long-context decode through paged_decode_splitk + combine with
+    the work line cut for fewer pipelines than the plan's (min chunk C =
+    ceil(T / k) units for k pipelines, T the line's units): how many pieces a
+    segment gets, against the time."""
+    import torch
+    from paged_kv_attention_12_gb300 import binding
+    B, Hkv, Hq, D = batch.num_requests, batch.num_kv_heads, batch.num_q_heads, batch.head_dim
+    nb = (batch.seq_lens.cpu() + 15) // 16
+    T = int(((nb + 4) * Hkv).sum())
+    tmax = (batch.max_seq_len + 15) // 16
+    nbytes = batch_kv_bytes(batch)
+    out = torch.empty_like(batch.q)
+    res = []
+    S0, C0 = binding.paged_decode_splitk_plan(B, Hkv, batch.max_seq_len, 16, batch.window)
+    for k in (0, 152, 76, 38, 19):
+        C = C0 if k == 0 else max(C0, -(-T // k))
+        S = S0 if k == 0 else -(-tmax // C) + 1
+        po = torch.empty((B, Hq, S, D), dtype=torch.float32, device=batch.q.device)
+        pl = torch.empty((B, Hq, S), dtype=torch.float32, device=batch.q.device)
+
+        def fn(C=C, S=S, po=po, pl=pl):
+            binding.paged_decode_splitk(batch.q, po, pl, batch.k_pool, batch.v_pool,
+                                        batch.block_tables, batch.seq_lens, batch.max_seq_len,
+                                        S, C, scale=batch.scale, softcap=batch.softcap,
+                                        window=batch.window)
+            binding.paged_decode_splitk_combine(po, pl, out)
+        ms = time_launches(fn, flush, iters, warmup)
+        res.append({"pipelines_used": "plan" if k == 0 else k, "min_chunk_units": C,
+                    "num_splits": S, "ms": ms, "kv_gbs": nbytes / (ms * 1e-3) / 1e9,
+                    "frac": nbytes / (ms * 1e-3) / 1e9 / hbm})
+        del po, pl
     return res
 
 
