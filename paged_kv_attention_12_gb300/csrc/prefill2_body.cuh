@@ -1,0 +1,791 @@
+// Chunked prefill at D = 256 on CTA pairs (sm_103a): the tcgen05 MMAs of
+// two SMs work as one, M = 256 rows over the pair.
+//
+// The same method as prefill_body.cuh ("Triton paged decode and prefill
+// kernels reading K/V through block tables", inference-server README,
+// engine feature list; causal attention over the cached prefix and the
+// chunk), with the work item doubled: a cluster of two CTAs takes two
+// consecutive query tiles of one (request, KV head) -- the rank-0 CTA the
+// first 128 rows, the rank-1 CTA the next 128 -- and streams the keys both
+// tiles see.  Every MMA is issued once, by the rank-0 CTA, for both
+// (tcgen05.mma.cta_group::2):
+//
+//  * S = Q K^T with M = 256 (each CTA's Q tile is its half of A) and the key
+//    tile's 64 keys split between the CTAs' shared memory (N = 64: each CTA
+//    holds 32 keys of every K stage);
+//  * O += P V with P from each CTA's own TMEM and V split by columns (each
+//    CTA holds 128 of the 256 columns of every V stage).
+//
+// So each SM receives and reads half of every K/V tile instead of all of
+// it: at D = 256 a single SM's shared memory (a 64 KB Q tile plus the K/V
+// rings) and its bandwidth set the pace of the one-CTA kernel, and the pair
+// halves the ring bytes per key and doubles the stages that fit.  TMEM
+// holds each CTA's own rows (S, P and O as in the one-CTA kernel).
+//
+// Cross-CTA signalling: both CTAs' TMA copies complete on the rank-0 CTA's
+// "full" barriers (cp.async.bulk.tensor ... .cta_group::2), the MMA commits
+// arrive on the barriers of both CTAs (multicast), and each CTA's softmax
+// reports its P with one remote arrive on the rank-0 CTA's barrier.  All
+// mbarrier waits are bounded; the TMEM allocation is a collective of the
+// pair, which both CTAs reach unconditionally, and the pair meets at a
+// cluster barrier before it frees TMEM and exits.
+#pragma once
+
+#include "prefill_body.cuh"
+
+namespace pka {
+
+template <int G>
+struct Prefill2Shape {
+  static constexpr int D = 256;
+  static constexpr int BM = 128;                    // rows per CTA (256 per pair)
+  static constexpr int TQ = BM / G;                 // query tokens per CTA tile
+  static constexpr int BN = 128;                    // keys per key tile (pair)
+  static constexpr int DC = D / 64;                 // 128-byte chunks of a row
+  static constexpr int kHalfKeys = BN / 2;          // keys of a K stage per CTA
+  static constexpr int kQChunk = BM * 128;
+  static constexpr int kKChunk = kHalfKeys * 128;   // K stage: [DC][64 keys][128 B]
+  static constexpr int kKStage = kHalfKeys * D * 2; // 32 KB
+  static constexpr int kVBlock = kBlockSize * (DC / 2) * 128;  // [2 chunks][16 rows][128 B]
+  static constexpr int kVStage = BN * (D / 2) * 2;  // 32 KB: 128 keys x 128 columns
+  static constexpr int kQBytes = BM * D * 2;
+  static constexpr int KST = 3;                     // K ring stages
+  static constexpr int VST = 2;                     // V ring stages
+  static constexpr int oQ = 0;
+  static constexpr int oK = oQ + kQBytes;
+  static constexpr int oV = oK + KST * kKStage;
+  static constexpr int oBar = oV + VST * kVStage;
+  // Q, K full/empty per stage, V full/empty per stage, S ready x2, P ready x2
+  static constexpr int kNumBars = 1 + 2 * KST + 2 * VST + 2 + 2;
+  static constexpr int oMisc = oBar + kNumBars * 8;
+  static constexpr int kSmemBytes = oMisc + 16 + 1024;
+  static constexpr uint32_t kTmemO = 256;
+  // P_j (bf16 pairs, BN / 2 columns) is written over the first half of
+  // S_j's own buffer once the softmax has read S_j: 2 S buffers of 128
+  // columns and O fill the 512 columns, so S_{j+2} is issued only once
+  // P_j V_j has completed.
+  static constexpr uint32_t kTmemCols = 512;
+  static constexpr int kThreads = 8 * 32;
+  static constexpr int kCostBuckets = 4096;
+  static_assert((kCostBuckets + 64) * 4 <= KST * kKStage, "ranking scratch");
+  static_assert((kReqCacheOffset + 2 * kReqCache) * 4 <= KST * kKStage, "request cache");
+  static_assert(kSmemBytes <= 232448, "shared memory");
+  static_assert(KST == 3 && VST == 2, "the barrier map below assumes 3 K and 2 V stages");
+  static_assert(2 * BN + D <= kTmemCols, "TMEM columns");
+};
+
+namespace pair2 {
+
+enum {
+  PB_Q = 0,
+  PB_KFULL = 1,                          // [KST], completed on the rank-0 CTA
+  PB_KEMPTY = PB_KFULL + 3,               // [KST], both CTAs (multicast commit)
+  PB_VFULL = PB_KEMPTY + 3,               // [VST], completed on the rank-0 CTA
+  PB_VEMPTY = PB_VFULL + 2,               // [VST], both CTAs (multicast commit)
+  PB_QK = PB_VEMPTY + 2,                  // [2] S_j ready, both CTAs
+  PB_PRDY = PB_QK + 2,                    // [2] P_j ready, rank-0 CTA, 8 arrivals
+};
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+// The shared::cluster address of this CTA's variable in the rank-0 CTA.
+__device__ __forceinline__ uint32_t leader_addr(const void* p) {
+  uint32_t a;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, 0;" : "=r"(a) : "r"(smem_u32(p)));
+  return a;
+}
+
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" :::
+                   "memory");
+}
+
+// TMA copies into this CTA's shared memory completing on a barrier of the
+// rank-0 CTA (a shared::cluster address).
+__device__ __forceinline__ void tma2_load_2d(void* dst, const CUtensorMap* map, int x, int y,
+                                             uint32_t bar_cluster) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes "
+      "[%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar_cluster)
+      : "memory");
+}
+
+__device__ __forceinline__ void tma2_load_3d(void* dst, const CUtensorMap* map, int x, int y,
+                                             int z, uint32_t bar_cluster) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes "
+      "[%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar_cluster)
+      : "memory");
+}
+
+__device__ __forceinline__ void umma2(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                      uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+__device__ __forceinline__ void umma2_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                         uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Arrive on the barrier at this offset in both CTAs once every MMA issued
+// so far by this thread has completed.
+__device__ __forceinline__ void commit2_both(uint64_t* bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 "
+      "[%0], %1;" ::"r"(smem_u32(bar)),
+      "h"(static_cast<uint16_t>(3))
+      : "memory");
+}
+
+__device__ __forceinline__ void remote_arrive(uint32_t bar_cluster) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster)
+               : "memory");
+}
+
+__device__ __forceinline__ void tmem2_alloc(uint32_t* slot, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                   smem_u32(slot)),
+               "r"(ncols)
+               : "memory");
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem2_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+               : "memory");
+}
+
+// The waits that consume another CTA's signals (remote arrivals, copies
+// of the peer) acquire at cluster scope.
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+__device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity, int32_t* err) {
+  if (mbar_try_wait_cluster(bar, parity)) return true;
+  const long long t0 = clock64();
+  while (true) {
+    if (mbar_try_wait_cluster(bar, parity)) return true;
+    if (clock64() - t0 > kWaitBudgetCycles) {
+      report(err, PKA_DEVERR_TIMEOUT);
+      return false;
+    }
+  }
+}
+
+// Every lane waits (cluster scope); the warp agrees on one outcome.
+__device__ __forceinline__ bool warp_wait_cluster(uint64_t* bar, uint32_t parity, int32_t* err,
+                                                  volatile int* failed) {
+  const bool ok = __all_sync(0xffffffffu, mbar_wait_cluster(bar, parity, err));
+  if (!ok) *failed = 1;
+  return ok;
+}
+
+}  // namespace pair2
+
+// One pair item per cluster of two CTAs on the S::kSmemBytes of shared
+// memory at smem_raw: the cluster of index blockIdx.x / 2 takes the pair
+// item of that rank (heaviest first over (request, two query tiles) pairs),
+// KV head rank % Hkv; ranks past the last item return at once (both CTAs of
+// a cluster decide alike: everything up to the TMEM allocation depends on
+// the arguments and the cluster's index only).
+template <int G>
+__device__ __forceinline__ void prefill2_body(const PrefillArgs& a, const CUtensorMap* tm_q,
+                                              const CUtensorMap* tm_k, const CUtensorMap* tm_v,
+                                              const CUtensorMap* tm_out, uint8_t* smem_raw) {
+  using S = Prefill2Shape<G>;
+  using namespace pair2;
+  constexpr int D = S::D, BN = S::BN, TQ = S::TQ, DC = S::DC;
+  constexpr int TQ2 = 2 * TQ;  // query tokens of a pair item
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  const int crank = static_cast<int>(cluster_rank());
+  const int rank = static_cast<int>(blockIdx.x) / 2;
+
+  // ---------------------------------------------------------- work item
+  Item it;
+  const int qtiles = (a.max_query_len + TQ2 - 1) / TQ2;
+  int* scratch = reinterpret_cast<int*>(smem + S::oK);
+  const bool cache = a.batch <= kReqCache;
+  int* rn = cache ? scratch + kReqCacheOffset : nullptr;
+  int* rL = cache ? rn + kReqCache : nullptr;
+  {
+    int cnt = 0;
+    for (int b = threadIdx.x; b < a.batch; b += blockDim.x) {
+      int q0;
+      const int n = query_span(a, b, &q0);
+      if (n < 0 && rank == 0 && crank == 0) report(a.err, PKA_DEVERR_QUERY_LOC);
+      const int L = min(a.seq_lens[b], a.max_blocks * kBlockSize);
+      if (cache) {
+        rn[b] = n;
+        rL[b] = L;
+      }
+      if (n > 0 && n <= L && !(a.skip_decode_rows != 0 && n == 1)) cnt += (n + TQ2 - 1) / TQ2;
+    }
+    block_excl_scan(cnt, scratch, scratch + 32);
+    const int pairs_with_work = scratch[32];
+    __syncthreads();
+    if (rank / a.Hkv >= pairs_with_work) return;  // uniform over the cluster
+  }
+  const int nbuck = min(S::kCostBuckets, (a.max_seq_len + BN - 1) / BN + 2);
+  const int pair = lpt_pair<TQ2, BN>(a, qtiles, rank / a.Hkv, scratch, nbuck, rn, rL);
+  it.b = pair / qtiles;
+  it.kvh = rank % a.Hkv;
+  const int qt2 = pair % qtiles;
+  it.n = query_span(a, it.b, &it.q0);
+  if (it.n < 0) return;  // uniform (reported by the first pass)
+  it.L = a.seq_lens[it.b];
+  if (it.L > a.max_blocks * kBlockSize) {
+    if (threadIdx.x == 0 && crank == 0 && qt2 == 0 && it.kvh == 0) report(a.err, PKA_DEVERR_SEQ_LEN);
+    it.L = a.max_blocks * kBlockSize;
+  }
+  if (it.n > it.L) {
+    if (threadIdx.x == 0 && crank == 0 && qt2 == 0 && it.kvh == 0) report(a.err, PKA_DEVERR_SEQ_LEN);
+    return;
+  }
+  it.it0 = qt2 * TQ2;
+  if (it.n <= 0 || it.it0 >= it.n || (a.skip_decode_rows != 0 && it.n == 1)) return;
+  it.it1 = min(it.n, it.it0 + TQ2) - 1;  // the pair's last query row
+  const int p_first = it.L - it.n + it.it0;
+  const int p_last = it.L - it.n + it.it1;
+  const int t_lo = (a.window > 0) ? max(0, p_first - a.window + 1) : 0;
+  it.kbase = t_lo & ~(kBlockSize - 1);
+  it.ntiles = (p_last + 1 - it.kbase + BN - 1) / BN;
+  it.nblk = (it.L + kBlockSize - 1) / kBlockSize;
+  const int my0 = it.it0 + crank * TQ;  // this CTA's first query row
+
+  uint8_t* sQ = smem + S::oQ;
+  uint8_t* sK = smem + S::oK;
+  uint8_t* sV = smem + S::oV;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S::oBar);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + S::oMisc);
+  volatile int* failed = reinterpret_cast<volatile int*>(smem + S::oMisc + 4);
+  const int warp = threadIdx.x / 32;
+  const int lane = threadIdx.x % 32;
+  const bool lead = (crank == 0);
+  const int stamp = static_cast<int>(blockIdx.x);  // instrumented builds: one row per CTA
+  if (threadIdx.x == 0) {
+    PKA_PF_SET(stamp, 0);
+    PKA_PF_VAL(stamp, 4, static_cast<unsigned long long>(it.ntiles));
+  }
+
+  if (threadIdx.x == 0) {
+    mbar_init(&bars[PB_Q], 1);
+    for (int i = 0; i < S::KST; ++i) {
+      mbar_init(&bars[PB_KFULL + i], 1);
+      mbar_init(&bars[PB_KEMPTY + i], 1);
+    }
+    for (int i = 0; i < S::VST; ++i) {
+      mbar_init(&bars[PB_VFULL + i], 1);
+      mbar_init(&bars[PB_VEMPTY + i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&bars[PB_QK + i], 1);
+      mbar_init(&bars[PB_PRDY + i], 8);  // each softmax warp of both CTAs
+    }
+    *failed = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == kWarpMma) tmem2_alloc(tmem_slot, S::kTmemCols);
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync_all();  // both CTAs' barriers exist before any signal crosses
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const uint32_t oob_row = static_cast<uint32_t>(a.num_blocks) * a.Hkv * kBlockSize;
+  const int32_t* trow = a.tables + static_cast<size_t>(it.b) * a.max_blocks;
+
+  if (warp == kWarpTmaK || warp == kWarpTmaK2 || warp == kWarpTmaV) {
+    // ============================ TMA producers ============================
+    // Each CTA loads its half of every stage -- K: 32 of the tile's 64 keys
+    // (blocks 2 crank, 2 crank + 1; one warp per block, one 2-D box per
+    // 64-column chunk), V: 128 of the 256 columns of all 64 keys (one 3-D
+    // box of two chunks per block) -- completing on the rank-0 CTA's "full"
+    // barrier, which expects both halves.  A stage is refilled once the MMA
+    // that read it has committed (the commit reaches both CTAs).
+    const bool is_k = (warp != kWarpTmaV);
+    const int kpart = (warp == kWarpTmaK2) ? 1 : 0;
+    const int nst = is_k ? S::KST : S::VST;
+    uint8_t* ring = is_k ? sK : sV;
+    const int full_base = is_k ? PB_KFULL : PB_VFULL;
+    const int empty_base = is_k ? PB_KEMPTY : PB_VEMPTY;
+    const uint32_t stage_bytes = is_k ? S::kKStage : S::kVStage;
+    int issued = 0;
+    if (lane == 0) {
+      prefetch_tensormap(is_k ? tm_k : tm_v);
+      if (warp == kWarpTmaK) {
+        prefetch_tensormap(tm_q);
+        if (lead) mbar_arrive_expect_tx(&bars[PB_Q], 2 * S::kQBytes);
+        const uint32_t qbar = leader_addr(&bars[PB_Q]);
+#pragma unroll
+        for (int c = 0; c < DC; ++c)
+          tma2_load_3d(sQ + c * S::kQChunk, tm_q, c * 64, it.kvh * G, it.q0 + my0, qbar);
+      }
+    }
+    // Pool rows of the item's blocks, 32 per coalesced load, in a window
+    // of 64 blocks held one per lane in two registers (see prefill_body).
+    constexpr int BPT = BN / kBlockSize;  // 8 blocks per key tile
+    const int jb0 = it.kbase / kBlockSize;
+    auto load_rows = [&](int base) -> uint32_t {
+      const int jb = jb0 + base + lane;
+      uint32_t row = oob_row;
+      if (jb < it.nblk) {
+        const int id = trow[jb];
+        if (static_cast<unsigned>(id) < static_cast<unsigned>(a.num_blocks))
+          row = (static_cast<uint32_t>(id) * a.Hkv + it.kvh) * kBlockSize;
+        else
+          report(a.err, PKA_DEVERR_BAD_TABLE);
+      }
+      return row;
+    };
+    int win = 0;
+    uint32_t rows_lo = load_rows(0), rows_hi = load_rows(32);
+    for (int j = 0; j < it.ntiles; ++j) {
+      if (__any_sync(0xffffffffu, stop_requested(failed))) break;
+      if (j * BPT >= win + 32) {
+        rows_lo = rows_hi;
+        rows_hi = load_rows(win + 64);
+        win += 32;
+      }
+      uint32_t rl[BPT];
+#pragma unroll
+      for (int kb = 0; kb < BPT; ++kb)
+        rl[kb] = __shfl_sync(0xffffffffu, rows_lo, (j * BPT + kb - win) & 31);
+      const int st = j % nst;
+      int good = 1;
+      if (lane == 0) {
+        if (j >= nst &&
+            !mbar_wait_cluster(&bars[empty_base + st], static_cast<uint32_t>((j / nst - 1) & 1), a.err)) {
+          *failed = 1;
+          good = 0;
+        }
+        if (good && lead && kpart == 0) mbar_arrive_expect_tx(&bars[full_base + st], 2 * stage_bytes);
+      }
+      if (!__shfl_sync(0xffffffffu, good, 0)) break;
+      const uint32_t fbar = leader_addr(&bars[full_base + st]);
+      uint8_t* dst = ring + st * stage_bytes;
+      if (is_k) {
+        if (lane < 2 * DC) {
+          // this CTA's keys: blocks 4 crank .. 4 crank + 3 of the tile; this
+          // warp: two of them, one box per (block, 64-column chunk)
+          const int kb = 2 * kpart + lane / DC, c = lane % DC;
+          uint32_t r = rl[0];
+#pragma unroll
+          for (int q = 1; q < BPT; ++q)
+            if ((BPT / 2) * crank + kb == q) r = rl[q];
+          tma2_load_2d(dst + c * S::kKChunk + kb * kBlockSize * 128, tm_k, c * 64,
+                       static_cast<int>(r), fbar);
+        }
+      } else if (lane < BPT) {
+        uint32_t r = rl[0];
+#pragma unroll
+        for (int q = 1; q < BPT; ++q)
+          if (lane == q) r = rl[q];
+        tma2_load_3d(dst + lane * S::kVBlock, tm_v, 0, static_cast<int>(r), (DC / 2) * crank, fbar);
+      }
+      issued = j + 1;
+    }
+    if (lane == 0 && lead) {
+      // every issued stage (both CTAs' halves) must land before the pair
+      // may finish
+      for (int j = issued - nst < 0 ? 0 : issued - nst; j < issued; ++j)
+        mbar_wait_cluster(&bars[full_base + j % nst], (j / nst) & 1, a.err);
+      if (warp == kWarpTmaK && stop_requested(failed)) mbar_wait_cluster(&bars[PB_Q], 0, a.err);
+    }
+    __syncwarp();
+  } else if (warp == kWarpMma) {
+    // ================================ MMA ================================
+    // Issued by the rank-0 CTA only, for both (M = 256).
+    if (lead) {
+      constexpr uint32_t idesc_qk = idesc_bf16_f32(256, BN, 0, 0);
+      constexpr uint32_t idesc_pv = idesc_bf16_f32(256, D, 0, 1);
+      const uint32_t aQ = smem_u32(sQ), aK = smem_u32(sK), aV = smem_u32(sV);
+      int committed_pv = 0;
+      bool ok = warp_wait_cluster(&bars[PB_Q], 0, a.err, failed);
+      auto issue_qk = [&](int j) -> bool {
+        const int st = j & 1;
+        const int ks = j % S::KST;
+        if (!warp_wait_cluster(&bars[PB_KFULL + ks], (j / S::KST) & 1, a.err, failed)) return false;
+        tc_fence_after();
+        if (lane == 0) {
+          const uint32_t kst = aK + ks * S::kKStage;
+#pragma unroll
+          for (int c = 0; c < DC; ++c)
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+              const uint64_t da = smem_desc_sw128(aQ + c * S::kQChunk + kk * 32, 16, 1024);
+              const uint64_t db = smem_desc_sw128(kst + c * S::kKChunk + kk * 32, 16, 1024);
+              umma2(tmem + st * BN, da, db, idesc_qk, (c | kk) != 0);
+            }
+          commit2_both(&bars[PB_QK + st]);
+          commit2_both(&bars[PB_KEMPTY + ks]);
+        }
+        __syncwarp();
+        return true;
+      };
+      if (ok) ok = issue_qk(0);
+      if (ok && it.ntiles > 1) ok = issue_qk(1);
+      for (int j = 0; ok && j < it.ntiles; ++j) {
+        if (__any_sync(0xffffffffu, stop_requested(failed))) break;
+        const int st = j & 1;
+        const uint32_t ph = (j >> 1) & 1;
+        const int vs = j % S::VST;
+        if (!warp_wait_cluster(&bars[PB_VFULL + vs], (j / S::VST) & 1, a.err, failed)) break;
+        // V rows at positions >= seq_len (stale slots of the last block,
+        // which may hold NaN) -> 0 in both CTAs' halves, before P V reads
+        // them (the peer's half through its cluster address)
+        const int t0 = it.kbase + j * BN;
+        const int z0 = it.L - t0;
+        const int z1 = min(BN, it.nblk * kBlockSize - t0);
+        if (z0 > 0 && z0 < z1) {
+          uint8_t* vst = sV + vs * S::kVStage;
+          const int per = (z1 - z0) * (DC / 2) * 8;  // 16-byte pieces per CTA
+          for (int idx = lane; idx < 2 * per; idx += 32) {
+            const int peer = idx / per;
+            const int rem = idx % per;
+            const int r = z0 + rem / ((DC / 2) * 8);
+            const int c = (rem / 8) % (DC / 2);
+            const int q = rem % 8;
+            uint8_t* ptr = vst + (r / kBlockSize) * S::kVBlock + c * (kBlockSize * 128) +
+                           (r % kBlockSize) * 128 + q * 16;
+            if (peer == 0) {
+              *reinterpret_cast<uint4*>(ptr) = make_uint4(0u, 0u, 0u, 0u);
+            } else {
+              uint32_t ra;
+              asm volatile("mapa.shared::cluster.u32 %0, %1, 1;" : "=r"(ra) : "r"(smem_u32(ptr)));
+              asm volatile("st.shared::cluster.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(ra), "r"(0u)
+                           : "memory");
+            }
+          }
+          fence_proxy_async_smem();
+          asm volatile("fence.proxy.async.shared::cluster;" ::: "memory");
+        }
+        __syncwarp();
+        if (!warp_wait_cluster(&bars[PB_PRDY + st], ph, a.err, failed)) break;
+        tc_fence_after();
+        if (lane == 0) {
+          const uint32_t vst = aV + vs * S::kVStage;
+#pragma unroll
+          for (int k = 0; k < BN / 16; ++k) {
+            // block k: two 64-column chunks 16 x 128 B apart
+            const uint64_t db = smem_desc_sw128(vst + k * S::kVBlock, kBlockSize * 128, 1024);
+            umma2_ts(tmem + S::kTmemO, tmem + st * BN + k * 8, db, idesc_pv,
+                     (j > 0 || k > 0) ? 1u : 0u);
+          }
+          commit2_both(&bars[PB_VEMPTY + vs]);
+        }
+        __syncwarp();
+        committed_pv = j + 1;
+        if (j + 2 < it.ntiles) {
+          // S_{j+2} overwrites S_j's buffer, which P_j V_j reads
+          ok = warp_wait_cluster(&bars[PB_VEMPTY + vs], (j / S::VST) & 1, a.err, failed);
+          if (ok) ok = issue_qk(j + 2);
+        }
+      }
+      // the last P V must finish before TMEM is freed
+      if (committed_pv > 0) {
+        const int jl = committed_pv - 1;
+        mbar_wait_cluster(&bars[PB_VEMPTY + jl % S::VST], (jl / S::VST) & 1, a.err);
+      }
+    }
+  } else {
+    constexpr bool kSplit = false;  // pieces along keys: the mixed launch's one-CTA body only
+    const Unit un{0, 0, 0, 0, 1, 0};
+    // ============================== softmax ==============================
+    const int r = threadIdx.x;  // row of the tile, TMEM lane
+    const int tok = r / G;
+    const int g = r % G;
+    const int qi = my0 + tok;
+    const bool row_valid = qi <= it.it1;
+    const int p = it.L - it.n + qi;
+    const int kmin = (a.window > 0) ? p - a.window + 1 : -0x40000000;
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+    const bool capped = a.softcap > 0.f;
+    const float sl2 = a.scale * kLog2e;
+    // The uncapped path masks the raw q.k and scales the row maximum, which is
+    // the maximum of the scaled logits only for scale > 0.  For scale <= 0
+    // (uniform over the launch) the logits are scaled before the mask, as the
+    // capped path does.
+    const bool prescale = capped || !(sl2 > 0.f);
+    const float cap_in = capped ? a.scale / a.softcap : 0.f;
+    const float cap_out = a.softcap * kLog2e;
+    float m_ref = -INFINITY;
+    float l = 0.f;
+    bool ok = true;
+    for (int j = 0; j < it.ntiles; ++j) {
+      if (__any_sync(0xffffffffu, stop_requested(failed))) {
+        ok = false;
+        break;
+      }
+      const int st = j & 1;
+      const uint32_t ph = (j >> 1) & 1;
+      if (!warp_wait_cluster(&bars[PB_QK + st], ph, a.err, failed)) {
+        ok = false;
+        break;
+      }
+      if (j == 0 && threadIdx.x == 0) PKA_PF_SET(stamp, 1);
+      tc_fence_after();
+      float s[BN];
+#pragma unroll
+      for (int c = 0; c < BN / 64; ++c) {  // 64 columns per load and wait
+        float t[64];
+        tmem_ld64(lane_base + st * BN + c * 64, t);
+#pragma unroll
+        for (int e = 0; e < 64; ++e) s[c * 64 + e] = t[e];
+      }
+      const int t0 = it.kbase + j * BN;
+      const int c_hi = row_valid ? min(BN - 1, p - t0) : -1;
+      const int c_lo = max(0, kmin - t0);
+      // Only rows on a causal diagonal or a window edge need the per-column
+      // mask; the warp takes the masked loop only if one of its rows does.
+      const bool need_mask = __any_sync(0xffffffffu, c_lo > 0 || c_hi < BN - 1);
+      if (capped) {
+        // log2-domain logits cap * tanh(s * scale / cap) * log2(e); a
+        // Taylor form when every |y| of the warp's rows is below 1/8 (three
+        // terms) or 0.5 (six terms), else the exp2 form
+        float amax = 0.f;
+#pragma unroll
+        for (int c = 0; c < BN; ++c) amax = fmaxf(amax, fabsf(s[c]));
+        if (__all_sync(0xffffffffu, amax * cap_in < 0.125f)) {
+#pragma unroll
+          for (int c = 0; c < BN; ++c) s[c] = cap_out * tanh_taylor_short(s[c] * cap_in);
+        } else if (__all_sync(0xffffffffu, amax * cap_in < 0.5f)) {
+#pragma unroll
+          for (int c = 0; c < BN; ++c) s[c] = cap_out * tanh_taylor(s[c] * cap_in);
+        } else {
+#pragma unroll
+          for (int c = 0; c < BN; ++c) s[c] = cap_out * tanh_via_exp2(s[c] * cap_in);
+        }
+      } else if (prescale) {
+#pragma unroll
+        for (int c = 0; c < BN; ++c) s[c] *= sl2;
+      }
+      // (otherwise s stays raw; scale > 0, so the raw max scales to the max)
+      if (need_mask) {
+#pragma unroll
+        for (int c = 0; c < BN; ++c)
+          if (!(c >= c_lo && c <= c_hi)) s[c] = -INFINITY;
+      }
+      float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+      for (int c = 0; c < BN; ++c) m4[c & 3] = fmaxf(m4[c & 3], s[c]);
+      float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+      if (!prescale) mx *= sl2;
+      const float m_new = fmaxf(m_ref, mx);
+      const bool resc = (j > 0) && (m_new > m_ref + 8.f);
+      if (__any_sync(0xffffffffu, resc)) {
+        // O must hold P_{j-1} V_{j-1} before it is rescaled
+        if (!warp_wait_cluster(&bars[PB_VEMPTY + (j - 1) % S::VST], ((j - 1) / S::VST) & 1, a.err,
+                               failed)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const float f = resc ? fast_exp2(m_ref - m_new) : 1.f;
+#pragma unroll 1
+        for (int c = 0; c < D / 32; ++c) {
+          float o[32];
+          tmem_ld32(lane_base + S::kTmemO + c * 32, o);
+#pragma unroll
+          for (int e = 0; e < 32; ++e) o[e] *= f;
+          tmem_st32(lane_base + S::kTmemO + c * 32, o);
+        }
+      }
+      if (resc) l *= fast_exp2(m_ref - m_new);
+      if (j == 0 || resc) m_ref = m_new;
+      const float ms = (m_ref == -INFINITY) ? 0.f : m_ref;
+      // P_j (bf16 pairs) over the first half of S_j's buffer: this thread
+      // has read S_j in full, and the MMA warp issues S_{j+2}, the buffer's
+      // next writer, only after P_j V_j has completed.
+      // p = 2^(x - ms), x the log2-domain logit (uncapped: x = s * scale * log2 e,
+      // fused into one FMA)
+      const float xs = prescale ? 1.f : sl2;
+      float lsum0 = 0.f, lsum1 = 0.f;
+#pragma unroll
+      for (int h = 0; h < BN / 64; ++h) {
+        uint32_t pk[32];
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+          const float p0 = fast_exp2(fmaf(s[h * 64 + 2 * e], xs, -ms));
+          const float p1 = fast_exp2(fmaf(s[h * 64 + 2 * e + 1], xs, -ms));
+          lsum0 += p0;
+          lsum1 += p1;
+          pk[e] = pack_bf16x2(p0, p1);
+        }
+        tmem_st32_u(lane_base + st * BN + h * 32, pk);
+      }
+      l += lsum0 + lsum1;
+      tmem_wait_st();
+      tc_fence_before();
+      // one arrival per warp on the rank-0 CTA's barrier once its 32 rows
+      // have written P_j (a warp that gave up does not arrive, and the MMA
+      // warp's bounded wait ends the item)
+      __syncwarp();
+      if (lane == 0) remote_arrive(leader_addr(&bars[PB_PRDY + st]));
+    }
+    // ------------------------------------------------------------ epilogue
+    if (ok) {
+      const int jl = it.ntiles - 1;
+      ok = warp_wait_cluster(&bars[PB_VEMPTY + jl % S::VST], (jl / S::VST) & 1, a.err, failed);
+    }
+    if (ok && threadIdx.x == 0) PKA_PF_SET(stamp, 2);
+    const bool full = (my0 + TQ - 1 <= it.it1);  // uniform over the CTA
+    // A piece of an item split along keys leaves its softmax-normalised rows
+    // (fp32) and their log2-domain LSEs in its workspace slot; the piece that
+    // arrives last on the item's counter merges every piece's slot, in piece
+    // order (the same bits whichever piece merges), and writes the output.
+    const bool split_item = kSplit && un.npieces > 1;  // uniform over the CTA
+    bool write_out = true;
+    if (split_item) {
+      const int slot = un.slot0 + un.piece;
+      if (ok) {
+        tc_fence_after();
+        const float inv = (l > 0.f) ? 1.f / l : 0.f;
+        // [slot][D / 4][128 rows] float4: the 128 rows of a column group are
+        // consecutive, so each store instruction of a warp is coalesced
+        float4* po = reinterpret_cast<float4*>(a.split_o) + static_cast<size_t>(slot) * (D / 4) * 128 + r;
+#pragma unroll 1
+        for (int c = 0; c < D / 64; ++c) {
+          float o[64];
+          tmem_ld64(lane_base + S::kTmemO + c * 64, o);
+#pragma unroll
+          for (int e = 0; e < 16; ++e)
+            po[(c * 16 + e) * 128] = make_float4(o[4 * e] * inv, o[4 * e + 1] * inv,
+                                                 o[4 * e + 2] * inv, o[4 * e + 3] * inv);
+        }
+        a.split_lse[static_cast<size_t>(slot) * 128 + r] =
+            (l > 0.f) ? m_ref + log2f(l) : -INFINITY;
+      }
+      volatile int* last = reinterpret_cast<volatile int*>(smem + S::oMisc + 8);
+      asm volatile("bar.sync %0, %1;" ::"r"(kBarSoftmax), "r"(128) : "memory");
+      if (threadIdx.x == 0) {
+        fence_acq_rel_gpu();  // the CTA's rows (ordered by the barrier) before its arrival
+        const int old = atomicAdd(a.split_cnt + un.slot0, 1);
+        *last = (old == un.npieces - 1) ? 1 : 0;
+        if (old == un.npieces - 1) a.split_cnt[un.slot0] = 0;  // for the next call
+      }
+      asm volatile("bar.sync %0, %1;" ::"r"(kBarSoftmax), "r"(128) : "memory");
+      write_out = (*last != 0);
+      if (write_out) fence_acq_rel_gpu();  // every piece's rows are visible now
+    }
+    if (write_out && ok) {
+      tc_fence_after();
+      float inv = (l > 0.f) ? 1.f / l : 0.f;
+      // split item: the pieces' weights 2^(LSE_k - max LSE)
+      float w[kMaxPieces];
+      const float4* pk = split_item ? reinterpret_cast<const float4*>(a.split_o) +
+                                          static_cast<size_t>(un.slot0) * (D / 4) * 128 + r
+                                    : nullptr;
+      if (split_item) {
+        float lk[kMaxPieces];
+        float M = -INFINITY;
+#pragma unroll
+        for (int k = 0; k < kMaxPieces; ++k) {
+          lk[k] = (k < un.npieces) ? __ldcg(a.split_lse + static_cast<size_t>(un.slot0 + k) * 128 + r)
+                                   : -INFINITY;
+          M = fmaxf(M, lk[k]);
+        }
+        float den = 0.f;
+#pragma unroll
+        for (int k = 0; k < kMaxPieces; ++k) {
+          w[k] = (M == -INFINITY) ? 0.f : fast_exp2(lk[k] - M);
+          den += w[k];
+        }
+        inv = (den > 0.f) ? 1.f / den : 0.f;
+      }
+      // A tile of TQ tokens of this request leaves through TMA stores from
+      // the Q tile's shared memory, which is free once the last MMA has
+      // completed (the last P V commit covers every earlier MMA): each row
+      // goes there in the 128-byte-swizzled layout the Q copies used, so the
+      // output tensor map, of the same geometry, writes back whole 2 KB runs
+      // (one token's G heads) instead of one 16-byte piece per row and
+      // store.  A tile at the end of the request's rows, whose box would
+      // cover the next request's rows, stores its valid rows one by one.
+      uint16_t* orow = a.out + (static_cast<size_t>(it.q0 + qi) * a.Hq + it.kvh * G + g) * D;
+#pragma unroll 1
+      for (int c = 0; c < D / 64; ++c) {  // 64 columns per load and wait
+        float o[64];
+        if (split_item) {
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+            for (int k = 0; k < kMaxPieces; ++k) {
+              if (k < un.npieces) {
+                const float4 v = __ldcg(pk + (static_cast<size_t>(k) * (D / 4) + c * 16 + e) * 128);
+                acc.x = fmaf(w[k], v.x, acc.x);
+                acc.y = fmaf(w[k], v.y, acc.y);
+                acc.z = fmaf(w[k], v.z, acc.z);
+                acc.w = fmaf(w[k], v.w, acc.w);
+              }
+            }
+            o[4 * e] = acc.x;
+            o[4 * e + 1] = acc.y;
+            o[4 * e + 2] = acc.z;
+            o[4 * e + 3] = acc.w;
+          }
+        } else {
+          tmem_ld64(lane_base + S::kTmemO + c * 64, o);
+        }
+        uint8_t* srow = sQ + c * S::kQChunk + r * 128;
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          const uint4 w = make_uint4(pack_bf16x2(o[q * 8 + 0] * inv, o[q * 8 + 1] * inv),
+                                     pack_bf16x2(o[q * 8 + 2] * inv, o[q * 8 + 3] * inv),
+                                     pack_bf16x2(o[q * 8 + 4] * inv, o[q * 8 + 5] * inv),
+                                     pack_bf16x2(o[q * 8 + 6] * inv, o[q * 8 + 7] * inv));
+          if (full)
+            *reinterpret_cast<uint4*>(srow + ((q ^ (r & 7)) << 4)) = w;
+          else if (row_valid)
+            *reinterpret_cast<uint4*>(orow + c * 64 + q * 8) = w;
+        }
+      }
+    }
+    if (full && write_out) {
+      // every softmax warp arrives, whatever its waits gave; the tile is
+      // stored only if no wait of the CTA ran out
+      fence_proxy_async_smem();
+      asm volatile("bar.sync %0, %1;" ::"r"(kBarSoftmax), "r"(128) : "memory");
+      if (threadIdx.x == 0 && !stop_requested(failed)) {
+#pragma unroll
+        for (int c = 0; c < DC; ++c)
+          tma_store_3d(tm_out, sQ + c * S::kQChunk, c * 64, it.kvh * G, it.q0 + my0);
+        bulk_commit();
+        bulk_wait_read_all();  // the shared memory may go once the stores have read it
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync_all();  // neither CTA leaves while the pair's MMAs or signals may touch it
+  tc_fence_after();
+  if (warp == kWarpMma) tmem2_dealloc(tmem, S::kTmemCols);
+  if (threadIdx.x == 0) PKA_PF_SET(stamp, 3);
+
+}
+
+}  // namespace pka

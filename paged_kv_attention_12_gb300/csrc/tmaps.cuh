@@ -49,6 +49,17 @@ inline bool tmap_pool_tiles(CUtensorMap* m, const void* base, int D, long long r
   return tmap_bf16(m, base, 3, dims, str, box);
 }
 
+// The same view read in boxes of (64, 16, nchunks): nchunks of the D / 64
+// column chunks of a (block, head) tile per copy.
+inline bool tmap_pool_tiles_chunks(CUtensorMap* m, const void* base, int D, long long rows,
+                                   int nchunks) {
+  const cuuint64_t dims[3] = {64, static_cast<cuuint64_t>(rows), static_cast<cuuint64_t>(D / 64)};
+  const cuuint64_t str[2] = {static_cast<cuuint64_t>(D) * 2, 128};
+  const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(kBlockSize),
+                             static_cast<cuuint32_t>(nchunks)};
+  return tmap_bf16(m, base, 3, dims, str, box);
+}
+
 // q [total_q][Hq][D] as a 3-D tensor (D, Hq, total_q) read in boxes of
 // (64 columns, the G heads of one KV group, TQ tokens): one box per 64-column
 // chunk of a 128-row query tile.
