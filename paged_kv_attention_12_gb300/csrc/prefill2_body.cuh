@@ -170,8 +170,10 @@ __device__ __forceinline__ void tmem2_dealloc(uint32_t taddr, uint32_t ncols) {
                : "memory");
 }
 
-// The waits that consume another CTA's signals (remote arrivals, copies
-// of the peer) acquire at cluster scope.
+// The waits that consume another CTA's arrivals (the P-ready barrier, fed
+// by the peer's softmax, and the Q barrier) acquire at cluster scope; the
+// waits on commits and on TMA transaction counts, which the tensor and TMA
+// units perform on the waiting CTA's own barrier, at CTA scope.
 __device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
@@ -378,7 +380,7 @@ __device__ __forceinline__ void prefill2_body(const PrefillArgs& a, const CUtens
       int good = 1;
       if (lane == 0) {
         if (j >= nst &&
-            !mbar_wait_cluster(&bars[empty_base + st], static_cast<uint32_t>((j / nst - 1) & 1), a.err)) {
+            !mbar_wait(&bars[empty_base + st], static_cast<uint32_t>((j / nst - 1) & 1), a.err)) {
           *failed = 1;
           good = 0;
         }
@@ -412,7 +414,7 @@ __device__ __forceinline__ void prefill2_body(const PrefillArgs& a, const CUtens
       // every issued stage (both CTAs' halves) must land before the pair
       // may finish
       for (int j = issued - nst < 0 ? 0 : issued - nst; j < issued; ++j)
-        mbar_wait_cluster(&bars[full_base + j % nst], (j / nst) & 1, a.err);
+        mbar_wait(&bars[full_base + j % nst], (j / nst) & 1, a.err);
       if (warp == kWarpTmaK && stop_requested(failed)) mbar_wait_cluster(&bars[PB_Q], 0, a.err);
     }
     __syncwarp();
@@ -428,7 +430,7 @@ __device__ __forceinline__ void prefill2_body(const PrefillArgs& a, const CUtens
       auto issue_qk = [&](int j) -> bool {
         const int st = j & 1;
         const int ks = j % S::KST;
-        if (!warp_wait_cluster(&bars[PB_KFULL + ks], (j / S::KST) & 1, a.err, failed)) return false;
+        if (!warp_wait(&bars[PB_KFULL + ks], (j / S::KST) & 1, a.err, failed)) return false;
         tc_fence_after();
         if (lane == 0) {
           const uint32_t kst = aK + ks * S::kKStage;
@@ -453,7 +455,7 @@ __device__ __forceinline__ void prefill2_body(const PrefillArgs& a, const CUtens
         const int st = j & 1;
         const uint32_t ph = (j >> 1) & 1;
         const int vs = j % S::VST;
-        if (!warp_wait_cluster(&bars[PB_VFULL + vs], (j / S::VST) & 1, a.err, failed)) break;
+        if (!warp_wait(&bars[PB_VFULL + vs], (j / S::VST) & 1, a.err, failed)) break;
         // V rows at positions >= seq_len (stale slots of the last block,
         // which may hold NaN) -> 0 in both CTAs' halves, before P V reads
         // them (the peer's half through its cluster address)
@@ -501,14 +503,14 @@ __device__ __forceinline__ void prefill2_body(const PrefillArgs& a, const CUtens
         committed_pv = j + 1;
         if (j + 2 < it.ntiles) {
           // S_{j+2} overwrites S_j's buffer, which P_j V_j reads
-          ok = warp_wait_cluster(&bars[PB_VEMPTY + vs], (j / S::VST) & 1, a.err, failed);
+          ok = warp_wait(&bars[PB_VEMPTY + vs], (j / S::VST) & 1, a.err, failed);
           if (ok) ok = issue_qk(j + 2);
         }
       }
       // the last P V must finish before TMEM is freed
       if (committed_pv > 0) {
         const int jl = committed_pv - 1;
-        mbar_wait_cluster(&bars[PB_VEMPTY + jl % S::VST], (jl / S::VST) & 1, a.err);
+        mbar_wait(&bars[PB_VEMPTY + jl % S::VST], (jl / S::VST) & 1, a.err);
       }
     }
   } else {
@@ -542,7 +544,7 @@ __device__ __forceinline__ void prefill2_body(const PrefillArgs& a, const CUtens
       }
       const int st = j & 1;
       const uint32_t ph = (j >> 1) & 1;
-      if (!warp_wait_cluster(&bars[PB_QK + st], ph, a.err, failed)) {
+      if (!warp_wait(&bars[PB_QK + st], ph, a.err, failed)) {
         ok = false;
         break;
       }
@@ -598,7 +600,7 @@ __device__ __forceinline__ void prefill2_body(const PrefillArgs& a, const CUtens
       const bool resc = (j > 0) && (m_new > m_ref + 8.f);
       if (__any_sync(0xffffffffu, resc)) {
         // O must hold P_{j-1} V_{j-1} before it is rescaled
-        if (!warp_wait_cluster(&bars[PB_VEMPTY + (j - 1) % S::VST], ((j - 1) / S::VST) & 1, a.err,
+        if (!warp_wait(&bars[PB_VEMPTY + (j - 1) % S::VST], ((j - 1) / S::VST) & 1, a.err,
                                failed)) {
           ok = false;
           break;
@@ -649,7 +651,7 @@ __device__ __forceinline__ void prefill2_body(const PrefillArgs& a, const CUtens
     // ------------------------------------------------------------ epilogue
     if (ok) {
       const int jl = it.ntiles - 1;
-      ok = warp_wait_cluster(&bars[PB_VEMPTY + jl % S::VST], (jl / S::VST) & 1, a.err, failed);
+      ok = warp_wait(&bars[PB_VEMPTY + jl % S::VST], (jl / S::VST) & 1, a.err, failed);
     }
     if (ok && threadIdx.x == 0) PKA_PF_SET(stamp, 2);
     const bool full = (my0 + TQ - 1 <= it.it1);  // uniform over the CTA
