@@ -342,16 +342,25 @@ def cpu_baseline(calls, prefill_batch, budget_s: float):
 
 
 def cpu_model() -> str:
-    """The host CPU's model name (/proc/cpuinfo), or the platform's machine."""
+    """The host CPU's model: /proc/cpuinfo's model name, or on Arm its
+    implementer and part numbers (0x41/0xd4f is an Arm Neoverse V2 core, the
+    core of NVIDIA Grace)."""
+    import platform
+    fields = {}
     try:
         with open("/proc/cpuinfo") as f:
             for line in f:
                 key, _, val = line.partition(":")
-                if key.strip() in ("model name", "CPU part", "Model"):
-                    return val.strip()
+                fields.setdefault(key.strip(), val.strip())
     except OSError:
         pass
-    import platform
+    if "model name" in fields:
+        return fields["model name"]
+    impl, part = fields.get("CPU implementer"), fields.get("CPU part")
+    if impl and part:
+        known = {("0x41", "0xd4f"): "Arm Neoverse V2"}
+        name = known.get((impl.lower(), part.lower()), "Arm")
+        return f"{name} (implementer {impl}, part {part}, {platform.machine()})"
     return platform.machine()
 
 

@@ -96,10 +96,11 @@ def test_mixed_batch_small(seed):
     check(b, f"cfg5 small {seed}")
 
 
-def test_one_hot_prefill_exact():
+@pytest.mark.parametrize("D", [128, 256])
+def test_one_hot_prefill_exact(D):
     """Each query row's own key is c*q (every other weight underflows): the
-    output row is exactly that key's V row."""
-    G, Hkv, D = 4, 1, 128
+    output row is exactly that key's V row (D = 256 runs on CTA pairs)."""
+    G, Hkv = 4, 1
     L, n = 50, 20
     batch = small([L], [n], D=D, G=G, Hkv=Hkv, seed=9)
     q = batch.q.view(n, Hkv, G, D)
@@ -258,3 +259,19 @@ def test_many_requests_rank_from_global_memory():
     assert_close(to_f64(mixed[arr["q_rows"]]), ref, "mixed launch, 4500 requests")
     torch.cuda.synchronize()
     assert err.item() == 0
+
+
+@pytest.mark.parametrize("G", [1, 4, 8])
+@pytest.mark.parametrize("window", [0, 45])
+def test_pair_items_odd_tiles_and_stale_slots(G, window):
+    """D = 256 runs two query tiles per CTA pair: a chunk with an odd number
+    of tiles (the last pair's second CTA has no rows), a chunk one row past a
+    pair, an exact pair, a one-token request and ragged sequence ends (the
+    last block's stale slots hold NaN and must be zeroed in both CTAs'
+    halves of V)."""
+    tq = 128 // G
+    Hkv = 2 if G < 8 else 1
+    n = [3 * tq, 2 * tq + 1, 2 * tq, 1, tq - 3]
+    L = [x + 131 for x in n[:3]] + [77, tq + 500]
+    check(small(L, n, D=256, G=G, Hkv=Hkv, window=window, softcap=30.0 if window else 0.0,
+                seed=G + window, cfg_id=24), f"pairs G={G} W={window}")
