@@ -210,7 +210,12 @@ int paged_prefill_attn(const void* q, void* out, const pka_kv_pool* kv,
  * go to decode pipelines in the same launch -- split-K over their keys with
  * the log-sum-exp merge fused in, as paged_decode_attn_ws -- instead of
  * filling G of the 128 rows of a tensor-core tile; requests with more tokens
- * run the tensor-core prefill pipeline.
+ * run the tensor-core prefill pipeline.  Exception: when the decode rows'
+ * B * Hkv segments (request, KV head) number at most the decode pipelines
+ * and none has more than q + 24 units on the split's line (q its chunk,
+ * the paged_decode_splitk partition over the decode pipelines), every
+ * segment streams whole on its own pipeline and writes its output with no
+ * partials and no merge.
  * SMs: the prefill side gets P of the GPU's N SMs, the decode pipelines the
  * rest (two per SM).  P shares N in proportion to estimated SM time, from
  * sizes only: prefill E = ceil((total_q - B) / TQ) * Hkv items (TQ = 128/G

@@ -241,14 +241,30 @@ struct PieceIter {
     // per lane for the search below when the batch has at most 32 requests
     int T = 0;
     int u_first = 0;
+    int u_max = 0;
     for (int base = 0; base < args.batch; base += 32) {
       const int bb = base + lane;
       const int u = units(bb < args.batch ? geo_of_len(args, len_of(bb)).nb : 0);
       if (base == 0) u_first = u;
       T += __shfl_sync(0xffffffffu, warp_incl_scan(u, lane), 31);
+      u_max = max(u_max, u);
     }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) u_max = max(u_max, __shfl_xor_sync(0xffffffffu, u_max, o));
     T *= args.Hkv;
     q = max(max(args.split_blocks, 1), (T + vgrid - 1) / vgrid);
+    // With the combine fused in and direct_slack > 0, a batch whose segments
+    // all fit one per pipeline and are all short of the split's chunk plus
+    // direct_slack units runs without splitting: each segment streams on its
+    // own pipeline and writes its output directly, with no partials and no
+    // merge (the merge at the end of the launch costs about as much as
+    // streaming a couple of dozen tiles).
+    if (args.seg_counters != nullptr && args.direct_slack > 0 &&
+        args.batch * args.Hkv <= vgrid && u_max <= q + args.direct_slack) {
+      direct = true;
+      item = vcta;
+      return;
+    }
     const int nch = T > 0 ? (T + q - 1) / q : 1;
     if (vcta >= nch) {
       done = true;
@@ -812,7 +828,7 @@ __device__ __forceinline__ void decode_body(const DecodeArgs& a, const CUtensorM
     // ---- split-K: slots of this segment no pipeline fills get LSE = -inf,
     // written at the start of the piece by the last consumer warp (hidden
     // behind the wait for the piece's first tiles)
-    if (a.split_blocks > 0 && a.seg_counters == nullptr && pc.fill_from >= 0 && warp == NW - 1) {
+    if (!iter.direct && a.seg_counters == nullptr && pc.fill_from >= 0 && warp == NW - 1) {
       if (pc.fill_from > a.num_splits && lane == 0) report(a.err, PKA_DEVERR_SEQ_LEN);
       for (int h = 0; h < G; ++h)
         for (int sl = pc.fill_from + lane; sl < a.num_splits; sl += 32)
@@ -843,7 +859,7 @@ __device__ __forceinline__ void decode_body(const DecodeArgs& a, const CUtensorM
     Piece nx;
     const bool have_next = iter.next(nx, true);
 
-    const bool split = a.split_blocks > 0;
+    const bool split = !iter.direct;
     const bool fused = split && a.seg_counters != nullptr;
     if (pc.ntiles > 0) {
       // ---- per-warp totals: sums over the 8 key rows held by lanes g

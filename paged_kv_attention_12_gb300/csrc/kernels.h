@@ -24,6 +24,9 @@ struct DecodeArgs {
   int32_t num_splits;              // items per (request, head); 1 in direct mode
   int32_t split_blocks;            // blocks per split; <= 0: direct mode (whole range)
   int32_t* seg_counters;           // split mode: non-null fuses the combine (zeroed [B*Hkv])
+  int32_t direct_slack;            // with seg_counters: > 0 lets a batch whose segments fit one
+                                   // per pipeline, none longer than the chunk + this many
+                                   // units, stream unsplit (no partials, no merge); 0: never
   float* logits;                   // optional fp32 [B][Hq][max_blocks*bs]: log2-domain logits
   float scale, softcap;
   int32_t window;

@@ -212,3 +212,40 @@ def test_split_pieces_short_and_ragged_tiles():
     b = small(L, n, seed=77, softcap=50.0)
     assert max(expected_pieces(b)) > 1
     check(b, "split ragged")
+
+
+def lse_region(runner):
+    """The decode rows' partial LSEs in the workspace ([B][Hq][S] fp32 after
+    the partial outputs, as paged_decode_attn_ws lays them out)."""
+    b = runner.batch
+    S, _ = binding.paged_decode_splitk_plan(b.num_requests, b.num_kv_heads, b.max_seq_len, 16,
+                                            b.window)
+    B, Hq, D = b.num_requests, b.num_q_heads, b.head_dim
+    off = B * Hq * S * D * 4
+    return runner.workspace[off:off + B * Hq * S * 4].view(torch.float32)
+
+
+@pytest.mark.parametrize("kind", ["short rows", "long rows"])
+def test_decode_rows_stream_whole_or_split(kind):
+    """Decode rows that fit one per pipeline and are short of the split's
+    chunk plus 24 units stream whole, writing no partial; long rows without
+    a window are split and merged.  The partial LSEs are filled with NaN
+    first: untouched in the first case, written in the second; the output
+    matches the oracle either way."""
+    if kind == "short rows":
+        L, n, W = [300, 900, 1, 60, 700, 1500], [1, 1, 1, 1, 60, 1], 256
+    else:
+        L, n, W = [3000, 4000, 1, 2500, 700, 1500], [1, 1, 1, 1, 60, 1], 0
+    b = small(L, n, window=W, softcap=50.0, seed=91)
+    runner = binding.MixedBatch(b)
+    lse_region(runner).fill_(float("nan"))
+    out = runner.run(torch.zeros(1, dtype=torch.int32, device=DEV)).clone()
+    torch.cuda.synchronize()
+    written = int((~torch.isnan(lse_region(runner))).sum())
+    if kind == "short rows":
+        assert written == 0, "short decode rows must not go through partials"
+    else:
+        assert written > 0, "long decode rows must be split"
+    ref, _ = oracle.run_batch(workload.to_numpy_f64(b))
+    assert_close(to_f64(out), ref, kind)
+    assert torch.all(counters(runner) == 0)
