@@ -297,16 +297,15 @@ __device__ __forceinline__ void prefill2_body(const PrefillArgs& a, const CUtens
   const uint32_t oob_row = static_cast<uint32_t>(a.num_blocks) * a.Hkv * kBlockSize;
   const int32_t* trow = a.tables + static_cast<size_t>(it.b) * a.max_blocks;
 
-  if (warp == kWarpTmaK || warp == kWarpTmaK2 || warp == kWarpTmaV) {
+  if (warp == kWarpTmaK || warp == kWarpTmaV) {
     // ============================ TMA producers ============================
-    // Each CTA loads its half of every stage -- K: 32 of the tile's 64 keys
-    // (blocks 2 crank, 2 crank + 1; one warp per block, one 2-D box per
-    // 64-column chunk), V: 128 of the 256 columns of all 64 keys (one 3-D
-    // box of two chunks per block) -- completing on the rank-0 CTA's "full"
-    // barrier, which expects both halves.  A stage is refilled once the MMA
-    // that read it has committed (the commit reaches both CTAs).
+    // Each CTA loads its half of every stage -- K: 64 of the tile's 128 keys
+    // (blocks 4 crank .. 4 crank + 3, one 2-D box per block and 64-column
+    // chunk, one lane each), V: 128 of the 256 columns of all 128 keys (one
+    // 3-D box of two chunks per block) -- completing on the rank-0 CTA's
+    // "full" barrier, which expects both halves.  A stage is refilled once
+    // the MMA that read it has committed (the commit reaches both CTAs).
     const bool is_k = (warp != kWarpTmaV);
-    const int kpart = (warp == kWarpTmaK2) ? 1 : 0;
     const int nst = is_k ? S::KST : S::VST;
     uint8_t* ring = is_k ? sK : sV;
     const int full_base = is_k ? PB_KFULL : PB_VFULL;
@@ -361,16 +360,16 @@ __device__ __forceinline__ void prefill2_body(const PrefillArgs& a, const CUtens
           *failed = 1;
           good = 0;
         }
-        if (good && lead && kpart == 0) mbar_arrive_expect_tx(&bars[full_base + st], 2 * stage_bytes);
+        if (good && lead) mbar_arrive_expect_tx(&bars[full_base + st], 2 * stage_bytes);
       }
       if (!__shfl_sync(0xffffffffu, good, 0)) break;
       const uint32_t fbar = leader_addr(&bars[full_base + st]);
       uint8_t* dst = ring + st * stage_bytes;
       if (is_k) {
-        if (lane < 2 * DC) {
-          // this CTA's keys: blocks 4 crank .. 4 crank + 3 of the tile; this
-          // warp: two of them, one box per (block, 64-column chunk)
-          const int kb = 2 * kpart + lane / DC, c = lane % DC;
+        if (lane < (BPT / 2) * DC) {
+          // this CTA's keys: blocks 4 crank .. 4 crank + 3 of the tile, one
+          // box per (block, 64-column chunk)
+          const int kb = lane / DC, c = lane % DC;
           uint32_t r = rl[0];
 #pragma unroll
           for (int q = 1; q < BPT; ++q)
@@ -396,13 +395,17 @@ __device__ __forceinline__ void prefill2_body(const PrefillArgs& a, const CUtens
     }
     __syncwarp();
   } else if (warp == kWarpMma) {
-    // ================================ MMA ================================
-    // Issued by the rank-0 CTA only, for both (M = 256).
+    // ============================== S MMAs ==============================
+    // Issued by the rank-0 CTA only, for both (M = 256).  S_{j+2} overwrites
+    // S_j's buffer, which holds P_j, so it waits for P_j V_j to complete.
+    // Issuing a tile's 16 MMAs holds the issuing thread until the tensor
+    // pipe has nearly run them, so the P V MMAs come from another warp
+    // (below): P_j V_j goes to the pipe as soon as P_j is ready, even while
+    // this warp is still issuing S_{j+1} (the two touch different TMEM
+    // columns, so their MMAs may interleave).
     if (lead) {
       constexpr uint32_t idesc_qk = idesc_bf16_f32(256, BN, 0, 0);
-      constexpr uint32_t idesc_pv = idesc_bf16_f32(256, D, 0, 1);
-      const uint32_t aQ = smem_u32(sQ), aK = smem_u32(sK), aV = smem_u32(sV);
-      int committed_pv = 0;
+      const uint32_t aQ = smem_u32(sQ), aK = smem_u32(sK);
       bool ok = warp_wait(&bars[PB_Q], 0, a.err, failed);
       auto issue_qk = [&](int j) -> bool {
         const int st = j & 1;
@@ -427,7 +430,21 @@ __device__ __forceinline__ void prefill2_body(const PrefillArgs& a, const CUtens
       };
       if (ok) ok = issue_qk(0);
       if (ok && it.ntiles > 1) ok = issue_qk(1);
-      for (int j = 0; ok && j < it.ntiles; ++j) {
+      for (int j = 0; ok && j + 2 < it.ntiles; ++j) {
+        if (__any_sync(0xffffffffu, stop_requested(failed))) break;
+        const int vs = j % S::VST;
+        ok = warp_wait(&bars[PB_VEMPTY + vs], (j / S::VST) & 1, a.err, failed);
+        if (ok) ok = issue_qk(j + 2);
+      }
+    }
+  } else if (warp == kWarpTmaK2) {
+    // ============================= P V MMAs =============================
+    // Rank-0 CTA only: P_j V_j as soon as P_j and V_j are there.
+    if (lead) {
+      constexpr uint32_t idesc_pv = idesc_bf16_f32(256, D, 0, 1);
+      const uint32_t aV = smem_u32(sV);
+      int committed_pv = 0;
+      for (int j = 0; j < it.ntiles; ++j) {
         if (__any_sync(0xffffffffu, stop_requested(failed))) break;
         const int st = j & 1;
         const uint32_t ph = (j >> 1) & 1;
@@ -478,11 +495,6 @@ __device__ __forceinline__ void prefill2_body(const PrefillArgs& a, const CUtens
         }
         __syncwarp();
         committed_pv = j + 1;
-        if (j + 2 < it.ntiles) {
-          // S_{j+2} overwrites S_j's buffer, which P_j V_j reads
-          ok = warp_wait(&bars[PB_VEMPTY + vs], (j / S::VST) & 1, a.err, failed);
-          if (ok) ok = issue_qk(j + 2);
-        }
       }
       // the last P V must finish before TMEM is freed
       if (committed_pv > 0) {
