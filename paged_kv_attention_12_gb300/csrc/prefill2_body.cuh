@@ -523,6 +523,16 @@ __device__ __forceinline__ void prefill2_body(const PrefillArgs& a, const CUtens
     const bool prescale = capped || !(sl2 > 0.f);
     const float cap_in = capped ? a.scale / a.softcap : 0.f;
     const float cap_out = a.softcap * kLog2e;
+    // The three-term form of cap_out * tanh(cap_in * s) written in s:
+    // x(s) = s (k1 + s^2 (k3 + k5 s^2)), k1 = cap_in cap_out,
+    // k3 = -cap_in^3 cap_out / 3, k5 = 2 cap_in^5 cap_out / 15.  For
+    // cap_in > 0 it increases with s, so the row maximum of x is x(max s),
+    // and a masked column (s = -inf) gives x = -inf, as long as k5 > 0
+    // (no 0 * inf).
+    const float k1 = cap_in * cap_out;
+    const float k3 = -cap_in * cap_in * k1 * (1.f / 3.f);
+    const float k5 = 2.f * cap_in * cap_in * cap_in * cap_in * k1 * (1.f / 15.f);
+    const bool fold_ok = capped && cap_in > 0.f && k5 > 0.f;
     float m_ref = -INFINITY;
     float l = 0.f;
     bool ok = true;
@@ -553,14 +563,18 @@ __device__ __forceinline__ void prefill2_body(const PrefillArgs& a, const CUtens
       // Only rows on a causal diagonal or a window edge need the per-column
       // mask; the warp takes the masked loop only if one of its rows does.
       const bool need_mask = __any_sync(0xffffffffu, c_lo > 0 || c_hi < BN - 1);
+      bool folded = false;
       if (capped) {
         // log2-domain logits cap * tanh(s * scale / cap) * log2(e); a
         // Taylor form when every |y| of the warp's rows is below 1/8 (three
-        // terms) or 0.5 (six terms), else the exp2 form
+        // terms) or 0.5 (six terms), else the exp2 form.  With scale > 0 the
+        // three-term form stays folded (see k1, k3, k5) and s stays raw.
         float amax = 0.f;
 #pragma unroll
         for (int c = 0; c < BN; ++c) amax = fmaxf(amax, fabsf(s[c]));
-        if (__all_sync(0xffffffffu, amax * cap_in < 0.125f)) {
+        if (fold_ok && __all_sync(0xffffffffu, amax * cap_in < 0.125f)) {
+          folded = true;
+        } else if (__all_sync(0xffffffffu, amax * cap_in < 0.125f)) {
 #pragma unroll
           for (int c = 0; c < BN; ++c) s[c] = cap_out * tanh_taylor_short(s[c] * cap_in);
         } else if (__all_sync(0xffffffffu, amax * cap_in < 0.5f)) {
@@ -584,7 +598,10 @@ __device__ __forceinline__ void prefill2_body(const PrefillArgs& a, const CUtens
 #pragma unroll
       for (int c = 0; c < BN; ++c) m4[c & 3] = fmaxf(m4[c & 3], s[c]);
       float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
-      if (!prescale) mx *= sl2;
+      if (folded)
+        mx = mx * fmaf(mx * mx, fmaf(mx * mx, k5, k3), k1);  // x(max s) = max x(s)
+      else if (!prescale)
+        mx *= sl2;
       const float m_new = fmaxf(m_ref, mx);
       const bool resc = (j > 0) && (m_new > m_ref + 8.f);
       if (__any_sync(0xffffffffu, resc)) {
@@ -614,21 +631,30 @@ __device__ __forceinline__ void prefill2_body(const PrefillArgs& a, const CUtens
       // p = 2^(x - ms), x the log2-domain logit (uncapped: x = s * scale * log2 e,
       // fused into one FMA)
       const float xs = prescale ? 1.f : sl2;
-      float lsum0 = 0.f, lsum1 = 0.f;
+      // x - ms for each column: the folded capped form, or the (scaled)
+      // logit; the two loops are compiled separately so that neither pays
+      // for the other's arithmetic
+      auto make_p = [&](auto arg) {
+        float lsum0 = 0.f, lsum1 = 0.f;
 #pragma unroll
-      for (int h = 0; h < BN / 64; ++h) {
-        uint32_t pk[32];
+        for (int h = 0; h < BN / 64; ++h) {
+          uint32_t pk[32];
 #pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          const float p0 = fast_exp2(fmaf(s[h * 64 + 2 * e], xs, -ms));
-          const float p1 = fast_exp2(fmaf(s[h * 64 + 2 * e + 1], xs, -ms));
-          lsum0 += p0;
-          lsum1 += p1;
-          pk[e] = pack_bf16x2(p0, p1);
+          for (int e = 0; e < 32; ++e) {
+            const float p0 = fast_exp2(arg(s[h * 64 + 2 * e]));
+            const float p1 = fast_exp2(arg(s[h * 64 + 2 * e + 1]));
+            lsum0 += p0;
+            lsum1 += p1;
+            pk[e] = pack_bf16x2(p0, p1);
+          }
+          tmem_st32_u(lane_base + st * BN + h * 32, pk);
         }
-        tmem_st32_u(lane_base + st * BN + h * 32, pk);
-      }
-      l += lsum0 + lsum1;
+        return lsum0 + lsum1;
+      };
+      const float lsum =
+          folded ? make_p([&](float x) { return fmaf(x, fmaf(x * x, fmaf(x * x, k5, k3), k1), -ms); })
+                 : make_p([&](float x) { return fmaf(x, xs, -ms); });
+      l += lsum;
       tmem_wait_st();
       tc_fence_before();
       // one arrival per warp on the rank-0 CTA's barrier once its 32 rows

@@ -71,6 +71,18 @@ def test_window_and_softcap(window, softcap):
                 seed=window), f"W={window} cap={softcap}")
 
 
+@pytest.mark.parametrize("scale,softcap", [(1e-3, 1e4), (0.0625, 1e6), (2.0, 0.5)])
+def test_softcap_scale_extremes(scale, softcap):
+    """Ratios scale / softcap at which the capped logit's Taylor terms
+    underflow (tiny ratio) or the exp2 form is needed (large ratio): every
+    path of the capped softmax against the oracle, on causal and ragged
+    tiles."""
+    check(small([400, 130, 57, 20], [130, 1, 57, 1], D=256, Hkv=2, softcap=softcap,
+                scale=scale, seed=19), f"scale={scale} cap={softcap}")
+    check(small([300, 75], [75, 75], D=128, Hkv=2, softcap=softcap, scale=scale, seed=20),
+          f"D=128 scale={scale} cap={softcap}")
+
+
 @pytest.mark.parametrize("scale", [0.0, -0.0625, -0.25])
 @pytest.mark.parametrize("softcap", [0.0, 30.0])
 def test_zero_and_negative_scale(scale, softcap):
