@@ -420,31 +420,39 @@ class L2Flush:
 
 
 def time_launches(fn, flush, iters, warmup):
-    """Median CUDA-event time (ms) of fn(), L2 flushed before every call.
-    fn() is captured once as a CUDA graph and replayed, as in the main step,
-    so the host's cost of issuing the launch is not in the measurement."""
+    """Median device time (ms) of fn() with the L2 flushed before it: CUDA
+    events around the replay of a CUDA graph of (L2 flush, fn), minus the
+    same around a graph of the flush alone -- as the serving step's launches
+    are timed -- so that neither the flush nor a graph's own start-up latency
+    counts as fn's time."""
     import torch
     stream = torch.cuda.current_stream()
     for _ in range(warmup):
         flush(1.0)
         fn()
     torch.cuda.synchronize()
-    graph = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(graph):
-        fn()
-    flush(1.0)
-    graph.replay()
+
+    def graph_of(body):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            body()
+        return g
+    g_flush = graph_of(lambda: flush(1.0))
+    g_both = graph_of(lambda: (flush(1.0), fn()))
+    for g in (g_flush, g_both):
+        g.replay()
     torch.cuda.synchronize()
-    ts = []
-    for i in range(iters):
-        flush(float(i))
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        graph.replay()
-        e1.record(stream)
-        ts.append((e0, e1))
+    t_flush, t_both = [], []
+    for _ in range(iters):
+        for g, acc in ((g_flush, t_flush), (g_both, t_both)):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            g.replay()
+            e1.record(stream)
+            acc.append((e0, e1))
     torch.cuda.synchronize()
-    return statistics.median(a.elapsed_time(b) for a, b in ts)
+    med = lambda ts: statistics.median(a.elapsed_time(b) for a, b in ts)
+    return med(t_both) - med(t_flush)
 
 
 def other_workloads(dev, flush, iters=10, warmup=3, cfgs=(1, 3, 4, 5)):
