@@ -469,7 +469,8 @@ def other_workloads(dev, flush, iters=10, warmup=3, cfgs=(1, 3, 4, 5)):
         flops = 4.0 * batch.head_dim * batch.num_q_heads * attention_pairs(batch)
         if cfg in (1, 3):
             r = binding.DecodeFused(batch)
-            fn, path = r.run, "paged_decode_attn_ws (split-K, combine fused)"
+            fn, path = r.run, ("paged_decode_attn_ws (split-K, combine fused; segments that "
+                               "fit one per pipeline stream whole)")
         elif cfg == 5:
             r = binding.MixedBatch(batch)
             fn, path = r.run, ("paged_prefill_attn_ws (one launch: decode rows on split-K "

@@ -161,6 +161,11 @@ int paged_decode_splitk(const void* q, float* partial_o, float* partial_lse,
  * (one launch instead of two).  Same partition and partials as
  * paged_decode_splitk with the plan's (S, C); the CTA that finishes a
  * segment's last piece merges its pieces and writes out bf16 [B][Hq][D].
+ * Exception: when the B * Hkv segments (request, KV head) number at most
+ * the decode pipelines (twice the GPU's SM count) and none has more than
+ * q + 24 units on the split's line (q its chunk), every segment streams
+ * whole on its own pipeline and writes its output with no partials and no
+ * merge -- the result of paged_decode_attn, bit for bit.
  * workspace: device, 16-byte aligned, at least paged_decode_attn_ws_bytes()
  * bytes: partial outputs fp32 [B][Hq][S][D], partial LSEs [B][Hq][S] (padded
  * to 16 bytes), then B*Hkv int32 arrival counters.  The counters must be

@@ -285,6 +285,15 @@ size_t paged_decode_attn_ws_bytes(int32_t B, int32_t Hq, int32_t Hkv, int32_t D,
   return L.total();
 }
 
+// With the combine fused in, a batch whose (request, KV head) segments fit
+// one per decode pipeline and are at most this many work units beyond the
+// split's chunk streams unsplit (no partials, no merge; the merge costs
+// about as much as streaming a couple of dozen tiles).  Measured: a batch
+// of 64 rows that all see a full 1024-key window beside prefill chunks,
+// 47 us per launch this way against 51 us split and merged; 4 rows of up to
+// 256 tokens, 8.7 us against 10.0 us.
+constexpr int32_t kDirectSlackUnits = 24;
+
 int paged_decode_attn_ws(const void* q, void* out, const pka_kv_pool* kv,
                          const int32_t* block_tables, int32_t max_blocks,
                          const int32_t* seq_lens, int32_t B, int32_t Hq, int32_t max_seq_len,
@@ -308,6 +317,7 @@ int paged_decode_attn_ws(const void* q, void* out, const pka_kv_pool* kv,
   a.seg_counters = reinterpret_cast<int32_t*>(ws + L.o_bytes + L.lse_bytes);
   a.num_splits = L.S;
   a.split_blocks = L.C;
+  a.direct_slack = kDirectSlackUnits;
   const int sms = pka::device_sm_count();
   if (sms <= 0) return PKA_ERR_CUDA;
   cudaError_t e = pka::launch_decode(a, kv->head_dim, Hq / kv->num_kv_heads, sms,
@@ -452,11 +462,7 @@ int paged_prefill_attn_ws(const void* q, void* out, const pka_kv_pool* kv,
   da.seg_counters = reinterpret_cast<int32_t*>(ws + L.o_bytes + L.lse_bytes);
   da.num_splits = L.S;
   da.split_blocks = L.C;
-  // Decode rows that fit one per pipeline and are at most this many tiles
-  // beyond the split's chunk stream unsplit: on a batch of 64 rows that all
-  // see a full 1024-key window, 47 us per launch this way against 51 us
-  // split and merged.
-  da.direct_slack = 24;
+  da.direct_slack = kDirectSlackUnits;
   const int sms = pka::device_sm_count();
   if (sms <= 0) return PKA_ERR_CUDA;
   // Decode CTAs and prefill SMs.  The host sees only sizes, so both sides'

@@ -52,3 +52,20 @@ def split_ranges(seq_lens, window, block_size, num_kv_heads, grid, min_chunk,
         ranges.append(per_head)
     return ranges
 
+
+
+DIRECT_SLACK = 24  # units beyond the chunk within which a fused launch streams whole
+
+
+def streams_whole(seq_lens, window, block_size, num_kv_heads, pipelines, min_chunk,
+                  piece_units=PIECE_UNITS, slack=DIRECT_SLACK):
+    """True when a fused launch (``paged_decode_attn_ws``, and the decode rows
+    of ``paged_prefill_attn_ws``) streams every segment whole instead of
+    splitting it: the B * Hkv segments fit one per pipeline and none is
+    longer than the chunk q plus ``slack`` units (the header's rule)."""
+    span = [visible_blocks(int(L), window, block_size) for L in seq_lens]
+    units = [(j1 - j0) + piece_units if j1 > j0 else 0 for j0, j1 in span]
+    total = num_kv_heads * sum(units)
+    q = max(min_chunk, -(-total // pipelines), 1)
+    return (len(seq_lens) * num_kv_heads <= pipelines and
+            max(units, default=0) <= q + slack)

@@ -10,7 +10,7 @@ import torch
 import oracle
 from paged_kv_attention_12_gb300 import _build, binding, workload
 from tests.parity import assert_close, to_f64
-from tests.splitk_partition import split_ranges
+from tests.splitk_partition import split_ranges, streams_whole
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda:0"
@@ -216,13 +216,46 @@ def ws_views(runner):
             ws[o2:o2 + B * Hkv * 4].view(torch.int32))
 
 
+def whole(batch):
+    """Whether the fused launch streams this batch's segments whole (the
+    rule of the paged_decode_attn_ws comment, restated in splitk_partition)."""
+    S, C = binding.paged_decode_splitk_plan(batch.num_requests, batch.num_kv_heads,
+                                            batch.max_seq_len, 16, batch.window)
+    pipes = 2 * torch.cuda.get_device_properties(0).multi_processor_count
+    return streams_whole(batch.seq_lens_host, batch.window, 16, batch.num_kv_heads, pipes, C)
+
+
 def test_fused_equals_two_launch_split_k():
     """Same partition and the same merge steps: the fused launch and split-K
-    + combine give the same bits."""
+    + combine give the same bits -- or, for a batch whose segments stream
+    whole, the fused launch gives paged_decode_attn's bits.  The scaled-down
+    serving layers have one batch of each kind."""
+    kinds = []
     for batch in workload.decode_serving(2, DEV, scale_down=True):
         a = binding.DecodeFused(batch).run().clone()
-        b = binding.DecodeSplitK(batch).run()
-        assert torch.equal(a, b), batch.name
+        kinds.append(whole(batch))
+        b = run_direct(batch) if kinds[-1] else binding.DecodeSplitK(batch).run()
+        assert torch.equal(a, b), (batch.name, kinds[-1])
+    assert sorted(kinds) == [False, True], kinds
+
+
+def test_tiny_batch_streams_whole():
+    """The tiny decode workload (4 requests of up to 256 tokens) streams its
+    segments whole in the fused launch: no partial is written (the LSEs,
+    filled with NaN first, stay NaN), the counters stay zero, and the output
+    is paged_decode_attn's bit for bit and matches the oracle."""
+    batch = workload.decode_tiny(1, DEV, poison=True)
+    assert whole(batch)
+    runner = binding.DecodeFused(batch)
+    po, pl, seg = ws_views(runner)
+    pl.fill_(float("nan"))
+    out = runner.run().clone()
+    torch.cuda.synchronize()
+    assert bool(torch.isnan(pl).all()), "no partial LSE may be written"
+    assert torch.all(seg == 0)
+    assert torch.equal(out, run_direct(batch))
+    ref, _, _ = oracle_decode(batch)
+    assert_close(to_f64(out), ref, "tiny fused, whole segments")
 
 
 @pytest.mark.parametrize("maker", ["serving0", "serving1", "long"])
@@ -235,6 +268,8 @@ def test_fused_combine_equals_combine_kernel_on_its_partials(maker):
         batch = workload.decode_long(3, DEV, scale_down=True)
     else:
         batch = workload.decode_serving(2, DEV, scale_down=True)[int(maker[-1])]
+    if whole(batch):
+        pytest.skip("segments stream whole: no partials to combine")
     runner = binding.DecodeFused(batch)
     po, pl, _ = ws_views(runner)
     pl.fill_(float("-inf"))
