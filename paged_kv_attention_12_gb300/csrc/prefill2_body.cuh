@@ -8,11 +8,12 @@
 // consecutive query tiles of one (request, KV head) -- the rank-0 CTA the
 // first 128 rows, the rank-1 CTA the next 128 -- and streams the keys both
 // tiles see.  Every MMA is issued once, by the rank-0 CTA, for both
-// (tcgen05.mma.cta_group::2):
+// (tcgen05.mma.cta_group::2), the S MMAs by one warp and the P V MMAs by
+// another:
 //
 //  * S = Q K^T with M = 256 (each CTA's Q tile is its half of A) and the key
-//    tile's 64 keys split between the CTAs' shared memory (N = 64: each CTA
-//    holds 32 keys of every K stage);
+//    tile's 128 keys split between the CTAs' shared memory (N = 128: each
+//    CTA holds 64 keys of every K stage);
 //  * O += P V with P from each CTA's own TMEM and V split by columns (each
 //    CTA holds 128 of the 256 columns of every V stage).
 //
@@ -20,7 +21,8 @@
 // it: at D = 256 a single SM's shared memory (a 64 KB Q tile plus the K/V
 // rings) and its bandwidth set the pace of the one-CTA kernel, and the pair
 // halves the ring bytes per key and doubles the stages that fit.  TMEM
-// holds each CTA's own rows (S, P and O as in the one-CTA kernel).
+// holds each CTA's own rows: two S buffers of 128 columns and O (256); P_j
+// is written over the first half of S_j's buffer.
 //
 // Cross-CTA signalling: both CTAs' TMA copies complete on the rank-0 CTA's
 // "full" barriers (cp.async.bulk.tensor ... .cta_group::2), the MMA commits
@@ -75,6 +77,11 @@ struct Prefill2Shape {
 };
 
 namespace pair2 {
+
+// Warp roles of a pair CTA: softmax 0-3, K copies kWarpTmaK, V copies
+// kWarpTmaV, S MMAs kWarpMma (rank-0 CTA), P V MMAs kWarpPv (rank-0 CTA;
+// the one-CTA kernel's second K warp).
+constexpr int kWarpPv = kWarpTmaK2;
 
 enum {
   PB_Q = 0,
@@ -437,7 +444,7 @@ __device__ __forceinline__ void prefill2_body(const PrefillArgs& a, const CUtens
         if (ok) ok = issue_qk(j + 2);
       }
     }
-  } else if (warp == kWarpTmaK2) {
+  } else if (warp == kWarpPv) {
     // ============================= P V MMAs =============================
     // Rank-0 CTA only: P_j V_j as soon as P_j and V_j are there.
     if (lead) {
