@@ -21,8 +21,8 @@
 // it: at D = 256 a single SM's shared memory (a 64 KB Q tile plus the K/V
 // rings) and its bandwidth set the pace of the one-CTA kernel, and the pair
 // halves the ring bytes per key and doubles the stages that fit.  TMEM
-// holds each CTA's own rows: two S buffers of 128 columns and O (256); P_j
-// is written over the first half of S_j's buffer.
+// holds each CTA's own rows: one S buffer of 128 columns, two P buffers of
+// 64 (bf16 pairs) and O (256).
 //
 // Cross-CTA signalling: both CTAs' TMA copies complete on the rank-0 CTA's
 // "full" barriers (cp.async.bulk.tensor ... .cta_group::2), the MMA commits
@@ -57,15 +57,17 @@ struct Prefill2Shape {
   static constexpr int oK = oQ + kQBytes;
   static constexpr int oV = oK + KST * kKStage;
   static constexpr int oBar = oV + VST * kVStage;
-  // Q, K full/empty per stage, V full/empty per stage, S ready x2, P ready x2
-  static constexpr int kNumBars = 1 + 2 * KST + 2 * VST + 2 + 2;
+  // Q, K full/empty per stage, V full/empty per stage, S ready x2, P ready
+  // x2, S read
+  static constexpr int kNumBars = 1 + 2 * KST + 2 * VST + 2 + 2 + 1;
   static constexpr int oMisc = oBar + kNumBars * 8;
   static constexpr int kSmemBytes = oMisc + 16 + 1024;
   static constexpr uint32_t kTmemO = 256;
-  // P_j (bf16 pairs, BN / 2 columns) is written over the first half of
-  // S_j's own buffer once the softmax has read S_j: 2 S buffers of 128
-  // columns and O fill the 512 columns, so S_{j+2} is issued only once
-  // P_j V_j has completed.
+  // One S buffer (BN columns at 0), P_j (bf16 pairs, BN / 2 columns) in
+  // buffer j % 2 at kTmemP, O at kTmemO: 128 + 2 x 64 + 256 = 512 columns.
+  // S_{j+1} may be written as soon as every softmax warp has read S_j into
+  // its registers, and P_{j+2} once P_j V_j has completed.
+  static constexpr uint32_t kTmemP = BN;
   static constexpr uint32_t kTmemCols = 512;
   static constexpr int kThreads = 8 * 32;
   static constexpr int kCostBuckets = 4096;
@@ -73,7 +75,7 @@ struct Prefill2Shape {
   static_assert((kReqCacheOffset + 2 * kReqCache) * 4 <= KST * kKStage, "request cache");
   static_assert(kSmemBytes <= 232448, "shared memory");
   static_assert(KST == 3 && VST == 2, "the barrier map below assumes 3 K and 2 V stages");
-  static_assert(2 * BN + D <= kTmemCols, "TMEM columns");
+  static_assert(kTmemP + BN <= kTmemO && kTmemO + D <= kTmemCols, "TMEM columns");
 };
 
 namespace pair2 {
@@ -91,6 +93,7 @@ enum {
   PB_VEMPTY = PB_VFULL + 2,               // [VST], both CTAs (multicast commit)
   PB_QK = PB_VEMPTY + 2,                  // [2] S_j ready, both CTAs
   PB_PRDY = PB_QK + 2,                    // [2] P_j ready, rank-0 CTA, 8 arrivals
+  PB_SREAD = PB_PRDY + 2,                 // S_j read by every softmax warp, rank-0 CTA, 8 arrivals
 };
 
 __device__ __forceinline__ uint32_t cluster_rank() {
@@ -292,6 +295,7 @@ __device__ __forceinline__ void prefill2_body(const PrefillArgs& a, const CUtens
       mbar_init(&bars[PB_QK + i], 1);
       mbar_init(&bars[PB_PRDY + i], 8);  // each softmax warp of both CTAs
     }
+    mbar_init(&bars[PB_SREAD], 8);
     *failed = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -403,9 +407,9 @@ __device__ __forceinline__ void prefill2_body(const PrefillArgs& a, const CUtens
     __syncwarp();
   } else if (warp == kWarpMma) {
     // ============================== S MMAs ==============================
-    // Issued by the rank-0 CTA only, for both (M = 256).  S_{j+2} overwrites
-    // S_j's buffer, which holds P_j, so it waits for P_j V_j to complete.
-    // Issuing a tile's 16 MMAs holds the issuing thread until the tensor
+    // Issued by the rank-0 CTA only, for both (M = 256).  S has one TMEM
+    // buffer: S_{j+1} waits until every softmax warp of both CTAs has read
+    // S_j into registers.  Issuing a tile's 16 MMAs holds the issuing thread until the tensor
     // pipe has nearly run them, so the P V MMAs come from another warp
     // (below): P_j V_j goes to the pipe as soon as P_j is ready, even while
     // this warp is still issuing S_{j+1} (the two touch different TMEM
@@ -427,7 +431,7 @@ __device__ __forceinline__ void prefill2_body(const PrefillArgs& a, const CUtens
             for (int kk = 0; kk < 4; ++kk) {
               const uint64_t da = smem_desc_sw128(aQ + c * S::kQChunk + kk * 32, 16, 1024);
               const uint64_t db = smem_desc_sw128(kst + c * S::kKChunk + kk * 32, 16, 1024);
-              umma2(tmem + st * BN, da, db, idesc_qk, (c | kk) != 0);
+              umma2(tmem, da, db, idesc_qk, (c | kk) != 0);
             }
           commit2_both(&bars[PB_QK + st]);
           commit2_both(&bars[PB_KEMPTY + ks]);
@@ -436,12 +440,11 @@ __device__ __forceinline__ void prefill2_body(const PrefillArgs& a, const CUtens
         return true;
       };
       if (ok) ok = issue_qk(0);
-      if (ok && it.ntiles > 1) ok = issue_qk(1);
-      for (int j = 0; ok && j + 2 < it.ntiles; ++j) {
+      for (int j = 0; ok && j + 1 < it.ntiles; ++j) {
         if (__any_sync(0xffffffffu, stop_requested(failed))) break;
-        const int vs = j % S::VST;
-        ok = warp_wait(&bars[PB_VEMPTY + vs], (j / S::VST) & 1, a.err, failed);
-        if (ok) ok = issue_qk(j + 2);
+        // S_{j+1} overwrites S_j: once all eight softmax warps have read it
+        ok = warp_wait(&bars[PB_SREAD], j & 1, a.err, failed);
+        if (ok) ok = issue_qk(j + 1);
       }
     }
   } else if (warp == kWarpPv) {
@@ -495,7 +498,7 @@ __device__ __forceinline__ void prefill2_body(const PrefillArgs& a, const CUtens
           for (int k = 0; k < BN / 16; ++k) {
             // block k: two 64-column chunks 16 x 128 B apart
             const uint64_t db = smem_desc_sw128(vst + k * S::kVBlock, kBlockSize * 128, 1024);
-            umma2_ts(tmem + S::kTmemO, tmem + st * BN + k * 8, db, idesc_pv,
+            umma2_ts(tmem + S::kTmemO, tmem + S::kTmemP + st * (BN / 2) + k * 8, db, idesc_pv,
                      (j > 0 || k > 0) ? 1u : 0u);
           }
           commit2_both(&bars[PB_VEMPTY + vs]);
@@ -560,10 +563,14 @@ __device__ __forceinline__ void prefill2_body(const PrefillArgs& a, const CUtens
 #pragma unroll
       for (int c = 0; c < BN / 64; ++c) {  // 64 columns per load and wait
         float t[64];
-        tmem_ld64(lane_base + st * BN + c * 64, t);
+        tmem_ld64(lane_base + c * 64, t);
 #pragma unroll
         for (int e = 0; e < 64; ++e) s[c * 64 + e] = t[e];
       }
+      // S_j is in registers: the S warp may overwrite the buffer with S_{j+1}
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) remote_arrive(leader_addr(&bars[PB_SREAD]));
       const int t0 = it.kbase + j * BN;
       const int c_hi = row_valid ? min(BN - 1, p - t0) : -1;
       const int c_lo = max(0, kmin - t0);
@@ -632,9 +639,14 @@ __device__ __forceinline__ void prefill2_body(const PrefillArgs& a, const CUtens
       if (resc) l *= fast_exp2(m_ref - m_new);
       if (j == 0 || resc) m_ref = m_new;
       const float ms = (m_ref == -INFINITY) ? 0.f : m_ref;
-      // P_j (bf16 pairs) over the first half of S_j's buffer: this thread
-      // has read S_j in full, and the MMA warp issues S_{j+2}, the buffer's
-      // next writer, only after P_j V_j has completed.
+      // P_j (bf16 pairs) into P buffer j % 2, whose last reader P_{j-2} V_{j-2}
+      // must have completed.
+      if (j >= 2 && !warp_wait(&bars[PB_VEMPTY + j % S::VST], ((j - 2) / S::VST) & 1, a.err,
+                               failed)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
       // p = 2^(x - ms), x the log2-domain logit (uncapped: x = s * scale * log2 e,
       // fused into one FMA)
       const float xs = prescale ? 1.f : sl2;
@@ -654,7 +666,7 @@ __device__ __forceinline__ void prefill2_body(const PrefillArgs& a, const CUtens
             lsum1 += p1;
             pk[e] = pack_bf16x2(p0, p1);
           }
-          tmem_st32_u(lane_base + st * BN + h * 32, pk);
+          tmem_st32_u(lane_base + S::kTmemP + st * (BN / 2) + h * 32, pk);
         }
         return lsum0 + lsum1;
       };
