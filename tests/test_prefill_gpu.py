@@ -140,6 +140,33 @@ def test_one_hot_prefill_exact(D):
         assert torch.equal(out[i, 0], want), i
 
 
+@pytest.mark.parametrize("D", [128, 256])
+def test_rising_logits_rescale_every_tile(D):
+    """Keys along one direction with growing length and every query along
+    it: each key's logit is 1/16 above the previous key's, so every 128-key
+    tile lifts the running maximum by far more than the lazy rescale's
+    threshold and O is rescaled at every tile -- through the pair kernel's
+    single S buffer and alternating P buffers at D = 256, the one-CTA
+    kernel at D = 128 -- against the oracle."""
+    G, Hkv = 4, 2
+    L, n = [1500, 900, 333], [300, 130, 333]
+    batch = small(L, n, D=D, G=G, Hkv=Hkv, seed=33)
+    gen = torch.Generator(device="cpu").manual_seed(5)
+    u = torch.randn(D, generator=gen)
+    u = (u / u.norm()).to(DEV)
+    q = u.to(torch.bfloat16).expand_as(batch.q).contiguous()
+    k = batch.k_pool.clone()
+    for b, Lb in enumerate(L):
+        blocks = batch.tables_host[b]
+        for t0 in range(0, Lb, 16):
+            rows = torch.arange(t0, min(Lb, t0 + 16), device=DEV, dtype=torch.float32)
+            vals = (rows[:, None] * u[None, :]).to(torch.bfloat16)
+            for h in range(Hkv):
+                k[blocks[t0 // 16], h, : rows.numel()] = vals
+    b2 = workload.PagedBatch(**{**batch.__dict__, "q": q, "k_pool": k, "scale": 1.0})
+    check(b2, f"rising logits D={D}")
+
+
 @pytest.mark.parametrize("cfg", [4, 5])
 def test_full_size_sampled_requests(cfg):
     batch = workload.workload(cfg, seed=0, device=DEV, poison=True)[0]
