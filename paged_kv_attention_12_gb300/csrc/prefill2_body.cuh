@@ -334,6 +334,11 @@ __device__ __forceinline__ void prefill2_body(const PrefillArgs& a, const CUtens
           tma2_load_3d(sQ + c * S::kQChunk, tm_q, c * 64, it.kvh * G, it.q0 + my0, qbar);
       }
     }
+    // V is first read by P_0 V_0, a softmax after S_0: the V warp issues
+    // its first stages once S_0 is done, so that Q and the first K stages,
+    // which S_0 and S_1 need, do not share the memory system with them
+    // (a failed wait sets the flag that ends the loop below).
+    if (!is_k) warp_wait(&bars[PB_QK], 0, a.err, failed);
     // Pool rows of the item's blocks, 32 per coalesced load, in a window
     // of 64 blocks held one per lane in two registers (see prefill_body).
     constexpr int BPT = BN / kBlockSize;  // 8 blocks per key tile
