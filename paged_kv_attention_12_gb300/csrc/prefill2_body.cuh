@@ -232,6 +232,14 @@ __device__ __forceinline__ void prefill2_body(const PrefillArgs& a, const CUtens
         rn[b] = n;
         rL[b] = L;
       }
+      if (a.window <= 0 && n > 0) {
+        // without a window every item of the request starts at its first
+        // block: bring the first 64 table entries into L2 while the items
+        // are ranked (the K warp reads them right after)
+        const int32_t* row = a.tables + static_cast<size_t>(b) * a.max_blocks;
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(row));
+        if (a.max_blocks > 32) asm volatile("prefetch.global.L2 [%0];" ::"l"(row + 32));
+      }
       if (n > 0 && n <= L && !(a.skip_decode_rows != 0 && n == 1)) cnt += (n + TQ2 - 1) / TQ2;
     }
     block_excl_scan(cnt, scratch, scratch + 32);

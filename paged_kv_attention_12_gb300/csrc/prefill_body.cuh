@@ -244,10 +244,37 @@ __device__ __forceinline__ int block_excl_scan(int x, int* warp_sums, int* total
 template <int TQ, int BN>
 __device__ int lpt_pair(const PrefillArgs& a, int qtiles, int rank, int* scratch, int nbuck,
                         const int* rn, const int* rL) {
+  const int npairs = a.batch * qtiles;
+  if (npairs <= static_cast<int>(blockDim.x)) {
+    // Few pairs: one thread per pair counts the pairs ahead of it in the
+    // same order (cost bucket descending, index ascending) -- the rank the
+    // counting sort below gives, in one pass over shared memory.
+    int* cost = scratch;                // [npairs]
+    int* found = scratch + blockDim.x;  // [1]
+    const int i = threadIdx.x;
+    int c = 0;
+    if (i < npairs) {
+      c = min(tile_cost<TQ, BN>(a, rn, rL, i / qtiles, i % qtiles), nbuck - 1);
+      cost[i] = c;
+    }
+    if (i == 0) *found = 0;
+    __syncthreads();
+    if (i < npairs) {
+      int ahead = 0;
+      for (int k = 0; k < npairs; ++k) {
+        const int ck = cost[k];
+        ahead += (ck > c || (ck == c && k < i)) ? 1 : 0;
+      }
+      if (ahead == rank) *found = i;
+    }
+    __syncthreads();
+    const int pair = *found;
+    __syncthreads();
+    return pair;
+  }
   int* hist = scratch;                  // [nbuck]
   int* warp_sums = scratch + nbuck;     // [32]
   int* misc = warp_sums + 32;           // [4]
-  const int npairs = a.batch * qtiles;
   for (int k = threadIdx.x; k < nbuck; k += blockDim.x) hist[k] = 0;
   __syncthreads();
   for (int i = threadIdx.x; i < npairs; i += blockDim.x)
