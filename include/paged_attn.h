@@ -231,6 +231,9 @@ int paged_prefill_attn(const void* q, void* out, const pka_kv_pool* kv,
  * per block and 70 GB/s per SM, K' = min(max_seq_len, window).  With
  * share = round(N * prefill / (prefill + decode)), P = share if share >= 2E,
  * else E; then clamped to [1, N - N/4] (P = 0 without prefill rows).
+ * At D = 256, when P < 2E (no room for pieces), the prefill items run whole
+ * on CTA pairs, two query tiles per pair of SMs, as in paged_prefill_attn
+ * (the decode CTAs then number N - P rounded down to even).
  * Prefill items: one per (request, query tile, KV head) with work.  When
  * they are fewer than P (and at most 160), they are cut along their keys:
  * with theta the smallest piece length >= 4 key tiles for which

@@ -19,7 +19,7 @@
 // once on n_decode SMs and the prefill items take the others.  The host
 // sizes n_decode from the number of prefill tokens.
 #include "decode_body.cuh"
-#include "prefill_body.cuh"
+#include "prefill2_body.cuh"
 #include "tmaps.cuh"
 
 namespace pka {
@@ -43,6 +43,22 @@ struct MixedDecodeTuning {
 
 }  // namespace
 
+// The decode CTAs' part of both mixed kernels: two pipelines per CTA.
+template <int D, int G>
+__device__ __forceinline__ void mixed_decode_part(const DecodeArgs& da, int n_decode,
+                                                  const CUtensorMap* tm_k_tiles,
+                                                  const CUtensorMap* tm_v_tiles,
+                                                  uint8_t* smem_raw) {
+  using T = MixedDecodeTuning<D, G>;
+  const int pipe = static_cast<int>(threadIdx.x) / T::kPipeThreads;  // 0 or 1
+  // named barriers 1, 2, 5 (pipeline 0) and 3, 4, 6 (pipeline 1)
+  const DecodeCtx cx{static_cast<int>(blockIdx.x) * 2 + pipe, n_decode * 2,
+                     static_cast<int>(threadIdx.x) % T::kPipeThreads, 1 + 2 * pipe, 2 + 2 * pipe,
+                     5 + pipe};
+  decode_body<D, G, T::NW, T::NSLOT>(da, tm_k_tiles, tm_v_tiles,
+                                     smem_raw + pipe * T::kPipeBytes, cx);
+}
+
 template <int D, int G>
 __global__ void __launch_bounds__(PrefillShape<D, G>::kThreads, 1)
     paged_mixed_kernel(const __grid_constant__ PrefillArgs pa,
@@ -58,14 +74,29 @@ __global__ void __launch_bounds__(PrefillShape<D, G>::kThreads, 1)
                        static_cast<int>(blockIdx.x) - n_decode);
     return;
   }
-  using T = MixedDecodeTuning<D, G>;
-  const int pipe = static_cast<int>(threadIdx.x) / T::kPipeThreads;  // 0 or 1
-  // named barriers 1, 2, 5 (pipeline 0) and 3, 4, 6 (pipeline 1)
-  const DecodeCtx cx{static_cast<int>(blockIdx.x) * 2 + pipe, n_decode * 2,
-                     static_cast<int>(threadIdx.x) % T::kPipeThreads, 1 + 2 * pipe, 2 + 2 * pipe,
-                     5 + pipe};
-  decode_body<D, G, T::NW, T::NSLOT>(da, &tm_k_tiles, &tm_v_tiles,
-                                     smem_raw + pipe * T::kPipeBytes, cx);
+  mixed_decode_part<D, G>(da, n_decode, &tm_k_tiles, &tm_v_tiles, smem_raw);
+}
+
+// D = 256 with every prefill item whole: the chunks' query tiles run on CTA
+// pairs (prefill2_body.cuh: two query tiles per cluster of two SMs, one MMA
+// of M = 256), the decode CTAs as above.  n_decode is even, so that every
+// cluster is either two decode CTAs or one pair.
+template <int G>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Prefill2Shape<G>::kThreads, 1)
+    paged_mixed_pair_kernel(const __grid_constant__ PrefillArgs pa,
+                            const __grid_constant__ DecodeArgs da, const int n_decode,
+                            const __grid_constant__ CUtensorMap tm_q,
+                            const __grid_constant__ CUtensorMap tm_k_rows,
+                            const __grid_constant__ CUtensorMap tm_k_tiles,
+                            const __grid_constant__ CUtensorMap tm_v_tiles,
+                            const __grid_constant__ CUtensorMap tm_v_half,
+                            const __grid_constant__ CUtensorMap tm_out) {
+  extern __shared__ uint8_t smem_raw[];
+  if (static_cast<int>(blockIdx.x) >= n_decode) {
+    prefill2_body<G>(pa, &tm_q, &tm_k_rows, &tm_v_half, &tm_out, smem_raw, n_decode);
+    return;
+  }
+  mixed_decode_part<256, G>(da, n_decode, &tm_k_tiles, &tm_v_tiles, smem_raw);
 }
 
 namespace {
@@ -95,6 +126,33 @@ cudaError_t launch_mixed_t(const PrefillArgs& pa, const DecodeArgs& da, int deco
   return cudaGetLastError();
 }
 
+template <int G>
+cudaError_t launch_mixed_pair_t(const PrefillArgs& pa, const DecodeArgs& da, int decode_ctas,
+                                cudaStream_t stream) {
+  using S = Prefill2Shape<G>;
+  using T = MixedDecodeTuning<256, G>;
+  static_assert(2 * T::kPipeThreads == S::kThreads, "two pipelines per CTA");
+  constexpr int kSmem = (2 * T::kPipeBytes > S::kSmemBytes) ? 2 * T::kPipeBytes : S::kSmemBytes;
+  CUtensorMap tq, tkr, tkt, tvt, tvh, to;
+  const long long rows = static_cast<long long>(pa.num_blocks) * pa.Hkv * kBlockSize;
+  if (!tmap_query_tiles(&tq, pa.q, 256, pa.Hq, pa.total_q, G, S::TQ) ||
+      !tmap_pool_rows(&tkr, pa.k, 256, rows) || !tmap_pool_tiles(&tkt, pa.k, 256, rows) ||
+      !tmap_pool_tiles(&tvt, pa.v, 256, rows) ||
+      !tmap_pool_tiles_chunks(&tvh, pa.v, 256, rows, S::DC / 2) ||
+      !tmap_query_tiles(&to, pa.out, 256, pa.Hq, pa.total_q, G, S::TQ))
+    return cudaErrorInvalidValue;
+  auto kern = paged_mixed_pair_kernel<G>;
+  cudaError_t e = set_smem_once(reinterpret_cast<const void*>(kern), kSmem);
+  if (e != cudaSuccess) return e;
+  if (decode_ctas <= 0 || (decode_ctas & 1) != 0) return cudaErrorInvalidValue;
+  const long long clusters = prefill_ranks(pa, 2 * S::TQ);
+  const long long ctas = static_cast<long long>(decode_ctas) + 2 * clusters;
+  if (ctas > 0x7fffffffLL) return cudaErrorInvalidValue;
+  kern<<<static_cast<unsigned>(ctas), S::kThreads, kSmem, stream>>>(pa, da, decode_ctas, tq, tkr,
+                                                                    tkt, tvt, tvh, to);
+  return cudaGetLastError();
+}
+
 }  // namespace
 
 int mixed_query_tile(int head_dim, int group) {
@@ -117,7 +175,16 @@ int mixed_query_tile(int head_dim, int group) {
 }
 
 cudaError_t launch_mixed(const PrefillArgs& pa, const DecodeArgs& da, int head_dim, int group,
-                         int decode_ctas, cudaStream_t stream) {
+                         int decode_ctas, bool pairs, cudaStream_t stream) {
+  if (pairs && head_dim == 256) {
+    switch (group) {
+      case 1: return launch_mixed_pair_t<1>(pa, da, decode_ctas, stream);
+      case 2: return launch_mixed_pair_t<2>(pa, da, decode_ctas, stream);
+      case 4: return launch_mixed_pair_t<4>(pa, da, decode_ctas, stream);
+      case 8: return launch_mixed_pair_t<8>(pa, da, decode_ctas, stream);
+    }
+    return cudaErrorInvalidValue;
+  }
 #define PKA_MIX(D_, G_) \
   if (head_dim == D_ && group == G_) return launch_mixed_t<D_, G_>(pa, da, decode_ctas, stream);
   PKA_MIX(128, 1)

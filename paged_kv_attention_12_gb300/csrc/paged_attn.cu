@@ -502,6 +502,12 @@ int paged_prefill_attn_ws(const void* q, void* out, const pka_kv_pool* kv,
   }
   long long decode_ctas = static_cast<long long>(sms) - prefill_sms;
   if (decode_ctas < 1) decode_ctas = 1;
+  // At D = 256, when the items are not expected to be cut along keys (no
+  // proportional share of twice the items), they run whole on CTA pairs
+  // (two query tiles per pair of SMs, as in paged_prefill_attn), which
+  // needs an even number of decode CTAs before them.
+  const bool pairs = (D == 256) && est_items > 0 && prefill_sms < 2 * est_items;
+  if (pairs && (decode_ctas & 1) != 0) --decode_ctas;
   // The prefill items run in the SMs the decode CTAs leave; when they fit
   // in one wave with room to spare, they are cut along keys into pieces
   // that fill it (the pieces' rows and counters after the decode part).
@@ -513,7 +519,7 @@ int paged_prefill_attn_ws(const void* q, void* out, const pka_kv_pool* kv,
   pa.split_cnt = reinterpret_cast<int32_t*>(split + static_cast<size_t>(kPrefillSplitSlots) * 128 *
                                                         (D + 1) * 4);
   pa.split_slots = kPrefillSplitSlots;
-  cudaError_t e = pka::launch_mixed(pa, da, D, G, static_cast<int>(decode_ctas),
+  cudaError_t e = pka::launch_mixed(pa, da, D, G, static_cast<int>(decode_ctas), pairs,
                                     static_cast<cudaStream_t>(stream));
   if (e == cudaErrorNotSupported) return PKA_ERR_UNSUPPORTED;
   return e == cudaSuccess ? PKA_OK : PKA_ERR_CUDA;

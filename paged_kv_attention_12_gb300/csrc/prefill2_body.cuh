@@ -196,15 +196,17 @@ __device__ __forceinline__ void tmem2_dealloc(uint32_t taddr, uint32_t ncols) {
 }  // namespace pair2
 
 // One pair item per cluster of two CTAs on the S::kSmemBytes of shared
-// memory at smem_raw: the cluster of index blockIdx.x / 2 takes the pair
-// item of that rank (heaviest first over (request, two query tiles) pairs),
+// memory at smem_raw: the cluster of index (blockIdx.x - rank_base) / 2
+// (rank_base even: the CTAs before it do other work) takes the pair item of
+// that rank (heaviest first over (request, two query tiles) pairs),
 // KV head rank % Hkv; ranks past the last item return at once (both CTAs of
 // a cluster decide alike: everything up to the TMEM allocation depends on
 // the arguments and the cluster's index only).
 template <int G>
 __device__ __forceinline__ void prefill2_body(const PrefillArgs& a, const CUtensorMap* tm_q,
                                               const CUtensorMap* tm_k, const CUtensorMap* tm_v,
-                                              const CUtensorMap* tm_out, uint8_t* smem_raw) {
+                                              const CUtensorMap* tm_out, uint8_t* smem_raw,
+                                              int rank_base) {
   using S = Prefill2Shape<G>;
   using namespace pair2;
   constexpr int D = S::D, BN = S::BN, TQ = S::TQ, DC = S::DC;
@@ -212,7 +214,7 @@ __device__ __forceinline__ void prefill2_body(const PrefillArgs& a, const CUtens
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   const int crank = static_cast<int>(cluster_rank());
-  const int rank = static_cast<int>(blockIdx.x) / 2;
+  const int rank = (static_cast<int>(blockIdx.x) - rank_base) / 2;  // the cluster's pair rank
 
   // ---------------------------------------------------------- work item
   Item it;
