@@ -473,8 +473,9 @@ def other_workloads(dev, flush, iters=10, warmup=3, cfgs=(1, 3, 4, 5)):
                                "fit one per pipeline stream whole)")
         elif cfg == 5:
             r = binding.MixedBatch(batch)
-            fn, path = r.run, ("paged_prefill_attn_ws (one launch: decode rows on split-K "
-                               "decode pipelines, chunks on the tcgen05 prefill pipeline)")
+            fn, path = r.run, ("paged_prefill_attn_ws (one launch: decode rows on decode "
+                               "pipelines, chunks on the tcgen05 prefill pipeline -- CTA "
+                               "pairs at D = 256 when no tile is cut along keys)")
         else:
             out = torch.empty_like(batch.q)
             fn, path = (lambda b=batch, o=out: binding.run_batch(b, o)), "paged_prefill_attn"
