@@ -846,16 +846,28 @@ __device__ __forceinline__ void prefill_body(const PrefillArgs& a, const CUtenso
       // mask; the warp takes the masked loop only if one of its rows does.
       const bool need_mask = __any_sync(0xffffffffu, c_lo > 0 || c_hi < BN - 1);
       bool folded = false;
+      // Row maximum in column pairs (three-input max); the capped path takes
+      // the minimum too, for the range of |s| that picks its form.  On a
+      // tile with no masked column the raw maximum is the one the folded
+      // form needs.
+      float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+      bool have_max = false;
       if (capped) {
+        float n4[4] = {INFINITY, INFINITY, INFINITY, INFINITY};
+#pragma unroll
+        for (int c = 0; c < BN / 2; ++c) {
+          m4[c & 3] = max3f(m4[c & 3], s[2 * c], s[2 * c + 1]);
+          n4[c & 3] = min3f(n4[c & 3], s[2 * c], s[2 * c + 1]);
+        }
+        const float amax = fmaxf(fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])),
+                                 -fminf(fminf(n4[0], n4[1]), fminf(n4[2], n4[3])));
         // log2-domain logits cap * tanh(s * scale / cap) * log2(e); a
         // Taylor form when every |y| of the warp's rows is below 1/8 (three
         // terms) or 0.5 (six terms), else the exp2 form.  With scale > 0 the
         // three-term form stays folded (see k1, k3, k5) and s stays raw.
-        float amax = 0.f;
-#pragma unroll
-        for (int c = 0; c < BN; ++c) amax = fmaxf(amax, fabsf(s[c]));
         if (fold_ok && __all_sync(0xffffffffu, amax * cap_in < 0.125f)) {
           folded = true;
+          have_max = !need_mask;
         } else if (__all_sync(0xffffffffu, amax * cap_in < 0.125f)) {
 #pragma unroll
           for (int c = 0; c < BN; ++c) s[c] = cap_out * tanh_taylor_short(s[c] * cap_in);
@@ -868,7 +880,11 @@ __device__ __forceinline__ void prefill_body(const PrefillArgs& a, const CUtenso
         }
       } else if (prescale) {
 #pragma unroll
-        for (int c = 0; c < BN; ++c) s[c] *= sl2;
+        for (int c = 0; c < BN; c += 2) {
+          const float2 v = mul2(make_float2(s[c], s[c + 1]), make_float2(sl2, sl2));
+          s[c] = v.x;
+          s[c + 1] = v.y;
+        }
       }
       // (otherwise s stays raw; scale > 0, so the raw max scales to the max)
       if (need_mask) {
@@ -876,9 +892,12 @@ __device__ __forceinline__ void prefill_body(const PrefillArgs& a, const CUtenso
         for (int c = 0; c < BN; ++c)
           if (!(c >= c_lo && c <= c_hi)) s[c] = -INFINITY;
       }
-      float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+      if (!have_max) {
 #pragma unroll
-      for (int c = 0; c < BN; ++c) m4[c & 3] = fmaxf(m4[c & 3], s[c]);
+        for (int e = 0; e < 4; ++e) m4[e] = -INFINITY;
+#pragma unroll
+        for (int c = 0; c < BN / 2; ++c) m4[c & 3] = max3f(m4[c & 3], s[2 * c], s[2 * c + 1]);
+      }
       float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
       if (folded)
         mx = mx * fmaf(mx * mx, fmaf(mx * mx, k5, k3), k1);  // x(max s) = max x(s)
@@ -915,26 +934,35 @@ __device__ __forceinline__ void prefill_body(const PrefillArgs& a, const CUtenso
       // x - ms for each column: the folded capped form, or the (scaled)
       // logit; the two loops are compiled separately so that neither pays
       // for the other's arithmetic
-      auto make_p = [&](auto arg) {
-        float lsum0 = 0.f, lsum1 = 0.f;
+      auto make_p = [&](auto arg2) {
+        float2 lsum0 = make_float2(0.f, 0.f), lsum1 = make_float2(0.f, 0.f);
 #pragma unroll
         for (int h = 0; h < BN / 64; ++h) {
           uint32_t pk[32];
 #pragma unroll
           for (int e = 0; e < 32; ++e) {
-            const float p0 = fast_exp2(arg(s[h * 64 + 2 * e]));
-            const float p1 = fast_exp2(arg(s[h * 64 + 2 * e + 1]));
-            lsum0 += p0;
-            lsum1 += p1;
-            pk[e] = pack_bf16x2(p0, p1);
+            const float2 x = arg2(make_float2(s[h * 64 + 2 * e], s[h * 64 + 2 * e + 1]));
+            const float2 pp = make_float2(fast_exp2(x.x), fast_exp2(x.y));
+            if (e & 1)
+              lsum1 = add2(lsum1, pp);
+            else
+              lsum0 = add2(lsum0, pp);
+            pk[e] = pack_bf16x2(pp.x, pp.y);
           }
           tmem_st32_u(lane_base + S::kTmemP + st * (BN / 2) + h * 32, pk);
         }
-        return lsum0 + lsum1;
+        const float2 ls = add2(lsum0, lsum1);
+        return ls.x + ls.y;
       };
+      const float2 nms = make_float2(-ms, -ms);
       const float lsum =
-          folded ? make_p([&](float x) { return fmaf(x, fmaf(x * x, fmaf(x * x, k5, k3), k1), -ms); })
-                 : make_p([&](float x) { return fmaf(x, xs, -ms); });
+          folded ? make_p([&](float2 x) {
+                     const float2 t = mul2(x, x);
+                     const float2 u = fma2(t, fma2(t, make_float2(k5, k5), make_float2(k3, k3)),
+                                           make_float2(k1, k1));
+                     return fma2(x, u, nms);
+                   })
+                 : make_p([&](float2 x) { return fma2(x, make_float2(xs, xs), nms); });
       l += lsum;
       tmem_wait_st();
       tc_fence_before();
