@@ -475,7 +475,7 @@ def other_workloads(dev, flush, iters=10, warmup=3, cfgs=(1, 3, 4, 5)):
             r = binding.MixedBatch(batch)
             fn, path = r.run, ("paged_prefill_attn_ws (one launch: decode rows on decode "
                                "pipelines, chunks on the tcgen05 prefill pipeline -- CTA "
-                               "pairs at D = 256 when no tile is cut along keys)")
+                               "pairs at D = 256)")
         else:
             out = torch.empty_like(batch.q)
             fn, path = (lambda b=batch, o=out: binding.run_batch(b, o)), "paged_prefill_attn"
@@ -539,8 +539,8 @@ def split_sweep(batch, flush, iters, warmup, hbm):
 def time_long_chunk(dev, flush, iters, warmup, tc, tc_kind):
     """One 512-token chunk at a 16K-token prefix beside 32 decode rows of 2K
     tokens (Hq=8, Hkv=2, D=256, softcap 50): through paged_prefill_attn_ws,
-    whose 32 query-tile items fill far less than their SMs and are cut along
-    their keys, and through paged_prefill_attn, whole tiles."""
+    whose 16 CTA-pair items fill far less than their pair slots and are cut
+    along their keys, and through paged_prefill_attn, whole pair items."""
     import torch
     from paged_kv_attention_12_gb300 import binding, workload
     L = [16896] + [2048] * 32

@@ -231,18 +231,22 @@ int paged_prefill_attn(const void* q, void* out, const pka_kv_pool* kv,
  * per block and 70 GB/s per SM, K' = min(max_seq_len, window).  With
  * share = round(N * prefill / (prefill + decode)), P = share if share >= 2E,
  * else E; then clamped to [1, N - N/4] (P = 0 without prefill rows).
- * At D = 256, when P < 2E (no room for pieces), the prefill items run whole
- * on CTA pairs, two query tiles per pair of SMs, as in paged_prefill_attn
- * (the decode CTAs then number N - P rounded down to even).
- * Prefill items: one per (request, query tile, KV head) with work.  When
- * they are fewer than P (and at most 160), they are cut along their keys:
- * with theta the smallest piece length >= 4 key tiles for which
- * sum over items of min(8, ceil(tiles / theta)) <= min(P, 160), an item of T
- * key tiles runs as p = min(8, ceil(T / theta)) pieces on separate CTAs,
- * piece k taking tiles [k T / p, (k + 1) T / p); each piece leaves its
- * normalised rows and their LSEs in the workspace and the piece that
- * arrives last on the item's counter merges them in piece order (the same
- * result whichever piece merges).
+ * Prefill items: one per (request, query tile, KV head) with work, on one
+ * CTA each at D = 128; at D = 256 on CTA pairs, two query tiles per pair of
+ * SMs, as in paged_prefill_attn (the decode CTAs then number N - P rounded
+ * down to even, and the P SMs give S = P / 2 pair slots and 80 piece slots;
+ * else S = P slots and 160 piece slots).  When the items are fewer than S
+ * (and at most the piece slots; at D = 256 only when also the estimate
+ * ceil((total_q - B) / (2 TQ)) * Hkv is below S and at most 80), they are
+ * cut along their keys: with theta
+ * the smallest piece length >= 4 key tiles for which sum over items of
+ * min(8, ceil(tiles / theta)) <= min(S, piece slots), an item of T key
+ * tiles runs as p = min(8, ceil(T / theta)) pieces on separate CTAs (CTA
+ * pairs), piece k taking tiles [k T / p, (k + 1) T / p); each piece leaves
+ * its normalised rows and their LSEs in the workspace (a CTA pair: each CTA
+ * its 128 rows in a slot of its own) and the piece that arrives last on the
+ * item's counter (at D = 256, each CTA's rows have their own) merges them
+ * in piece order (the same result whichever piece merges).
  * workspace: device, 16-byte aligned, at least paged_prefill_attn_ws_bytes()
  * bytes: the layout of paged_decode_attn_ws for B requests, then 160 piece
  * slots of 128 fp32 rows of D columns, their 160 * 128 fp32 LSEs and 160

@@ -90,11 +90,13 @@ cudaError_t launch_prefill(const PrefillArgs& a, int head_dim, int group, int sm
 // Mixed batch in one launch: the prefill items of `pa` (skip_decode_rows set)
 // on prefill CTAs, the decode rows of `da` (decode_rows_only set, split-K
 // with the fused combine) on `decode_ctas` CTAs of two decode pipelines each.
-// pairs (D = 256 only, decode_ctas even): the prefill items run whole on
-// CTA pairs instead of one CTA each (pieces along keys need the one-CTA
-// kernel).
+// pairs (D = 256 only, decode_ctas even): the prefill items run on CTA
+// pairs instead of one CTA each (pa.one_wave SMs give one_wave / 2 pair
+// slots; a piece along keys takes two workspace slots, one per CTA).
+// pair_pieces: the pair kernel that may cut its items along keys (else the
+// items run whole, whatever their number).
 cudaError_t launch_mixed(const PrefillArgs& pa, const DecodeArgs& da, int head_dim, int group,
-                         int decode_ctas, bool pairs, cudaStream_t stream);
+                         int decode_ctas, bool pairs, bool pair_pieces, cudaStream_t stream);
 
 // Query tokens per 128-row prefill tile (0: unsupported shape).
 int mixed_query_tile(int head_dim, int group);

@@ -77,11 +77,12 @@ __global__ void __launch_bounds__(PrefillShape<D, G>::kThreads, 1)
   mixed_decode_part<D, G>(da, n_decode, &tm_k_tiles, &tm_v_tiles, smem_raw);
 }
 
-// D = 256 with every prefill item whole: the chunks' query tiles run on CTA
-// pairs (prefill2_body.cuh: two query tiles per cluster of two SMs, one MMA
-// of M = 256), the decode CTAs as above.  n_decode is even, so that every
-// cluster is either two decode CTAs or one pair.
-template <int G>
+// D = 256: the chunks' query tiles run on CTA pairs (prefill2_body.cuh: two
+// query tiles per cluster of two SMs, one MMA of M = 256), the decode CTAs
+// as above.  n_decode is even, so that every cluster is either two decode
+// CTAs or one pair.  kSplit: the pair items may be cut along keys (the
+// merge code is compiled in only then; it costs the softmax registers).
+template <int G, bool kSplit>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Prefill2Shape<G>::kThreads, 1)
     paged_mixed_pair_kernel(const __grid_constant__ PrefillArgs pa,
                             const __grid_constant__ DecodeArgs da, const int n_decode,
@@ -93,7 +94,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Prefill2Shape<G>::kT
                             const __grid_constant__ CUtensorMap tm_out) {
   extern __shared__ uint8_t smem_raw[];
   if (static_cast<int>(blockIdx.x) >= n_decode) {
-    prefill2_body<G>(pa, &tm_q, &tm_k_rows, &tm_v_half, &tm_out, smem_raw, n_decode);
+    prefill2_body<G, kSplit>(pa, &tm_q, &tm_k_rows, &tm_v_half, &tm_out, smem_raw, n_decode);
     return;
   }
   mixed_decode_part<256, G>(da, n_decode, &tm_k_tiles, &tm_v_tiles, smem_raw);
@@ -128,7 +129,7 @@ cudaError_t launch_mixed_t(const PrefillArgs& pa, const DecodeArgs& da, int deco
 
 template <int G>
 cudaError_t launch_mixed_pair_t(const PrefillArgs& pa, const DecodeArgs& da, int decode_ctas,
-                                cudaStream_t stream) {
+                                bool pieces, cudaStream_t stream) {
   using S = Prefill2Shape<G>;
   using T = MixedDecodeTuning<256, G>;
   static_assert(2 * T::kPipeThreads == S::kThreads, "two pipelines per CTA");
@@ -141,11 +142,15 @@ cudaError_t launch_mixed_pair_t(const PrefillArgs& pa, const DecodeArgs& da, int
       !tmap_pool_tiles_chunks(&tvh, pa.v, 256, rows, S::DC / 2) ||
       !tmap_query_tiles(&to, pa.out, 256, pa.Hq, pa.total_q, G, S::TQ))
     return cudaErrorInvalidValue;
-  auto kern = paged_mixed_pair_kernel<G>;
+  auto kern = pieces ? paged_mixed_pair_kernel<G, true> : paged_mixed_pair_kernel<G, false>;
   cudaError_t e = set_smem_once(reinterpret_cast<const void*>(kern), kSmem);
   if (e != cudaSuccess) return e;
   if (decode_ctas <= 0 || (decode_ctas & 1) != 0) return cudaErrorInvalidValue;
-  const long long clusters = prefill_ranks(pa, 2 * S::TQ);
+  long long clusters = prefill_ranks(pa, 2 * S::TQ);
+  // with pieces along keys, up to one wave of units (pair slots, two
+  // workspace slots each)
+  if (pieces && pa.split_o != nullptr && pa.one_wave / 2 > clusters)
+    clusters = min(pa.one_wave / 2, pa.split_slots / 2);
   const long long ctas = static_cast<long long>(decode_ctas) + 2 * clusters;
   if (ctas > 0x7fffffffLL) return cudaErrorInvalidValue;
   kern<<<static_cast<unsigned>(ctas), S::kThreads, kSmem, stream>>>(pa, da, decode_ctas, tq, tkr,
@@ -175,13 +180,13 @@ int mixed_query_tile(int head_dim, int group) {
 }
 
 cudaError_t launch_mixed(const PrefillArgs& pa, const DecodeArgs& da, int head_dim, int group,
-                         int decode_ctas, bool pairs, cudaStream_t stream) {
+                         int decode_ctas, bool pairs, bool pair_pieces, cudaStream_t stream) {
   if (pairs && head_dim == 256) {
     switch (group) {
-      case 1: return launch_mixed_pair_t<1>(pa, da, decode_ctas, stream);
-      case 2: return launch_mixed_pair_t<2>(pa, da, decode_ctas, stream);
-      case 4: return launch_mixed_pair_t<4>(pa, da, decode_ctas, stream);
-      case 8: return launch_mixed_pair_t<8>(pa, da, decode_ctas, stream);
+      case 1: return launch_mixed_pair_t<1>(pa, da, decode_ctas, pair_pieces, stream);
+      case 2: return launch_mixed_pair_t<2>(pa, da, decode_ctas, pair_pieces, stream);
+      case 4: return launch_mixed_pair_t<4>(pa, da, decode_ctas, pair_pieces, stream);
+      case 8: return launch_mixed_pair_t<8>(pa, da, decode_ctas, pair_pieces, stream);
     }
     return cudaErrorInvalidValue;
   }

@@ -502,11 +502,11 @@ int paged_prefill_attn_ws(const void* q, void* out, const pka_kv_pool* kv,
   }
   long long decode_ctas = static_cast<long long>(sms) - prefill_sms;
   if (decode_ctas < 1) decode_ctas = 1;
-  // At D = 256, when the items are not expected to be cut along keys (no
-  // proportional share of twice the items), they run whole on CTA pairs
-  // (two query tiles per pair of SMs, as in paged_prefill_attn), which
-  // needs an even number of decode CTAs before them.
-  const bool pairs = (D == 256) && est_items > 0 && prefill_sms < 2 * est_items;
+  // At D = 256 the items run on CTA pairs (two query tiles per pair of SMs,
+  // as in paged_prefill_attn, cut along keys as below when they fit the
+  // pair slots with room to spare), which needs an even number of decode
+  // CTAs before them.
+  const bool pairs = (D == 256) && est_items > 0;
   if (pairs && (decode_ctas & 1) != 0) --decode_ctas;
   // The prefill items run in the SMs the decode CTAs leave; when they fit
   // in one wave with room to spare, they are cut along keys into pieces
@@ -519,8 +519,15 @@ int paged_prefill_attn_ws(const void* q, void* out, const pka_kv_pool* kv,
   pa.split_cnt = reinterpret_cast<int32_t*>(split + static_cast<size_t>(kPrefillSplitSlots) * 128 *
                                                         (D + 1) * 4);
   pa.split_slots = kPrefillSplitSlots;
+  // The pair kernel that can cut its items along keys only when the items
+  // the sizes suggest (the query tokens beyond one per request, in pair
+  // items of 2 TQ) are fewer than the pair slots: the merge code it carries
+  // slows its softmax, and with as many items as slots it would not cut.
+  const long long est_pair_items = extra > 0 ? (extra + 2 * tq - 1) / (2 * tq) * Hkv : 0;
+  const bool pair_pieces =
+      pairs && est_pair_items < pa.one_wave / 2 && est_pair_items <= kPrefillSplitSlots / 2;
   cudaError_t e = pka::launch_mixed(pa, da, D, G, static_cast<int>(decode_ctas), pairs,
-                                    static_cast<cudaStream_t>(stream));
+                                    pair_pieces, static_cast<cudaStream_t>(stream));
   if (e == cudaErrorNotSupported) return PKA_ERR_UNSUPPORTED;
   return e == cudaSuccess ? PKA_OK : PKA_ERR_CUDA;
 }

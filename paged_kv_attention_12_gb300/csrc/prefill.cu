@@ -26,7 +26,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Prefill2Shape<G>::kT
                           const __grid_constant__ CUtensorMap tm_v,
                           const __grid_constant__ CUtensorMap tm_out) {
   extern __shared__ uint8_t smem_raw[];
-  prefill2_body<G>(a, &tm_q, &tm_k, &tm_v, &tm_out, smem_raw, 0);
+  prefill2_body<G, false>(a, &tm_q, &tm_k, &tm_v, &tm_out, smem_raw, 0);
 }
 
 // ------------------------------------------------------------- launchers

@@ -73,6 +73,9 @@ struct Prefill2Shape {
   static constexpr int kCostBuckets = 4096;
   static_assert((kCostBuckets + 64) * 4 <= KST * kKStage, "ranking scratch");
   static_assert((kReqCacheOffset + 2 * kReqCache) * 4 <= KST * kKStage, "request cache");
+  static_assert(kListOffset >= kReqCacheOffset + 2 * kReqCache &&
+                    (kListOffset + 5 * kMaxList + 4) * 4 <= KST * kKStage,
+                "the pair list fits in the K stages, past the request cache");
   static_assert(kSmemBytes <= 232448, "shared memory");
   static_assert(KST == 3 && VST == 2, "the barrier map below assumes 3 K and 2 V stages");
   static_assert(kTmemP + BN <= kTmemO && kTmemO + D <= kTmemCols, "TMEM columns");
@@ -202,7 +205,7 @@ __device__ __forceinline__ void tmem2_dealloc(uint32_t taddr, uint32_t ncols) {
 // KV head rank % Hkv; ranks past the last item return at once (both CTAs of
 // a cluster decide alike: everything up to the TMEM allocation depends on
 // the arguments and the cluster's index only).
-template <int G>
+template <int G, bool kSplit>
 __device__ __forceinline__ void prefill2_body(const PrefillArgs& a, const CUtensorMap* tm_q,
                                               const CUtensorMap* tm_k, const CUtensorMap* tm_v,
                                               const CUtensorMap* tm_out, uint8_t* smem_raw,
@@ -223,6 +226,7 @@ __device__ __forceinline__ void prefill2_body(const PrefillArgs& a, const CUtens
   const bool cache = a.batch <= kReqCache;
   int* rn = cache ? scratch + kReqCacheOffset : nullptr;
   int* rL = cache ? rn + kReqCache : nullptr;
+  int pairs_with_work = 0;
   {
     int cnt = 0;
     for (int b = threadIdx.x; b < a.batch; b += blockDim.x) {
@@ -245,15 +249,35 @@ __device__ __forceinline__ void prefill2_body(const PrefillArgs& a, const CUtens
       if (n > 0 && n <= L && !(a.skip_decode_rows != 0 && n == 1)) cnt += (n + TQ2 - 1) / TQ2;
     }
     block_excl_scan(cnt, scratch, scratch + 32);
-    const int pairs_with_work = scratch[32];
+    pairs_with_work = scratch[32];
     __syncthreads();
-    if (rank / a.Hkv >= pairs_with_work) return;  // uniform over the cluster
   }
-  const int nbuck = min(S::kCostBuckets, (a.max_seq_len + BN - 1) / BN + 2);
-  const int pair = lpt_pair<TQ2, BN>(a, qtiles, rank / a.Hkv, scratch, nbuck, rn, rL);
-  it.b = pair / qtiles;
-  it.kvh = rank % a.Hkv;
-  const int qt2 = pair % qtiles;
+  // With the split workspace (the mixed launch) and every pair item in one
+  // wave of the pair slots (a.one_wave SMs, two per slot), the items go in
+  // index order and are cut along keys into pieces that fill the wave, as
+  // in the one-CTA body: counted in pair slots, each piece takes two
+  // workspace slots, one per CTA of the pair (its 128 rows).  Otherwise the
+  // items are ranked heaviest first and run whole.
+  Unit un{0, 0, 0, 0, 1, 0};
+  int qt2;
+  const long long items = static_cast<long long>(pairs_with_work) * a.Hkv;
+  if (kSplit && items <= a.one_wave / 2 && pairs_with_work <= kMaxList) {
+    PrefillArgs ap = a;
+    ap.one_wave = a.one_wave / 2;
+    ap.split_slots = a.split_slots / 2;
+    const bool split = a.split_o != nullptr && items < ap.one_wave && items <= ap.split_slots;
+    if (!one_wave_unit<TQ2, BN>(ap, rank, pairs_with_work, split, scratch, rn, rL, &un)) return;
+    it.b = un.b;
+    it.kvh = un.kvh;
+    qt2 = un.qt;
+  } else {
+    if (rank / a.Hkv >= pairs_with_work) return;  // uniform over the cluster
+    const int nbuck = min(S::kCostBuckets, (a.max_seq_len + BN - 1) / BN + 2);
+    const int pair = lpt_pair<TQ2, BN>(a, qtiles, rank / a.Hkv, scratch, nbuck, rn, rL);
+    it.b = pair / qtiles;
+    it.kvh = rank % a.Hkv;
+    qt2 = pair % qtiles;
+  }
   it.n = query_span(a, it.b, &it.q0);
   if (it.n < 0) return;  // uniform (reported by the first pass)
   it.L = a.seq_lens[it.b];
@@ -274,6 +298,13 @@ __device__ __forceinline__ void prefill2_body(const PrefillArgs& a, const CUtens
   it.kbase = t_lo & ~(kBlockSize - 1);
   it.ntiles = (p_last + 1 - it.kbase + BN - 1) / BN;
   it.nblk = (it.L + kBlockSize - 1) / kBlockSize;
+  if (un.npieces > 1) {
+    // this piece's key tiles
+    const int j0 = un.piece * it.ntiles / un.npieces;
+    const int j1 = (un.piece + 1) * it.ntiles / un.npieces;
+    it.kbase += j0 * BN;
+    it.ntiles = j1 - j0;
+  }
   const int my0 = it.it0 + crank * TQ;  // this CTA's first query row
 
   uint8_t* sQ = smem + S::oQ;
@@ -528,8 +559,6 @@ __device__ __forceinline__ void prefill2_body(const PrefillArgs& a, const CUtens
       }
     }
   } else {
-    constexpr bool kSplit = false;  // pieces along keys: the mixed launch's one-CTA body only
-    const Unit un{0, 0, 0, 0, 1, 0};
     // ============================== softmax ==============================
     const int r = threadIdx.x;  // row of the tile, TMEM lane
     const int tok = r / G;
@@ -737,9 +766,12 @@ __device__ __forceinline__ void prefill2_body(const PrefillArgs& a, const CUtens
     // arrives last on the item's counter merges every piece's slot, in piece
     // order (the same bits whichever piece merges), and writes the output.
     const bool split_item = kSplit && un.npieces > 1;  // uniform over the CTA
+    // workspace slot of piece k for this CTA's rows; the arrival counter of
+    // the item's rows on this CTA
+    auto slot_of = [&](int k) { return 2 * (un.slot0 + k) + crank; };
     bool write_out = true;
     if (split_item) {
-      const int slot = un.slot0 + un.piece;
+      const int slot = slot_of(un.piece);
       if (ok) {
         tc_fence_after();
         const float inv = (l > 0.f) ? 1.f / l : 0.f;
@@ -762,9 +794,9 @@ __device__ __forceinline__ void prefill2_body(const PrefillArgs& a, const CUtens
       asm volatile("bar.sync %0, %1;" ::"r"(kBarSoftmax), "r"(128) : "memory");
       if (threadIdx.x == 0) {
         fence_acq_rel_gpu();  // the CTA's rows (ordered by the barrier) before its arrival
-        const int old = atomicAdd(a.split_cnt + un.slot0, 1);
+        const int old = atomicAdd(a.split_cnt + slot_of(0), 1);
         *last = (old == un.npieces - 1) ? 1 : 0;
-        if (old == un.npieces - 1) a.split_cnt[un.slot0] = 0;  // for the next call
+        if (old == un.npieces - 1) a.split_cnt[slot_of(0)] = 0;  // for the next call
       }
       asm volatile("bar.sync %0, %1;" ::"r"(kBarSoftmax), "r"(128) : "memory");
       write_out = (*last != 0);
@@ -775,15 +807,13 @@ __device__ __forceinline__ void prefill2_body(const PrefillArgs& a, const CUtens
       float inv = (l > 0.f) ? 1.f / l : 0.f;
       // split item: the pieces' weights 2^(LSE_k - max LSE)
       float w[kMaxPieces];
-      const float4* pk = split_item ? reinterpret_cast<const float4*>(a.split_o) +
-                                          static_cast<size_t>(un.slot0) * (D / 4) * 128 + r
-                                    : nullptr;
+      const float4* pk = split_item ? reinterpret_cast<const float4*>(a.split_o) + r : nullptr;
       if (split_item) {
         float lk[kMaxPieces];
         float M = -INFINITY;
 #pragma unroll
         for (int k = 0; k < kMaxPieces; ++k) {
-          lk[k] = (k < un.npieces) ? __ldcg(a.split_lse + static_cast<size_t>(un.slot0 + k) * 128 + r)
+          lk[k] = (k < un.npieces) ? __ldcg(a.split_lse + static_cast<size_t>(slot_of(k)) * 128 + r)
                                    : -INFINITY;
           M = fmaxf(M, lk[k]);
         }
@@ -814,7 +844,8 @@ __device__ __forceinline__ void prefill2_body(const PrefillArgs& a, const CUtens
 #pragma unroll
             for (int k = 0; k < kMaxPieces; ++k) {
               if (k < un.npieces) {
-                const float4 v = __ldcg(pk + (static_cast<size_t>(k) * (D / 4) + c * 16 + e) * 128);
+                const float4 v =
+                    __ldcg(pk + (static_cast<size_t>(slot_of(k)) * (D / 4) + c * 16 + e) * 128);
                 acc.x = fmaf(w[k], v.x, acc.x);
                 acc.y = fmaf(w[k], v.y, acc.y);
                 acc.z = fmaf(w[k], v.z, acc.z);

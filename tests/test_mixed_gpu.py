@@ -142,8 +142,9 @@ def expected_pieces(batch):
     qsl = batch.query_start_loc.tolist()
     B, Hkv, D = batch.num_requests, batch.num_kv_heads, batch.head_dim
     G = batch.num_q_heads // Hkv
-    TQ = 128 // G
-    BN = 64 if D == 256 else 128
+    pair = D == 256  # CTA pairs: two query tiles per item, 128-key tiles
+    TQ = 128 // G * (2 if pair else 1)
+    BN = 128
     W = batch.window
     tiles = []
     for r in range(B):
@@ -157,10 +158,12 @@ def expected_pieces(batch):
             tiles.append(-(-(p_last + 1 - (t_lo // 16) * 16) // BN))
     # the SMs left to the prefill items (the host's split of the SMs)
     extra = qsl[-1] - B
-    est = -(-extra // TQ) * Hkv if extra > 0 else 0
+    tq = 128 // G  # the host's estimate: one-CTA tiles, 64 keys at D = 256
+    bn = 64 if D == 256 else 128
+    est = -(-extra // tq) * Hkv if extra > 0 else 0
     mql, msl = batch.max_query_len, batch.max_seq_len
-    keys = min(msl, W + TQ) if W > 0 else msl
-    prefill_us = est * (-(-keys // BN) + 1) * 2.0
+    keys = min(msl, W + tq) if W > 0 else msl
+    prefill_us = est * (-(-keys // bn) + 1) * 2.0
     chunks = -(-extra // (mql - 1)) if extra > 0 and mql > 1 else 0
     dec_rows = max(0, B - chunks)
     dec_keys = min(msl, W) if W > 0 else msl
@@ -170,10 +173,21 @@ def expected_pieces(batch):
         share = int(sms * prefill_us / (prefill_us + decode_us) + 0.5)
         wave = share if share >= 2 * est else est
         wave = min(max(wave, 1), sms - sms // 4)
+    slots, piece_slots = wave, SPLIT_SLOTS
+    if pair and est > 0:
+        dec = max(1, sms - wave)
+        dec -= dec % 2  # an even number of decode CTAs before the pairs
+        slots, piece_slots = (sms - dec) // 2, SPLIT_SLOTS // 2
     items = len(tiles) * Hkv
-    if not (0 < items < wave and items <= SPLIT_SLOTS):
+    if not (0 < items < slots and items <= piece_slots):
         return [1] * len(tiles)
-    budget = min(wave, SPLIT_SLOTS)
+    if pair:
+        # the host launches the pair kernel that cuts items only when the
+        # items the sizes suggest are fewer than the pair slots
+        est_pairs = -(-extra // (2 * tq)) * Hkv
+        if not (est_pairs < slots and est_pairs <= piece_slots):
+            return [1] * len(tiles)
+    budget = min(slots, piece_slots)
 
     def pieces(t, th):
         return min(8, max(1, -(-t // th)))
