@@ -1079,6 +1079,14 @@ __device__ __forceinline__ void prefill_body(const PrefillArgs& a, const CUtenso
         }
         inv = (den > 0.f) ? 1.f / den : 0.f;
       }
+      // w[k] for a k known only at run time, by selects (w stays in registers)
+      auto w_of = [&](int k) {
+        float x = w[0];
+#pragma unroll
+        for (int kk = 1; kk < kMaxPieces; ++kk)
+          if (k == kk) x = w[kk];
+        return x;
+      };
       // A tile of TQ tokens of this request leaves through TMA stores from
       // the Q tile's shared memory, which is free once the last MMA has
       // completed (the last P V commit covers every earlier MMA): each row
@@ -1092,23 +1100,24 @@ __device__ __forceinline__ void prefill_body(const PrefillArgs& a, const CUtenso
       for (int c = 0; c < D / 64; ++c) {  // 64 columns per load and wait
         float o[64];
         if (split_item) {
+          // piece by piece (the same order of terms for every element), the
+          // 16 loads of a piece's 64 columns issued together
 #pragma unroll
-          for (int e = 0; e < 16; ++e) {
-            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+          for (int e = 0; e < 64; ++e) o[e] = 0.f;
+#pragma unroll 1
+          for (int k = 0; k < un.npieces; ++k) {
+            const float4* src = pk + (static_cast<size_t>(k) * (D / 4) + c * 16) * 128;
+            float4 v[16];
 #pragma unroll
-            for (int k = 0; k < kMaxPieces; ++k) {
-              if (k < un.npieces) {
-                const float4 v = __ldcg(pk + (static_cast<size_t>(k) * (D / 4) + c * 16 + e) * 128);
-                acc.x = fmaf(w[k], v.x, acc.x);
-                acc.y = fmaf(w[k], v.y, acc.y);
-                acc.z = fmaf(w[k], v.z, acc.z);
-                acc.w = fmaf(w[k], v.w, acc.w);
-              }
+            for (int e = 0; e < 16; ++e) v[e] = __ldcg(src + e * 128);
+            const float wk = w_of(k);
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+              o[4 * e] = fmaf(wk, v[e].x, o[4 * e]);
+              o[4 * e + 1] = fmaf(wk, v[e].y, o[4 * e + 1]);
+              o[4 * e + 2] = fmaf(wk, v[e].z, o[4 * e + 2]);
+              o[4 * e + 3] = fmaf(wk, v[e].w, o[4 * e + 3]);
             }
-            o[4 * e] = acc.x;
-            o[4 * e + 1] = acc.y;
-            o[4 * e + 2] = acc.z;
-            o[4 * e + 3] = acc.w;
           }
         } else {
           tmem_ld64(lane_base + S::kTmemO + c * 64, o);
