@@ -204,7 +204,11 @@ __device__ __forceinline__ void tmem2_dealloc(uint32_t taddr, uint32_t ncols) {
 // that rank (heaviest first over (request, two query tiles) pairs),
 // KV head rank % Hkv; ranks past the last item return at once (both CTAs of
 // a cluster decide alike: everything up to the TMEM allocation depends on
-// the arguments and the cluster's index only).
+// the arguments and the cluster's index only).  kSplit (the mixed launch,
+// with its workspace): when every item fits the a.one_wave / 2 pair slots,
+// rank r takes unit r in index order instead, and with room to spare the
+// items are cut along keys into pieces merged through the workspace (two
+// slots per piece, one per CTA; see one_wave_unit in prefill_body.cuh).
 template <int G, bool kSplit>
 __device__ __forceinline__ void prefill2_body(const PrefillArgs& a, const CUtensorMap* tm_q,
                                               const CUtensorMap* tm_k, const CUtensorMap* tm_v,
