@@ -34,20 +34,18 @@ __global__ void __launch_bounds__(128) combine_kernel(const CombineArgs a) {
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
   for (int base = 0; base < S; base += 32) {
     const float lreg = (base + lane < S) ? lse[base + lane] : -INFINITY;
-    const int n = min(32, S - base);
-    for (int c = 0; c < n; c += 8) {
-      float lv[8];
-      float4 x[8];
+    // all of the (up to) 32 pieces' loads in flight before the first merge
+    float lv[32];
+    float4 x[32];
 #pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        lv[u] = __shfl_sync(0xffffffffu, lreg, (c + u) & 31);  // -inf past the row's end
-        x[u] = (lv[u] != -INFINITY)
-                   ? *reinterpret_cast<const float4*>(po + static_cast<size_t>(base + c + u) * D)
-                   : make_float4(0.f, 0.f, 0.f, 0.f);
-      }
-      lse_merge4(M, den, acc, lv, x);
-      lse_merge4(M, den, acc, lv + 4, x + 4);
+    for (int u = 0; u < 32; ++u) {
+      lv[u] = __shfl_sync(0xffffffffu, lreg, u);  // -inf past the row's end
+      x[u] = (lv[u] != -INFINITY)
+                 ? *reinterpret_cast<const float4*>(po + static_cast<size_t>(base + u) * D)
+                 : make_float4(0.f, 0.f, 0.f, 0.f);
     }
+#pragma unroll
+    for (int u = 0; u < 32; u += 4) lse_merge4(M, den, acc, lv + u, x + u);
   }
   const float inv = den > 0.f ? 1.f / den : 0.f;
   uint16_t* dst = a.out + static_cast<size_t>(row) * D + seg * 128 + lane * 4;
