@@ -203,7 +203,8 @@ def expected_pieces(batch):
 
 @pytest.mark.parametrize("D,G,window,softcap", [(256, 4, 0, 0.0), (256, 4, 1024, 50.0),
                                                 (128, 4, 0, 30.0), (256, 8, 0, 0.0),
-                                                (128, 1, 2000, 0.0)])
+                                                (128, 1, 2000, 0.0), (256, 1, 0, 0.0),
+                                                (256, 2, 512, 30.0)])
 def test_prefill_tiles_split_along_keys(D, G, window, softcap):
     """A few long-context chunk tiles next to decode rows: the items fill far
     less than the wave of SMs left to them, so each is cut along its keys
